@@ -1,0 +1,91 @@
+"""Shapes of the benchmark workloads (synthetic, seeded; no model file is read).
+
+Every weight is N(0, 0.02) before encoding, activations N(0, 1).  Tensor names
+follow the GGUF naming of "GGUF Inferencer in R" section 2.1 (blk.N.attn_q.weight,
+..., token_embd.weight).  rows = output features, cols = input features (ne0).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+from . import TYPE_Q4_K, TYPE_Q8_0, stream_id
+
+W_SIGMA = 0.02
+X_SIGMA = 1.0
+
+
+@dataclass(frozen=True)
+class Gemv:
+    name: str
+    qtype: int
+    rows: int
+    cols: int
+
+    @property
+    def stream(self) -> int:
+        return stream_id("w", self.name, self.qtype, self.rows, self.cols)
+
+    @property
+    def x_stream(self) -> int:
+        return stream_id("x", self.name, self.rows, self.cols)
+
+
+def _layer(prefix: str, hidden: int, n_q: int, n_kv: int, head_dim: int, ffn: int,
+           qtype: int):
+    kv = n_kv * head_dim
+    return [
+        Gemv(f"{prefix}.attn_q.weight", qtype, n_q * head_dim, hidden),
+        Gemv(f"{prefix}.attn_k.weight", qtype, kv, hidden),
+        Gemv(f"{prefix}.attn_v.weight", qtype, kv, hidden),
+        Gemv(f"{prefix}.attn_output.weight", qtype, hidden, n_q * head_dim),
+        Gemv(f"{prefix}.ffn_gate.weight", qtype, ffn, hidden),
+        Gemv(f"{prefix}.ffn_up.weight", qtype, ffn, hidden),
+        Gemv(f"{prefix}.ffn_down.weight", qtype, hidden, ffn),
+    ]
+
+
+# single Q8_0 GEMV 2048 x 2048, M = 1
+CFG1 = [Gemv("cfg1.q8_0.weight", TYPE_Q8_0, 2048, 2048)]
+
+# one SmolLM3-shaped layer (hidden 2048, 16 q heads, 4 kv heads, head_dim 128,
+# ffn 11008), all Q4_K, M = 1
+CFG2 = _layer("smollm3.blk.0", 2048, 16, 4, 128, 11008, TYPE_Q4_K)
+
+
+def llama8b_pass(n_layers: int = 32):
+    """Batch-1 decode weight pass over a Llama-8B-shaped stack: 32 layers of Q4_K
+    projections (hidden 4096, 32 q / 8 kv heads of 128, ffn 14336) and a Q8_0
+    4096 -> 128256 output head."""
+    out = []
+    for L in range(n_layers):
+        out += _layer(f"blk.{L}", 4096, 32, 8, 128, 14336, TYPE_Q4_K)
+    out.append(Gemv("output.weight", TYPE_Q8_0, 128256, 4096))
+    return out
+
+
+def llama8b_stages(n_layers: int = 32):
+    """The pass grouped into dependency stages: GEMVs within a stage share their
+    input vector (q/k/v; gate/up) and can run in one launch."""
+    gem = llama8b_pass(n_layers)
+    stages = []
+    for L in range(n_layers):
+        g = gem[7 * L: 7 * L + 7]
+        stages += [g[0:3], [g[3]], g[4:6], [g[6]]]
+    stages.append([gem[-1]])
+    return stages
+
+
+CFG3 = llama8b_pass()
+
+# small-batch Q8_0 GEMM on 14336 x 4096
+CFG4 = Gemv("cfg4.q8_0.weight", TYPE_Q8_0, 14336, 4096)
+CFG4_M = (1, 2, 4, 8, 16)
+
+# prefill: Q4_K 14336 x 4096 times bf16 X [512, 4096]
+CFG5 = Gemv("cfg5.q4_k.weight", TYPE_Q4_K, 14336, 4096)
+CFG5_M = 512
+
+
+def weight_bytes(gemvs) -> int:
+    from . import row_bytes
+    return sum(g.rows * row_bytes(g.qtype, g.cols) for g in gemvs)

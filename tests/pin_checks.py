@@ -1,0 +1,291 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``check_*`` takes an ``oracle.Oracle`` (the real build, or a deliberately
+broken copy in test_oracle_mutants.py) and raises AssertionError on a mismatch.
+Expected values come from the pages (golden fixtures), from closed forms worked
+out by hand for hand-built blocks, from IEEE-754 special values, from integer
+arithmetic (exact), or from numpy library routines on tiny inputs.
+"""
+from __future__ import annotations
+
+import struct
+
+import numpy as np
+
+F32, F16, Q8_0, Q4_K = 0, 1, 8, 12
+
+
+# ------------------------------------------------------------ fp16 / bf16 ----
+
+def check_fp16(orc):
+    # IEEE-754 binary16 special values, written out by hand
+    literal = {
+        0x3C00: 1.0, 0xC000: -2.0, 0x3800: 0.5, 0x7BFF: 65504.0,
+        0x0400: 2.0 ** -14, 0x0001: 2.0 ** -24, 0x03FF: 1023 * 2.0 ** -24,
+        0x3555: 1365 / 4096, 0x0000: 0.0, 0x4B00: 14.0, 0x5BD0: 250.0,
+    }
+    for h, v in literal.items():
+        assert orc.fp16_value(h) == v, hex(h)
+    assert str(orc.fp16_value(0x8000)) == "-0.0"
+    assert orc.fp16_value(0x7C00) == float("inf")
+    assert orc.fp16_value(0xFC00) == float("-inf")
+    assert np.isnan(orc.fp16_value(0x7E00)) and np.isnan(orc.fp16_value(0xFC01))
+    # every pattern against numpy's binary16 (a library routine)
+    pats = np.arange(65536, dtype=np.uint16)
+    ref = pats.view(np.float16).astype(np.float64)
+    got = np.array([orc.fp16_value(int(h)) for h in pats])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all((ref == got) | both_nan)
+    assert np.array_equal(np.signbit(ref[~both_nan]), np.signbit(got[~both_nan]))
+
+
+def check_bf16(orc):
+    assert orc.bf16_value(0x3F80) == 1.0
+    assert orc.bf16_value(0xC040) == -3.0
+    assert orc.bf16_value(0x0001) == 2.0 ** -133
+    rng = np.random.default_rng(1)
+    for b in rng.integers(0, 65536, 500):
+        v = np.array([int(b) << 16], dtype=np.uint32).view(np.float32)[0]
+        g = orc.bf16_value(int(b))
+        assert (np.isnan(v) and np.isnan(g)) or g == float(v)
+
+
+# ------------------------------------------------------------------- Q8_0 ----
+
+def q8_block(d_bits: int, qs) -> bytes:
+    assert len(qs) == 32
+    return struct.pack("<H", d_bits) + bytes((q & 0xFF) for q in qs)
+
+
+Q8_PATTERN = [-128, -127, 0, 1, 127, 2, -2, 64, -64, 3, 5, 7, 11, 13, 17, 19,
+              23, 29, 31, 37, -41, -43, -47, 53, 59, 61, -67, 71, 73, -79, 83, 89]
+
+
+def check_q8_0_blocks(orc):
+    # d = 1 (0x3C00): weights are the signed bytes themselves
+    got = orc.decode_q8_0_block(q8_block(0x3C00, Q8_PATTERN))
+    assert got.tolist() == [float(q) for q in Q8_PATTERN]
+    # d = 0.5 (0x3800)
+    got = orc.decode_q8_0_block(q8_block(0x3800, Q8_PATTERN))
+    assert got.tolist() == [q / 2 for q in Q8_PATTERN]
+    # d = -2 (0xC000): sign of d applies
+    got = orc.decode_q8_0_block(q8_block(0xC000, Q8_PATTERN))
+    assert got.tolist() == [-2.0 * q for q in Q8_PATTERN]
+    # d = smallest subnormal 2^-24
+    got = orc.decode_q8_0_block(q8_block(0x0001, Q8_PATTERN))
+    assert got.tolist() == [q * 2.0 ** -24 for q in Q8_PATTERN]
+    # d = 65504 (largest finite half); 65504 * -128 = -8384512 is exact in fp32
+    got = orc.decode_q8_0_block(q8_block(0x7BFF, [-128] + [0] * 30 + [127]))
+    assert got[0] == -8384512.0 and got[31] == 65504.0 * 127 and not got[1:31].any()
+    # block byte size from bits/weight: 8.5 bits * 32 = 34 bytes
+    assert orc.row_bytes(Q8_0, 32) == 34 and orc.row_bytes(Q8_0, 2048) == 64 * 34
+    assert orc.row_bytes(Q8_0, 48) == 0  # not a whole number of blocks
+
+
+# ------------------------------------------------------------------- Q4_K ----
+
+def q4k_block(d_bits: int, dmin_bits: int, scales12, qs128) -> bytes:
+    assert len(scales12) == 12 and len(qs128) == 128
+    return struct.pack("<HH", d_bits, dmin_bits) + bytes(scales12) + bytes(qs128)
+
+
+def check_q4_k_blocks(orc):
+    # A: d = 1, dmin = 0, sc_j = j+1, m_j = 0, every nibble 1 -> w[k] = k//32 + 1
+    #    scales bytes worked out by hand: s[0..3] = sc0..3, s[4..7] = m0..3 = 0,
+    #    s[8..11] = low nibbles of sc4..7 (5,6,7,8) | m4..7 << 4 (0)
+    blk = q4k_block(0x3C00, 0x0000, [1, 2, 3, 4, 0, 0, 0, 0, 5, 6, 7, 8], [0x11] * 128)
+    got = orc.decode_q4_k_block(blk)
+    assert got.tolist() == [float(k // 32 + 1) for k in range(256)]
+
+    # B: the 2-bit high parts of sub-blocks 4..7.  sc = (0,0,0,0,63,32,16,48),
+    #    m = (0,0,0,0,33,17,63,2), d = dmin = 1, every q = 2  ->  w = 2 sc - m
+    #    bytes by hand: s[0..3] = (sc4..7 >> 4) << 6 = C0 80 40 C0,
+    #    s[4..7] = (m4..7 >> 4) << 6 = 80 40 C0 00,
+    #    s[8..11] = (sc & 15) | (m & 15) << 4 = 1F 10 F0 20
+    blk = q4k_block(0x3C00, 0x3C00,
+                    [0xC0, 0x80, 0x40, 0xC0, 0x80, 0x40, 0xC0, 0x00, 0x1F, 0x10, 0xF0, 0x20],
+                    [0x22] * 128)
+    got = orc.decode_q4_k_block(blk)
+    expect = [0.0] * 128 + [93.0] * 32 + [47.0] * 32 + [-31.0] * 32 + [94.0] * 32
+    assert got.tolist() == expect
+
+    # C: mins and sign. d = 0.5, dmin = 0.25, sc = 1..8, m = 8..1, q = 3:
+    #    w_j = 1.5 sc_j - 0.25 m_j = -0.5, 1.25, 3, 4.75, 6.5, 8.25, 10, 11.75
+    blk = q4k_block(0x3800, 0x3400,
+                    [1, 2, 3, 4, 8, 7, 6, 5, 0x45, 0x36, 0x27, 0x18], [0x33] * 128)
+    got = orc.decode_q4_k_block(blk)
+    vals = [-0.5, 1.25, 3.0, 4.75, 6.5, 8.25, 10.0, 11.75]
+    assert got.tolist() == [vals[k // 32] for k in range(256)]
+
+    # D: nibble positions.  d = 1, all sc = 1, m = 0; one nibble = 15.
+    #    qs[i] low nibble -> weight 64*(i//32) + i%32, high nibble -> +32
+    ones = [1, 1, 1, 1, 0, 0, 0, 0, 0x01, 0x01, 0x01, 0x01]
+    cases = {(0, 0): 0, (0, 1): 32, (31, 0): 31, (31, 1): 63, (32, 0): 64, (32, 1): 96,
+             (70, 0): 134, (70, 1): 166, (127, 0): 223, (127, 1): 255, (100, 0): 196,
+             (100, 1): 228}
+    for (i, hi), k in cases.items():
+        qs = [0] * 128
+        qs[i] = 0xF0 if hi else 0x0F
+        got = orc.decode_q4_k_block(q4k_block(0x3C00, 0x0000, ones, qs))
+        assert got[k] == 15.0 and np.count_nonzero(got) == 1, (i, hi, k)
+    # every (byte, nibble) lands on a distinct weight
+    seen = set()
+    for i in range(128):
+        for hi in (0, 1):
+            qs = [0] * 128
+            qs[i] = 0xF0 if hi else 0x0F
+            got = orc.decode_q4_k_block(q4k_block(0x3C00, 0x0000, ones, qs))
+            nz = np.flatnonzero(got)
+            assert nz.size == 1
+            seen.add(int(nz[0]))
+    assert seen == set(range(256))
+
+    # E: subnormal d = 2^-24 and dmin = 2^-23, sc = 1 everywhere, m_0 = 1, q = 1:
+    #    sub-block 0 -> 2^-24 - 2^-23 = -2^-24, the others -> 2^-24
+    blk = q4k_block(0x0001, 0x0002, [1, 1, 1, 1, 1, 0, 0, 0, 0x01, 0x01, 0x01, 0x01],
+                    [0x11] * 128)
+    got = orc.decode_q4_k_block(blk)
+    assert got.tolist() == [-(2.0 ** -24)] * 32 + [2.0 ** -24] * 224
+    # F: one rounding only: d*sc*q - dmin*m with d = 1 + 2^-10, sc = 63, q = 15,
+    #    dmin = 2^-14 (0x0400), m = 1 -> exact 945.9228515625 - 2^-14, rounded to fp32
+    blk = q4k_block(0x3C01, 0x0400, [63, 0, 0, 0, 1, 0, 0, 0, 0, 0, 0, 0], [0x0F] + [0] * 127)
+    got = orc.decode_q4_k_block(blk)
+    exact = (1 + 2.0 ** -10) * 63 * 15 - 2.0 ** -14
+    assert got[0] == np.float32(exact)
+    assert orc.row_bytes(Q4_K, 256) == 144 and orc.row_bytes(Q4_K, 4096) == 16 * 144
+    assert orc.row_bytes(Q4_K, 128) == 0
+
+
+# --------------------------------------------------------------- helpers ----
+
+def pack_q4_k(d_bits, dmin_bits, sc, m, q):
+    """Test-side packer for hand-chosen 6-bit scales/mins and 4-bit values."""
+    s = [0] * 12
+    for j in range(4):
+        s[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+        s[j + 4] = (m[j] & 63) | ((m[j + 4] >> 4) << 6)
+        s[j + 8] = (sc[j + 4] & 15) | ((m[j + 4] & 15) << 4)
+    qs = [0] * 128
+    for c in range(4):
+        for l in range(32):
+            qs[32 * c + l] = q[64 * c + l] | (q[64 * c + 32 + l] << 4)
+    return q4k_block(d_bits, dmin_bits, s, qs)
+
+
+# ------------------------------------------------------------------- GEMV ----
+
+def check_one_hot(orc):
+    """x = e_c extracts column c exactly (every other product is an exact 0)."""
+    rows = 3
+    # Q8_0, cols 64: row r block b has d = 1 and q[i] = Q8_PATTERN[(i + 5r + 7b) % 32]
+    W = b"".join(q8_block(0x3C00, [Q8_PATTERN[(i + 5 * r + 7 * b) % 32] for i in range(32)])
+                 for r in range(rows) for b in range(2))
+    for c in (0, 1, 31, 32, 45, 63):
+        x = np.zeros(64, dtype=np.float32)
+        x[c] = 1.0
+        y, _ = orc.gemv(Q8_0, np.frombuffer(W, np.uint8), rows, 64, x)
+        b, i = divmod(c, 32)
+        assert y[0].tolist() == [float(Q8_PATTERN[(i + 5 * r + 7 * b) % 32]) for r in range(rows)]
+    # Q4_K, cols 512: super-block (r, b): d = 1, dmin = 1, sc_j = j + 1 + r, m_j = 2b + j,
+    # q = (k + r) % 16 -> w[k] = (j+1+r) * ((k+r)%16) - (2b + j), j = (k % 256) // 32
+    blocks = []
+    for r in range(rows):
+        for b in range(2):
+            sc = [j + 1 + r for j in range(8)]
+            m = [2 * b + j for j in range(8)]
+            q = [(k + r) % 16 for k in range(256)]
+            blocks.append(pack_q4_k(0x3C00, 0x3C00, sc, m, q))
+    W = b"".join(blocks)
+    for c in (0, 31, 32, 100, 255, 256, 300, 511):
+        x = np.zeros(512, dtype=np.float32)
+        x[c] = 1.0
+        y, _ = orc.gemv(Q4_K, np.frombuffer(W, np.uint8), rows, 512, x)
+        b, k = divmod(c, 256)
+        j = k // 32
+        assert y[0].tolist() == [float((j + 1 + r) * ((k + r) % 16) - (2 * b + j))
+                                 for r in range(rows)], c
+
+
+def check_integer_exact(orc):
+    """Integer-valued weights and x: every partial sum is an exact integer."""
+    rng = np.random.default_rng(7)
+    rows, cols, M = 17, 512, 3
+    q = rng.integers(-128, 128, size=(rows, cols))
+    W = b"".join(q8_block(0x3C00, list(q[r, 32 * b: 32 * b + 32]))
+                 for r in range(rows) for b in range(cols // 32))
+    x = rng.integers(-8, 9, size=(M, cols))
+    y, ay = orc.gemv(Q8_0, np.frombuffer(W, np.uint8), rows, cols, x.astype(np.float32))
+    ref = x @ q.T
+    assert np.array_equal(y, ref.astype(np.float64))
+    assert np.array_equal(ay, (np.abs(x) @ np.abs(q).T).astype(np.float64))
+    # Q4_K with d = dmin = 1: w = sc*q - m
+    sc = rng.integers(0, 64, size=(rows, cols // 256, 8))
+    mm = rng.integers(0, 64, size=(rows, cols // 256, 8))
+    qq = rng.integers(0, 16, size=(rows, cols))
+    W = b"".join(pack_q4_k(0x3C00, 0x3C00, list(sc[r, b]), list(mm[r, b]),
+                           list(qq[r, 256 * b: 256 * b + 256]))
+                 for r in range(rows) for b in range(cols // 256))
+    j = (np.arange(cols) % 256) // 32
+    bidx = np.arange(cols) // 256
+    w = sc[:, bidx, j] * qq - mm[:, bidx, j]
+    y, _ = orc.gemv(Q4_K, np.frombuffer(W, np.uint8), rows, cols, x.astype(np.float32))
+    assert np.array_equal(y, (x @ w.T).astype(np.float64))
+
+
+def check_brute_force(orc):
+    """Tiny shapes: oracle GEMV vs numpy float64 matmul of independently built weights."""
+    rng = np.random.default_rng(11)
+    for rows in (1, 3, 17):
+        for cols in (256, 512, 2048):
+            for M in (1, 2, 3, 16):
+                # Q8_0 with random fp16 scales
+                d = rng.uniform(0.001, 0.01, size=(rows, cols // 32)).astype(np.float16)
+                q = rng.integers(-127, 128, size=(rows, cols))
+                W = b"".join(struct.pack("<e", d[r, b]) +
+                             bytes((int(v) & 0xFF) for v in q[r, 32 * b:32 * b + 32])
+                             for r in range(rows) for b in range(cols // 32))
+                w = np.repeat(d.astype(np.float64), 32, axis=1) * q
+                x = rng.standard_normal((M, cols)).astype(np.float32)
+                y, ay = orc.gemv(Q8_0, np.frombuffer(W, np.uint8), rows, cols, x)
+                ref = x.astype(np.float64) @ w.T
+                assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+                assert np.allclose(ay, np.abs(x.astype(np.float64)) @ np.abs(w).T, rtol=1e-12)
+        # Q4_K with random fp16 d / dmin and 6-bit scales
+        cols = 512
+        d = rng.uniform(1e-4, 1e-3, size=(rows, 2)).astype(np.float16)
+        dm = rng.uniform(1e-4, 1e-3, size=(rows, 2)).astype(np.float16)
+        sc = rng.integers(0, 64, size=(rows, 2, 8))
+        mm = rng.integers(0, 64, size=(rows, 2, 8))
+        qq = rng.integers(0, 16, size=(rows, cols))
+        W = b"".join(pack_q4_k(int(d[r, b].view(np.uint16)), int(dm[r, b].view(np.uint16)),
+                               list(sc[r, b]), list(mm[r, b]), list(qq[r, 256 * b:256 * b + 256]))
+                     for r in range(rows) for b in range(2))
+        j = (np.arange(cols) % 256) // 32
+        bi = np.arange(cols) // 256
+        w = (d.astype(np.float64)[:, bi] * sc[:, bi, j] * qq
+             - dm.astype(np.float64)[:, bi] * mm[:, bi, j]).astype(np.float32)
+        x = rng.standard_normal((2, cols)).astype(np.float32)
+        y, _ = orc.gemv(Q4_K, np.frombuffer(W, np.uint8), rows, cols, x)
+        assert np.allclose(y, x.astype(np.float64) @ w.astype(np.float64).T, rtol=1e-12, atol=1e-15)
+        Wd = orc.dequantize(Q4_K, np.frombuffer(W, np.uint8), rows, cols)
+        assert np.array_equal(Wd, w)
+
+
+def check_gemm_bf16(orc):
+    """bf16 X is widened exactly: Y = X W^T with X taken as the bf16 values."""
+    rng = np.random.default_rng(13)
+    rows, cols, M = 5, 256, 4
+    q = rng.integers(-127, 128, size=(rows, cols))
+    W = b"".join(q8_block(0x3800, list(q[r, 32 * b:32 * b + 32]))
+                 for r in range(rows) for b in range(cols // 32))
+    xf = rng.standard_normal((M, cols)).astype(np.float32)
+    bits = (xf.view(np.uint32) >> 16).astype(np.uint16)      # truncation: any bf16 pattern
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Y, _ = orc.gemm_bf16(Q8_0, np.frombuffer(W, np.uint8), rows, cols, bits)
+    assert np.allclose(Y, xv @ (0.5 * q).T, rtol=1e-12, atol=1e-12)
+    y2, _ = orc.gemv(Q8_0, np.frombuffer(W, np.uint8), rows, cols, xv.astype(np.float32))
+    assert np.array_equal(Y, y2)
+
+
+ALL_CHECKS = [check_fp16, check_bf16, check_q8_0_blocks, check_q4_k_blocks,
+              check_one_hot, check_integer_exact, check_brute_force, check_gemm_bf16]

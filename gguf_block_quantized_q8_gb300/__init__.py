@@ -1,0 +1,9 @@
+"""ggq -- GB300-native block-quantized (Q8_0 / Q4_K) dequantize + GEMV.
+
+The compute path is ``libggq.so`` (C ABI in ``include/ggq.h``), built in-tree for
+sm_103a by ``build.build()``.  This package is its thin Python binding.
+"""
+from . import build  # noqa: F401
+from ._ggq import (F16, F32, Q4_0, Q4_K, Q6_K, Q8_0, GGQError, Model, check, dequantize,  # noqa: F401
+                   device_status, gemm_prefill, gemv, ggq_dequantize, ggq_device_status,
+                   ggq_gemm_prefill, ggq_gemv, lib, LIB_PATH, strerror)

@@ -1,0 +1,230 @@
+"""ctypes binding of libggq.so (include/ggq.h): argument marshalling only.
+
+Every entry point of the C ABI is exposed under its own name.  The torch
+helpers below accept CUDA tensors and pass their data pointers and the current
+stream; torch is used for device memory and streams only.  If the shared
+library is missing or cannot be loaded, importing this module raises: there is
+no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+OK, EINVAL, ETYPE, EIO, EFORMAT, ENOMEM, ECUDA, ETIMEOUT, ENOTFOUND = 0, -1, -2, -3, -4, -5, -6, -7, -8
+F32, F16, Q4_0, Q8_0, Q4_K, Q6_K = 0, 1, 2, 8, 12, 14
+LOAD_METADATA_ONLY = 1
+
+
+class GGQError(RuntimeError):
+    def __init__(self, code: int, where: str, message: str):
+        super().__init__(f"{where}: {message} (code {code})")
+        self.code = code
+
+
+class Tensor(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("type", ctypes.c_int32), ("n_dims", ctypes.c_int32),
+                ("ne", ctypes.c_int64 * 4), ("offset", ctypes.c_uint64), ("nbytes", ctypes.c_uint64),
+                ("data", ctypes.c_void_p)]
+
+
+def _bind(lib):
+    vp, i64, u64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int32
+    sig = {
+        "ggq_load": ([ctypes.c_char_p, ctypes.POINTER(vp)], ctypes.c_int),
+        "ggq_load_ex": ([ctypes.c_char_p, ctypes.c_uint, ctypes.POINTER(vp)], ctypes.c_int),
+        "ggq_load_memory": ([vp, ctypes.c_size_t, ctypes.c_uint, ctypes.POINTER(vp)], ctypes.c_int),
+        "ggq_free": ([vp], None),
+        "ggq_version_of": ([vp, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+        "ggq_data_start": ([vp, ctypes.POINTER(u64)], ctypes.c_int),
+        "ggq_num_tensors": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
+        "ggq_tensor_info": ([vp, i64, ctypes.POINTER(Tensor)], ctypes.c_int),
+        "ggq_find_tensor": ([vp, ctypes.c_char_p, ctypes.POINTER(i64)], ctypes.c_int),
+        "ggq_num_kv": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
+        "ggq_kv_info": ([vp, i64, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32),
+                         ctypes.POINTER(vp), ctypes.POINTER(u64)], ctypes.c_int),
+        "ggq_kv_find": ([vp, ctypes.c_char_p, ctypes.POINTER(i64)], ctypes.c_int),
+        "ggq_gemv": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
+        "ggq_gemm_prefill": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
+        "ggq_dequantize": ([ctypes.c_int, vp, i64, i64, vp, vp], ctypes.c_int),
+        "ggq_device_status": ([], ctypes.c_int),
+        "ggq_strerror": ([ctypes.c_int], ctypes.c_char_p),
+        "ggq_last_error": ([], ctypes.c_char_p),
+        "ggq_abi_version": ([], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+def _load():
+    path = _build.LIB
+    if _build.is_stale():
+        if os.environ.get("GGQ_NO_AUTOBUILD"):
+            raise ImportError(f"{path} is missing or stale; run __graft_entry__.build()")
+        _build.build()
+    return _bind(ctypes.CDLL(path))
+
+
+lib = _load()
+LIB_PATH = _build.LIB
+
+
+def check(rc: int, where: str) -> None:
+    if rc != OK:
+        msg = lib.ggq_last_error().decode(errors="replace") or lib.ggq_strerror(rc).decode()
+        raise GGQError(rc, where, msg)
+
+
+def strerror(code: int) -> str:
+    return lib.ggq_strerror(code).decode()
+
+
+# ------------------------------------------------------------------ raw calls
+
+def ggq_gemv(qtype: int, W: int, rows: int, cols: int, x: int, y: int, M: int, stream: int) -> int:
+    return lib.ggq_gemv(qtype, W, rows, cols, x, y, M, stream)
+
+
+def ggq_gemm_prefill(qtype: int, W: int, rows: int, cols: int, X: int, Y: int, M: int, stream: int) -> int:
+    return lib.ggq_gemm_prefill(qtype, W, rows, cols, X, Y, M, stream)
+
+
+def ggq_dequantize(qtype: int, W: int, rows: int, cols: int, out: int, stream: int) -> int:
+    return lib.ggq_dequantize(qtype, W, rows, cols, out, stream)
+
+
+def ggq_device_status() -> int:
+    return lib.ggq_device_status()
+
+
+# --------------------------------------------------------------- model handle
+
+class Model:
+    """A loaded GGUF file (ggq_load / ggq_load_memory); payloads live on the device."""
+
+    def __init__(self, handle: int):
+        self._h = ctypes.c_void_p(handle)
+
+    @classmethod
+    def load(cls, path: str, metadata_only: bool = False) -> "Model":
+        h = ctypes.c_void_p()
+        check(lib.ggq_load_ex(path.encode(), LOAD_METADATA_ONLY if metadata_only else 0, ctypes.byref(h)),
+              "ggq_load")
+        return cls(h.value)
+
+    @classmethod
+    def from_bytes(cls, buf: bytes, metadata_only: bool = False) -> "Model":
+        h = ctypes.c_void_p()
+        b = ctypes.create_string_buffer(bytes(buf), len(buf)) if buf else None
+        check(lib.ggq_load_memory(b, len(buf), LOAD_METADATA_ONLY if metadata_only else 0, ctypes.byref(h)),
+              "ggq_load_memory")
+        return cls(h.value)
+
+    def close(self):
+        if self._h:
+            lib.ggq_free(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    @property
+    def version(self) -> int:
+        v = ctypes.c_uint32()
+        check(lib.ggq_version_of(self._h, ctypes.byref(v)), "ggq_version_of")
+        return v.value
+
+    @property
+    def data_start(self) -> int:
+        v = ctypes.c_uint64()
+        check(lib.ggq_data_start(self._h, ctypes.byref(v)), "ggq_data_start")
+        return v.value
+
+    def __len__(self) -> int:
+        n = ctypes.c_int64()
+        check(lib.ggq_num_tensors(self._h, ctypes.byref(n)), "ggq_num_tensors")
+        return n.value
+
+    def tensor(self, i: int) -> dict:
+        t = Tensor()
+        check(lib.ggq_tensor_info(self._h, i, ctypes.byref(t)), "ggq_tensor_info")
+        return dict(name=t.name.decode(), type=t.type, n_dims=t.n_dims, ne=list(t.ne)[:t.n_dims],
+                    offset=t.offset, nbytes=t.nbytes, data=t.data or 0)
+
+    def tensors(self):
+        return [self.tensor(i) for i in range(len(self))]
+
+    def find(self, name: str) -> dict:
+        i = ctypes.c_int64()
+        check(lib.ggq_find_tensor(self._h, name.encode(), ctypes.byref(i)), "ggq_find_tensor")
+        return self.tensor(i.value)
+
+    def kvs(self):
+        n = ctypes.c_int64()
+        check(lib.ggq_num_kv(self._h, ctypes.byref(n)), "ggq_num_kv")
+        out = []
+        for i in range(n.value):
+            key, vt, val, nb = ctypes.c_char_p(), ctypes.c_int32(), ctypes.c_void_p(), ctypes.c_uint64()
+            check(lib.ggq_kv_info(self._h, i, ctypes.byref(key), ctypes.byref(vt), ctypes.byref(val),
+                                  ctypes.byref(nb)), "ggq_kv_info")
+            raw = ctypes.string_at(val.value, nb.value) if nb.value else b""
+            out.append((key.value.decode(), vt.value, raw))
+        return out
+
+
+# -------------------------------------------------------------- torch helpers
+
+def _stream_ptr(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def gemv(qtype: int, W, rows: int, cols: int, x, y=None, stream=None):
+    """y[M, rows] = x[M, cols] @ W^T with W a uint8 CUDA tensor of encoded blocks."""
+    import torch
+    x2 = x.reshape(-1, cols)
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, rows), dtype=torch.float32, device=x.device)
+    check(ggq_gemv(qtype, W.data_ptr(), rows, cols, x2.data_ptr(), y.data_ptr(), M, _stream_ptr(stream)),
+          "ggq_gemv")
+    return y
+
+
+def gemm_prefill(qtype: int, W, rows: int, cols: int, X_bf16, Y=None, stream=None):
+    """Y[M, rows] = X[M, cols] @ W^T, X a bf16 CUDA tensor (or uint16 bit patterns)."""
+    import torch
+    M = X_bf16.shape[0]
+    if Y is None:
+        Y = torch.empty((M, rows), dtype=torch.float32, device=X_bf16.device)
+    check(ggq_gemm_prefill(qtype, W.data_ptr(), rows, cols, X_bf16.data_ptr(), Y.data_ptr(), M,
+                           _stream_ptr(stream)), "ggq_gemm_prefill")
+    return Y
+
+
+def dequantize(qtype: int, W, rows: int, cols: int, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32, device=W.device)
+    check(ggq_dequantize(qtype, W.data_ptr(), rows, cols, out.data_ptr(), _stream_ptr(stream)),
+          "ggq_dequantize")
+    return out
+
+
+def device_status() -> int:
+    return ggq_device_status()

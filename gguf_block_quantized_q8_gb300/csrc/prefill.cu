@@ -1,0 +1,378 @@
+// Prefill dequant-GEMM on the tcgen05 tensor cores:  Y[M, rows] = X[M, cols] * W^T.
+//
+// "GGUF Inferencer in R" section 4: prefill runs the whole prompt through the same
+// weights "at once with big matrix multiplications".  W is Q4_K ("GGUF: The File
+// Format...", k-quant paragraph of "How a Q8_0 block is stored"): 256 weights per
+// 144-byte super-block, w = d*sc_j*q - dmin*m_j.  X is bf16.
+//
+// One CTA computes a 128 (W rows) x 256 (tokens) tile of Y^T in tensor memory:
+//   warp 0      TMA producer: raw Q4_K super-blocks [128 rows x 144 B] and X tiles
+//               [256 tokens x 64 k] (128-byte swizzle) into shared-memory rings;
+//   warp 1      allocates 256 TMEM columns; one thread issues tcgen05.mma
+//               (kind::f16, bf16 x bf16 -> fp32, M=128, N=256, K=16) per 16 k and
+//               commits each stage back to its "empty" barrier;
+//   warps 2..5  decoders: thread = W row; each 64-k stage decodes 64 weights exactly
+//               in fp32, rounds them to bf16 and writes the row in the canonical
+//               K-major 128-byte-swizzle layout the MMA reads; afterwards the same
+//               warps read the accumulator (tcgen05.ld) and store Y (each warp may
+//               only reach its own quarter of the 128 TMEM lanes).
+// Every wait is bounded (ptx.cuh: mbar_wait); a timeout is recorded in the device
+// status word and the kernel runs to completion without the data.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ggq_internal.h"
+#include "ptx.cuh"
+
+namespace ggq {
+
+namespace {
+
+constexpr int kTileRows = 128;        // UMMA M (W rows)
+constexpr int kTileTok = 256;         // UMMA N (tokens)
+constexpr int kKStage = 64;           // k per stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 3;
+constexpr int kRawStages = 2;
+constexpr int kRawBytes = kTileRows * 144;              // one super-block column
+constexpr int kABytes = kTileRows * kKStage * 2;        // 16 KB
+constexpr int kBBytes = kTileTok * kKStage * 2;         // 32 KB
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 256;
+
+constexpr size_t kSmemPayload = (size_t)kStages * (kABytes + kBBytes) + (size_t)kRawStages * kRawBytes;
+constexpr size_t kSmemBytes = kSmemPayload + 1024 /* alignment */ + 256 /* barriers */;
+
+struct PrefillParams {
+    float* Y;
+    int rows;        // W rows (Y columns)
+    int cols;        // K
+    int M;           // tokens
+    int tok_tiles;   // M / 256 (rounded up)
+    int* status;
+};
+
+// ------------------------------------------------------------- tcgen05 wrappers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// arrive on `bar` once every tcgen05 operation issued so far by this thread is done
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 TMEM lanes x 16 consecutive 32-bit columns -> 16 registers per thread
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B
+// apart (stride byte offset), leading byte offset unused for this layout (1),
+// descriptor version 1, base offset 0 (tiles are 1024-byte aligned).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTileTok >> 3) << 17) |
+                            ((uint32_t)(kTileRows >> 4) << 24);
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 6-bit scale and min of sub-block j from the 12 packed bytes (three words)
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc, int& m) {
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63;
+        m = (s1 >> (8 * j)) & 63;
+    } else {
+        const int k = j - 4;
+        sc = ((s2 >> (8 * k)) & 15) | (((s0 >> (8 * k + 6)) & 3) << 4);
+        m = ((s2 >> (8 * k + 4)) & 15) | (((s1 >> (8 * k + 6)) & 3) << 4);
+    }
+}
+
+// ------------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                  const __grid_constant__ CUtensorMap xmap,
+                                                                  const PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_tile = blockIdx.x / p.tok_tiles;
+    const int tok_tile = blockIdx.x % p.tok_tiles;
+    const int row0 = row_tile * kTileRows;
+    const int tok0 = tok_tile * kTileTok;
+    const int nks = p.cols / kKStage;     // k stages
+    const int nsb = p.cols / 256;         // super-blocks
+
+    // 1024-aligned carve-out
+    const uint32_t base_u32 = smem_u32(smem_raw);
+    uint8_t* base = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
+    uint8_t* sB = base;                                      // kStages x 32 KB
+    uint8_t* sA = sB + (size_t)kStages * kBBytes;            // kStages x 16 KB
+    uint8_t* sRaw = sA + (size_t)kStages * kABytes;          // kRawStages x 18 KB
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + (size_t)kRawStages * kRawBytes);
+    uint64_t* full_b = bars;                     // [kStages]
+    uint64_t* full_a = bars + kStages;           // [kStages]
+    uint64_t* empty = bars + 2 * kStages;        // [kStages]
+    uint64_t* full_raw = bars + 3 * kStages;     // [kRawStages]
+    uint64_t* empty_raw = full_raw + kRawStages; // [kRawStages]
+    uint64_t* acc_full = empty_raw + kRawStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&wmap);
+        prefetch_tensormap(&xmap);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_b[s], 1);
+            mbar_init(&full_a[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        for (int r = 0; r < kRawStages; ++r) {
+            mbar_init(&full_raw[r], 1);
+            mbar_init(&empty_raw[r], 128);
+        }
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            pdl_wait();   // X may come from the previous kernel in the stream
+            for (int ks = 0; ks < nks; ++ks) {
+                if ((ks & 3) == 0) {
+                    const int sb = ks >> 2, r = sb % kRawStages;
+                    mbar_wait(&empty_raw[r], ((sb / kRawStages) & 1) ^ 1, p.status);
+                    mbar_arrive_expect_tx(&full_raw[r], kRawBytes);
+                    tma_load_2d(sRaw + (size_t)r * kRawBytes, &wmap, &full_raw[r], sb * 144, row0);
+                }
+                const int s = ks % kStages;
+                mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
+                mbar_arrive_expect_tx(&full_b[s], kBBytes);
+                tma_load_2d(sB + (size_t)s * kBBytes, &xmap, &full_b[s], ks * kKStage, tok0);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int ks = 0; ks < nks; ++ks) {
+                const int s = ks % kStages;
+                const uint32_t ph = (ks / kStages) & 1;
+                mbar_wait(&full_b[s], ph, p.status);
+                mbar_wait(&full_a[s], ph, p.status);
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + (size_t)s * kABytes);
+                const uint32_t b_addr = smem_u32(sB + (size_t)s * kBBytes);
+#pragma unroll
+                for (int kk = 0; kk < kKStage / 16; ++kk) {
+                    // 16 bf16 = 32 bytes further along the swizzled 128-byte rows
+                    umma_bf16(tmem, sw128_desc(a_addr + 32 * kk), sw128_desc(b_addr + 32 * kk), kIdesc,
+                              (ks | kk) != 0);
+                }
+                umma_commit(&empty[s]);
+            }
+            umma_commit(acc_full);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ decoders (warps 2..5)
+        const int t = (warp - 2) * 32 + lane;   // W row within the tile
+        for (int sb = 0; sb < nsb; ++sb) {
+            const int r = sb % kRawStages;
+            mbar_wait(&full_raw[r], (sb / kRawStages) & 1, p.status);
+            const uint8_t* rp = sRaw + (size_t)r * kRawBytes + (size_t)t * 144;
+            const uint4 h = *reinterpret_cast<const uint4*>(rp);
+            const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const int ks = sb * 4 + c;
+                const int s = ks % kStages;
+                int sc_lo, m_lo, sc_hi, m_hi;
+                q4k_scale_min(h.y, h.z, h.w, 2 * c, sc_lo, m_lo);
+                q4k_scale_min(h.y, h.z, h.w, 2 * c + 1, sc_hi, m_hi);
+                const float a_lo = d * (float)sc_lo, b_lo = dmin * (float)m_lo;
+                const float a_hi = d * (float)sc_hi, b_hi = dmin * (float)m_hi;
+                const uint4 q0 = *reinterpret_cast<const uint4*>(rp + 16 + 32 * c);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(rp + 32 + 32 * c);
+                const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
+                uint8_t* arow = sA + (size_t)s * kABytes + (size_t)t * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    // chunk j: k = 8j..8j+7 (low nibbles, sub-block 2c);
+                    // chunk j+4: k = 32+8j..32+8j+7 (high nibbles, sub-block 2c+1)
+                    uint32_t lo[4], hi[4];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t w = qw[2 * j + half];
+                        float fl[4], fh[4];
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const uint32_t byte = (w >> (8 * b)) & 0xFFu;
+                            fl[b] = fmaf(a_lo, __uint_as_float(0x4B000000u | (byte & 15u)) - 8388608.0f, -b_lo);
+                            fh[b] = fmaf(a_hi, __uint_as_float(0x4B000000u | (byte >> 4)) - 8388608.0f, -b_hi);
+                        }
+                        lo[2 * half] = pack_bf16x2(fl[0], fl[1]);
+                        lo[2 * half + 1] = pack_bf16x2(fl[2], fl[3]);
+                        hi[2 * half] = pack_bf16x2(fh[0], fh[1]);
+                        hi[2 * half + 1] = pack_bf16x2(fh[2], fh[3]);
+                    }
+                    const int sw = t & 7;
+                    *reinterpret_cast<uint4*>(arow + ((j ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(arow + (((j + 4) ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&full_a[s]);
+            }
+            mbar_arrive(&empty_raw[r]);
+        }
+
+        // ------------------------------------------------------------ epilogue
+        mbar_wait(acc_full, 0, p.status);
+        tc_fence_after();
+        const int q = warp & 3;                  // TMEM lane quarter of this warp
+        const int row = row0 + 32 * q + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+        for (int col = 0; col < kTileTok; col += 16) {
+            float v[16];
+            tmem_ld16(taddr + (uint32_t)col, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int tok = tok0 + col + i;
+                if (tok < p.M) p.Y[(size_t)tok * p.rows + row] = v[i];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+int launch_prefill(int /*type*/, const void* W, int64_t rows, int64_t cols, const uint16_t* X, float* Y, int M,
+                   cudaStream_t stream) {
+    auto enc = encoder();
+    if (!enc) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled unavailable");
+    CUtensorMap wmap, xmap;
+    {
+        const int64_t rb = cols / 256 * 144;
+        cuuint64_t dims[2] = {(cuuint64_t)rb, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)rb};
+        cuuint32_t box[2] = {144, kTileRows};
+        cuuint32_t es[2] = {1, 1};
+        CUresult r = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(GGQ_ECUDA, "tensor map (W) failed (%d)", (int)r);
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+        cuuint32_t box[2] = {kKStage, kTileTok};
+        cuuint32_t es[2] = {1, 1};
+        CUresult r = enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box,
+                         es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(GGQ_ECUDA, "tensor map (X) failed (%d)", (int)r);
+    }
+    PrefillParams p = {};
+    p.Y = Y;
+    p.rows = (int)rows;
+    p.cols = (int)cols;
+    p.M = M;
+    p.tok_tiles = (M + kTileTok - 1) / kTileTok;
+    p.status = device_status_word();
+    if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
+
+    cudaError_t e = cudaFuncSetAttribute(prefill_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows / kTileRows) * p.tok_tiles));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prefill_q4k_kernel, wmap, xmap, p);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return GGQ_OK;
+}
+
+}  // namespace ggq

@@ -1,0 +1,206 @@
+/*
+ * ggq.h -- C ABI of the GB300 block-quantized dequantize + GEMV library.
+ *
+ * The library covers the hot path of GGUF local decode: read a GGUF v3 file,
+ * copy its tensor payloads to device memory unchanged, and multiply
+ * block-quantized weight matrices (Q8_0, Q4_K) by activation vectors with the
+ * blocks decoded in registers.  Conventions follow the kernel list of the
+ * culpeo.ws C++ engine blog ("none of these allocate, the memory for the output
+ * will always be provided by the caller"): every compute entry point writes into
+ * caller-provided device memory and enqueues its work on the caller's CUDA
+ * stream without synchronising it.
+ *
+ * Shapes: a weight matrix has `rows` output features and `cols` input features
+ * (GGUF ne0 = cols, stored fastest).  Row r is cols/32 consecutive 34-byte Q8_0
+ * blocks, or cols/256 consecutive 144-byte Q4_K super-blocks.
+ *
+ * Return codes: 0 on success, a negative GGQ_E* code on failure (no partial
+ * results are promised after a failure).  `ggq_strerror` names a code;
+ * `ggq_last_error` gives a message for the last failure in the calling thread.
+ *
+ * Streams are passed as `void*` holding a cudaStream_t (NULL = legacy default).
+ * Device pointers are plain `cudaMalloc`-style device addresses owned by the
+ * caller unless stated otherwise.
+ */
+#ifndef GGQ_H
+#define GGQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------- return codes */
+#define GGQ_OK 0
+#define GGQ_EINVAL (-1)    /* bad argument: NULL pointer, bad shape, M out of range, misaligned pointer */
+#define GGQ_ETYPE (-2)     /* tensor type not supported by this operation */
+#define GGQ_EIO (-3)       /* file could not be opened, mapped or read */
+#define GGQ_EFORMAT (-4)   /* malformed GGUF: magic, version, truncation, offset, size overflow */
+#define GGQ_ENOMEM (-5)    /* host or device allocation failed */
+#define GGQ_ECUDA (-6)     /* a CUDA runtime call or kernel launch failed */
+#define GGQ_ETIMEOUT (-7)  /* a kernel's bounded wait on its own copies ran out */
+#define GGQ_ENOTFOUND (-8) /* no tensor / metadata key with that name */
+
+/* ---------------------------------------------------- tensor type ids
+ * F32 = 0 ("GGUF: The File Format...", gguf_demo.py: "type F32=0") and
+ * Q8_0 = 8 ("GGUF Inferencer in R" section 2.1: "Tensor Data Type = 8 (Q8_0)")
+ * are on the pages; F16, Q4_0, Q4_K and Q6_K use the ggml ids of real files. */
+enum {
+    GGQ_F32 = 0,
+    GGQ_F16 = 1,
+    GGQ_Q4_0 = 2,
+    GGQ_Q8_0 = 8,
+    GGQ_Q4_K = 12,
+    GGQ_Q6_K = 14
+};
+
+/* GGUF metadata value types (GGUF v3): 4 = uint32, 8 = string, 9 = array are on
+ * the pages; the others complete the v3 table. */
+enum {
+    GGQ_KV_U8 = 0, GGQ_KV_I8 = 1, GGQ_KV_U16 = 2, GGQ_KV_I16 = 3, GGQ_KV_U32 = 4,
+    GGQ_KV_I32 = 5, GGQ_KV_F32 = 6, GGQ_KV_BOOL = 7, GGQ_KV_STRING = 8,
+    GGQ_KV_ARRAY = 9, GGQ_KV_U64 = 10, GGQ_KV_I64 = 11, GGQ_KV_F64 = 12
+};
+
+/* ------------------------------------------------------------- loading */
+
+typedef struct ggq_model ggq_model;
+
+typedef struct {
+    const char* name;  /* NUL-terminated; owned by the model */
+    int32_t type;      /* GGQ_F32, GGQ_Q8_0, ... */
+    int32_t n_dims;    /* 1..4 */
+    int64_t ne[4];     /* extents, fastest first: ne[0] = cols; unused dims = 1 */
+    uint64_t offset;   /* byte offset of the payload in the file's data blob */
+    uint64_t nbytes;   /* payload size in bytes */
+    const void* data;  /* device address of the payload (256-byte aligned), or NULL
+                          for a model opened with GGQ_LOAD_METADATA_ONLY */
+} ggq_tensor;
+
+/* ggq_load_ex flags */
+#define GGQ_LOAD_METADATA_ONLY 1u /* parse and validate; allocate no device memory */
+
+/*
+ * ggq_load -- read a GGUF v3 file and copy every tensor payload to the current
+ * CUDA device, unchanged.
+ *
+ * The file is walked as "GGUF Inferencer in R" section 2.1 and "GGUF: The File
+ * Format..." ("What is stored inside a GGUF file") lay it out: magic "GGUF",
+ * uint32 version (3), uint64 tensor count, uint64 metadata count; typed
+ * key/value entries (strings are uint64 length + bytes; unknown keys are
+ * stepped over by their type); the tensor-info table (name, uint32 n_dims,
+ * n_dims x uint64 extents, uint32 type, uint64 offset); padding to the next
+ * multiple of 32; the data blob.  Offsets must be multiples of 32 and every
+ * payload must lie inside the file.
+ *
+ * On success *out owns one device allocation holding all payloads (each at a
+ * 256-byte-aligned address) plus host copies of names and metadata; release it
+ * with ggq_free.  Errors: GGQ_EINVAL (NULL argument), GGQ_EIO, GGQ_EFORMAT,
+ * GGQ_ETYPE (a tensor type whose payload size is unknown), GGQ_ENOMEM,
+ * GGQ_ECUDA.  The copy is synchronous (the function returns after the data is
+ * on the device).
+ */
+int ggq_load(const char* path, ggq_model** out);
+int ggq_load_ex(const char* path, unsigned flags, ggq_model** out);
+
+/* Same from a host buffer holding the file's bytes (not retained after return). */
+int ggq_load_memory(const void* buf, size_t len, unsigned flags, ggq_model** out);
+
+void ggq_free(ggq_model* model);
+
+int ggq_version_of(const ggq_model* model, uint32_t* version);
+int ggq_data_start(const ggq_model* model, uint64_t* offset);   /* file offset of the blob */
+int ggq_num_tensors(const ggq_model* model, int64_t* n);
+int ggq_tensor_info(const ggq_model* model, int64_t i, ggq_tensor* out);
+int ggq_find_tensor(const ggq_model* model, const char* name, int64_t* i); /* GGQ_ENOTFOUND */
+
+/*
+ * Metadata access.  For scalar types *value points to the little-endian value
+ * (value_bytes = its size); for strings to the bytes (not NUL-terminated;
+ * value_bytes = length); for arrays to the raw encoded array starting at its
+ * uint32 element type (value_bytes = encoded size).  Pointers stay valid until
+ * ggq_free.
+ */
+int ggq_num_kv(const ggq_model* model, int64_t* n);
+int ggq_kv_info(const ggq_model* model, int64_t i, const char** key, int32_t* vtype,
+                const void** value, uint64_t* value_bytes);
+int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENOTFOUND */
+
+/* ------------------------------------------------------------- compute */
+
+/*
+ * ggq_gemv -- y = W x for M activation rows, with W block-quantized.
+ *
+ *   y[m*rows + r] = sum_c w[r, c] * x[m*cols + c],   m < M, r < rows
+ *
+ * This is the matvec of the culpeo.ws kernel list (matvec(w:[r,c], x:[c]) -> [r])
+ * and of "GGUF Inferencer in R" section 5.2 (Q = NormIn %*% t(W)), with the
+ * weights decoded on the fly: Q8_0 w = d*q ("GGUF: The File Format...", "How
+ * a Q8_0 block is stored"), Q4_K w = d*sc_j*q - dmin*m_j (the k-quant paragraph
+ * of the same section; byte layout: fp16 d, fp16 dmin, 12 bytes of packed
+ * 6-bit scales/mins, 128 bytes of nibbles).  Decoded weights are never written
+ * to memory; products accumulate in fp32 (any order).
+ *
+ *   type   GGQ_Q8_0 (cols % 32 == 0) or GGQ_Q4_K (cols % 256 == 0)
+ *   W      device, rows x row-bytes, row-major, 16-byte aligned
+ *   x      device, fp32 [M, cols] row-major, 16-byte aligned
+ *   y      device, fp32 [M, rows] row-major, 4-byte aligned; fully overwritten
+ *   M      1..16 (M > 1 is the small-batch variant: each decoded block is used
+ *          for all M rows of x)
+ *   stream cudaStream_t
+ *
+ * Finite inputs with |x| < 2^70 are supported.  Errors: GGQ_EINVAL (NULL
+ * pointer, rows < 1, cols not a multiple of the block, M outside 1..16, W not
+ * 16-byte aligned, x not 16-byte or y not 4-byte aligned), GGQ_ETYPE, GGQ_ECUDA (launch
+ * failure).  Asynchronous: returns after the launch.
+ */
+int ggq_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x,
+             float* y, int M, void* stream);
+
+/*
+ * ggq_gemm_prefill -- Y = X W^T for a whole prompt (M activation rows),
+ * "GGUF Inferencer in R" section 4 (prefill runs the prompt "at once with big
+ * matrix multiplications").  Q4_K weight tiles are decoded to bf16 in shared
+ * memory and multiplied on the tcgen05 tensor cores with fp32 accumulation.
+ *
+ *   type   GGQ_Q4_K (cols % 256 == 0)
+ *   W      device, rows x (cols/256*144) bytes, 16-byte aligned; rows % 128 == 0
+ *   X      device, bf16 bit patterns [M, cols] row-major, 16-byte aligned
+ *   Y      device, fp32 [M, rows] row-major; fully overwritten
+ *   M      multiple of 128, 128..65536
+ *
+ * Errors: GGQ_EINVAL, GGQ_ETYPE, GGQ_ECUDA.  The kernel's waits on its own
+ * copies are bounded; if one runs out the kernel records it and
+ * ggq_device_status reports GGQ_ETIMEOUT.  Asynchronous.
+ */
+int ggq_gemm_prefill(int type, const void* W, int64_t rows, int64_t cols,
+                     const uint16_t* X, float* Y, int M, void* stream);
+
+/*
+ * ggq_dequantize -- out[r*cols + c] = w[r, c] as fp32 (test and inspection
+ * aid; the GEMV path never writes decoded weights).  Types GGQ_Q8_0, GGQ_Q4_K.
+ * W 16-byte aligned, out 4-byte aligned.  Asynchronous.
+ */
+int ggq_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out,
+                   void* stream);
+
+/*
+ * ggq_device_status -- synchronise the current device, then return GGQ_ETIMEOUT
+ * if any kernel of this library recorded a bounded-wait timeout since the last
+ * call (and clear the record), GGQ_ECUDA if the device reports an error, else
+ * GGQ_OK.
+ */
+int ggq_device_status(void);
+
+/* --------------------------------------------------------------- misc */
+const char* ggq_strerror(int code);
+const char* ggq_last_error(void);   /* thread-local message of the last failure */
+int ggq_abi_version(void);          /* 1 */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GGQ_H */

@@ -1,0 +1,176 @@
+"""C-ABI library: loads, exports every declared symbol, and its host logic
+(GGUF parsing/validation, argument checks) behaves -- no GPU needed."""
+import ctypes
+import os
+import random
+import re
+import struct
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ggq.h")
+
+
+@pytest.fixture(scope="module")
+def ggq():
+    import gguf_block_quantized_q8_gb300 as g
+    return g
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ggq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(ggq):
+    names = _declared_functions()
+    assert len(names) >= 18
+    lib = ctypes.CDLL(ggq.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert ggq.lib.ggq_abi_version() == 1
+    assert ggq.strerror(-4) == "malformed GGUF file"
+
+
+def _tiny():
+    """tiny.gguf of the lesson, via the synthetic writer."""
+    head, offsets, end = synth.gguf_header(
+        [("general.architecture", 8, "llama"), ("general.name", 8, "tiny-demo"),
+         ("llama.context_length", 4, 4096)], [("blk.0.ffn_up.weight", [4, 2], 0)])
+    return head + np.arange(8, dtype=np.float32).tobytes()
+
+
+def test_metadata_only_load_of_tiny_gguf(ggq):
+    with ggq.Model.from_bytes(_tiny(), metadata_only=True) as m:
+        assert m.version == 3 and m.data_start == 224 and len(m) == 1
+        t = m.tensor(0)
+        assert t["name"] == "blk.0.ffn_up.weight" and t["ne"] == [4, 2] and t["type"] == 0
+        assert t["nbytes"] == 32 and t["offset"] == 0 and t["data"] == 0
+        kv = m.kvs()
+        assert kv[0] == ("general.architecture", 8, b"llama")
+        assert kv[2] == ("llama.context_length", 4, struct.pack("<I", 4096))
+        assert m.find("blk.0.ffn_up.weight")["ne"] == [4, 2]
+        with pytest.raises(ggq.GGQError) as e:
+            m.find("nope")
+        assert e.value.code == -8
+
+
+def _mixed_file():
+    kvs = [("general.architecture", 8, "llama"),
+           ("general.languages", 9, (8, ["en", "fr"])),
+           ("x.nested", 9, (9, [(4, [1, 2]), (6, [1.5])])),
+           ("x.f64", 12, 2.5), ("x.bool", 7, True), ("x.i64", 11, -3), ("x.u8", 0, 7)]
+    q8 = synth.weight_rows(synth.TYPE_Q8_0, 1, 3, 64)
+    q4 = synth.weight_rows(synth.TYPE_Q4_K, 2, 2, 512)
+    tensors = [("a.weight", [64, 3], 8), ("norm", [64], 0), ("b.weight", [512, 2], 12)]
+    head, offs, end = synth.gguf_header(kvs, tensors)
+    payloads = [q8.tobytes(), np.ones(64, np.float32).tobytes(), q4.tobytes()]
+    blob = bytearray(end)
+    for o, p in zip(offs, payloads):
+        blob[o:o + len(p)] = p
+    return head + bytes(blob), head, offs
+
+
+def test_metadata_only_load_of_mixed_file(ggq):
+    buf, head, offs = _mixed_file()
+    with ggq.Model.from_bytes(buf, metadata_only=True) as m:
+        ts = m.tensors()
+        assert [t["offset"] for t in ts] == offs
+        assert [t["nbytes"] for t in ts] == [3 * 68, 256, 2 * 288]
+        assert m.data_start == len(head)
+        keys = [k for k, _, _ in m.kvs()]
+        assert keys[-1] == "x.u8" and len(keys) == 7
+
+
+def test_loader_rejects_malformed(ggq):
+    good, head, _ = _mixed_file()
+    cases = {
+        "magic": b"GGUX" + good[4:],
+        "version": good[:4] + struct.pack("<I", 2) + good[8:],
+        "truncated_header": good[:20],
+        "truncated_payload": good[:-10],
+        "huge_tensor_count": good[:8] + struct.pack("<Q", 1 << 60) + good[16:],
+        "huge_kv_count": good[:16] + struct.pack("<Q", 1 << 60) + good[24:],
+    }
+    for name, buf in cases.items():
+        with pytest.raises(ggq.GGQError) as e:
+            ggq.Model.from_bytes(buf, metadata_only=True)
+        assert e.value.code == -4, name
+    with pytest.raises(ggq.GGQError) as e:
+        ggq.Model.load("/nonexistent/file.gguf", metadata_only=True)
+    assert e.value.code == -3
+
+
+def test_loader_rejects_bad_tensor_fields(ggq):
+    def one(ne, qtype, off):
+        out = b"GGUF" + struct.pack("<IQQ", 3, 1, 0)
+        out += synth.gguf_string("t") + struct.pack("<I", len(ne)) + struct.pack(f"<{len(ne)}Q", *ne)
+        out += struct.pack("<IQ", qtype, off)
+        out += b"\0" * (-len(out) % 32)
+        return out + b"\0" * 4096
+    assert ggq.Model.from_bytes(one([64, 2], 8, 0), metadata_only=True).tensor(0)["nbytes"] == 136
+    bad = {
+        "unaligned_offset": (one([64, 2], 8, 16), -4),
+        "past_end": (one([64, 2], 8, 4096), -4),
+        "ragged_q8_row": (one([48, 2], 8, 0), -4),
+        "ragged_q4k_row": (one([128, 2], 12, 0), -4),
+        "unknown_type": (one([64], 99, 0), -2),
+        "zero_dims": (one([], 0, 0), -4),
+        "overflowing_dims": (one([1 << 40, 1 << 40], 0, 0), -4),
+    }
+    for name, (buf, code) in bad.items():
+        with pytest.raises(ggq.GGQError) as e:
+            ggq.Model.from_bytes(buf, metadata_only=True)
+        assert e.value.code == code, name
+
+
+def test_loader_fuzz_never_crashes(ggq):
+    """Every truncation and random byte flips of a valid file: an error code or a
+    consistent model, never a crash."""
+    buf, _, _ = _mixed_file()
+    for n in range(0, len(buf), 7):
+        try:
+            ggq.Model.from_bytes(buf[:n], metadata_only=True).close()
+        except ggq.GGQError as e:
+            assert e.code in (-4, -2)
+    rnd = random.Random(3)
+    for _ in range(400):
+        b = bytearray(buf)
+        for _ in range(rnd.randint(1, 6)):
+            b[rnd.randrange(0, 200)] = rnd.randrange(256)
+        try:
+            with ggq.Model.from_bytes(bytes(b), metadata_only=True) as m:
+                for t in m.tensors():
+                    assert t["offset"] % 32 == 0
+                    assert m.data_start + t["offset"] + t["nbytes"] <= len(b)
+        except ggq.GGQError as e:
+            assert e.code in (-4, -2, -5)
+
+
+def test_compute_entry_points_validate_arguments(ggq):
+    """Argument errors are reported before any device work."""
+    g = ggq.ggq_gemv
+    assert g(ggq.Q8_0, 0, 4, 64, 16, 16, 1, 0) == -1                 # NULL W
+    assert g(ggq.Q8_0, 16, 4, 48, 16, 16, 1, 0) == -1                # ragged cols
+    assert g(ggq.Q4_K, 16, 4, 128, 16, 16, 1, 0) == -1
+    assert g(ggq.Q8_0, 16, 4, 64, 16, 16, 0, 0) == -1                # M = 0
+    assert g(ggq.Q8_0, 16, 4, 64, 16, 16, 17, 0) == -1               # M = 17
+    assert g(ggq.Q8_0, 8, 4, 64, 16, 16, 1, 0) == -1                 # W misaligned
+    assert g(ggq.Q8_0, 16, 0, 64, 16, 16, 1, 0) == -1                # rows = 0
+    assert g(ggq.Q8_0, 16, 4, 64, 8, 16, 1, 0) == -1                 # x misaligned
+    assert g(ggq.F32, 16, 4, 64, 16, 16, 1, 0) == -2                 # type
+    p = ggq.ggq_gemm_prefill
+    assert p(ggq.Q8_0, 16, 128, 256, 16, 16, 128, 0) == -2
+    assert p(ggq.Q4_K, 16, 100, 256, 16, 16, 128, 0) == -1           # rows % 128
+    assert p(ggq.Q4_K, 16, 128, 256, 16, 16, 100, 0) == -1           # M % 128
+    assert p(ggq.Q4_K, 16, 128, 256, 8, 16, 128, 0) == -1            # X misaligned
+    d = ggq.ggq_dequantize
+    assert d(ggq.Q4_K, 16, 2, 100, 16, 0) == -1
+    assert d(ggq.F16, 16, 2, 256, 16, 0) == -2
+    assert g(ggq.Q8_0, 16, 4, 64, 16, 16, 17, 0) == -1
+    assert "M 17 outside 1..16" in ggq.lib.ggq_last_error().decode()

@@ -1,0 +1,290 @@
+"""GPU parity: ggq_dequantize / ggq_gemv (through the C ABI) against the CPU oracle.
+
+Bar: decoded weights bit-exact; GEMV outputs within
+|y - y_ref| <= 1e-3 * sum_c |w[r,c] x[c]| + 1e-6  (y_ref in double);
+integer-valued and one-hot cases exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-3, 1e-6
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("-m gpu tests need a CUDA device")
+    import gguf_block_quantized_q8_gb300 as ggq
+    return torch, ggq
+
+
+def _dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def gpu_gemv(env, qtype, W, rows, cols, x, guard=64):
+    """Run ggq_gemv with guard cells around y; check they survive."""
+    torch, ggq = env
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, cols)
+    M = x.shape[0]
+    Wd, xd = _dev(torch, W), _dev(torch, x)
+    buf = torch.full((M * rows + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
+    y = buf[guard:guard + M * rows]
+    rc = ggq.ggq_gemv(qtype, Wd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr(), M,
+                      torch.cuda.current_stream().cuda_stream)
+    ggq.check(rc, "ggq_gemv")
+    torch.cuda.synchronize()
+    assert ggq.device_status() == 0
+    out = buf.cpu().numpy()
+    assert np.isnan(out[:guard]).all() and np.isnan(out[guard + M * rows:]).all(), "write outside y"
+    return out[guard:guard + M * rows].reshape(M, rows)
+
+
+def assert_close(y, y_ref, a_ref, what=""):
+    ok, worst = oracle.tolerance_ok(y, y_ref, a_ref, REL, ABS)
+    assert ok, f"{what}: worst error / bound = {worst:.3g}"
+    return worst
+
+
+def weights(qtype, rows, cols, stream=7):
+    return synth.weight_rows(qtype, stream, rows, cols)
+
+
+def xs(M, cols, stream=8):
+    return synth.normal_f32(M * cols, stream).reshape(M, cols)
+
+
+# ----------------------------------------------------------------- dequant ----
+
+@pytest.mark.parametrize("qtype,rows,cols", [(8, 1, 32), (8, 3, 96), (8, 17, 512), (8, 65, 2304),
+                                             (12, 1, 256), (12, 3, 512), (12, 40, 2304)])
+def test_dequantize_bit_exact(env, qtype, rows, cols):
+    torch, ggq = env
+    W = weights(qtype, rows, cols)
+    out = ggq.dequantize(qtype, _dev(torch, W), rows, cols)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    ref = oracle.dequantize(qtype, W, rows, cols)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequantize_special_scales(env):
+    """fp16 scales that are subnormal, the largest finite, inf and NaN."""
+    torch, ggq = env
+    from tests.pin_checks import Q8_PATTERN, q8_block, pack_q4_k
+    d_bits = [0x0001, 0x03FF, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0x8000]
+    W8 = b"".join(q8_block(d, Q8_PATTERN) for d in d_bits)
+    rng = np.random.default_rng(0)
+    W4 = b"".join(pack_q4_k(d, dm, list(rng.integers(0, 64, 8)), list(rng.integers(0, 64, 8)),
+                            list(rng.integers(0, 16, 256)))
+                  for d, dm in [(0x0001, 0x0002), (0x7BFF, 0x03FF), (0x7C00, 0x3C00), (0x3C00, 0x7E00)])
+    for qtype, W, cols in [(8, W8, 32), (12, W4, 256)]:
+        Wn = np.frombuffer(W, np.uint8).copy()
+        rows = Wn.size // oracle.row_bytes(qtype, cols)
+        got = ggq.dequantize(qtype, _dev(torch, Wn), rows, cols).cpu().numpy()
+        ref = oracle.dequantize(qtype, Wn, rows, cols)
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+# -------------------------------------------------------------------- GEMV ----
+
+SHAPES_Q8 = [(1, 32), (3, 96), (31, 256), (33, 512), (100, 2048), (257, 2304), (64, 4096 + 32)]
+SHAPES_Q4 = [(1, 256), (31, 512), (33, 2304), (100, 4096), (257, 11008)]
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES_Q8)
+def test_gemv_q8_0_m1(env, rows, cols):
+    W = weights(8, rows, cols)
+    x = xs(1, cols)
+    y_ref, a_ref = oracle.gemv(8, W, rows, cols, x)
+    assert_close(gpu_gemv(env, 8, W, rows, cols, x), y_ref, a_ref, f"q8_0 {rows}x{cols}")
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES_Q4)
+def test_gemv_q4_k_m1(env, rows, cols):
+    W = weights(12, rows, cols)
+    x = xs(1, cols)
+    y_ref, a_ref = oracle.gemv(12, W, rows, cols, x)
+    assert_close(gpu_gemv(env, 12, W, rows, cols, x), y_ref, a_ref, f"q4_k {rows}x{cols}")
+
+
+@pytest.mark.parametrize("qtype,rows,cols", [(8, 33, 512), (8, 70, 2304), (8, 9, 96), (12, 33, 512),
+                                             (12, 70, 2304)])
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 8, 9, 16])
+def test_gemv_small_m(env, qtype, rows, cols, M):
+    W = weights(qtype, rows, cols)
+    x = xs(M, cols)
+    y_ref, a_ref = oracle.gemv(qtype, W, rows, cols, x)
+    y = gpu_gemv(env, qtype, W, rows, cols, x)
+    assert_close(y, y_ref, a_ref, f"type {qtype} M={M}")
+    # the last activation row alone (M = 1 kernel) meets the same bar
+    y1 = gpu_gemv(env, qtype, W, rows, cols, x[M - 1:M])
+    assert_close(y1, y_ref[M - 1:M], a_ref[M - 1:M], f"type {qtype} row {M - 1} alone")
+
+
+def test_gemv_many_rounds(env):
+    """Columns wide enough that a CTA streams its slice in several rounds."""
+    for qtype, cols, M in [(12, 65536, 16), (8, 65536, 16), (12, 65536, 1)]:
+        rows = 40
+        W = weights(qtype, rows, cols, stream=21)
+        x = xs(M, cols, stream=22)
+        y_ref, a_ref = oracle.gemv(qtype, W, rows, cols, x)
+        assert_close(gpu_gemv(env, qtype, W, rows, cols, x), y_ref, a_ref, f"wide {qtype} M={M}")
+
+
+@pytest.mark.parametrize("qtype,cols", [(8, 512), (8, 96), (12, 512), (12, 2304)])
+def test_gemv_one_hot_extracts_exact_columns(env, qtype, cols):
+    rows = 37
+    W = weights(qtype, rows, cols, stream=3)
+    Wf = oracle.dequantize(qtype, W, rows, cols)
+    for c in [0, 1, cols // 2 + 3, cols - 1]:
+        x = np.zeros((1, cols), np.float32)
+        x[0, c] = 1.0
+        y = gpu_gemv(env, qtype, W, rows, cols, x)
+        assert np.array_equal(y[0].view(np.uint32), Wf[:, c].view(np.uint32)), c
+
+
+def test_gemv_integer_inputs_are_exact(env):
+    from tests.pin_checks import q8_block, pack_q4_k
+    rng = np.random.default_rng(5)
+    rows, cols = 45, 2048
+    q = rng.integers(-128, 128, size=(rows, cols))
+    W = np.frombuffer(b"".join(q8_block(0x3C00, list(q[r, 32 * b:32 * b + 32]))
+                               for r in range(rows) for b in range(cols // 32)), np.uint8).copy()
+    x = rng.integers(-8, 9, size=(3, cols)).astype(np.float32)
+    y = gpu_gemv(env, 8, W, rows, cols, x)
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ q.T)
+    sc = rng.integers(0, 8, size=(rows, cols // 256, 8))
+    mm = rng.integers(0, 8, size=(rows, cols // 256, 8))
+    qq = rng.integers(0, 16, size=(rows, cols))
+    W = np.frombuffer(b"".join(pack_q4_k(0x3C00, 0x3C00, list(sc[r, b]), list(mm[r, b]),
+                                         list(qq[r, 256 * b:256 * b + 256]))
+                               for r in range(rows) for b in range(cols // 256)), np.uint8).copy()
+    j = (np.arange(cols) % 256) // 32
+    bi = np.arange(cols) // 256
+    w = sc[:, bi, j] * qq - mm[:, bi, j]
+    x = rng.integers(-4, 5, size=(2, cols)).astype(np.float32)
+    y = gpu_gemv(env, 12, W, rows, cols, x)
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ w.T)
+
+
+def test_gemv_zero_weights_and_zero_x(env):
+    rows, cols = 33, 512
+    x = xs(2, cols)
+    for qtype in (8, 12):
+        W = np.zeros(rows * oracle.row_bytes(qtype, cols), np.uint8)
+        assert not gpu_gemv(env, qtype, W, rows, cols, x).any()
+        W = weights(qtype, rows, cols)
+        assert not gpu_gemv(env, qtype, W, rows, cols, np.zeros((1, cols), np.float32)).any()
+
+
+def test_gemv_on_a_side_stream(env):
+    torch, ggq = env
+    rows, cols = 300, 4096
+    W = weights(12, rows, cols, stream=30)
+    x = xs(1, cols, stream=31)
+    y_ref, a_ref = oracle.gemv(12, W, rows, cols, x)
+    s = torch.cuda.Stream()
+    Wd, xd = _dev(torch, W), _dev(torch, x)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        y = ggq.gemv(12, Wd, rows, cols, xd)
+    s.synchronize()
+    assert_close(y.cpu().numpy(), y_ref, a_ref, "side stream")
+
+
+# ----------------------------------------------------- the benchmark shapes ----
+
+def test_cfg1_q8_0_2048(env):
+    g = WL.CFG1[0]
+    W = synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)
+    x = synth.normal_f32(g.cols, g.x_stream).reshape(1, -1)
+    y_ref, a_ref = oracle.gemv(g.qtype, W, g.rows, g.cols, x)
+    assert_close(gpu_gemv(env, g.qtype, W, g.rows, g.cols, x), y_ref, a_ref, "cfg1")
+
+
+@pytest.mark.parametrize("g", WL.CFG2, ids=lambda g: g.name.split(".")[-2])
+def test_cfg2_smollm3_layer(env, g):
+    W = synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)
+    x = synth.normal_f32(g.cols, g.x_stream).reshape(1, -1)
+    y_ref, a_ref = oracle.gemv(g.qtype, W, g.rows, g.cols, x)
+    assert_close(gpu_gemv(env, g.qtype, W, g.rows, g.cols, x), y_ref, a_ref, g.name)
+
+
+@pytest.mark.parametrize("M", WL.CFG4_M)
+def test_cfg4_q8_0_small_batch(env, M):
+    g = WL.CFG4
+    W = synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)
+    x = synth.normal_f32(M * g.cols, g.x_stream).reshape(M, -1)
+    rows_s = np.r_[0:64, g.rows - 64:g.rows, np.arange(64, g.rows - 64, 97)]
+    y = gpu_gemv(env, g.qtype, W, g.rows, g.cols, x)
+    rb = oracle.row_bytes(g.qtype, g.cols)
+    Ws = np.concatenate([W[r * rb:(r + 1) * rb] for r in rows_s])
+    y_ref, a_ref = oracle.gemv(g.qtype, Ws, len(rows_s), g.cols, x)
+    assert_close(y[:, rows_s], y_ref, a_ref, f"cfg4 M={M}")
+
+
+def _distinct_shapes():
+    seen, out = set(), []
+    for g in WL.llama8b_pass(1):
+        key = (g.qtype, g.rows, g.cols)
+        if key not in seen:
+            seen.add(key)
+            out.append(g)
+    return out
+
+
+@pytest.mark.parametrize("g", _distinct_shapes(), ids=lambda g: g.name)
+def test_cfg3_llama8b_shapes_sampled(env, g):
+    """Full-size decode-pass tensors in the bench's launch configuration; rows
+    sampled for the oracle (regenerated alone from their counters)."""
+    W = synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)
+    x = synth.normal_f32(g.cols, g.x_stream).reshape(1, -1)
+    y = gpu_gemv(env, g.qtype, W, g.rows, g.cols, x)
+    rng = np.random.default_rng(1)
+    rows_s = np.unique(np.r_[0, 31, 32, g.rows - 1, rng.integers(0, g.rows, 96)])
+    for r in rows_s[:8]:
+        assert np.array_equal(synth.weight_rows(g.qtype, g.stream, 1, g.cols, row0=int(r)),
+                              W[r * oracle.row_bytes(g.qtype, g.cols):(r + 1) * oracle.row_bytes(g.qtype, g.cols)])
+    Ws = np.concatenate([synth.weight_rows(g.qtype, g.stream, 1, g.cols, row0=int(r)) for r in rows_s])
+    y_ref, a_ref = oracle.gemv(g.qtype, Ws, len(rows_s), g.cols, x)
+    assert_close(y[:, rows_s], y_ref, a_ref, g.name)
+
+
+# ---------------------------------------------------------------- loading ----
+
+def test_load_file_to_device_and_multiply(env, tmp_path):
+    torch, ggq = env
+    q8 = synth.weight_rows(8, 41, 70, 512)
+    q4 = synth.weight_rows(12, 42, 50, 2304)
+    norm = synth.normal_f32(512, 43)
+    kvs = [("general.architecture", 8, "llama"), ("llama.block_count", 4, 1)]
+    tensors = [("blk.0.attn_q.weight", [512, 70], 8), ("blk.0.attn_norm.weight", [512], 0),
+               ("blk.0.ffn_up.weight", [2304, 50], 12)]
+    path = str(tmp_path / "m.gguf")
+    synth.write_gguf(path, kvs, tensors, [q8.tobytes(), norm.tobytes(), q4.tobytes()])
+    with ggq.Model.load(path) as m:
+        t8, t4 = m.find("blk.0.attn_q.weight"), m.find("blk.0.ffn_up.weight")
+        assert t8["data"] % 256 == 0 and t4["data"] % 256 == 0
+        for t, W, rows, cols, qt in [(t8, q8, 70, 512, 8), (t4, q4, 50, 2304, 12)]:
+            out = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+            ggq.check(ggq.ggq_dequantize(qt, t["data"], rows, cols, out.data_ptr(),
+                                         torch.cuda.current_stream().cuda_stream), "dequantize")
+            got = out.cpu().numpy()
+            assert np.array_equal(got.view(np.uint32), oracle.dequantize(qt, W, rows, cols).view(np.uint32))
+            x = xs(1, cols, stream=44)
+            xd = _dev(torch, x)
+            y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+            ggq.check(ggq.ggq_gemv(qt, t["data"], rows, cols, xd.data_ptr(), y.data_ptr(), 1,
+                                   torch.cuda.current_stream().cuda_stream), "gemv")
+            y_ref, a_ref = oracle.gemv(qt, W, rows, cols, x)
+            assert_close(y.cpu().numpy(), y_ref, a_ref, t["name"])

@@ -47,6 +47,8 @@ def _bind(lib):
                          ctypes.POINTER(vp), ctypes.POINTER(u64)], ctypes.c_int),
         "ggq_kv_find": ([vp, ctypes.c_char_p, ctypes.POINTER(i64)], ctypes.c_int),
         "ggq_gemv": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
+        "ggq_gemv_multi": ([ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(i64), i64, vp,
+                            ctypes.POINTER(vp), ctypes.c_int, vp], ctypes.c_int),
         "ggq_gemm_prefill": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
         "ggq_dequantize": ([ctypes.c_int, vp, i64, i64, vp, vp], ctypes.c_int),
         "ggq_device_status": ([], ctypes.c_int),
@@ -88,6 +90,14 @@ def strerror(code: int) -> str:
 
 def ggq_gemv(qtype: int, W: int, rows: int, cols: int, x: int, y: int, M: int, stream: int) -> int:
     return lib.ggq_gemv(qtype, W, rows, cols, x, y, M, stream)
+
+
+def ggq_gemv_multi(qtype: int, Ws, rows, cols: int, x: int, ys, M: int, stream: int) -> int:
+    n = len(Ws)
+    Wa = (ctypes.c_void_p * n)(*Ws)
+    ra = (ctypes.c_int64 * n)(*rows)
+    ya = (ctypes.c_void_p * n)(*ys)
+    return lib.ggq_gemv_multi(qtype, n, Wa, ra, cols, x, ya, M, stream)
 
 
 def ggq_gemm_prefill(qtype: int, W: int, rows: int, cols: int, X: int, Y: int, M: int, stream: int) -> int:
@@ -204,6 +214,18 @@ def gemv(qtype: int, W, rows: int, cols: int, x, y=None, stream=None):
     check(ggq_gemv(qtype, W.data_ptr(), rows, cols, x2.data_ptr(), y.data_ptr(), M, _stream_ptr(stream)),
           "ggq_gemv")
     return y
+
+
+def gemv_multi(qtype: int, Ws, rows, cols: int, x, ys=None, stream=None):
+    """ys[i][M, rows[i]] = x[M, cols] @ W_i^T for matrices sharing x, one launch."""
+    import torch
+    x2 = x.reshape(-1, cols)
+    M = x2.shape[0]
+    if ys is None:
+        ys = [torch.empty((M, r), dtype=torch.float32, device=x.device) for r in rows]
+    check(ggq_gemv_multi(qtype, [w.data_ptr() for w in Ws], list(rows), cols, x2.data_ptr(),
+                         [y.data_ptr() for y in ys], M, _stream_ptr(stream)), "ggq_gemv_multi")
+    return ys
 
 
 def gemm_prefill(qtype: int, W, rows: int, cols: int, X_bf16, Y=None, stream=None):

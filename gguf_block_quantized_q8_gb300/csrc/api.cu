@@ -84,6 +84,32 @@ extern "C" int ggq_gemv(int type, const void* W, int64_t rows, int64_t cols, con
     return launch_gemv(type, W, rows, cols, x, y, M, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int ggq_gemv_multi(int type, int n, const void* const* W, const int64_t* rows, int64_t cols,
+                              const float* x, float* const* y, int M, void* stream) {
+    clear_error();
+    if (type != GGQ_Q8_0 && type != GGQ_Q4_K) return fail(GGQ_ETYPE, "ggq_gemv_multi: type %d not supported", type);
+    if (n < 1 || n > 4) return fail(GGQ_EINVAL, "ggq_gemv_multi: n %d outside 1..4", n);
+    if (!W || !rows || !y || !x) return fail(GGQ_EINVAL, "ggq_gemv_multi: NULL pointer");
+    const int64_t blk = type == GGQ_Q4_K ? 256 : 32;
+    if (cols < blk || cols % blk) return fail(GGQ_EINVAL, "ggq_gemv_multi: cols %lld not a positive multiple of %lld",
+                                              (long long)cols, (long long)blk);
+    if (M < 1 || M > 16) return fail(GGQ_EINVAL, "ggq_gemv_multi: M %d outside 1..16", M);
+    if (!aligned(x, 16)) return fail(GGQ_EINVAL, "ggq_gemv_multi: x not 16-byte aligned");
+    for (int i = 0; i < n; ++i) {
+        if (!W[i] || !y[i]) return fail(GGQ_EINVAL, "ggq_gemv_multi: NULL pointer");
+        if (rows[i] < 1 || rows[i] > 0x7fffffff) return fail(GGQ_EINVAL, "ggq_gemv_multi: rows out of range");
+        if (!aligned(W[i], 16)) return fail(GGQ_EINVAL, "ggq_gemv_multi: W not 16-byte aligned");
+        if (!aligned(y[i], 4)) return fail(GGQ_EINVAL, "ggq_gemv_multi: y not 4-byte aligned");
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (stream_gemv_supported(type, cols, M, n, rows)) return launch_gemv_stream(type, n, W, rows, cols, x, y, M, s);
+    for (int i = 0; i < n; ++i) {
+        int rc = launch_gemv(type, W[i], rows[i], cols, x, y[i], M, s);
+        if (rc) return rc;
+    }
+    return GGQ_OK;
+}
+
 extern "C" int ggq_gemm_prefill(int type, const void* W, int64_t rows, int64_t cols, const uint16_t* X, float* Y,
                                 int M, void* stream) {
     clear_error();

@@ -34,6 +34,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "gemv_tile.cuh"
 #include "ggq_internal.h"
 #include "ptx.cuh"
 
@@ -55,8 +56,6 @@ constexpr int kQ8RowBytes = 272;
 constexpr int kQ8Tile = kRows * kQ8RowBytes;     // 8704
 constexpr int kQ8Xp = 272;                       // x' floats per unit (indexed by byte)
 
-constexpr float kTwo96 = pow2f(96);              // P = 2^-96 * sum(q x)
-
 struct GemvParams {
     const float* x;
     float* y;
@@ -68,12 +67,6 @@ struct GemvParams {
     int rbuf;       // unit buffers per CTA (units processed per round)
     int* status;
 };
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 struct Smem {
     uint8_t* tiles;
@@ -176,87 +169,34 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const __grid_constan
         }
         mbar_wait(s.xbar, round & 1, p.status);
 
-        // x' = x * 2^(53 - p) in place (p = bit position of the weight's nibble in
-        // its 32-bit word: 0/8/16 low nibbles, +4 high, byte 3 shifted down to 16),
-        // and the sums of x per 32-weight sub-block for the min term
-        const int per_m = n * 256;
-        for (int base = warp * 32; base < p.M * per_m; base += kThreads) {
-            const int m = base / per_m;
-            const int kk = base - m * per_m + lane;
-            const int u = kk >> 8, kw = kk & 255;
-            float* px = s.xp + (size_t)(m * p.rbuf + u) * kQ4kXp + kw;
-            const float v = *px;
-            const int hi = (kw >> 5) & 1, b = kw & 3;
-            const float f = hi ? (b == 0 ? pow2f(49) : b == 1 ? pow2f(41) : pow2f(33))
-                               : (b == 0 ? pow2f(53) : b == 1 ? pow2f(45) : pow2f(37));
-            *px = v * f;
-            const float sum = warp_sum(v);
-            if (lane == 0) s.sums[(m * p.rbuf + u) * 8 + (kw >> 5)] = sum;
+        // x' = x * 2^(53 - p) (p = bit position of the weight's nibble in its
+        // 32-bit word, see gemv_tile.cuh) and the sums of x per 32-weight
+        // sub-block for the min term; one warp per unit reads the 256 floats in
+        // natural order and writes them back in q4k_xslot order
+        for (int job = warp; job < p.M * n; job += kWarps) {
+            const int m = job / n, u = job - m * n;
+            float* blk = s.xp + (size_t)(m * p.rbuf + u) * kQ4kXp;
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = blk[32 * i + lane];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float sum = warp_sum(v[i]);
+                if (lane == 0) s.sums[(m * p.rbuf + u) * 8 + i] = sum;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = 32 * i + lane;
+                blk[q4k_xslot(k)] = v[i] * q4k_xscale(k);
+            }
         }
         __syncthreads();
 
         for (int u = warp; u < n; u += kWarps) {
             mbar_wait(&s.bars[u], round & 1, p.status);
-            const uint8_t* rp = s.tiles + (size_t)u * kQ4kTile + lane * kQ4kRowBytes;
-            const uint4 h = *reinterpret_cast<const uint4*>(rp);
-            const float d96 = half_bits_to_float(h.x) * kTwo96;
-            const float dmin = half_bits_to_float(h.x >> 16);
-            const uint32_t sc03 = h.y & 0x3F3F3F3Fu, m03 = h.z & 0x3F3F3F3Fu;
-            const uint32_t sc47 = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
-            const uint32_t m47 = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-            const float* xu = s.xp + (size_t)u * kQ4kXp;
-            const float* su = s.sums + u * 8;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float plo[MMAX], phi[MMAX];
-#pragma unroll
-                for (int m = 0; m < MMAX; ++m) plo[m] = phi[m] = 0.0f;
-#pragma unroll
-                for (int ii = 0; ii < 2; ++ii) {
-                    const int i = 2 * c + ii;
-                    const uint4 q = *reinterpret_cast<const uint4*>(rp + 16 + 16 * i);
-                    const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t w = wq[t], w8 = w >> 8;
-                        const float l0 = __uint_as_float(w & 0x0000000Fu);
-                        const float l1 = __uint_as_float(w & 0x00000F00u);
-                        const float l2 = __uint_as_float(w & 0x000F0000u);
-                        const float l3 = __uint_as_float(w8 & 0x000F0000u);
-                        const float h0 = __uint_as_float(w & 0x000000F0u);
-                        const float h1 = __uint_as_float(w & 0x0000F000u);
-                        const float h2 = __uint_as_float(w & 0x00F00000u);
-                        const float h3 = __uint_as_float(w8 & 0x00F00000u);
-#pragma unroll
-                        for (int m = 0; m < MMAX; ++m) {
-                            // weights 64c + 16ii + 4t + (0..3) and the same + 32
-                            const float* xm = xu + (size_t)m * p.rbuf * kQ4kXp + 64 * c + 16 * ii + 4 * t;
-                            const float4 a = *reinterpret_cast<const float4*>(xm);
-                            const float4 b = *reinterpret_cast<const float4*>(xm + 32);
-                            plo[m] = fmaf(l0, a.x, plo[m]);
-                            plo[m] = fmaf(l1, a.y, plo[m]);
-                            plo[m] = fmaf(l2, a.z, plo[m]);
-                            plo[m] = fmaf(l3, a.w, plo[m]);
-                            phi[m] = fmaf(h0, b.x, phi[m]);
-                            phi[m] = fmaf(h1, b.y, phi[m]);
-                            phi[m] = fmaf(h2, b.z, phi[m]);
-                            phi[m] = fmaf(h3, b.w, phi[m]);
-                        }
-                    }
-                }
-                const uint32_t scw = c < 2 ? sc03 : sc47, mw = c < 2 ? m03 : m47;
-                const int jl = (2 * c) & 3, jh = (2 * c + 1) & 3;
-                const float a_lo = d96 * byte_to_float(scw, jl), a_hi = d96 * byte_to_float(scw, jh);
-                const float b_lo = dmin * byte_to_float(mw, jl), b_hi = dmin * byte_to_float(mw, jh);
-#pragma unroll
-                for (int m = 0; m < MMAX; ++m) {
-                    const float* sm = su + m * p.rbuf * 8;
-                    acc[m] = fmaf(a_lo, plo[m], acc[m]);
-                    acc[m] = fmaf(-b_lo, sm[2 * c], acc[m]);
-                    acc[m] = fmaf(a_hi, phi[m], acc[m]);
-                    acc[m] = fmaf(-b_hi, sm[2 * c + 1], acc[m]);
-                }
-            }
+            q4k_tile_row<MMAX>(s.tiles + (size_t)u * kQ4kTile + lane * kQ4kRowBytes, s.xp + (size_t)u * kQ4kXp,
+                               p.rbuf * kQ4kXp, s.sums + u * 8, p.rbuf * 8, acc);
         }
         __syncthreads();  // buffers are reused by the next round
     }
@@ -322,8 +262,7 @@ __global__ void __launch_bounds__(kThreads) gemv_q8_kernel(const __grid_constant
                 const float v = reg[16 + 32 * b + lane];
                 const float sum = warp_sum(v);   // also orders the reads before the writes
                 const int B = 34 * b + 2 + lane;
-                const int pos = B & 3;
-                reg[B] = v * (pos == 0 ? pow2f(53) : pos == 1 ? pow2f(45) : pow2f(37));
+                reg[B] = v * q8_xscale(B);
                 if (lane == 0) s.sums[(m * p.rbuf + u) * 8 + b] = 128.0f * sum;
                 __syncwarp();
             }
@@ -332,51 +271,8 @@ __global__ void __launch_bounds__(kThreads) gemv_q8_kernel(const __grid_constant
 
         for (int u = warp; u < n; u += kWarps) {
             mbar_wait(&s.bars[u], round & 1, p.status);
-            const uint8_t* rp = s.tiles + (size_t)u * kQ8Tile + lane * kQ8RowBytes;
-            const float* xu = s.xp + (size_t)u * kQ8Xp;
-            const float* su = s.sums + u * 8;
-            float pc[MMAX];
-            float dcur = 0.0f;
-#pragma unroll
-            for (int m = 0; m < MMAX; ++m) pc[m] = 0.0f;
-#pragma unroll
-            for (int ch = 0; ch < kQ8RowBytes / 16; ++ch) {
-                const uint4 q = *reinterpret_cast<const uint4*>(rp + 16 * ch);
-                const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int wi = ch * 4 + t;
-                    const uint32_t w = wq[t];
-                    float4 xv[MMAX];
-#pragma unroll
-                    for (int m = 0; m < MMAX; ++m)
-                        xv[m] = *reinterpret_cast<const float4*>(xu + (size_t)m * p.rbuf * kQ8Xp + 4 * wi);
-#pragma unroll
-                    for (int pos = 0; pos < 4; ++pos) {
-                        const int B = 4 * wi + pos;
-                        const int b = B / 34, o = B % 34;
-                        if (o == 0) {
-                            dcur = half_bits_to_float(w >> (8 * pos));
-                        } else if (o >= 2) {
-                            const uint32_t pat = pos < 3 ? ((w ^ 0x80808080u) & (0xFFu << (8 * pos)))
-                                                         : (((w >> 8) ^ 0x00800000u) & 0x00FF0000u);
-                            const float fw = __uint_as_float(pat);
-#pragma unroll
-                            for (int m = 0; m < MMAX; ++m) {
-                                const float xs = pos == 0 ? xv[m].x : pos == 1 ? xv[m].y : pos == 2 ? xv[m].z : xv[m].w;
-                                pc[m] = fmaf(fw, xs, pc[m]);
-                            }
-                            if (o == 33) {
-#pragma unroll
-                                for (int m = 0; m < MMAX; ++m) {
-                                    acc[m] = fmaf(dcur, fmaf(pc[m], kTwo96, -su[m * p.rbuf * 8 + b]), acc[m]);
-                                    pc[m] = 0.0f;
-                                }
-                            }
-                        }
-                    }
-                }
-            }
+            q8_tile_row<MMAX>(s.tiles + (size_t)u * kQ8Tile + lane * kQ8RowBytes, s.xp + (size_t)u * kQ8Xp,
+                              p.rbuf * kQ8Xp, s.sums + u * 8, p.rbuf * 8, acc);
         }
         __syncthreads();
     }
@@ -535,6 +431,11 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
         cfg.numAttrs = 1;
         cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_q8_simple_kernel, static_cast<const uint8_t*>(W), p);
         return e == cudaSuccess ? GGQ_OK : cuda_fail(e, "gemv launch");
+    }
+    if (stream_gemv_supported(type, cols, M, 1, &rows)) {
+        const void* Ws[1] = {W};
+        float* ys[1] = {y};
+        return launch_gemv_stream(type, 1, Ws, &rows, cols, x, ys, M, stream);
     }
     if (M <= 1) return launch_tma_gemv<1>(type, W, rows, cols, p, stream);
     if (M <= 2) return launch_tma_gemv<2>(type, W, rows, cols, p, stream);

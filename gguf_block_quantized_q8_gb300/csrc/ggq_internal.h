@@ -47,6 +47,10 @@ int payload_bytes(int32_t type, uint64_t ne0, uint64_t n, uint64_t* out);
 // kernel entry points (launchers live next to their kernels)
 int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x,
                 float* y, int M, cudaStream_t stream);
+// persistent stream-K GEMV over one or more matrices sharing x (M <= 4)
+bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_t* rows);
+int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* rows, int64_t cols,
+                       const float* x, float* const* y, int M, cudaStream_t stream);
 int launch_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out,
                       cudaStream_t stream);
 int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const uint16_t* X,

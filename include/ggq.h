@@ -155,9 +155,29 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  * pointer, rows < 1, cols not a multiple of the block, M outside 1..16, W not
  * 16-byte aligned, x not 16-byte or y not 4-byte aligned), GGQ_ETYPE, GGQ_ECUDA (launch
  * failure).  Asynchronous: returns after the launch.
+ *
+ * For M <= 4 the kernel finishes rows whose columns were split between warps
+ * through a small per-stream workspace that the library allocates on the first
+ * call on each (device, stream) pair; make that first call before capturing the
+ * stream into a CUDA graph.  Calls on one stream run in stream order; a graph
+ * replay must not overlap other work of the stream it was captured from.
  */
 int ggq_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x,
              float* y, int M, void* stream);
+
+/*
+ * ggq_gemv_multi -- ggq_gemv for n weight matrices of the same type and width
+ * that share the activations x (the q, k and v projections of a layer, or its
+ * gate and up projections), in one launch:
+ *
+ *   y[i][m*rows[i] + r] = sum_c w_i[r, c] * x[m*cols + c],   i < n
+ *
+ * W[i], rows[i], y[i] as for ggq_gemv; n in 1..4.  The work of all n matrices
+ * is spread evenly over the GPU as one stream of tiles.  Same errors as
+ * ggq_gemv.  Asynchronous.
+ */
+int ggq_gemv_multi(int type, int n, const void* const* W, const int64_t* rows, int64_t cols,
+                   const float* x, float* const* y, int M, void* stream);
 
 /*
  * ggq_gemm_prefill -- Y = X W^T for a whole prompt (M activation rows),

@@ -288,3 +288,43 @@ def test_load_file_to_device_and_multiply(env, tmp_path):
                                    torch.cuda.current_stream().cuda_stream), "gemv")
             y_ref, a_ref = oracle.gemv(qt, W, rows, cols, x)
             assert_close(y.cpu().numpy(), y_ref, a_ref, t["name"])
+
+
+@pytest.mark.parametrize("qtype,rows,cols,M", [(12, 33, 4096, 1), (8, 100, 2048, 1), (12, 1000, 11008, 2),
+                                               (8, 4000, 4096, 4)])
+def test_gemv_repeated_calls_are_bit_identical(env, qtype, rows, cols, M):
+    """Row blocks split between warps are finished through a workspace whose
+    counters must be back at zero after every launch: repeated calls agree bit
+    for bit."""
+    torch, ggq = env
+    W = weights(qtype, rows, cols, stream=50)
+    x = xs(M, cols, stream=51)
+    y_ref, a_ref = oracle.gemv(qtype, W, rows, cols, x)
+    Wd, xd = _dev(torch, W), _dev(torch, x)
+    outs = [ggq.gemv(qtype, Wd, rows, cols, xd).cpu().numpy() for _ in range(4)]
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+    assert_close(outs[0], y_ref, a_ref, "repeat")
+    assert ggq.device_status() == 0
+
+
+def test_gemv_in_cuda_graph(env):
+    torch, ggq = env
+    rows, cols = 2000, 4096
+    W = weights(12, rows, cols, stream=52)
+    x = xs(1, cols, stream=53)
+    y_ref, a_ref = oracle.gemv(12, W, rows, cols, x)
+    Wd, xd = _dev(torch, W), _dev(torch, x)
+    y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ggq.gemv(12, Wd, rows, cols, xd, y)       # first call on this stream sets up its workspace
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ggq.gemv(12, Wd, rows, cols, xd, y)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(y.cpu().numpy(), y_ref, a_ref, "graph replay")

@@ -49,6 +49,7 @@ def _bind(lib):
         "ggq_gemv": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
         "ggq_gemv_multi": ([ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(i64), i64, vp,
                             ctypes.POINTER(vp), ctypes.c_int, vp], ctypes.c_int),
+        "ggq_gemv_noalloc": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
         "ggq_gemm_prefill": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
         "ggq_dequantize": ([ctypes.c_int, vp, i64, i64, vp, vp], ctypes.c_int),
         "ggq_device_status": ([], ctypes.c_int),
@@ -90,6 +91,10 @@ def strerror(code: int) -> str:
 
 def ggq_gemv(qtype: int, W: int, rows: int, cols: int, x: int, y: int, M: int, stream: int) -> int:
     return lib.ggq_gemv(qtype, W, rows, cols, x, y, M, stream)
+
+
+def ggq_gemv_noalloc(qtype: int, W: int, rows: int, cols: int, x: int, y: int, M: int, stream: int) -> int:
+    return lib.ggq_gemv_noalloc(qtype, W, rows, cols, x, y, M, stream)
 
 
 def ggq_gemv_multi(qtype: int, Ws, rows, cols: int, x: int, ys, M: int, stream: int) -> int:

@@ -560,4 +560,69 @@ int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* 
     return launch_stream_t<false, 4, 1, 8, 1>(maps, p, grid, stream);
 }
 
+// Same launch with caller-provided scratch instead of the per-stream workspace:
+// `partials` holds max_groups * 2 * kMaxM * 32 floats and `counters`
+// max_row_blocks ints.  The counters this call uses are cleared first
+// (cudaMemsetAsync on `stream`); nothing is allocated.
+int launch_gemv_stream_scratch(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
+                               cudaStream_t stream, float* partials, int max_groups, int* counters,
+                               int max_row_blocks) {
+    const bool q4k = type == GGQ_Q4_K;
+    const int mmax = M <= 1 ? 1 : M <= 2 ? 2 : 4;
+    const int64_t units = cols / 256;
+    const int64_t row_bytes = q4k ? units * 144 : units * 272;
+    const int trows = kRows * rows_per_lane(q4k, mmax);
+    const int64_t rb = (rows + trows - 1) / trows;
+    if (rb > max_row_blocks)
+        return fail(GGQ_EINVAL, "rows %lld exceed the %lld rows the built-in scratch can finish",
+                    (long long)rows, (long long)max_row_blocks * trows);
+    Maps maps;
+    StreamParams p = {};
+    p.x = x;
+    p.cols = cols;
+    p.M = M;
+    p.units = (int)units;
+    p.nseg = 1;
+    int rc = encode_map(&maps.m[0], W, rows, row_bytes, q4k, trows);
+    if (rc) return rc;
+    p.seg[0].y = y;
+    p.seg[0].rows = (int)rows;
+    p.seg[0].rb0 = 0;
+    p.rb_total = (int)rb;
+    p.tiles = rb * units;
+    const Shape sh = stream_shape(q4k, mmax);
+    int ring = 8;
+    while (ring > 1 && stream_smem(q4k, mmax, ring, cols) > kSmemLimit) --ring;
+    if (stream_smem(q4k, mmax, ring, cols) > kSmemLimit) return fail(GGQ_EINVAL, "shape needs too much shared memory");
+    p.ring = ring;
+    const int ng = sh.warps / sh.group;
+    const int64_t most = std::min<int64_t>((int64_t)num_sms() * ng, max_groups);
+    p.ngroups = (int)std::max<int64_t>(1, std::min<int64_t>(most, p.tiles));
+    const int grid = (int)std::min<int64_t>(num_sms(), p.ngroups);
+    p.partials = partials;
+    p.counters = counters;
+    p.status = device_status_word();
+    if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
+    cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)rb * sizeof(int), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
+    if (q4k) {
+        if (mmax == 1) {
+            if (sh.group == 4) {
+                if (sh.rows == 2) return sh.warps == 16 ? launch_stream_t<true, 1, 2, 16, 4>(maps, p, grid, stream)
+                                                        : launch_stream_t<true, 1, 2, 8, 4>(maps, p, grid, stream);
+                return sh.warps == 16 ? launch_stream_t<true, 1, 1, 16, 4>(maps, p, grid, stream)
+                                      : launch_stream_t<true, 1, 1, 8, 4>(maps, p, grid, stream);
+            }
+            if (sh.rows == 2) return launch_stream_t<true, 1, 2, 8, 1>(maps, p, grid, stream);
+            return launch_stream_t<true, 1, 1, 8, 1>(maps, p, grid, stream);
+        }
+        if (mmax == 2) return launch_stream_t<true, 2, 1, 16, 4>(maps, p, grid, stream);
+        return launch_stream_t<true, 4, 1, 16, 4>(maps, p, grid, stream);
+    }
+    if (mmax == 1) return sh.warps == 16 ? launch_stream_t<false, 1, 1, 16, 1>(maps, p, grid, stream)
+                                         : launch_stream_t<false, 1, 1, 8, 1>(maps, p, grid, stream);
+    if (mmax == 2) return launch_stream_t<false, 2, 1, 8, 1>(maps, p, grid, stream);
+    return launch_stream_t<false, 4, 1, 8, 1>(maps, p, grid, stream);
+}
+
 }  // namespace ggq

@@ -180,6 +180,34 @@ int ggq_gemv_multi(int type, int n, const void* const* W, const int64_t* rows, i
                    const float* x, float* const* y, int M, void* stream);
 
 /*
+ * ggq_gemv_noalloc -- ggq_gemv that allocates nothing.  (No counterpart on the
+ * pages: it exists for callers that may not allocate device memory.)
+ *
+ * ggq_gemv allocates a small per-stream workspace on its first call on a
+ * stream.  Callers that cannot allow any device allocation at call time -- a
+ * server that hands all device memory to its own pool at start-up and treats
+ * a later cudaMalloc as a failure, or a latency-critical loop in which
+ * cudaMalloc / cudaFree (which may synchronise the device) must never run --
+ * use this entry point instead.  It runs the same kernel with its scratch in
+ * one fixed array of device memory inside the library (about 2.2 MB on every
+ * device that loads the library, held until the process exits).  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments and result as for ggq_gemv, within these limits: type GGQ_Q8_0 or
+ * GGQ_Q4_K, cols a multiple of 256, M in 1..4, at most 32768 row blocks (32
+ * rows each, 64 for Q4_K at M = 1); larger shapes fail with GGQ_EINVAL.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call clears the counters it uses (cudaMemsetAsync on `stream`).  All
+ * calls on a device share the one array, which keeps the last call's
+ * contents: calls whose executions overlap on the GPU (other streams, or
+ * other host threads) race on it and give wrong results -- order them.
+ */
+int ggq_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
+                     void* stream);
+
+/*
  * ggq_gemm_prefill -- Y = X W^T for a whole prompt (M activation rows),
  * "GGUF Inferencer in R" section 4 (prefill runs the prompt "at once with big
  * matrix multiplications").  Q4_K weight tiles are decoded to bf16 in shared

@@ -1,0 +1,61 @@
+"""ggq_gemv_noalloc: the GEMV for callers that may not allocate device memory
+(a server whose device memory all belongs to its own pool, or a loop where a
+cudaMalloc/cudaFree and the device-wide synchronisation it may bring are not
+allowed).  It must give the same result as ggq_gemv, through the C ABI, on
+two calls in a row (the second one reuses the built-in scratch as the first
+left it).
+
+Kept in a file pytest collects last, so that a run stopping at the first
+failure has already run every other test; it also passes alone in a fresh
+process (its first call sets up the scratch address on the device).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("-m gpu tests need a CUDA device")
+    import gguf_block_quantized_q8_gb300 as ggq
+    return torch, ggq
+
+
+@pytest.mark.parametrize("qtype,rows,cols,M", [(12, 4096, 4096, 1), (12, 1000, 11008, 2), (8, 2048, 2048, 1),
+                                               (8, 777, 4096, 3)])
+def test_noalloc_matches_gemv_twice(env, qtype, rows, cols, M):
+    torch, ggq = env
+    W = synth.weight_rows(qtype, 70 + qtype, rows, cols)
+    x = synth.normal_f32(M * cols, 71).reshape(M, cols)
+    _, a_ref = oracle.gemv(qtype, W, rows, cols, x)          # sum |w x| for the tolerance
+    Wd = torch.from_numpy(W).cuda()
+    xd = torch.from_numpy(x).cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    y_ref = torch.empty((M, rows), dtype=torch.float32, device="cuda")
+    ggq.check(ggq.ggq_gemv(qtype, Wd.data_ptr(), rows, cols, xd.data_ptr(), y_ref.data_ptr(), M, stream), "ggq_gemv")
+    torch.cuda.synchronize()
+    ref = y_ref.cpu().numpy().astype(np.float64)
+    for call in range(2):
+        y = torch.full((M, rows), float("nan"), dtype=torch.float32, device="cuda")
+        rc = ggq.ggq_gemv_noalloc(qtype, Wd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr(), M, stream)
+        ggq.check(rc, "ggq_gemv_noalloc")
+        torch.cuda.synchronize()
+        assert ggq.device_status() == 0
+        err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+        assert np.all(err <= 1e-3 * a_ref + 1e-6), f"call {call}: worst {np.nanmax(err / (1e-3 * a_ref + 1e-6))}"
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch(env):
+    torch, ggq = env
+    buf = torch.empty(64, dtype=torch.float32, device="cuda")
+    p = buf.data_ptr()
+    assert ggq.ggq_gemv_noalloc(12, p, 32768 * 64 + 1, 256, p, p, 1, 0) == -1      # too many row blocks
+    assert "built-in scratch" in ggq.lib.ggq_last_error().decode()
+    assert ggq.ggq_gemv_noalloc(12, p, 64, 256, p, p, 5, 0) == -1                  # M > 4
+    assert ggq.ggq_gemv_noalloc(8, p, 64, 96, p, p, 1, 0) == -1                    # cols % 256

@@ -7,10 +7,12 @@ Default workload: one batch-1 decode weight pass over a Llama-8B-shaped stack
 weights are seeded synthetic N(0, 0.02) values encoded to Q4_K / Q8_0, written
 to a GGUF file and loaded with ggq_load; activations are N(0, 1).
 
-A step is one pass in dependency order: per layer [q,k,v] (one ggq_gemv_multi
-launch), [o], [gate,up] (one launch), [down], then the head -- 129 launches,
-replayed as a CUDA graph.  The weights (4.48 GB) exceed the L2 cache, so
-successive steps read them from HBM.
+A step is one pass in dependency order: per layer the stages [q,k,v], [o],
+[gate,up], [down] (128 Q4_K stages, each reading its own x only after the
+previous stage's outputs are complete) run as ONE ggq_chain launch, then the
+Q8_0 head (ggq_gemv) -- 2 launches, replayed as a CUDA graph.  The same pass
+as one launch per stage (129 launches) is reported beside it.  The weights
+(4.48 GB) exceed the L2 cache, so successive steps read them from HBM.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead.
 """
@@ -151,7 +153,11 @@ def stage_plan(layers: int):
 
 
 class DecodePass:
-    """Device state for one pass: loaded weights, per-stage x and y, launch list."""
+    """Device state for one pass: loaded weights, per-stage x and y, launch list.
+
+    run(): the Q4_K stages (128 for 32 layers) as ONE ggq_chain launch, then
+    the Q8_0 head with ggq_gemv -- 2 launches.  run_launches(): every stage as
+    its own ggq_gemv / ggq_gemv_multi launch (129), for comparison."""
 
     def __init__(self, model, stages, torch, ggq, synth):
         self.torch, self.ggq = torch, ggq
@@ -177,6 +183,11 @@ class DecodePass:
         self.io_bytes = sum(s["io_bytes"] for s in self.stages)
         self.x_bytes = sum(4 * s["cols"] for s in self.stages)
         self.y_bytes = sum(4 * sum(s["rows"]) for s in self.stages)
+        self.q4 = [s for s in self.stages if s["qtype"] == 12]
+        self.rest = [s for s in self.stages if s["qtype"] != 12]
+        rc, self.chain = ggq.ggq_chain_create(12, 1, [(s["W"], s["rows"], s["cols"], s["x"], s["y"]) for s in self.q4])
+        ggq.check(rc, "ggq_chain_create")
+        self.q4_bytes = sum(s["nbytes"] + s["io_bytes"] for s in self.q4)
 
     def launch_stage(self, st, stream_ptr):
         ggq = self.ggq
@@ -186,13 +197,26 @@ class DecodePass:
             rc = ggq.ggq_gemv_multi(st["qtype"], st["W"], st["rows"], st["cols"], st["x"], st["y"], 1, stream_ptr)
         ggq.check(rc, "gemv")
 
+    def run_chain(self, stream_ptr):
+        self.ggq.check(self.ggq.ggq_chain_run(self.chain, stream_ptr), "ggq_chain_run")
+
     def run(self, stream_ptr):
+        self.run_chain(stream_ptr)
+        for st in self.rest:
+            self.launch_stage(st, stream_ptr)
+
+    def run_launches(self, stream_ptr):
         for st in self.stages:
             self.launch_stage(st, stream_ptr)
 
     @property
     def launches(self):
-        return len(self.stages)
+        return 1 + len(self.rest)
+
+    def close(self):
+        if self.chain:
+            self.ggq.ggq_chain_free(self.chain)
+            self.chain = 0
 
 
 def time_graph(torch, graph, stream, steps):
@@ -207,25 +231,23 @@ def time_graph(torch, graph, stream, steps):
     return e0.elapsed_time(e1) / steps   # ms per step
 
 
-def roofline_q4k(torch, dp, stream, steps):
-    """Per-launch durations of the dominant kernel (the Q4_K GEMV launches) on
-    the launching stream, CUDA events around each launch."""
-    sp = stream.cuda_stream
-    q4 = [s for s in dp.stages if s["qtype"] == 12]
-    evs = []
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    g.replay()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for _ in range(steps):
-            for st in q4:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                dp.launch_stage(st, sp)
-                b.record(stream)
-                evs.append((a, b, st["nbytes"] + st["io_bytes"]))
-    torch.cuda.synchronize()
-    t = sum(a.elapsed_time(b) for a, b, _ in evs) * 1e-3
-    nbytes = sum(n for _, _, n in evs)
-    return nbytes / len(evs), t / len(evs)
+    return g
+
+
+def roofline_chain(torch, dp, stream, steps):
+    """Average launch of the dominant kernel (the Q4_K chain kernel running the
+    pass's Q4_K stages) in the bench's launch configuration: one launch per
+    CUDA-graph replay, CUDA events on the launching stream around `steps`
+    replays.  Returns (algorithmic bytes per launch, seconds per launch)."""
+    g = capture(torch, lambda: dp.run_chain(stream.cuda_stream), stream)
+    ms = time_graph(torch, g, stream, steps)
+    return dp.q4_bytes, ms * 1e-3
 
 
 def cpu_oracle_sample(budget_s: float, layers: int = 32):
@@ -478,7 +500,11 @@ def main():
 
     # ---- roofline of the dominant kernel (Q4_K GEMV launches)
     r_steps = max(3, min(a.steps, 20))
-    per_launch_bytes, per_launch_s = roofline_q4k(torch, dp, stream, r_steps)
+    per_launch_bytes, per_launch_s = roofline_chain(torch, dp, stream, r_steps)
+    # the same pass as one launch per stage (129 launches), for comparison
+    g_l = capture(torch, lambda: dp.run_launches(sp), stream)
+    ms_launches = time_graph(torch, g_l, stream, r_steps)
+    del g_l
     clk = clocks.stop()
     rc = ggq.device_status()
     if rc:
@@ -517,9 +543,12 @@ def main():
         "gpu_launches": dp.launches * a.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                     "kernel": "gemv_stream_kernel<Q4_K, M=1>",
+                     "kernel": f"chain_kernel<Q4_K, M=1> over {len(dp.q4)} stages",
                      "peak_kind": f"{peak_kind} (copy, burst)",
-                     "bytes_per_launch": int(per_launch_bytes), "us_per_launch": round(per_launch_s * 1e6, 3)},
+                     "bytes_per_launch": int(per_launch_bytes), "us_per_launch": round(per_launch_s * 1e6, 3),
+                     "timing": "one chain launch per CUDA-graph replay, events on its stream"},
+        "per_stage_launches": {"ms_per_step": round(ms_launches, 4), "launches_per_pass": len(dp.stages),
+                               "value": round(step_bytes * ws / (ms_launches * 1e-3) / 1e9, 1), "unit": "GB/s"},
         "clocks": clk,
         "load": {"generate_s": round(t_gen, 2), "ggq_load_s": round(t_load, 3), "file_bytes": file_bytes},
         "configs": extra,
@@ -532,6 +561,7 @@ def main():
                                 "host_cpus": multiprocessing.cpu_count()}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    dp.close()
     model.close()
     if ws > 1:
         import torch.distributed as dist

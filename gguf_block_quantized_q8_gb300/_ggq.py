@@ -30,6 +30,11 @@ class Tensor(ctypes.Structure):
                 ("data", ctypes.c_void_p)]
 
 
+class ChainStage(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int), ("W", ctypes.c_void_p * 4), ("rows", ctypes.c_int64 * 4),
+                ("cols", ctypes.c_int64), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p * 4)]
+
+
 def _bind(lib):
     vp, i64, u64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int32
     sig = {
@@ -50,6 +55,10 @@ def _bind(lib):
         "ggq_gemv_multi": ([ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(i64), i64, vp,
                             ctypes.POINTER(vp), ctypes.c_int, vp], ctypes.c_int),
         "ggq_gemv_noalloc": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
+        "ggq_chain_create": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ChainStage),
+                              ctypes.POINTER(vp)], ctypes.c_int),
+        "ggq_chain_run": ([vp, vp], ctypes.c_int),
+        "ggq_chain_free": ([vp], None),
         "ggq_gemm_prefill": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
         "ggq_dequantize": ([ctypes.c_int, vp, i64, i64, vp, vp], ctypes.c_int),
         "ggq_device_status": ([], ctypes.c_int),
@@ -103,6 +112,31 @@ def ggq_gemv_multi(qtype: int, Ws, rows, cols: int, x: int, ys, M: int, stream: 
     ra = (ctypes.c_int64 * n)(*rows)
     ya = (ctypes.c_void_p * n)(*ys)
     return lib.ggq_gemv_multi(qtype, n, Wa, ra, cols, x, ya, M, stream)
+
+
+def ggq_chain_create(qtype: int, M: int, stages) -> tuple[int, int]:
+    """stages: sequence of (Ws, rows, cols, x, ys) with device pointers; returns (rc, handle)."""
+    arr = (ChainStage * len(stages))()
+    for i, (Ws, rows, cols, x, ys) in enumerate(stages):
+        st = arr[i]
+        st.n = len(Ws)                     # n > 4 is passed through for the library to reject
+        for j in range(min(len(Ws), 4)):
+            st.W[j] = Ws[j]
+            st.rows[j] = rows[j]
+            st.y[j] = ys[j]
+        st.cols = cols
+        st.x = x
+    h = ctypes.c_void_p()
+    rc = lib.ggq_chain_create(qtype, M, len(stages), arr, ctypes.byref(h))
+    return rc, (h.value or 0)
+
+
+def ggq_chain_run(chain: int, stream: int) -> int:
+    return lib.ggq_chain_run(chain, stream)
+
+
+def ggq_chain_free(chain: int) -> None:
+    lib.ggq_chain_free(chain)
 
 
 def ggq_gemm_prefill(qtype: int, W: int, rows: int, cols: int, X: int, Y: int, M: int, stream: int) -> int:
@@ -231,6 +265,36 @@ def gemv_multi(qtype: int, Ws, rows, cols: int, x, ys=None, stream=None):
     check(ggq_gemv_multi(qtype, [w.data_ptr() for w in Ws], list(rows), cols, x2.data_ptr(),
                          [y.data_ptr() for y in ys], M, _stream_ptr(stream)), "ggq_gemv_multi")
     return ys
+
+
+class Chain:
+    """A sequence of GEMV stages run as one launch (ggq_chain_create / ggq_chain_run).
+
+    stages: sequence of (Ws, rows, cols, x, ys) with CUDA tensors; the chain keeps
+    references to them (their memory is bound at creation).
+    """
+
+    def __init__(self, qtype: int, M: int, stages):
+        raw = [([w.data_ptr() for w in Ws], list(rows), cols, x.data_ptr(), [y.data_ptr() for y in ys])
+               for (Ws, rows, cols, x, ys) in stages]
+        rc, h = ggq_chain_create(qtype, M, raw)
+        check(rc, "ggq_chain_create")
+        self._h = h
+        self._keep = list(stages)
+
+    def run(self, stream=None) -> None:
+        check(ggq_chain_run(self._h, _stream_ptr(stream)), "ggq_chain_run")
+
+    def close(self) -> None:
+        if self._h:
+            ggq_chain_free(self._h)
+            self._h = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def gemm_prefill(qtype: int, W, rows: int, cols: int, X_bf16, Y=None, stream=None):

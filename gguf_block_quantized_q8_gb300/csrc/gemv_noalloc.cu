@@ -22,11 +22,11 @@ namespace {
 constexpr int kNoAllocMaxGroups = 2048;        // warp groups a launch may use
 constexpr int kNoAllocMaxRowBlocks = 32768;    // 32- or 64-row blocks per matrix
 constexpr size_t kNoAllocPartialFloats = (size_t)kNoAllocMaxGroups * 2 * 4 * 32;
-constexpr size_t kNoAllocBytes = kNoAllocPartialFloats * sizeof(float) + (size_t)kNoAllocMaxRowBlocks * sizeof(int);
+constexpr size_t kNoAllocBytes = kNoAllocPartialFloats * sizeof(float) + (size_t)(kNoAllocMaxRowBlocks + 32) * sizeof(int);
 
-// Partial sums of split row blocks, then one counter per row block.  Every
-// device that loads the library holds these ~2.2 MB until the process exits;
-// all calls on a device share them.
+// Partial sums of split row blocks, then a stage counter padded to 128 bytes
+// and one counter per row block.  Every device that loads the library holds these ~2.2 MB until
+// the process exits; all calls on a device share them.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;

@@ -180,6 +180,63 @@ int ggq_gemv_multi(int type, int n, const void* const* W, const int64_t* rows, i
                    const float* x, float* const* y, int M, void* stream);
 
 /*
+ * ggq_chain -- a fixed sequence of GEMV stages run by ONE kernel launch: the
+ * weight-streaming part of a decode step ("GGUF Inferencer in R" section 4:
+ * each generated token multiplies its activations by every weight matrix of
+ * every layer, one matrix product after another).
+ *
+ * A stage is up to four matrices of the chain's type that share one x (as in
+ * ggq_gemv_multi).  Stage s+1 starts reading its x only after every y of
+ * stages 0..s has been written, so a stage's x may be an earlier stage's y.
+ * Work that is not a GEMV between stages (norms, attention, activations) is
+ * the caller's; a chain holds the GEMVs that follow one another directly.
+ * Weights of later stages are streamed into shared memory while earlier
+ * stages finish, so the chain keeps HBM busy across stage boundaries.
+ *
+ *   n        matrices in the stage, 1..4
+ *   W[i]     device, rows[i] x row-bytes, 16-byte aligned
+ *   rows[i]  1..2^31-1
+ *   cols     multiple of 256, at most 2^20
+ *   x        device fp32 [M, cols], 16-byte aligned
+ *   y[i]     device fp32 [M, rows[i]], 4-byte aligned; fully overwritten
+ */
+typedef struct {
+    int n;
+    const void* W[4];
+    int64_t rows[4];
+    int64_t cols;
+    const float* x;
+    float* y[4];
+} ggq_chain_stage;
+
+typedef struct ggq_chain ggq_chain;
+
+/*
+ * ggq_chain_create -- validate `nstages` stages (1..65536) of type GGQ_Q8_0 or
+ * GGQ_Q4_K for M activation rows (1..4), encode their copy descriptors and
+ * store them in device memory on the current device.  The pointers are bound
+ * at creation: the chain reads and writes the same buffers on every run.  The
+ * caller owns the returned chain and frees it with ggq_chain_free.  Errors:
+ * GGQ_EINVAL (malformed stage, misaligned pointer, unsupported shape; the
+ * message names the stage), GGQ_ETYPE, GGQ_ENOMEM, GGQ_ECUDA.  Synchronous.
+ */
+int ggq_chain_create(int type, int M, int nstages, const ggq_chain_stage* stages, ggq_chain** out);
+
+/*
+ * ggq_chain_run -- run every stage of the chain, in order, as one launch on
+ * `stream` (cudaStream_t) on the device the chain was created on.  Uses the
+ * same per-stream workspace as ggq_gemv (allocated on the first call on a
+ * stream; make that call before stream capture).  The launch needs every CTA
+ * resident at once (one per SM); it must not overlap other work of the same
+ * stream.  Stage-boundary waits are bounded: if one runs out, the kernel
+ * records it and ggq_device_status reports GGQ_ETIMEOUT.  Asynchronous.
+ */
+int ggq_chain_run(const ggq_chain* chain, void* stream);
+
+/* ggq_chain_free -- release a chain (NULL is ignored).  No run may be pending. */
+void ggq_chain_free(ggq_chain* chain);
+
+/*
  * ggq_gemv_noalloc -- ggq_gemv that allocates nothing.  (No counterpart on the
  * pages: it exists for callers that may not allocate device memory.)
  *
@@ -238,7 +295,12 @@ int ggq_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* o
  * ggq_device_status -- synchronise the current device, then return GGQ_ETIMEOUT
  * if any kernel of this library recorded a bounded-wait timeout since the last
  * call (and clear the record), GGQ_ECUDA if the device reports an error, else
- * GGQ_OK.
+ * GGQ_OK.  Outputs of the launch that timed out, and of launches made after it
+ * before this call, are undefined.  On a timeout
+ * it also clears the split-row counters of the device's per-stream workspaces
+ * (left mid-count by the aborted launch), so later calls are correct again.
+ * When one wait of a multi-CTA kernel runs out, the kernel's other waits end
+ * within about a millisecond each, so the launch finishes promptly.
  */
 int ggq_device_status(void);
 

@@ -174,3 +174,21 @@ def test_compute_entry_points_validate_arguments(ggq):
     assert d(ggq.F16, 16, 2, 256, 16, 0) == -2
     assert g(ggq.Q8_0, 16, 4, 64, 16, 16, 17, 0) == -1
     assert "M 17 outside 1..16" in ggq.lib.ggq_last_error().decode()
+
+
+def test_chain_create_validates_stages(ggq):
+    """ggq_chain_create rejects malformed stages before touching the device."""
+    ok = ([16], [64], 256, 16, [16])
+    assert ggq.ggq_chain_create(ggq.F32, 1, [ok])[0] == -2                          # type
+    assert ggq.ggq_chain_create(ggq.Q4_K, 0, [ok])[0] == -1                         # M = 0
+    assert ggq.ggq_chain_create(ggq.Q4_K, 5, [ok])[0] == -1                         # M = 5
+    assert ggq.ggq_chain_create(ggq.Q4_K, 1, [])[0] == -1                           # no stages
+    assert ggq.ggq_chain_create(ggq.Q4_K, 1, [ok, ([0], [64], 256, 16, [16])])[0] == -1      # NULL W
+    assert "stage 1" in ggq.lib.ggq_last_error().decode()
+    assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([16], [64], 256, 8, [16])])[0] == -1          # x misaligned
+    assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([8], [64], 256, 16, [16])])[0] == -1          # W misaligned
+    assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([16], [0], 256, 16, [16])])[0] == -1          # rows = 0
+    assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([16], [64], 320, 16, [16])])[0] == -1         # cols % 256
+    assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([16] * 5, [64] * 5, 256, 16, [16] * 5)])[0] == -1   # n = 5
+    assert ggq.ggq_chain_run(0, 0) == -1
+    ggq.ggq_chain_free(0)

@@ -1,0 +1,173 @@
+"""GPU parity: ggq_chain (a sequence of dependent GEMV stages in one launch)
+against the CPU oracle, through the C ABI.
+
+Each stage is checked against the oracle fed with the x that stage actually
+read on the GPU (the y the chain wrote for the stage before it), so a stage
+that started before its input was complete shows up as a mismatch: outputs
+start as NaN and the input of the second run differs from the first.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-3, 1e-6
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("-m gpu tests need a CUDA device")
+    import gguf_block_quantized_q8_gb300 as ggq
+    return torch, ggq
+
+
+def _dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+class Net:
+    """Stages given as lists of (name, rows, cols, source); source is 'x0' or
+    the name of an earlier output whose rows equal this stage's cols."""
+
+    def __init__(self, env, qtype, M, stages, seed=0):
+        torch, ggq = env
+        self.torch, self.ggq, self.qtype, self.M = torch, ggq, qtype, M
+        self.W, self.Wd, self.y, self.shape = {}, {}, {}, {}
+        cols0 = stages[0][0][2]
+        self.x0 = torch.empty((M, cols0), dtype=torch.float32, device="cuda")
+        self.plan = []
+        for si, stage in enumerate(stages):
+            src = stage[0][3]
+            cols = stage[0][2]
+            assert all(s[2] == cols and s[3] == src for s in stage)
+            for (name, rows, _, _) in stage:
+                self.W[name] = synth.weight_rows(qtype, 100 + 17 * seed + len(self.W), rows, cols)
+                self.Wd[name] = _dev(torch, self.W[name])
+                self.y[name] = torch.full((M, rows), float("nan"), dtype=torch.float32, device="cuda")
+                self.shape[name] = (rows, cols)
+            x = self.x0 if src == "x0" else self.y[src]
+            self.plan.append(([self.Wd[n] for (n, _, _, _) in stage], [r for (_, r, _, _) in stage], cols, x,
+                              [self.y[n] for (n, _, _, _) in stage]))
+        self.names = [[n for (n, _, _, _) in stage] for stage in stages]
+        self.srcs = [stage[0][3] for stage in stages]
+        self.chain = ggq.Chain(qtype, M, self.plan)
+
+    def run(self, x0):
+        self.x0.copy_(self.torch.from_numpy(x0))
+        for y in self.y.values():
+            y.fill_(float("nan"))
+        self.chain.run()
+        self.torch.cuda.synchronize()
+        assert self.ggq.device_status() == 0
+        return {n: y.cpu().numpy() for n, y in self.y.items()}
+
+    def check(self, x0, out):
+        worst = 0.0
+        for names, src in zip(self.names, self.srcs):
+            x = x0 if src == "x0" else out[src]
+            assert np.isfinite(x).all()
+            for n in names:
+                rows, cols = self.shape[n]
+                y_ref, a_ref = oracle.gemv(self.qtype, self.W[n], rows, cols, x)
+                ok, w = oracle.tolerance_ok(out[n], y_ref, a_ref, REL, ABS)
+                assert ok, f"{n}: worst error / bound = {w:.3g}"
+                worst = max(worst, w)
+        return worst
+
+
+def _layer(prefix, hidden, kv, ffn, src):
+    return [
+        [(f"{prefix}q", hidden, hidden, src), (f"{prefix}k", kv, hidden, src), (f"{prefix}v", kv, hidden, src)],
+        [(f"{prefix}o", hidden, hidden, f"{prefix}q")],
+        [(f"{prefix}gate", ffn, hidden, f"{prefix}o"), (f"{prefix}up", ffn, hidden, f"{prefix}o")],
+        [(f"{prefix}down", hidden, ffn, f"{prefix}gate")],
+    ]
+
+
+@pytest.mark.parametrize("qtype,M", [(12, 1), (12, 2), (12, 3), (8, 1), (8, 4)])
+def test_chain_two_layers(env, qtype, M):
+    """Two small layers: every stage after the first reads the previous stage's y."""
+    stages = _layer("a.", 1024, 256, 2816, "x0") + _layer("b.", 1024, 256, 2816, "a.down")
+    net = Net(env, qtype, M, stages)
+    for run in range(2):
+        x0 = synth.normal_f32(M * 1024, 40 + run).reshape(M, 1024)
+        net.check(x0, net.run(x0))
+
+
+def test_chain_repeat_is_bit_identical(env):
+    stages = _layer("a.", 2048, 512, 5632, "x0")
+    net = Net(env, 12, 1, stages, seed=1)
+    x0 = synth.normal_f32(2048, 50).reshape(1, 2048)
+    a = net.run(x0)
+    b = net.run(x0)
+    for n in a:
+        assert np.array_equal(a[n].view(np.uint32), b[n].view(np.uint32)), n
+    net.check(x0, a)
+
+
+def test_chain_single_stage_equals_gemv(env):
+    torch, ggq = env
+    rows, cols = 3000, 4096
+    W = synth.weight_rows(12, 60, rows, cols)
+    x = synth.normal_f32(cols, 61).reshape(1, cols)
+    Wd, xd = _dev(torch, W), _dev(torch, x)
+    y1 = ggq.gemv(12, Wd, rows, cols, xd)
+    y2 = torch.empty_like(y1)
+    ch = ggq.Chain(12, 1, [([Wd], [rows], cols, xd, [y2])])
+    ch.run()
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
+def test_chain_uneven_stages(env):
+    """Stages far smaller than the grid (a few tiles) next to large ones, and
+    ragged row counts that end inside a row block."""
+    stages = [
+        [("s0", 512, 256, "x0"), ("t0", 33, 256, "x0")],
+        [("s1", 4099, 512, "s0"), ("s2", 1, 512, "s0"), ("s3", 65, 512, "s0")],
+        [("s4", 256, 512, "s0")],                  # reads the output of two stages back
+        [("s5", 70000, 256, "s4")],
+    ]
+    net = Net(env, 12, 1, stages, seed=2)
+    x0 = synth.normal_f32(256, 70).reshape(1, 256)
+    net.check(x0, net.run(x0))
+
+
+def test_chain_llama8b_layers(env):
+    """Two Llama-8B-shaped Q4_K layers (hidden 4096, kv 1024, ffn 14336)."""
+    stages = _layer("a.", 4096, 1024, 14336, "x0") + _layer("b.", 4096, 1024, 14336, "a.down")
+    net = Net(env, 12, 1, stages, seed=3)
+    x0 = synth.normal_f32(4096, 80).reshape(1, 4096)
+    net.check(x0, net.run(x0))
+
+
+def test_chain_in_cuda_graph(env):
+    torch, ggq = env
+    stages = _layer("a.", 1024, 256, 2816, "x0")
+    net = Net(env, 12, 1, stages, seed=4)
+    x0 = synth.normal_f32(1024, 90).reshape(1, 1024)
+    net.run(x0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    net.chain.run(s)                           # first run on s: its workspace is allocated outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            net.chain.run(s)
+    torch.cuda.synchronize()
+    x1 = synth.normal_f32(1024, 91).reshape(1, 1024)
+    net.x0.copy_(torch.from_numpy(x1))
+    for y in net.y.values():
+        y.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ggq.device_status() == 0
+    out = {n: y.cpu().numpy() for n, y in net.y.items()}
+    net.check(x1, out)

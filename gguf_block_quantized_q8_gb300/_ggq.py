@@ -58,6 +58,7 @@ def _bind(lib):
         "ggq_chain_create": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ChainStage),
                               ctypes.POINTER(vp)], ctypes.c_int),
         "ggq_chain_run": ([vp, vp], ctypes.c_int),
+        "ggq_chain_reset": ([vp], ctypes.c_int),
         "ggq_chain_free": ([vp], None),
         "ggq_gemm_prefill": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
         "ggq_dequantize": ([ctypes.c_int, vp, i64, i64, vp, vp], ctypes.c_int),
@@ -133,6 +134,10 @@ def ggq_chain_create(qtype: int, M: int, stages) -> tuple[int, int]:
 
 def ggq_chain_run(chain: int, stream: int) -> int:
     return lib.ggq_chain_run(chain, stream)
+
+
+def ggq_chain_reset(chain: int) -> int:
+    return lib.ggq_chain_reset(chain)
 
 
 def ggq_chain_free(chain: int) -> None:

@@ -59,7 +59,6 @@ int read_and_clear_status(int* status) {
         const int zero = 0;
         e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
         if (e != cudaSuccess) return cuda_fail(e, "clear status word");
-        reset_stream_workspaces();
     }
     *status = v;
     return GGQ_OK;

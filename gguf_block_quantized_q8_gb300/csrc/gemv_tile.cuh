@@ -84,9 +84,12 @@ __device__ __forceinline__ void f2_fma64(F2& acc, uint64_t a, float b0, float b1
 
 // Chunk c (weights 64c .. 64c+63, sub-blocks 2c and 2c+1) of R rows of Q4_K
 // super-blocks per lane (rp: the lane's first row, `rstride` bytes to the next
-// of its rows) against x' of that super-block (xu: 256 floats per activation
-// row in the q4k_xslot layout, rows `xs` floats apart) and the per-sub-block
-// sums of x (su: 8 per activation row, rows `ss` apart).
+// of its rows) against x' of that super-block and the per-sub-block sums of x.
+// x' is read as float4 groups: group q (x' slots 4q .. 4q+3 of the q4k_xslot
+// layout) of activation row m at xu + m*xs + q*gs (gs = 4: the 256 values
+// contiguous; gs = 4*U: groups of U super-blocks interleaved so that lanes
+// reading different super-blocks hit different banks).  The sum of sub-block
+// j of activation row m is su[m*ss + j*sj].
 // acc[r][m] += sum_{k in chunk c} w_r[k] * x[m][k].
 //
 // Two consecutive qs words are handled as one 64-bit value: AND-ing it with a
@@ -94,7 +97,8 @@ __device__ __forceinline__ void f2_fma64(F2& acc, uint64_t a, float b0, float b1
 // both words in one aligned register pair, the first operand of fma.f32x2.
 template <int MMAX, int R>
 __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, int c, const float* xu, int xs,
-                                               const float* su, int ss, float (&acc)[R][MMAX]) {
+                                               const float* su, int ss, float (&acc)[R][MMAX], int gs = 4,
+                                               int sj = 1) {
     // nibble masks (both halves): low nibble of bytes 0,1,2 in place, byte 3 after >> 8
     constexpr uint64_t kLo0 = 0x0000000F0000000Full, kLo1 = 0x00000F0000000F00ull, kLo2 = 0x000F0000000F0000ull;
     constexpr uint64_t kHi0 = 0x000000F0000000F0ull, kHi1 = 0x0000F0000000F000ull, kHi2 = 0x00F0000000F00000ull;
@@ -131,11 +135,11 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
         float4 xl[MMAX][2], xh[MMAX][2];
 #pragma unroll
         for (int m = 0; m < MMAX; ++m) {
-            const float* xm = xu + m * xs + 64 * c + 8 * b;
+            const float* xm = xu + m * xs + (16 * c + 2 * b) * gs;
             xl[m][0] = *reinterpret_cast<const float4*>(xm);
-            xl[m][1] = *reinterpret_cast<const float4*>(xm + 4);
-            xh[m][0] = *reinterpret_cast<const float4*>(xm + 32);
-            xh[m][1] = *reinterpret_cast<const float4*>(xm + 36);
+            xl[m][1] = *reinterpret_cast<const float4*>(xm + gs);
+            xh[m][0] = *reinterpret_cast<const float4*>(xm + 8 * gs);
+            xh[m][1] = *reinterpret_cast<const float4*>(xm + 9 * gs);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -166,9 +170,9 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
             const float* sm = su + m * ss;
             float a = acc[r][m];
             a = fmaf(a_lo[r], f2_sum(lo[r][m][0], lo[r][m][1]), a);
-            a = fmaf(-b_lo[r], sm[2 * c], a);
+            a = fmaf(-b_lo[r], sm[2 * c * sj], a);
             a = fmaf(a_hi[r], f2_sum(hi[r][m][0], hi[r][m][1]), a);
-            a = fmaf(-b_hi[r], sm[2 * c + 1], a);
+            a = fmaf(-b_hi[r], sm[(2 * c + 1) * sj], a);
             acc[r][m] = a;
         }
     }
@@ -177,9 +181,10 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
 // All four chunks of R rows.
 template <int MMAX, int R>
 __device__ __forceinline__ void q4k_tile_rows(const uint8_t* rp, int rstride, const float* xu, int xs,
-                                              const float* su, int ss, float (&acc)[R][MMAX]) {
+                                              const float* su, int ss, float (&acc)[R][MMAX], int gs = 4,
+                                              int sj = 1) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) q4k_chunk_rows<MMAX, R>(rp, rstride, c, xu, xs, su, ss, acc);
+    for (int c = 0; c < 4; ++c) q4k_chunk_rows<MMAX, R>(rp, rstride, c, xu, xs, su, ss, acc, gs, sj);
 }
 
 // One row (R = 1) of the above.
@@ -195,11 +200,12 @@ __device__ __forceinline__ void q4k_tile_row(const uint8_t* rp, const float* xu,
 }
 
 // One 8-block Q8_0 period of one row (rp: 272 bytes) against x' indexed by
-// byte position (xu: 272 floats per activation row, rows `xs` apart) and
-// 128 * sum(x) per block (su: 8 per row, rows `ss` apart).
+// byte position (272 values per activation row, read as float4 groups: group
+// q of row m at xu + m*xs + q*gs) and 128 * sum(x) per block (block b of row m
+// at su[m*ss + b*sj]).
 template <int MMAX>
 __device__ __forceinline__ void q8_tile_row(const uint8_t* rp, const float* xu, int xs, const float* su, int ss,
-                                            float (&acc)[MMAX]) {
+                                            float (&acc)[MMAX], int gs = 4, int sj = 1) {
     float pa[MMAX], pb[MMAX];
     float dcur = 0.0f;
 #pragma unroll
@@ -214,7 +220,7 @@ __device__ __forceinline__ void q8_tile_row(const uint8_t* rp, const float* xu, 
             const uint32_t w = wq[t];
             float4 xv[MMAX];
 #pragma unroll
-            for (int m = 0; m < MMAX; ++m) xv[m] = *reinterpret_cast<const float4*>(xu + m * xs + 4 * wi);
+            for (int m = 0; m < MMAX; ++m) xv[m] = *reinterpret_cast<const float4*>(xu + m * xs + wi * gs);
 #pragma unroll
             for (int pos = 0; pos < 4; ++pos) {
                 const int B = 4 * wi + pos;
@@ -234,7 +240,7 @@ __device__ __forceinline__ void q8_tile_row(const uint8_t* rp, const float* xu, 
                     if (o == 33) {
 #pragma unroll
                         for (int m = 0; m < MMAX; ++m) {
-                            acc[m] = fmaf(dcur, fmaf(pa[m] + pb[m], kTwo96, -su[m * ss + b]), acc[m]);
+                            acc[m] = fmaf(dcur, fmaf(pa[m] + pb[m], kTwo96, -su[m * ss + b * sj]), acc[m]);
                             pa[m] = pb[m] = 0.0f;
                         }
                     }

@@ -47,18 +47,11 @@ int payload_bytes(int32_t type, uint64_t ne0, uint64_t n, uint64_t* out);
 // kernel entry points (launchers live next to their kernels)
 int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x,
                 float* y, int M, cudaStream_t stream);
-// persistent stream-K GEMV over one or more matrices sharing x (M <= 4)
+// persistent row-partitioned GEMV over one or more matrices sharing x (M <= 4);
+// needs no workspace
 bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_t* rows);
 int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* rows, int64_t cols,
                        const float* x, float* const* y, int M, cudaStream_t stream);
-// the same with caller-provided scratch (partials for max_groups groups; a
-// stage counter padded to 32 ints, then one counter per row block), cleared as
-// needed; allocates nothing
-int launch_gemv_stream_scratch(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
-                               int M, cudaStream_t stream, float* partials, int max_groups, int* counters,
-                               int max_row_blocks);
-// clear the stream workspaces' counters on the current device (after a timeout)
-void reset_stream_workspaces();
 int launch_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out,
                       cudaStream_t stream);
 int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const uint16_t* X,

@@ -156,11 +156,8 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  * 16-byte aligned, x not 16-byte or y not 4-byte aligned), GGQ_ETYPE, GGQ_ECUDA (launch
  * failure).  Asynchronous: returns after the launch.
  *
- * For M <= 4 the kernel finishes rows whose columns were split between warps
- * through a small per-stream workspace that the library allocates on the first
- * call on each (device, stream) pair; make that first call before capturing the
- * stream into a CUDA graph.  Calls on one stream run in stream order; a graph
- * replay must not overlap other work of the stream it was captured from.
+ * The call allocates no device memory and may be captured into a CUDA graph.
+ * Calls on one stream run in stream order.
  */
 int ggq_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x,
              float* y, int M, void* stream);
@@ -172,9 +169,9 @@ int ggq_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x
  *
  *   y[i][m*rows[i] + r] = sum_c w_i[r, c] * x[m*cols + c],   i < n
  *
- * W[i], rows[i], y[i] as for ggq_gemv; n in 1..4.  The work of all n matrices
- * is spread evenly over the GPU as one stream of tiles.  Same errors as
- * ggq_gemv.  Asynchronous.
+ * W[i], rows[i], y[i] as for ggq_gemv; n in 1..4.  The rows of all n matrices
+ * are spread evenly over the GPU as one list.  Same errors as ggq_gemv.
+ * Asynchronous.
  */
 int ggq_gemv_multi(int type, int n, const void* const* W, const int64_t* rows, int64_t cols,
                    const float* x, float* const* y, int M, void* stream);
@@ -223,15 +220,20 @@ typedef struct ggq_chain ggq_chain;
 int ggq_chain_create(int type, int M, int nstages, const ggq_chain_stage* stages, ggq_chain** out);
 
 /*
- * ggq_chain_run -- run every stage of the chain, in order, as one launch on
- * `stream` (cudaStream_t) on the device the chain was created on.  Uses the
- * same per-stream workspace as ggq_gemv (allocated on the first call on a
- * stream; make that call before stream capture).  The launch needs every CTA
- * resident at once (one per SM); it must not overlap other work of the same
- * stream.  Stage-boundary waits are bounded: if one runs out, the kernel
- * records it and ggq_device_status reports GGQ_ETIMEOUT.  Asynchronous.
+ * ggq_chain_run -- run every stage of the chain, in order, as one cooperative
+ * launch (every CTA resident at once, one per SM) on `stream` (cudaStream_t)
+ * on the device the chain was created on.  The chain's stage counter lives in
+ * the chain and is back at zero after each run, so runs may be captured into
+ * a CUDA graph and replayed; runs of one chain must not overlap each other
+ * (other streams).  Stage-boundary waits are bounded: if one runs out, the
+ * kernel records it and ggq_device_status reports GGQ_ETIMEOUT; then call
+ * ggq_chain_reset before the next run.  Allocates nothing.  Asynchronous.
  */
 int ggq_chain_run(const ggq_chain* chain, void* stream);
+
+/* ggq_chain_reset -- zero the chain's stage counter (after a run that timed
+ * out).  Synchronous. */
+int ggq_chain_reset(ggq_chain* chain);
 
 /* ggq_chain_free -- release a chain (NULL is ignored).  No run may be pending. */
 void ggq_chain_free(ggq_chain* chain);
@@ -240,26 +242,19 @@ void ggq_chain_free(ggq_chain* chain);
  * ggq_gemv_noalloc -- ggq_gemv that allocates nothing.  (No counterpart on the
  * pages: it exists for callers that may not allocate device memory.)
  *
- * ggq_gemv allocates a small per-stream workspace on its first call on a
- * stream.  Callers that cannot allow any device allocation at call time -- a
- * server that hands all device memory to its own pool at start-up and treats
- * a later cudaMalloc as a failure, or a latency-critical loop in which
- * cudaMalloc / cudaFree (which may synchronise the device) must never run --
- * use this entry point instead.  It runs the same kernel with its scratch in
- * one fixed array of device memory inside the library (about 2.2 MB on every
- * device that loads the library, held until the process exits).  It calls no
- * cudaMalloc, cudaFree or other allocating routine.
+ * Callers that cannot allow any device allocation at call time -- a server
+ * that hands all device memory to its own pool at start-up and treats a later
+ * cudaMalloc as a failure, or a latency-critical loop in which cudaMalloc /
+ * cudaFree (which may synchronise the device) must never run -- use this
+ * entry point: it is guaranteed to run the row-partitioned kernel, which
+ * needs no scratch memory (no output row is split between CTAs), and it calls
+ * no cudaMalloc, cudaFree or other allocating routine.  Shapes that would need
+ * another kernel fail instead of falling back.
  *
  * Arguments and result as for ggq_gemv, within these limits: type GGQ_Q8_0 or
- * GGQ_Q4_K, cols a multiple of 256, M in 1..4, at most 32768 row blocks (32
- * rows each, 64 for Q4_K at M = 1); larger shapes fail with GGQ_EINVAL.
- *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * Every call clears the counters it uses (cudaMemsetAsync on `stream`).  All
- * calls on a device share the one array, which keeps the last call's
- * contents: calls whose executions overlap on the GPU (other streams, or
- * other host threads) race on it and give wrong results -- order them.
+ * GGQ_Q4_K, cols a multiple of 256, M in 1..4, x' of one activation row in
+ * shared memory (cols up to about 40000 at M = 1); other shapes fail with
+ * GGQ_EINVAL.  Calls may overlap on the GPU and may be captured into graphs.
  */
 int ggq_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
                      void* stream);
@@ -296,11 +291,10 @@ int ggq_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* o
  * if any kernel of this library recorded a bounded-wait timeout since the last
  * call (and clear the record), GGQ_ECUDA if the device reports an error, else
  * GGQ_OK.  Outputs of the launch that timed out, and of launches made after it
- * before this call, are undefined.  On a timeout
- * it also clears the split-row counters of the device's per-stream workspaces
- * (left mid-count by the aborted launch), so later calls are correct again.
- * When one wait of a multi-CTA kernel runs out, the kernel's other waits end
- * within about a millisecond each, so the launch finishes promptly.
+ * before this call, are undefined; a chain that timed out needs
+ * ggq_chain_reset.  When one wait of a multi-CTA kernel runs out, the kernel's
+ * other waits end within about a millisecond each, so the launch finishes
+ * promptly.
  */
 int ggq_device_status(void);
 

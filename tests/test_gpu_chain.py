@@ -154,7 +154,7 @@ def test_chain_in_cuda_graph(env):
     net.run(x0)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    net.chain.run(s)                           # first run on s: its workspace is allocated outside capture
+    net.chain.run(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):

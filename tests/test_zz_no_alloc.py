@@ -2,12 +2,11 @@
 (a server whose device memory all belongs to its own pool, or a loop where a
 cudaMalloc/cudaFree and the device-wide synchronisation it may bring are not
 allowed).  It must give the same result as ggq_gemv, through the C ABI, on
-two calls in a row (the second one reuses the built-in scratch as the first
-left it).
+two calls in a row.
 
 Kept in a file pytest collects last, so that a run stopping at the first
 failure has already run every other test; it also passes alone in a fresh
-process (its first call sets up the scratch address on the device).
+process.
 """
 import numpy as np
 import pytest
@@ -51,11 +50,11 @@ def test_noalloc_matches_gemv_twice(env, qtype, rows, cols, M):
         assert np.all(err <= 1e-3 * a_ref + 1e-6), f"call {call}: worst {np.nanmax(err / (1e-3 * a_ref + 1e-6))}"
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch(env):
+def test_noalloc_refuses_shapes_it_cannot_run_without_allocating(env):
     torch, ggq = env
     buf = torch.empty(64, dtype=torch.float32, device="cuda")
     p = buf.data_ptr()
-    assert ggq.ggq_gemv_noalloc(12, p, 32768 * 64 + 1, 256, p, p, 1, 0) == -1      # too many row blocks
-    assert "built-in scratch" in ggq.lib.ggq_last_error().decode()
     assert ggq.ggq_gemv_noalloc(12, p, 64, 256, p, p, 5, 0) == -1                  # M > 4
     assert ggq.ggq_gemv_noalloc(8, p, 64, 96, p, p, 1, 0) == -1                    # cols % 256
+    assert ggq.ggq_gemv_noalloc(12, p, 64, 1 << 20, p, p, 1, 0) == -1              # x' beyond shared memory
+    assert "allocation-free kernel" in ggq.lib.ggq_last_error().decode()

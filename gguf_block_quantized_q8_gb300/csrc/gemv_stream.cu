@@ -7,34 +7,36 @@
 // one.  A single GEMV is a chain of one stage.
 //
 // Work unit: one 256-column block of one row (SB) -- a Q4_K super-block
-// (144 B) or a Q8_0 period of 8 blocks (272 B).  The rows of a stage's
-// matrices are numbered one after another; SB S = row * U + u (U = cols/256)
-// sits right after SB S - 1 in memory inside one matrix.
+// (144 B) or a Q8_0 period of 8 blocks (272 B) -- split into four 64-column
+// chunks.  The rows of a stage's matrices are numbered one after another.
 //
 //   * CTA b (one per SM) owns rows [R*b/G, R*(b+1)/G): whole rows, so no output
 //     is ever split between CTAs and no cross-CTA reduction exists.
-//   * Its SB range is cut into W equal contiguous pieces, one per warp.  A warp
-//     streams its piece through its own ring of tiles of 32 SBs with 1-D bulk
-//     copies (lane 0 issues them; weights do not depend on earlier stages, so
-//     the ring runs ahead into the next stages while the chain waits at a stage
-//     boundary).
-//   * Lane l decodes SB l of a tile in registers against x', the pre-scaled
-//     activations of its column block (interleaved across column blocks so
-//     lanes reading different blocks hit different banks).  A segmented warp
-//     sum adds the SBs of each row; a row that a warp sees from start to end is
-//     stored directly, a row cut between warps is finished in shared memory by
-//     the warp where it starts, adding the others' parts in warp order
+//   * Its rows form groups of 8 (inside one matrix); the (group, SB) tiles are
+//     cut into W equal contiguous runs, one per warp.  A warp streams its run
+//     through its own ring of 2-D bulk tensor copies (8 rows x up to NSB SBs);
+//     weights do not depend on earlier stages, so the ring runs ahead into the
+//     next stages while the chain waits at a stage boundary.
+//   * Lane (r, c) = (lane / 4, lane % 4) decodes chunk c of row r of each SB in
+//     registers against x', the pre-scaled activations.  The 8 lanes of one
+//     chunk read the same x' address (a broadcast), and chunks are padded so
+//     that the four addresses of one load sit in different banks.  Two
+//     shuffles add a row's chunks; a group that a warp sees over all its SBs is
+//     stored directly, a group cut between warps is finished in shared memory
+//     by the warp where it starts, adding the others' parts in warp order
 //     (deterministic).
 //   * Stage boundary: every CTA adds one to a device counter with release
 //     semantics after its outputs are stored; CTAs wait (acquire, bounded) for
 //     the count of all CTAs before reading the next stage's x.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -48,12 +50,13 @@ namespace {
 
 constexpr int kMaxSeg = 4;
 constexpr int kMaxM = 4;
-constexpr int kLanes = 32;
 constexpr size_t kSmemLimit = 227 * 1024;
+
+constexpr int kGroupRows = 8;
 
 // One stage of a chain (device-visible: kernel parameter or global table).
 struct StageDesc {
-    const uint8_t* W[kMaxSeg];
+    CUtensorMap maps[kMaxSeg];  // per matrix: 8-byte elements, box of 8 rows x (NSB SBs + pad)
     float* y[kMaxSeg];          // [M][rows]
     const float* x;             // [M][cols]
     int rows[kMaxSeg];
@@ -68,16 +71,24 @@ struct ChainParams {
     int nstages;
     int M;
     int ring;                   // tiles per warp ring
-    int xs;                     // x' floats per activation row (widest stage)
-    int nsub;                   // x sums per activation row (widest stage)
+    int xs;                     // x' floats per activation row (272 per SB of the widest stage)
+    int nsub;                   // x sums per activation row (8 per SB of the widest stage)
     int* counter;               // stage counter (chains of > 1 stage); zero between launches
     int* status;
 };
 
+// Tile of one bulk tensor copy: 8 rows x NSB SBs, each row padded so that
+// rows r and r+1 of one chunk fall in different banks.  Copies of a few KB:
+// much smaller ones cost more per copy than the bytes they bring.
 template <bool Q4K>
 struct Blk {
-    static constexpr int kBytes = Q4K ? 144 : 272;   // one SB
-    static constexpr int kTile = kLanes * kBytes;
+    static constexpr int kBytes = Q4K ? 144 : 272;      // one SB
+    static constexpr int kElems = kBytes / 8;            // 8-byte elements per SB
+    static constexpr int kNsb = Q4K ? 4 : 1;             // SBs per copy
+    static constexpr int kPad = Q4K ? 2 : 0;             // elements of padding per row
+    static constexpr int kRow = (kElems * kNsb + kPad) * 8;    // smem bytes per row: 304 / 272
+    static constexpr int kCopy = kGroupRows * kRow;            // bytes per copy
+    static constexpr int kTile = (kCopy + 127) / 128 * 128;    // smem stride: 128-byte aligned
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -146,36 +157,49 @@ __device__ __forceinline__ void wait_full(uint64_t* bar, uint32_t parity, int* s
     }
 }
 
-// The SB range [ws, we) of warp w (of nw) of CTA b (of nb) in a stage.
-__device__ __forceinline__ void warp_range(const StageDesc* sd, int b, int nb, int w, int nw, int& ws, int& we) {
+// Row groups of CTA b (of nb) in a stage: its rows [r0, r1) cut at matrix
+// boundaries, then into groups of up to 8 rows.
+struct Groups {
+    int r0, r1;
+    int n;                 // groups
+    int first[kMaxSeg];    // index of the first group of each matrix
+};
+
+__device__ __forceinline__ Groups cta_groups(const StageDesc* sd, int b, int nb) {
+    Groups G;
     const long long R = sd->row0[sd->nseg];
-    const long long rlo = R * b / nb, rhi = R * (b + 1) / nb;
-    const long long base = rlo * sd->units, n = (rhi - rlo) * sd->units;
-    ws = (int)(base + n * w / nw);
-    we = (int)(base + n * (w + 1) / nw);
-}
-
-__device__ __forceinline__ int seg_of_row(const StageDesc* sd, int g) {
-    int s = 0;
+    G.r0 = (int)(R * b / nb);
+    G.r1 = (int)(R * (b + 1) / nb);
+    int n = 0;
 #pragma unroll
-    for (int i = 1; i < kMaxSeg; ++i)
-        if (i < sd->nseg && g >= sd->row0[i]) s = i;
-    return s;
+    for (int s = 0; s < kMaxSeg; ++s) {
+        G.first[s] = n;
+        if (s < sd->nseg) {
+            const int lo = max(G.r0, sd->row0[s]), hi = min(G.r1, sd->row0[s + 1]);
+            if (lo < hi) n += (hi - lo + kGroupRows - 1) / kGroupRows;
+        }
+    }
+    G.n = n;
+    return G;
 }
 
-// Issue the bulk copies of SBs [a, b) of a stage into `dst` (one thread).
-template <bool Q4K>
-__device__ __forceinline__ void issue_tile(const StageDesc* sd, int a, int b, uint8_t* dst, uint64_t* bar) {
-    using B = Blk<Q4K>;
-    fence_proxy_async_smem();   // this warp's reads of the buffer come before the copy's writes
-    mbar_arrive_expect_tx(bar, (uint32_t)(b - a) * B::kBytes);
-    const int U = sd->units;
-    for (int s = 0; s < sd->nseg; ++s) {
-        const int lo = max(a, sd->row0[s] * U), hi = min(b, sd->row0[s + 1] * U);
-        if (lo < hi)
-            bulk_load(dst + (size_t)(lo - a) * B::kBytes, sd->W[s] + (size_t)(lo - sd->row0[s] * U) * B::kBytes,
-                      (uint32_t)(hi - lo) * B::kBytes, bar);
-    }
+// Group gi: matrix, first row (in the matrix), rows in the group.
+__device__ __forceinline__ void group_at(const StageDesc* sd, const Groups& G, int gi, int& seg, int& row, int& nrows) {
+    seg = 0;
+#pragma unroll
+    for (int s = 1; s < kMaxSeg; ++s)
+        if (s < sd->nseg && gi >= G.first[s]) seg = s;
+    const int lo = max(G.r0, sd->row0[seg]), hi = min(G.r1, sd->row0[seg + 1]);
+    const int g0 = lo + (gi - G.first[seg]) * kGroupRows;
+    row = g0 - sd->row0[seg];
+    nrows = min(kGroupRows, hi - g0);
+}
+
+// The tile run [t0, t1) of warp w (of nw): tile t = group * U + SB.
+__device__ __forceinline__ void warp_run(const Groups& G, int U, int w, int nw, int& t0, int& t1) {
+    const long long T = (long long)G.n * U;
+    t0 = (int)(T * w / nw);
+    t1 = (int)(T * (w + 1) / nw);
 }
 
 template <bool Q4K, int MMAX, int W>
@@ -184,15 +208,16 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     constexpr int kThreads = 32 * W;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = lane >> 2, c = lane & 3;   // row of the group, chunk of the SB
     const int D = p.ring;
 
-    // shared memory: [warp rings][x'][sums][cut-row parts][barriers]
+    // shared memory: [warp rings][x'][sums][cut-group parts][barriers]
     uint8_t* ring = smem + (size_t)warp * D * B::kTile;
     float* xp = reinterpret_cast<float*>(smem + (size_t)W * D * B::kTile);
     float* sums = xp + (size_t)MMAX * p.xs;
-    float* cut_val = sums + (size_t)MMAX * p.nsub;                 // [2][W][MMAX]: row part before / after
-    int* cut_row = reinterpret_cast<int*>(cut_val + 2 * W * MMAX);   // [2][W]
-    uint64_t* full = reinterpret_cast<uint64_t*>(cut_row + 2 * W) + warp * D;   // 8-byte aligned: all sizes even
+    float* cut_val = sums + (size_t)MMAX * p.nsub;                                // [2][W][8][MMAX]
+    int* cut_grp = reinterpret_cast<int*>(cut_val + 2 * W * kGroupRows * MMAX);   // [2][W]
+    uint64_t* full = reinterpret_cast<uint64_t*>(cut_grp + 2 * W) + warp * D;     // 8-byte aligned: all sizes even
 
     if (lane == 0) {
         for (int i = 0; i < D; ++i) mbar_init(&full[i], 1);
@@ -201,24 +226,33 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     __syncwarp();
     pdl_launch_dependents();
 
-    // ---- copy cursor of this warp: its tiles of every stage, in order
-    int cs = -1, cj = 0, cn = 0, cws = 0, cwe = 0;   // stage, next tile, tiles in stage, range
+    // ---- copy cursor of this warp: its tiles of every stage, in order, one
+    // copy per (group, up to NSB consecutive SBs)
+    int cs = -1, ct = 0, ct1 = 0;   // stage, next tile, end of the run
+    Groups cg{};
     int issued = 0, consumed = 0;
-    auto refill = [&]() {   // keep up to D tiles in flight or resident
+    auto refill = [&]() {   // keep up to D copies in flight or resident
         while (issued - consumed < D) {
-            while (cj == cn && cs < p.nstages) {   // next stage in which this warp has tiles
+            while (ct == ct1 && cs < p.nstages) {   // next stage in which this warp has tiles
                 if (++cs == p.nstages) break;
                 const StageDesc* sd = p.table ? p.table + cs : &inl;
-                warp_range(sd, blockIdx.x, gridDim.x, warp, W, cws, cwe);
-                cj = 0;
-                cn = (cwe - cws + kLanes - 1) / kLanes;
+                cg = cta_groups(sd, blockIdx.x, gridDim.x);
+                warp_run(cg, sd->units, warp, W, ct, ct1);
             }
             if (cs >= p.nstages) break;
             const StageDesc* sd = p.table ? p.table + cs : &inl;
-            const int a = cws + cj * kLanes, b = min(a + kLanes, cwe);
+            const int U = sd->units;
+            const int gi = ct / U, u = ct - gi * U;
+            const int nv = min(min(B::kNsb, U - u), ct1 - ct);
             const int slot = issued % D;
-            if (lane == 0) issue_tile<Q4K>(sd, a, b, ring + (size_t)slot * B::kTile, &full[slot]);
-            ++cj;
+            if (lane == 0) {
+                int seg, row, nrows;
+                group_at(sd, cg, gi, seg, row, nrows);
+                fence_proxy_async_smem();   // this warp's reads of the buffer come before the copy's writes
+                mbar_arrive_expect_tx(&full[slot], B::kCopy);
+                tma_load_2d(ring + (size_t)slot * B::kTile, &sd->maps[seg], &full[slot], u * B::kElems, row);
+            }
+            ct += nv;
             ++issued;
         }
     };
@@ -236,146 +270,149 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         const int cols = sd->cols, U = sd->units;
         const int xs = p.xs, nsub = p.nsub;
 
-        // ---- x' and the 32-column sums of this stage, interleaved over column
-        // blocks: float4 group q of block u at index q*U + u.  x may have been
-        // written by other CTAs: read it from L2.
+        // ---- x' and the 32-column sums of this stage: 272 floats per SB (Q4_K:
+        // four chunks of 64 in the q4k_xslot order, each padded by 4; Q8_0: one
+        // float per byte position of the period).  x may have been written by
+        // other CTAs: read it from L2.
         {
+            // every load of a batch is issued before any is used: one L2 round
+            // trip per 32 values a thread (one batch up to 32 * 32 * W values)
+            constexpr int kBatch = 32;
             const int nx = p.M * cols;
-            for (int k0 = warp * 32; k0 < nx; k0 += kThreads * 4) {
-                float v[4];
+            for (int k0 = warp * 32; k0 < nx; k0 += kThreads * kBatch) {
+                float v[kBatch];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < kBatch; ++i) {
                     const int k = k0 + i * kThreads + lane;
                     v[i] = k < nx ? __ldcg(sd->x + k) : 0.0f;
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < kBatch; ++i) {
                     const int kb = k0 + i * kThreads;   // warp-uniform: one 32-column block of x
                     if (kb >= nx) break;
                     const int m = kb / cols, kc = kb - m * cols + lane;
                     const int u = kc >> 8, kk = kc & 255;
                     const float sum = warp_sum(v[i]);
-                    float* xm = xp + (size_t)m * xs;
+                    float* xm = xp + (size_t)m * xs + u * 272;
                     if (Q4K) {
-                        const int slot = q4k_xslot(kk);
-                        xm[((slot >> 2) * U + u) * 4 + (slot & 3)] = v[i] * q4k_xscale(kk);
-                        if (lane == 0) sums[m * nsub + (kk >> 5) * U + u] = sum;
+                        xm[(kk >> 6) * 68 + (q4k_xslot(kk) & 63)] = v[i] * q4k_xscale(kk);
+                        if (lane == 0) sums[m * nsub + u * 8 + (kk >> 5)] = sum;
                     } else {
                         const int pos = 34 * (kk >> 5) + 2 + (kk & 31);   // byte position in the period
-                        xm[((pos >> 2) * U + u) * 4 + (pos & 3)] = v[i] * q8_xscale(pos);
-                        if (lane == 0) sums[m * nsub + (kk >> 5) * U + u] = 128.0f * sum;
+                        xm[pos] = v[i] * q8_xscale(pos);
+                        if (lane == 0) sums[m * nsub + u * 8 + (kk >> 5)] = 128.0f * sum;
                     }
                 }
             }
         }
-        if (tid < 2 * W) cut_row[tid] = -1;
+        if (tid < 2 * W) cut_grp[tid] = -1;
         __syncthreads();
 
-        // ---- this warp's SBs
-        int ws, we;
-        warp_range(sd, blockIdx.x, gridDim.x, warp, W, ws, we);
-        int g_open = -1;          // row continued from the previous tile (warp-uniform)
-        float acc_open[MMAX];
+        // ---- this warp's tiles
+        const Groups G = cta_groups(sd, blockIdx.x, gridDim.x);
+        int t0, t1;
+        warp_run(G, U, warp, W, t0, t1);
+        float acc[MMAX];
 #pragma unroll
-        for (int m = 0; m < MMAX; ++m) acc_open[m] = 0.0f;
-        for (int a = ws; a < we; a += kLanes) {
-            const int b = min(a + kLanes, we);
+        for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
+        int cur = -1;   // group being accumulated
+
+        // finish group gi: add the row's four chunks, then store the 8 rows if
+        // this warp saw all of the group's SBs, else keep this warp's part
+        auto flush = [&](int gi) {
+#pragma unroll
+            for (int m = 0; m < MMAX; ++m) {
+                acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], 1);
+                acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], 2);
+            }
+            const bool started = gi * U >= t0;
+            const bool whole = started && (gi + 1) * U <= t1;
+            if (whole) {
+                int seg, row, nrows;
+                group_at(sd, G, gi, seg, row, nrows);
+                if (c == 0 && r < nrows) {
+                    const int rows = sd->rows[seg];
+                    float* ys = sd->y[seg] + row + r;
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m)
+                        if (m < p.M) ys[(int64_t)m * rows] = acc[m];
+                }
+            } else {
+                // part of a group that started before this run (slot 0) or that
+                // goes on past it (slot 1)
+                const int k = started ? 1 : 0;
+                if (c == 0) {
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m) cut_val[((k * W + warp) * kGroupRows + r) * MMAX + m] = acc[m];
+                }
+                if (lane == 0) cut_grp[k * W + warp] = gi;
+            }
+#pragma unroll
+            for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
+        };
+
+        for (int t = t0; t < t1;) {
+            const int gi = t / U, u = t - gi * U;
+            const int nv = min(min(B::kNsb, U - u), t1 - t);
+            if (gi != cur) {
+                if (cur >= 0) flush(cur);
+                cur = gi;
+            }
             const int slot = consumed % D;
             wait_full(&full[slot], (uint32_t)(consumed / D) & 1u, p.status);
-            const int S = a + lane;
-            const bool valid = S < b;
-            const int g = valid ? S / U : -1;   // row in the stage's numbering
-            const int u = valid ? S - g * U : 0;
-            float v[MMAX];
+            const uint8_t* rowp = ring + (size_t)slot * B::kTile + r * B::kRow;
 #pragma unroll
-            for (int m = 0; m < MMAX; ++m) v[m] = 0.0f;
-            if (valid) {
-                const uint8_t* blk = ring + (size_t)slot * B::kTile + lane * B::kBytes;
-                if constexpr (Q4K) {
-                    float r1[1][MMAX];
+            for (int j = 0; j < B::kNsb; ++j) {
+                if (j < nv) {
+                    const int uj = u + j;
+                    if constexpr (Q4K) {
+                        float a1[1][MMAX];
 #pragma unroll
-                    for (int m = 0; m < MMAX; ++m) r1[0][m] = 0.0f;
-                    q4k_tile_rows<MMAX, 1>(blk, 0, xp + 4 * u, xs, sums + u, nsub, r1, 4 * U, U);
+                        for (int m = 0; m < MMAX; ++m) a1[0][m] = acc[m];
+                        q4k_chunk_rows<MMAX, 1>(rowp + j * B::kBytes, 0, c, xp + uj * 272, xs, sums + uj * 8, nsub,
+                                                a1, 4, 1, 68);
 #pragma unroll
-                    for (int m = 0; m < MMAX; ++m) v[m] = r1[0][m];
-                } else {
-                    q8_tile_row<MMAX>(blk, xp + 4 * u, xs, sums + u, nsub, v, 4 * U, U);
+                        for (int m = 0; m < MMAX; ++m) acc[m] = a1[0][m];
+                    } else {
+                        q8_chunk<MMAX>(rowp + j * B::kBytes + 68 * c, xp + uj * 272 + 68 * c, xs,
+                                       sums + uj * 8 + 2 * c, nsub, acc);
+                    }
                 }
             }
             __syncwarp();   // every lane is done with the buffer
             ++consumed;
             refill();
-
-            // segmented sum over lanes of the same row: afterwards the first lane
-            // of each row's run holds the run's total
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int go = __shfl_down_sync(0xffffffffu, g, off);
-#pragma unroll
-                for (int m = 0; m < MMAX; ++m) {
-                    const float t = __shfl_down_sync(0xffffffffu, v[m], off);
-                    if (lane + off < 32 && go == g) v[m] += t;
-                }
-            }
-            const int gp = __shfl_up_sync(0xffffffffu, g, 1);
-            const bool head = valid && (lane == 0 || gp != g);
-            if (head && g == g_open) {
-#pragma unroll
-                for (int m = 0; m < MMAX; ++m) v[m] += acc_open[m];
-            }
-            const bool ends = (g + 1) * U <= b;   // the row's last SB is in this tile
-            const bool started = g * U >= ws;      // the row's first SB is in this warp's range
-            // the tile's last run may continue into the next tile of this warp
-            const unsigned heads = __ballot_sync(0xffffffffu, head);
-            const int last = 31 - __clz(heads);
-            const bool cont = head && lane == last && !ends && b < we;
-            if (head && !cont) {
-                if (ends && started) {
-                    const int sg = seg_of_row(sd, g);
-                    const int r = g - sd->row0[sg], rows = sd->rows[sg];
-                    float* ys = sd->y[sg];
-#pragma unroll
-                    for (int m = 0; m < MMAX; ++m)
-                        if (m < p.M) ys[(int64_t)m * rows + r] = v[m];
-                } else {
-                    // cut by the warp range: part of a row that started before it
-                    // (slot 0) or that goes on past it (slot 1)
-                    const int k = started ? 1 : 0;
-#pragma unroll
-                    for (int m = 0; m < MMAX; ++m) cut_val[(k * W + warp) * MMAX + m] = v[m];
-                    cut_row[k * W + warp] = g;
-                }
-            }
-            const bool any_cont = __shfl_sync(0xffffffffu, cont, last);
-            g_open = any_cont ? __shfl_sync(0xffffffffu, g, last) : -1;
-#pragma unroll
-            for (int m = 0; m < MMAX; ++m) acc_open[m] = __shfl_sync(0xffffffffu, v[m], last);
+            t += nv;
         }
+        if (cur >= 0) flush(cur);
         __syncthreads();
 
-        // ---- rows cut between warps: the warp where the row starts adds the
-        // later warps' parts in order and stores it
-        if (lane == 0 && cut_row[W + warp] >= 0) {
-            const int g = cut_row[W + warp];
-            float t[MMAX];
+        // ---- groups cut between warps: the warp where the group starts adds the
+        // later warps' parts in order and stores it (lane r: row r)
+        if (cut_grp[W + warp] >= 0 && lane < kGroupRows) {
+            const int gi = cut_grp[W + warp];
+            float tsum[MMAX];
 #pragma unroll
-            for (int m = 0; m < MMAX; ++m) t[m] = cut_val[(W + warp) * MMAX + m];
-            // the row goes on in the next warps that have SBs (warps with an empty
-            // range are skipped) while their part of a started row is this row
+            for (int m = 0; m < MMAX; ++m) tsum[m] = cut_val[((W + warp) * kGroupRows + lane) * MMAX + m];
+            // the group goes on in the next warps that have tiles (warps with an
+            // empty run are skipped) while their part of a started group is this one
             for (int w2 = warp + 1; w2 < W; ++w2) {
-                int ws2, we2;
-                warp_range(sd, blockIdx.x, gridDim.x, w2, W, ws2, we2);
-                if (ws2 == we2) continue;
-                if (cut_row[w2] != g) break;
+                int a2, b2;
+                warp_run(G, U, w2, W, a2, b2);
+                if (a2 == b2) continue;
+                if (cut_grp[w2] != gi) break;
 #pragma unroll
-                for (int m = 0; m < MMAX; ++m) t[m] += cut_val[w2 * MMAX + m];
+                for (int m = 0; m < MMAX; ++m) tsum[m] += cut_val[(w2 * kGroupRows + lane) * MMAX + m];
             }
-            const int sg = seg_of_row(sd, g);
-            const int r = g - sd->row0[sg], rows = sd->rows[sg];
-            float* ys = sd->y[sg];
+            int seg, row, nrows;
+            group_at(sd, G, gi, seg, row, nrows);
+            if (lane < nrows) {
+                const int rows = sd->rows[seg];
+                float* ys = sd->y[seg] + row + lane;
 #pragma unroll
-            for (int m = 0; m < MMAX; ++m)
-                if (m < p.M) ys[(int64_t)m * rows + r] = t[m];
+                for (int m = 0; m < MMAX; ++m)
+                    if (m < p.M) ys[(int64_t)m * rows] = tsum[m];
+            }
         }
 
         // ---- stage s done in this CTA: publish it (the CTA barrier orders every
@@ -416,31 +453,67 @@ int warps_of(bool q4k, int mmax) {
         return (w == 8 || w == 12 || w == 16) ? w : 0;
     }();
     if (env && mmax == 1) return env;
-    if (!q4k) return 8;
+    (void)q4k;
     return mmax == 4 ? 8 : 16;
 }
+
+constexpr int kMaxRing = 8;
+
+size_t tile_bytes(bool q4k) { return q4k ? (size_t)Blk<true>::kTile : (size_t)Blk<false>::kTile; }
 
 size_t rows_smem(bool q4k, int mmax, int ring, int64_t cols_max) {
     const int W = warps_of(q4k, mmax);
     const int64_t U = cols_max / 256;
-    const size_t tile = (size_t)kLanes * (q4k ? 144 : 272);
-    const size_t xs = (size_t)(q4k ? U * 256 : U * 272);
-    const size_t cut = (size_t)2 * W * mmax * 4 + (size_t)2 * W * 4;
-    return (size_t)W * ring * tile + (size_t)mmax * xs * 4 + (size_t)mmax * 8 * U * 4 + cut + (size_t)W * ring * 8;
+    const size_t cut = (size_t)2 * W * kGroupRows * mmax * 4 + (size_t)2 * W * 4;
+    return (size_t)W * ring * tile_bytes(q4k) + (size_t)mmax * U * 272 * 4 + (size_t)mmax * U * 8 * 4 + cut +
+           (size_t)W * ring * 8;
 }
 
 int rows_ring(bool q4k, int mmax, int64_t cols_max) {
-    int ring = 4;
+    int ring = kMaxRing;
     while (ring > 1 && rows_smem(q4k, mmax, ring, cols_max) > kSmemLimit) --ring;
     return rows_smem(q4k, mmax, ring, cols_max) <= kSmemLimit ? ring : 0;
 }
 
-void make_stage(int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x, float* const* y,
-                StageDesc* sd) {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Tensor map of one matrix: rows of `row_bytes` as 8-byte elements, box of
+// 8 rows x (NSB SBs + pad).  Out-of-range parts of a box read as zeros.
+int encode_map(CUtensorMap* map, const void* W, int64_t rows, int64_t row_bytes, bool q4k) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(q4k ? Blk<true>::kRow / 8 : Blk<false>::kRow / 8), (cuuint32_t)kGroupRows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(W), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return GGQ_OK;
+}
+
+int make_stage(int type, int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
+               float* const* y, StageDesc* sd) {
+    const bool q4k = type == GGQ_Q4_K;
     memset(sd, 0, sizeof(*sd));
     int r = 0;
     for (int s = 0; s < n; ++s) {
-        sd->W[s] = static_cast<const uint8_t*>(W[s]);
+        const int64_t row_bytes = cols / 256 * (q4k ? 144 : 272);
+        int rc = encode_map(&sd->maps[s], W[s], rows[s], row_bytes, q4k);
+        if (rc) return rc;
         sd->y[s] = y[s];
         sd->rows[s] = (int)rows[s];
         sd->row0[s] = r;
@@ -451,6 +524,7 @@ void make_stage(int n, const void* const* W, const int64_t* rows, int64_t cols, 
     sd->x = x;
     sd->cols = (int)cols;
     sd->units = (int)(cols / 256);
+    return GGQ_OK;
 }
 
 template <bool Q4K, int MMAX, int W>
@@ -495,7 +569,7 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
     p.M = M;
     p.ring = rows_ring(q4k, mmax, cols_max);
     if (p.ring == 0) return fail(GGQ_EINVAL, "shape needs too much shared memory");
-    p.xs = (int)(q4k ? cols_max : cols_max / 256 * 272);
+    p.xs = (int)(cols_max / 256 * 272);
     p.nsub = (int)(cols_max / 32);
     p.counter = counter;
     p.status = device_status_word();
@@ -512,11 +586,11 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
         return launch_t<true, 4, 8>(inl, p, stream, smem, coop);
     }
     if (mmax == 1) {
+        if (W == 8) return launch_t<false, 1, 8>(inl, p, stream, smem, coop);
         if (W == 12) return launch_t<false, 1, 12>(inl, p, stream, smem, coop);
-        if (W == 16) return launch_t<false, 1, 16>(inl, p, stream, smem, coop);
-        return launch_t<false, 1, 8>(inl, p, stream, smem, coop);
+        return launch_t<false, 1, 16>(inl, p, stream, smem, coop);
     }
-    if (mmax == 2) return launch_t<false, 2, 8>(inl, p, stream, smem, coop);
+    if (mmax == 2) return launch_t<false, 2, 16>(inl, p, stream, smem, coop);
     return launch_t<false, 4, 8>(inl, p, stream, smem, coop);
 }
 
@@ -524,6 +598,8 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
 
 bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_t* rows) {
     if (M > kMaxM || nseg < 1 || nseg > kMaxSeg || cols % 256 || cols > (1 << 20)) return false;
+    // a Q4_K copy box (4 SBs + pad) must not be wider than a row
+    if (type == GGQ_Q4_K && cols < 1280) return false;
     int64_t r = 0;
     for (int s = 0; s < nseg; ++s) r += rows[s];
     if (r * (cols / 256) >= (1ll << 31)) return false;   // SB indices are 32-bit
@@ -533,7 +609,8 @@ bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_
 int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
                        float* const* y, int M, cudaStream_t stream) {
     StageDesc sd;
-    make_stage(nseg, W, rows, cols, x, y, &sd);
+    int rc = make_stage(type, nseg, W, rows, cols, x, y, &sd);
+    if (rc) return rc;
     return launch_rows(type, M, sd, nullptr, 1, cols, nullptr, stream);
 }
 
@@ -581,7 +658,8 @@ extern "C" int ggq_chain_create(int type, int M, int nstages, const ggq_chain_st
         return fail(GGQ_EINVAL, "ggq_chain_create: widest stage needs too much shared memory");
     for (int s = 0; s < nstages; ++s) {   // all stages valid: encode them
         const ggq_chain_stage& st = stages[s];
-        make_stage(st.n, st.W, st.rows, st.cols, st.x, st.y, &host[(size_t)s]);
+        int rc = make_stage(type, st.n, st.W, st.rows, st.cols, st.x, st.y, &host[(size_t)s]);
+        if (rc) return rc;
     }
     ggq_chain* c = new (std::nothrow) ggq_chain();
     if (!c) return fail(GGQ_ENOMEM, "host allocation failed");

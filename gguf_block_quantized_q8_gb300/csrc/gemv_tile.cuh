@@ -85,11 +85,11 @@ __device__ __forceinline__ void f2_fma64(F2& acc, uint64_t a, float b0, float b1
 // Chunk c (weights 64c .. 64c+63, sub-blocks 2c and 2c+1) of R rows of Q4_K
 // super-blocks per lane (rp: the lane's first row, `rstride` bytes to the next
 // of its rows) against x' of that super-block and the per-sub-block sums of x.
-// x' is read as float4 groups: group q (x' slots 4q .. 4q+3 of the q4k_xslot
-// layout) of activation row m at xu + m*xs + q*gs (gs = 4: the 256 values
-// contiguous; gs = 4*U: groups of U super-blocks interleaved so that lanes
-// reading different super-blocks hit different banks).  The sum of sub-block
-// j of activation row m is su[m*ss + j*sj].
+// x' is read as float4 groups: slots 64c + 4q' .. +3 of the q4k_xslot layout
+// (group q' of chunk c) of activation row m at xu + m*xs + c*cs + q'*gs.
+// gs = 4, cs = 64: the 256 values contiguous; cs = 68: each chunk padded by 4
+// floats, so lanes reading different chunks of one super-block hit different
+// banks.  The sum of sub-block j of activation row m is su[m*ss + j*sj].
 // acc[r][m] += sum_{k in chunk c} w_r[k] * x[m][k].
 //
 // Two consecutive qs words are handled as one 64-bit value: AND-ing it with a
@@ -98,7 +98,7 @@ __device__ __forceinline__ void f2_fma64(F2& acc, uint64_t a, float b0, float b1
 template <int MMAX, int R>
 __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, int c, const float* xu, int xs,
                                                const float* su, int ss, float (&acc)[R][MMAX], int gs = 4,
-                                               int sj = 1) {
+                                               int sj = 1, int cs = 64) {
     // nibble masks (both halves): low nibble of bytes 0,1,2 in place, byte 3 after >> 8
     constexpr uint64_t kLo0 = 0x0000000F0000000Full, kLo1 = 0x00000F0000000F00ull, kLo2 = 0x000F0000000F0000ull;
     constexpr uint64_t kHi0 = 0x000000F0000000F0ull, kHi1 = 0x0000F0000000F000ull, kHi2 = 0x00F0000000F00000ull;
@@ -135,7 +135,7 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
         float4 xl[MMAX][2], xh[MMAX][2];
 #pragma unroll
         for (int m = 0; m < MMAX; ++m) {
-            const float* xm = xu + m * xs + (16 * c + 2 * b) * gs;
+            const float* xm = xu + m * xs + c * cs + 2 * b * gs;
             xl[m][0] = *reinterpret_cast<const float4*>(xm);
             xl[m][1] = *reinterpret_cast<const float4*>(xm + gs);
             xh[m][0] = *reinterpret_cast<const float4*>(xm + 8 * gs);
@@ -182,9 +182,9 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
 template <int MMAX, int R>
 __device__ __forceinline__ void q4k_tile_rows(const uint8_t* rp, int rstride, const float* xu, int xs,
                                               const float* su, int ss, float (&acc)[R][MMAX], int gs = 4,
-                                              int sj = 1) {
+                                              int sj = 1, int cs = 64) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) q4k_chunk_rows<MMAX, R>(rp, rstride, c, xu, xs, su, ss, acc, gs, sj);
+    for (int c = 0; c < 4; ++c) q4k_chunk_rows<MMAX, R>(rp, rstride, c, xu, xs, su, ss, acc, gs, sj, cs);
 }
 
 // One row (R = 1) of the above.
@@ -243,6 +243,52 @@ __device__ __forceinline__ void q8_tile_row(const uint8_t* rp, const float* xu, 
                             acc[m] = fmaf(dcur, fmaf(pa[m] + pb[m], kTwo96, -su[m * ss + b * sj]), acc[m]);
                             pa[m] = pb[m] = 0.0f;
                         }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// One quarter of a Q8_0 period: blocks 2c and 2c+1 (rp: their 68 bytes, 4-byte
+// aligned) against x' of those byte positions (xu: 68 floats per activation
+// row, 16-byte aligned, rows `xs` apart) and 128 * sum(x) of the two blocks
+// (su[m*ss + 0 / 1]).  acc[m] += the 64 products.
+template <int MMAX>
+__device__ __forceinline__ void q8_chunk(const uint8_t* rp, const float* xu, int xs, const float* su, int ss,
+                                         float (&acc)[MMAX]) {
+    float pa[MMAX], pb[MMAX];
+    float dcur = 0.0f;
+#pragma unroll
+    for (int m = 0; m < MMAX; ++m) pa[m] = pb[m] = 0.0f;
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rp);
+#pragma unroll
+    for (int wi = 0; wi < 17; ++wi) {
+        const uint32_t w = wp[wi];
+        float4 xv[MMAX];
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) xv[m] = *reinterpret_cast<const float4*>(xu + m * xs + 4 * wi);
+#pragma unroll
+        for (int pos = 0; pos < 4; ++pos) {
+            const int B = 4 * wi + pos;
+            const int b = B / 34, o = B % 34;
+            if (o == 0) {
+                dcur = half_bits_to_float(w >> (8 * pos));
+            } else if (o >= 2) {
+                const uint32_t pat = pos < 3 ? ((w ^ 0x80808080u) & (0xFFu << (8 * pos)))
+                                             : (((w >> 8) ^ 0x00800000u) & 0x00FF0000u);
+                const float fw = __uint_as_float(pat);
+#pragma unroll
+                for (int m = 0; m < MMAX; ++m) {
+                    const float xsv = pos == 0 ? xv[m].x : pos == 1 ? xv[m].y : pos == 2 ? xv[m].z : xv[m].w;
+                    if (pos & 1) pb[m] = fmaf(fw, xsv, pb[m]);
+                    else pa[m] = fmaf(fw, xsv, pa[m]);
+                }
+                if (o == 33) {
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m) {
+                        acc[m] = fmaf(dcur, fmaf(pa[m] + pb[m], kTwo96, -su[m * ss + b]), acc[m]);
+                        pa[m] = pb[m] = 0.0f;
                     }
                 }
             }

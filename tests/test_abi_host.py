@@ -178,7 +178,7 @@ def test_compute_entry_points_validate_arguments(ggq):
 
 def test_chain_create_validates_stages(ggq):
     """ggq_chain_create rejects malformed stages before touching the device."""
-    ok = ([16], [64], 256, 16, [16])
+    ok = ([16], [64], 2048, 16, [16])
     assert ggq.ggq_chain_create(ggq.F32, 1, [ok])[0] == -2                          # type
     assert ggq.ggq_chain_create(ggq.Q4_K, 0, [ok])[0] == -1                         # M = 0
     assert ggq.ggq_chain_create(ggq.Q4_K, 5, [ok])[0] == -1                         # M = 5

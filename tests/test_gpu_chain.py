@@ -92,10 +92,10 @@ def _layer(prefix, hidden, kv, ffn, src):
 @pytest.mark.parametrize("qtype,M", [(12, 1), (12, 2), (12, 3), (8, 1), (8, 4)])
 def test_chain_two_layers(env, qtype, M):
     """Two small layers: every stage after the first reads the previous stage's y."""
-    stages = _layer("a.", 1024, 256, 2816, "x0") + _layer("b.", 1024, 256, 2816, "a.down")
+    stages = _layer("a.", 1280, 256, 2816, "x0") + _layer("b.", 1280, 256, 2816, "a.down")
     net = Net(env, qtype, M, stages)
     for run in range(2):
-        x0 = synth.normal_f32(M * 1024, 40 + run).reshape(M, 1024)
+        x0 = synth.normal_f32(M * 1280, 40 + run).reshape(M, 1280)
         net.check(x0, net.run(x0))
 
 
@@ -128,13 +128,13 @@ def test_chain_uneven_stages(env):
     """Stages far smaller than the grid (a few tiles) next to large ones, and
     ragged row counts that end inside a row block."""
     stages = [
-        [("s0", 512, 256, "x0"), ("t0", 33, 256, "x0")],
-        [("s1", 4099, 512, "s0"), ("s2", 1, 512, "s0"), ("s3", 65, 512, "s0")],
-        [("s4", 256, 512, "s0")],                  # reads the output of two stages back
-        [("s5", 70000, 256, "s4")],
+        [("s0", 1280, 1280, "x0"), ("t0", 33, 1280, "x0")],
+        [("s1", 4099, 1280, "s0"), ("s2", 1, 1280, "s0"), ("s3", 65, 1280, "s0")],
+        [("s4", 1536, 1280, "s0")],                 # reads the output of two stages back
+        [("s5", 70000, 1536, "s4")],
     ]
     net = Net(env, 12, 1, stages, seed=2)
-    x0 = synth.normal_f32(256, 70).reshape(1, 256)
+    x0 = synth.normal_f32(1280, 70).reshape(1, 1280)
     net.check(x0, net.run(x0))
 
 
@@ -148,9 +148,9 @@ def test_chain_llama8b_layers(env):
 
 def test_chain_in_cuda_graph(env):
     torch, ggq = env
-    stages = _layer("a.", 1024, 256, 2816, "x0")
+    stages = _layer("a.", 1280, 256, 2816, "x0")
     net = Net(env, 12, 1, stages, seed=4)
-    x0 = synth.normal_f32(1024, 90).reshape(1, 1024)
+    x0 = synth.normal_f32(1280, 90).reshape(1, 1280)
     net.run(x0)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -161,7 +161,7 @@ def test_chain_in_cuda_graph(env):
         with torch.cuda.graph(g, stream=s):
             net.chain.run(s)
     torch.cuda.synchronize()
-    x1 = synth.normal_f32(1024, 91).reshape(1, 1024)
+    x1 = synth.normal_f32(1280, 91).reshape(1, 1280)
     net.x0.copy_(torch.from_numpy(x1))
     for y in net.y.values():
         y.fill_(float("nan"))

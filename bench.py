@@ -383,6 +383,27 @@ def extras(torch, ggq, synth, stream):
     return out
 
 
+def roofline_traffic(bytes_per_launch: int):
+    """DRAM traffic per launch of the dominant kernel from the committed ncu
+    capture (profiles/roofline_traffic.json), scaled to the full launch by the
+    bytes it streams; None if the kernel sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        h = hashlib.sha256()
+        for src in t["kernel_sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != t["kernel_sources_sha256_16"]:
+            return None
+        captured = t["dram_bytes_read"] + t["dram_bytes_write"]
+        return int(captured * bytes_per_launch / t["captured_algorithmic_bytes"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -396,26 +417,33 @@ def measured_peaks():
 # ------------------------------------------------------------------- main ----
 
 def run_reference(a, ws, rank):
+    """The reference arm: the CPU oracle as it stands, on the bench workload.
+    K timed steps after W warm-up steps, each step a bounded sample of the
+    pass (whole rows of every tensor in turn) sized so the whole run stays
+    within about two minutes.  Under torchrun only rank 0 runs and prints."""
     if rank != 0:
         return 0
     import multiprocessing
-    steps = max(1, a.steps // 100) if a.steps > 3 else a.steps
-    per = max(2.0, min(a.cpu_seconds, 120.0 / (steps + a.warmup)))
-    for _ in range(min(a.warmup, 1)):
-        cpu_oracle_sample(min(per, 2.0), a.layers)
-    vals = []
+    steps = max(1, a.steps)
+    per = max(0.05, min(a.cpu_seconds, 120.0 / (steps + a.warmup)))
+    for _ in range(a.warmup):
+        cpu_oracle_sample(per, a.layers)
+    vals, walls = [], []
     desc = ""
     for _ in range(steps):
+        t0 = time.perf_counter()
         v, desc, _ = cpu_oracle_sample(per, a.layers)
+        walls.append(time.perf_counter() - t0)
         vals.append(v)
     value = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
-        "n_gpus": a.gpus, "steps": steps, "warmup": a.warmup, "ms_per_step": None,
+        "n_gpus": a.gpus, "steps": steps, "warmup": a.warmup,
+        "ms_per_step": round(1e3 * statistics.median(walls), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "layers": a.layers, "sampled": True},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": desc, "host_cpus": multiprocessing.cpu_count()},
+                         "sample": f"per step: {desc}", "host_cpus": multiprocessing.cpu_count()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -542,8 +570,8 @@ def main():
                 "ms_per_step": round(ms_e2e, 4)},
         "gpu_launches": dp.launches * a.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                     "kernel": f"chain_kernel<Q4_K, M=1> over {len(dp.q4)} stages",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": roofline_traffic(int(per_launch_bytes)),
+                     "kernel": f"rows_kernel<Q4_K, M=1, 16 warps> (one ggq_chain_run over {len(dp.q4)} stages)",
                      "peak_kind": f"{peak_kind} (copy, burst)",
                      "bytes_per_launch": int(per_launch_bytes), "us_per_launch": round(per_launch_s * 1e6, 3),
                      "timing": "one chain launch per CUDA-graph replay, events on its stream"},

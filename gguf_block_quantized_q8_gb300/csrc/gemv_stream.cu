@@ -12,13 +12,14 @@
 //
 //   * CTA b (one per SM) owns rows [R*b/G, R*(b+1)/G): whole rows, so no output
 //     is ever split between CTAs and no cross-CTA reduction exists.
-//   * Its rows form groups of 8 (inside one matrix); the (group, SB) tiles are
+//   * Its rows form groups of 16 (inside one matrix); the (group, SB) tiles are
 //     cut into W equal contiguous runs, one per warp.  A warp streams its run
-//     through its own ring of 2-D bulk tensor copies (8 rows x up to NSB SBs);
+//     through its own ring of 2-D bulk tensor copies (16 rows x up to NSB SBs);
 //     weights do not depend on earlier stages, so the ring runs ahead into the
 //     next stages while the chain waits at a stage boundary.
-//   * Lane (r, c) = (lane / 4, lane % 4) decodes chunk c of row r of each SB in
-//     registers against x', the pre-scaled activations.  The 8 lanes of one
+//   * Lane (r, c) = (lane / 4, lane % 4) decodes chunk c of rows r and r + 8 of
+//     each SB in registers against x', the pre-scaled activations (each x' value
+//     loaded once for both rows).  The 8 lanes of one
 //     chunk read the same x' address (a broadcast), and chunks are padded so
 //     that the four addresses of one load sit in different banks.  Two
 //     shuffles add a row's chunks; a group that a warp sees over all its SBs is
@@ -52,11 +53,12 @@ constexpr int kMaxSeg = 4;
 constexpr int kMaxM = 4;
 constexpr size_t kSmemLimit = 227 * 1024;
 
-constexpr int kGroupRows = 8;
+constexpr int kRowsPerLane = 2;                 // rows r and r + 8 of a group
+constexpr int kGroupRows = 8 * kRowsPerLane;
 
 // One stage of a chain (device-visible: kernel parameter or global table).
 struct StageDesc {
-    CUtensorMap maps[kMaxSeg];  // per matrix: 8-byte elements, box of 8 rows x (NSB SBs + pad)
+    CUtensorMap maps[kMaxSeg];  // per matrix: 8-byte elements, box of 16 rows x (NSB SBs + pad)
     float* y[kMaxSeg];          // [M][rows]
     const float* x;             // [M][cols]
     int rows[kMaxSeg];
@@ -77,14 +79,14 @@ struct ChainParams {
     int* status;
 };
 
-// Tile of one bulk tensor copy: 8 rows x NSB SBs, each row padded so that
+// Tile of one bulk tensor copy: 16 rows x NSB SBs, each row padded so that
 // rows r and r+1 of one chunk fall in different banks.  Copies of a few KB:
 // much smaller ones cost more per copy than the bytes they bring.
 template <bool Q4K>
 struct Blk {
     static constexpr int kBytes = Q4K ? 144 : 272;      // one SB
     static constexpr int kElems = kBytes / 8;            // 8-byte elements per SB
-    static constexpr int kNsb = Q4K ? 4 : 1;             // SBs per copy
+    static constexpr int kNsb = Q4K ? 2 : 1;             // SBs per copy
     static constexpr int kPad = Q4K ? 2 : 0;             // elements of padding per row
     static constexpr int kRow = (kElems * kNsb + kPad) * 8;    // smem bytes per row: 304 / 272
     static constexpr int kCopy = kGroupRows * kRow;            // bytes per copy
@@ -158,7 +160,7 @@ __device__ __forceinline__ void wait_full(uint64_t* bar, uint32_t parity, int* s
 }
 
 // Row groups of CTA b (of nb) in a stage: its rows [r0, r1) cut at matrix
-// boundaries, then into groups of up to 8 rows.
+// boundaries, then into groups of up to 16 rows.
 struct Groups {
     int r0, r1;
     int n;                 // groups
@@ -312,30 +314,39 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         const Groups G = cta_groups(sd, blockIdx.x, gridDim.x);
         int t0, t1;
         warp_run(G, U, warp, W, t0, t1);
-        float acc[MMAX];
+        constexpr int R = kRowsPerLane;
+        float acc[R][MMAX];   // rows r + 8i of the group
 #pragma unroll
-        for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int m = 0; m < MMAX; ++m) acc[i][m] = 0.0f;
         int cur = -1;   // group being accumulated
 
-        // finish group gi: add the row's four chunks, then store the 8 rows if
-        // this warp saw all of the group's SBs, else keep this warp's part
+        // finish group gi: add each row's four chunks, then store the group's
+        // rows if this warp saw all of its SBs, else keep this warp's part
         auto flush = [&](int gi) {
 #pragma unroll
-            for (int m = 0; m < MMAX; ++m) {
-                acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], 1);
-                acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], 2);
-            }
+            for (int i = 0; i < R; ++i)
+#pragma unroll
+                for (int m = 0; m < MMAX; ++m) {
+                    acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], 1);
+                    acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], 2);
+                }
             const bool started = gi * U >= t0;
             const bool whole = started && (gi + 1) * U <= t1;
             if (whole) {
                 int seg, row, nrows;
                 group_at(sd, G, gi, seg, row, nrows);
-                if (c == 0 && r < nrows) {
+                if (c == 0) {
                     const int rows = sd->rows[seg];
-                    float* ys = sd->y[seg] + row + r;
 #pragma unroll
-                    for (int m = 0; m < MMAX; ++m)
-                        if (m < p.M) ys[(int64_t)m * rows] = acc[m];
+                    for (int i = 0; i < R; ++i)
+                        if (r + 8 * i < nrows) {
+                            float* ys = sd->y[seg] + row + r + 8 * i;
+#pragma unroll
+                            for (int m = 0; m < MMAX; ++m)
+                                if (m < p.M) ys[(int64_t)m * rows] = acc[i][m];
+                        }
                 }
             } else {
                 // part of a group that started before this run (slot 0) or that
@@ -343,12 +354,17 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 const int k = started ? 1 : 0;
                 if (c == 0) {
 #pragma unroll
-                    for (int m = 0; m < MMAX; ++m) cut_val[((k * W + warp) * kGroupRows + r) * MMAX + m] = acc[m];
+                    for (int i = 0; i < R; ++i)
+#pragma unroll
+                        for (int m = 0; m < MMAX; ++m)
+                            cut_val[((k * W + warp) * kGroupRows + r + 8 * i) * MMAX + m] = acc[i][m];
                 }
                 if (lane == 0) cut_grp[k * W + warp] = gi;
             }
 #pragma unroll
-            for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
+            for (int i = 0; i < R; ++i)
+#pragma unroll
+                for (int m = 0; m < MMAX; ++m) acc[i][m] = 0.0f;
         };
 
         for (int t = t0; t < t1;) {
@@ -366,16 +382,13 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 if (j < nv) {
                     const int uj = u + j;
                     if constexpr (Q4K) {
-                        float a1[1][MMAX];
-#pragma unroll
-                        for (int m = 0; m < MMAX; ++m) a1[0][m] = acc[m];
-                        q4k_chunk_rows<MMAX, 1>(rowp + j * B::kBytes, 0, c, xp + uj * 272, xs, sums + uj * 8, nsub,
-                                                a1, 4, 1, 68);
-#pragma unroll
-                        for (int m = 0; m < MMAX; ++m) acc[m] = a1[0][m];
+                        q4k_chunk_rows<MMAX, R>(rowp + j * B::kBytes, 8 * B::kRow, c, xp + uj * 272, xs,
+                                                sums + uj * 8, nsub, acc, 4, 1, 68);
                     } else {
-                        q8_chunk<MMAX>(rowp + j * B::kBytes + 68 * c, xp + uj * 272 + 68 * c, xs,
-                                       sums + uj * 8 + 2 * c, nsub, acc);
+#pragma unroll
+                        for (int i = 0; i < R; ++i)
+                            q8_chunk<MMAX>(rowp + 8 * i * B::kRow + j * B::kBytes + 68 * c, xp + uj * 272 + 68 * c,
+                                           xs, sums + uj * 8 + 2 * c, nsub, acc[i]);
                     }
                 }
             }
@@ -490,7 +503,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Tensor map of one matrix: rows of `row_bytes` as 8-byte elements, box of
-// 8 rows x (NSB SBs + pad).  Out-of-range parts of a box read as zeros.
+// 16 rows x (NSB SBs + pad).  Out-of-range parts of a box read as zeros.
 int encode_map(CUtensorMap* map, const void* W, int64_t rows, int64_t row_bytes, bool q4k) {
     auto fn = tensor_map_encoder();
     if (!fn) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled unavailable");
@@ -598,8 +611,8 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
 
 bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_t* rows) {
     if (M > kMaxM || nseg < 1 || nseg > kMaxSeg || cols % 256 || cols > (1 << 20)) return false;
-    // a Q4_K copy box (4 SBs + pad) must not be wider than a row
-    if (type == GGQ_Q4_K && cols < 1280) return false;
+    // a Q4_K copy box (2 SBs + pad) must not be wider than a row
+    if (type == GGQ_Q4_K && cols < 768) return false;
     int64_t r = 0;
     for (int s = 0; s < nseg; ++s) r += rows[s];
     if (r * (cols / 256) >= (1ll << 31)) return false;   // SB indices are 32-bit

@@ -277,32 +277,45 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         // float per byte position of the period).  x may have been written by
         // other CTAs: read it from L2.
         {
-            // every load of a batch is issued before any is used: one L2 round
-            // trip per 32 values a thread (one batch up to 32 * 32 * W values)
-            constexpr int kBatch = 32;
-            const int nx = p.M * cols;
-            for (int k0 = warp * 32; k0 < nx; k0 += kThreads * kBatch) {
-                float v[kBatch];
+            // Lane l of a warp step takes 4 consecutive values (one float4) of x:
+            // 8 lanes cover a 32-column sub-block, whose sum takes 3 shuffles.
+            // Every load of a batch is issued before any is used (one L2 round
+            // trip per batch of kBatch float4 per lane).
+            constexpr int kBatch = 8;
+            const int n4 = p.M * cols / 4;   // float4 of x (cols % 256 == 0)
+            const float4* x4 = reinterpret_cast<const float4*>(sd->x);
+            const int a = lane & 7;          // float4 index inside the sub-block
+            for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                float4 v[kBatch];
 #pragma unroll
                 for (int i = 0; i < kBatch; ++i) {
-                    const int k = k0 + i * kThreads + lane;
-                    v[i] = k < nx ? __ldcg(sd->x + k) : 0.0f;
+                    const int q = q0 + i * kThreads + lane;
+                    v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int i = 0; i < kBatch; ++i) {
-                    const int kb = k0 + i * kThreads;   // warp-uniform: one 32-column block of x
-                    if (kb >= nx) break;
-                    const int m = kb / cols, kc = kb - m * cols + lane;
-                    const int u = kc >> 8, kk = kc & 255;
-                    const float sum = warp_sum(v[i]);
+                    const int qb = q0 + i * kThreads;   // warp-uniform: 4 sub-blocks of x
+                    if (qb >= n4) break;
+                    float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                    const int k = 4 * (qb + lane);      // first of the lane's 4 columns
+                    const int m = k / cols, kc = k - m * cols;
+                    const int u = kc >> 8, kk = kc & 255, sb = kk >> 5;
                     float* xm = xp + (size_t)m * xs + u * 272;
+                    const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
                     if (Q4K) {
-                        xm[(kk >> 6) * 68 + (q4k_xslot(kk) & 63)] = v[i] * q4k_xscale(kk);
-                        if (lane == 0) sums[m * nsub + u * 8 + (kk >> 5)] = sum;
+                        // q4k_xslot(kk + b) = (kk & ~31) | (b << 3) | a, chunk padded to 68
+                        float* dst = xm + (kk >> 6) * 68 + (kk & 32) + a;
+#pragma unroll
+                        for (int bb = 0; bb < 4; ++bb) dst[8 * bb] = e[bb] * q4k_xscale(kk + bb);
+                        if (a == 0) sums[m * nsub + u * 8 + sb] = sum;
                     } else {
-                        const int pos = 34 * (kk >> 5) + 2 + (kk & 31);   // byte position in the period
-                        xm[pos] = v[i] * q8_xscale(pos);
-                        if (lane == 0) sums[m * nsub + u * 8 + (kk >> 5)] = 128.0f * sum;
+                        const int pos = 34 * sb + 2 + (kk & 31);   // byte position in the period
+#pragma unroll
+                        for (int bb = 0; bb < 4; ++bb) xm[pos + bb] = e[bb] * q8_xscale(pos + bb);
+                        if (a == 0) sums[m * nsub + u * 8 + sb] = 128.0f * sum;
                     }
                 }
             }

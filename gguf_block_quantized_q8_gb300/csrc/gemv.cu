@@ -432,6 +432,8 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
         cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_q8_simple_kernel, static_cast<const uint8_t*>(W), p);
         return e == cudaSuccess ? GGQ_OK : cuda_fail(e, "gemv launch");
     }
+    if (M >= kSmallMMin && smallm_supported(type, rows, cols, M))
+        return launch_smallm(type, W, rows, cols, x, y, M, stream);
     if (stream_gemv_supported(type, cols, M, 1, &rows)) {
         const void* Ws[1] = {W};
         float* ys[1] = {y};

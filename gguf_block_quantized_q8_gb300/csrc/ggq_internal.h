@@ -52,6 +52,12 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
 bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_t* rows);
 int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* rows, int64_t cols,
                        const float* x, float* const* y, int M, cudaStream_t stream);
+// small-batch dequant-GEMM on the tensor cores (M up to 16, cols % 256 == 0);
+// ggq_gemv uses it from kSmallMMin activation rows on
+constexpr int kSmallMMin = 5;
+bool smallm_supported(int type, int64_t rows, int64_t cols, int M);
+int launch_smallm(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
+                  cudaStream_t stream);
 int launch_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out,
                       cudaStream_t stream);
 int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const uint16_t* X,

@@ -1,0 +1,413 @@
+// Small-batch dequant-GEMM on the tcgen05 tensor cores: Y[M, rows] = X[M, cols] W^T
+// for a few activation rows (M <= 16), W in Q8_0 or Q4_K ("GGUF: The File
+// Format...", "How a Q8_0 block is stored": w = d*q; k-quant paragraph:
+// w = d*sc_j*q - dmin*m_j).  Each decoded block is used for all M rows of X.
+//
+// One CTA computes a 128-row tile of W against all M activation rows
+// (UMMA M = 128 W rows, N = 16 activation rows padded with zeros, K = 16):
+//   warp 0      TMA producer: raw blocks of 128 W rows x 256 columns;
+//   warp 1      allocates 32 TMEM columns; one thread issues the MMAs and
+//               commits each stage back to its "empty" barrier;
+//   warps 2..17 decoders: four threads a W row, 16 columns each per 64-column
+//               stage (packed f32x2 arithmetic).  A weight is decoded exactly in fp32 and split into two
+//               bf16 parts, hi = bf16(w) and lo = bf16(w - hi); X is split the
+//               same way.  Three MMAs per 16 columns (hi*hi + hi*lo + lo*hi)
+//               keep each product to ~2^-16 relative with fp32 accumulation,
+//               and every operand keeps the fp32 exponent range.
+//   epilogue    warps 2..5 read the 128 x 16 accumulator (tcgen05.ld; a warp
+//               reaches only its own quarter of the 128 TMEM lanes) and store Y.
+// Every wait is bounded (ptx.cuh: mbar_wait); a timeout is recorded in the device
+// status word and the kernel runs to completion without the data.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ggq_internal.h"
+#include "ptx.cuh"
+
+namespace ggq {
+
+namespace {
+
+constexpr int kTileRows = 128;   // UMMA M (W rows)
+constexpr int kN = 16;           // UMMA N (activation rows, zero padded)
+constexpr int kKStage = 64;      // columns per stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kRawStages = 2;
+constexpr int kDecoders = 512;
+constexpr int kThreads = 64 + kDecoders;
+constexpr int kTmemCols = 32;
+
+constexpr int kAPiece = kTileRows * kKStage * 2;   // 16 KB: one bf16 part of a W tile
+constexpr int kBPiece = kN * kKStage * 2;          // 2 KB: one bf16 part of an X tile
+constexpr int kStageBytes = 2 * kAPiece + 2 * kBPiece;   // [A hi][A lo][B hi][B lo], 1024-aligned parts
+constexpr int kRawMax = kTileRows * 272;                  // Q8_0: 8 blocks a row; Q4_K uses 144 of it
+
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kRawStages * kRawMax + 1024 + 256;
+
+struct SmallParams {
+    const float* x;   // [M, cols]
+    float* y;         // [M, rows]
+    int rows;
+    int cols;
+    int M;
+    int* status;
+};
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 x bf16 -> fp32
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// K-major, 128-byte swizzle: 8-row groups 1024 B apart, descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// kind::f16: D fp32, A and B bf16, both K-major, N = 16, M = 128.
+constexpr uint32_t kIdesc =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kTileRows >> 4) << 24);
+
+// w -> bf16 pairs hi = bf16(w), lo = bf16(w - hi) (w - hi is exact in fp32)
+__device__ __forceinline__ void split_bf16x2(float2 w, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(w);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __float22bfloat162_rn(__ffma2_rn(hf, make_float2(-1.0f, -1.0f), w));
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// 6-bit scale and min of sub-block j from the 12 packed bytes (three words)
+__device__ __forceinline__ void q4k_sm(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc, int& m) {
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63;
+        m = (s1 >> (8 * j)) & 63;
+    } else {
+        const int k = j - 4;
+        sc = ((s2 >> (8 * k)) & 15) | (((s0 >> (8 * k + 6)) & 3) << 4);
+        m = ((s2 >> (8 * k + 4)) & 15) | (((s1 >> (8 * k + 6)) & 3) << 4);
+    }
+}
+
+template <bool Q4K>
+__global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                             const SmallParams p) {
+    constexpr int kRowBytes = Q4K ? 144 : 272;   // raw bytes of one W row per 256 columns
+    constexpr int kRawBytes = kTileRows * kRowBytes;
+    extern __shared__ uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = blockIdx.x * kTileRows;
+    const int nsb = p.cols / 256;
+    const int nks = nsb * 4;
+
+    const uint32_t base_u32 = smem_u32(smem_raw);
+    uint8_t* base = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
+    uint8_t* sStage = base;                                          // kStages x [A hi][A lo][B hi][B lo]
+    uint8_t* sRaw = sStage + (size_t)kStages * kStageBytes;         // kRawStages x kRawMax
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + (size_t)kRawStages * kRawMax);
+    uint64_t* full = bars;                          // [kStages]  decoders -> MMA
+    uint64_t* empty = bars + kStages;               // [kStages]  MMA -> decoders
+    uint64_t* full_raw = bars + 2 * kStages;        // [kRawStages]  TMA -> decoders
+    uint64_t* empty_raw = full_raw + kRawStages;    // [kRawStages]  decoders -> TMA
+    uint64_t* acc_full = empty_raw + kRawStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&wmap);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], kDecoders);
+            mbar_init(&empty[s], 1);
+        }
+        for (int r = 0; r < kRawStages; ++r) {
+            mbar_init(&full_raw[r], 1);
+            mbar_init(&empty_raw[r], kDecoders);
+        }
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        // weights do not depend on the previous kernel: no wait before streaming them
+        if (lane == 0) {
+            for (int sb = 0; sb < nsb; ++sb) {
+                const int r = sb % kRawStages;
+                mbar_wait(&empty_raw[r], ((sb / kRawStages) & 1) ^ 1, p.status);
+                mbar_arrive_expect_tx(&full_raw[r], kRawBytes);
+                tma_load_2d(sRaw + (size_t)r * kRawMax, &wmap, &full_raw[r], sb * (Q4K ? 144 : 136), row0);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int ks = 0; ks < nks; ++ks) {
+                const int s = ks % kStages;
+                mbar_wait(&full[s], (ks / kStages) & 1, p.status);
+                tc_fence_after();
+                const uint32_t a_hi = smem_u32(sStage + (size_t)s * kStageBytes);
+                const uint32_t a_lo = a_hi + kAPiece, b_hi = a_hi + 2 * kAPiece, b_lo = b_hi + kBPiece;
+#pragma unroll
+                for (int kk = 0; kk < kKStage / 16; ++kk) {
+                    const uint32_t o = 32 * kk;   // 16 bf16 further along the swizzled rows
+                    umma_bf16(tmem, sw128_desc(a_hi + o), sw128_desc(b_hi + o), kIdesc, (ks | kk) != 0);
+                    umma_bf16(tmem, sw128_desc(a_hi + o), sw128_desc(b_lo + o), kIdesc, 1);
+                    umma_bf16(tmem, sw128_desc(a_lo + o), sw128_desc(b_hi + o), kIdesc, 1);
+                }
+                umma_commit(&empty[s]);
+            }
+            umma_commit(acc_full);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- decoders (warps 2..9)
+        const int t = threadIdx.x - 64;
+        const int row = t & (kTileRows - 1);   // W row within the tile
+        const int qt = t >> 7;                 // which 16 columns of a 64-column stage
+        // X part of a stage: activation row t / 32, columns 2*(t % 32), +1
+        const int xt = t >> 5, xk = 2 * (t & 31);
+        const bool xv = xt < p.M;
+        const float* xrow = p.x + (size_t)(xv ? xt : 0) * p.cols + xk;
+        pdl_wait();   // X may come from the previous kernel in the stream
+        // X of the next 4 stages in registers, so its loads are in flight early
+        float2 xb[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            xb[c] = (xv && c < nks) ? __ldg(reinterpret_cast<const float2*>(xrow + kKStage * c))
+                                    : make_float2(0.f, 0.f);
+        for (int sb = 0; sb < nsb; ++sb) {
+            const int r = sb % kRawStages;
+            mbar_wait(&full_raw[r], (sb / kRawStages) & 1, p.status);
+            const uint8_t* rp = sRaw + (size_t)r * kRawMax + (size_t)row * kRowBytes;
+            uint4 hdr = make_uint4(0, 0, 0, 0);
+            if constexpr (Q4K) hdr = *reinterpret_cast<const uint4*>(rp);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int ks = sb * 4 + c;
+                const int s = ks % kStages;
+                // 16 weights of this thread, exact in fp32, as 8 pairs
+                float2 w[8];
+                if constexpr (Q4K) {
+                    // columns 64c + 16qt .. +15: sub-block 2c + qt/2, qs bytes 32c + 16(qt&1) ..
+                    int sc, m;
+                    q4k_sm(hdr.y, hdr.z, hdr.w, 2 * c + (qt >> 1), sc, m);
+                    const float a = half_bits_to_float(hdr.x) * (float)sc;
+                    const float bm = half_bits_to_float(hdr.x >> 16) * (float)m;
+                    const uint4 q = *reinterpret_cast<const uint4*>(rp + 16 + 32 * c + 16 * (qt & 1));
+                    const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+                    const int ns = 4 * (qt >> 1);   // low or high nibbles
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        // 0x4B000000 | q is the float 2^23 + q
+                        const uint32_t n0 = (qw[i >> 1] >> (16 * (i & 1) + ns)) & 15u;
+                        const uint32_t n1 = (qw[i >> 1] >> (16 * (i & 1) + 8 + ns)) & 15u;
+                        const float2 f = make_float2(__uint_as_float(0x4B000000u | n0), __uint_as_float(0x4B000000u | n1));
+                        const float2 qf = __fadd2_rn(f, make_float2(-8388608.0f, -8388608.0f));
+                        w[i] = __ffma2_rn(qf, make_float2(a, a), make_float2(-bm, -bm));
+                    }
+                } else {
+                    // block 2c + qt/2 of the row's period: fp16 d at its start, then
+                    // q bytes 16(qt&1) .. +15 of its 32
+                    const int off = 34 * (2 * c + (qt >> 1));
+                    const uint16_t dh = *reinterpret_cast<const uint16_t*>(rp + off);
+                    const int qo = off + 2 + 16 * (qt & 1);   // 2-byte aligned
+                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rp + (qo & ~3));
+                    const int sh = 8 * (qo & 3);   // 0 or 16
+                    uint32_t v[5];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = wp[i];
+                    v[4] = sh ? wp[4] : 0u;   // only a misaligned start reaches a fifth word
+                    uint32_t u[4];   // the 16 q bytes, four a word, made unsigned (q + 128)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) u[i] = __funnelshift_r(v[i], v[i + 1], sh) ^ 0x80808080u;
+                    const float d = half_bits_to_float(dh);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        // 0x4B0000 | (q + 128) is the float 2^23 + 128 + q
+                        const uint32_t f0 = __byte_perm(u[i >> 1], 0x4B000000u, 0x7650u | (uint32_t)(2 * (i & 1)));
+                        const uint32_t f1 = __byte_perm(u[i >> 1], 0x4B000000u, 0x7650u | (uint32_t)(2 * (i & 1) + 1));
+                        const float2 qf = __fadd2_rn(make_float2(__uint_as_float(f0), __uint_as_float(f1)),
+                                                     make_float2(-8388736.0f, -8388736.0f));
+                        w[i] = __fmul2_rn(qf, make_float2(d, d));
+                    }
+                }
+                mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
+                uint8_t* sA = sStage + (size_t)s * kStageBytes;
+                uint8_t* ahi = sA + (size_t)row * 128;
+                uint8_t* alo = ahi + kAPiece;
+                const int sw = row & 7;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {   // 16-byte chunk 2qt + j of the row: columns 16qt + 8j .. +7
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) split_bf16x2(w[4 * j + e], hi[e], lo[e]);
+                    const int ch = ((2 * qt + j) ^ sw) << 4;
+                    *reinterpret_cast<uint4*>(ahi + ch) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(alo + ch) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                {
+                    // X: activation row xt, columns xk, xk+1 of this stage
+                    uint32_t hi, lo;
+                    split_bf16x2(xb[c], hi, lo);
+                    uint8_t* bhi = sA + 2 * kAPiece + (size_t)xt * 128;
+                    const int ch = (((xk >> 3) ^ (xt & 7)) << 4) + 4 * ((xk >> 1) & 3);
+                    *reinterpret_cast<uint32_t*>(bhi + ch) = hi;
+                    *reinterpret_cast<uint32_t*>(bhi + kBPiece + ch) = lo;
+                    // next use of this register: stage ks + 4
+                    xb[c] = (xv && ks + 4 < nks) ? __ldg(reinterpret_cast<const float2*>(xrow + kKStage * (ks + 4)))
+                                                 : make_float2(0.f, 0.f);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&full[s]);
+            }
+            mbar_arrive(&empty_raw[r]);
+        }
+
+        // ------------------------------------------------------------ epilogue
+        if (warp < 6) {   // warps 2..5 cover the four TMEM lane quarters
+            mbar_wait(acc_full, 0, p.status);
+            tc_fence_after();
+            const int q = warp & 3;   // TMEM lane quarter of this warp
+            const int yrow = row0 + 32 * q + lane;
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16), v);
+            if (yrow < p.rows) {
+#pragma unroll
+                for (int i = 0; i < kN; ++i)
+                    if (i < p.M) p.y[(size_t)i * p.rows + yrow] = v[i];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+template <bool Q4K>
+int launch_t(const CUtensorMap& wmap, const SmallParams& p, cudaStream_t stream) {
+    static int configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(smallm_kernel<Q4K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        if (dev >= 0 && dev < 64) configured[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.rows + kTileRows - 1) / kTileRows));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, smallm_kernel<Q4K>, wmap, p);
+    if (e != cudaSuccess) return cuda_fail(e, "small-M launch");
+    return GGQ_OK;
+}
+
+}  // namespace
+
+bool smallm_supported(int type, int64_t rows, int64_t cols, int M) {
+    return (type == GGQ_Q8_0 || type == GGQ_Q4_K) && M >= 1 && M <= kN && cols >= 256 && cols % 256 == 0 &&
+           cols <= (1 << 24) && rows >= 1 && rows <= 0x7fffffff;
+}
+
+int launch_smallm(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
+                  cudaStream_t stream) {
+    auto enc = encoder();
+    if (!enc) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled unavailable");
+    const bool q4k = type == GGQ_Q4_K;
+    const int64_t row_bytes = cols / 256 * (q4k ? 144 : 272);
+    CUtensorMap wmap;
+    cuuint64_t dims[2] = {(cuuint64_t)(q4k ? row_bytes : row_bytes / 2), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(q4k ? 144 : 136), (cuuint32_t)kTileRows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(&wmap, q4k ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                     const_cast<void*>(W), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GGQ_ECUDA, "tensor map (W) failed (%d)", (int)r);
+    SmallParams p = {};
+    p.x = x;
+    p.y = y;
+    p.rows = (int)rows;
+    p.cols = (int)cols;
+    p.M = M;
+    p.status = device_status_word();
+    if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
+    return q4k ? launch_t<true>(wmap, p, stream) : launch_t<false>(wmap, p, stream);
+}
+
+}  // namespace ggq

@@ -131,6 +131,33 @@ def test_gemv_small_m(env, qtype, rows, cols, M):
     assert_close(y1, y_ref[M - 1:M], a_ref[M - 1:M], f"type {qtype} row {M - 1} alone")
 
 
+@pytest.mark.parametrize("qtype,rows,cols,M", [(8, 1, 256, 5), (8, 129, 2304, 8), (8, 300, 4096, 16),
+                                             (12, 127, 256, 6), (12, 257, 11008, 13), (12, 1000, 4096, 16)])
+def test_gemv_tensor_core_small_batch(env, qtype, rows, cols, M):
+    """M >= 5 runs on the tcgen05 path: ragged 128-row tiles, one and many
+    256-column periods, padded activation rows."""
+    W = weights(qtype, rows, cols, stream=11)
+    x = xs(M, cols, stream=12)
+    y_ref, a_ref = oracle.gemv(qtype, W, rows, cols, x)
+    y = gpu_gemv(env, qtype, W, rows, cols, x)
+    assert_close(y, y_ref, a_ref, f"type {qtype} {rows}x{cols} M={M}")
+
+
+def test_gemv_tensor_core_integer_inputs_are_exact(env):
+    """Q8_0 with d = 1 and small integer x at M = 8: every product and sum is an
+    exact integer in fp32, so the bf16 hi/lo parts and the tensor-core sums give
+    the exact result."""
+    from tests.pin_checks import q8_block
+    rng = np.random.default_rng(9)
+    rows, cols, M = 200, 1024, 8
+    q = rng.integers(-128, 128, size=(rows, cols))
+    W = np.frombuffer(b"".join(q8_block(0x3C00, list(q[r, 32 * b:32 * b + 32]))
+                               for r in range(rows) for b in range(cols // 32)), np.uint8).copy()
+    x = rng.integers(-8, 9, size=(M, cols)).astype(np.float32)
+    y = gpu_gemv(env, 8, W, rows, cols, x)
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ q.T)
+
+
 def test_gemv_many_rounds(env):
     """Columns wide enough that a CTA streams its slice in several rounds."""
     for qtype, cols, M in [(12, 65536, 16), (8, 65536, 16), (12, 65536, 1)]:

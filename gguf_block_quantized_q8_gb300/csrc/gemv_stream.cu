@@ -262,6 +262,11 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
 
     for (int s = 0; s < p.nstages; ++s) {
         const StageDesc* sd = p.table ? p.table + s : &inl;
+        // this CTA's row groups and this warp's tile run: independent of x, so
+        // worked out before the stage barrier
+        const Groups G = cta_groups(sd, blockIdx.x, gridDim.x);
+        int t0, t1;
+        warp_run(G, sd->units, warp, W, t0, t1);
         if (s == 0) {
             pdl_wait();   // x may come from the previous kernel in the stream
         } else {
@@ -324,9 +329,6 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         __syncthreads();
 
         // ---- this warp's tiles
-        const Groups G = cta_groups(sd, blockIdx.x, gridDim.x);
-        int t0, t1;
-        warp_run(G, U, warp, W, t0, t1);
         constexpr int R = kRowsPerLane;
         float acc[R][MMAX];   // rows r + 8i of the group
 #pragma unroll
@@ -380,8 +382,8 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 for (int m = 0; m < MMAX; ++m) acc[i][m] = 0.0f;
         };
 
+        int gi = t0 / U, u = t0 - (t0 / U) * U;   // (group, SB) of tile t, advanced without dividing
         for (int t = t0; t < t1;) {
-            const int gi = t / U, u = t - gi * U;
             const int nv = min(min(B::kNsb, U - u), t1 - t);
             if (gi != cur) {
                 if (cur >= 0) flush(cur);
@@ -409,6 +411,11 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             ++consumed;
             refill();
             t += nv;
+            u += nv;
+            if (u == U) {
+                u = 0;
+                ++gi;
+            }
         }
         if (cur >= 0) flush(cur);
         __syncthreads();

@@ -192,18 +192,21 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
+            // a descriptor's address field is (address >> 4): descriptors of the
+            // other parts and offsets are the stage-0 one plus (offset >> 4)
+            const uint64_t d0 = sw128_desc(smem_u32(sStage));
+            constexpr uint32_t kLo = kAPiece >> 4, kBhi = (2 * kAPiece) >> 4, kBlo = (2 * kAPiece + kBPiece) >> 4;
             for (int ks = 0; ks < nks; ++ks) {
                 const int s = ks % kStages;
                 mbar_wait(&full[s], (ks / kStages) & 1, p.status);
                 tc_fence_after();
-                const uint32_t a_hi = smem_u32(sStage + (size_t)s * kStageBytes);
-                const uint32_t a_lo = a_hi + kAPiece, b_hi = a_hi + 2 * kAPiece, b_lo = b_hi + kBPiece;
+                const uint64_t ds = d0 + (uint64_t)((s * kStageBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kKStage / 16; ++kk) {
-                    const uint32_t o = 32 * kk;   // 16 bf16 further along the swizzled rows
-                    umma_bf16(tmem, sw128_desc(a_hi + o), sw128_desc(b_hi + o), kIdesc, (ks | kk) != 0);
-                    umma_bf16(tmem, sw128_desc(a_hi + o), sw128_desc(b_lo + o), kIdesc, 1);
-                    umma_bf16(tmem, sw128_desc(a_lo + o), sw128_desc(b_hi + o), kIdesc, 1);
+                    const uint64_t a = ds + 2 * kk;   // 16 bf16 = 32 bytes further along the swizzled rows
+                    umma_bf16(tmem, a, a + kBhi, kIdesc, (ks | kk) != 0);
+                    umma_bf16(tmem, a, a + kBlo, kIdesc, 1);
+                    umma_bf16(tmem, a + kLo, a + kBhi, kIdesc, 1);
                 }
                 umma_commit(&empty[s]);
             }

@@ -230,35 +230,50 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
 
     // ---- copy cursor of this warp: its tiles of every stage, in order, one
     // copy per (group, up to NSB consecutive SBs)
-    int cs = -1, ct = 0, ct1 = 0;   // stage, next tile, end of the run
+    // stage, next tile, end of the run; (group, SB) of the next tile and the
+    // group's matrix and first row, advanced without dividing
+    int cs = -1, ct = 0, ct1 = 0, cU = 1, cgi = 0, cu = 0, cseg = 0, crow = 0;
+    const StageDesc* csd = &inl;
     Groups cg{};
-    int issued = 0, consumed = 0;
+    int inflight = 0;   // copies issued and not yet consumed
+    int islot = 0;      // ring slot of the next copy
     auto refill = [&]() {   // keep up to D copies in flight or resident
-        while (issued - consumed < D) {
-            while (ct == ct1 && cs < p.nstages) {   // next stage in which this warp has tiles
-                if (++cs == p.nstages) break;
-                const StageDesc* sd = p.table ? p.table + cs : &inl;
-                cg = cta_groups(sd, blockIdx.x, gridDim.x);
-                warp_run(cg, sd->units, warp, W, ct, ct1);
+        while (inflight < D) {
+            if (ct == ct1) {
+                while (ct == ct1 && cs < p.nstages) {   // next stage in which this warp has tiles
+                    if (++cs == p.nstages) break;
+                    csd = p.table ? p.table + cs : &inl;
+                    cg = cta_groups(csd, blockIdx.x, gridDim.x);
+                    warp_run(cg, csd->units, warp, W, ct, ct1);
+                }
+                if (cs >= p.nstages) break;
+                cU = csd->units;
+                cgi = ct / cU;
+                cu = ct - cgi * cU;
+                int nrows;
+                group_at(csd, cg, cgi, cseg, crow, nrows);
             }
-            if (cs >= p.nstages) break;
-            const StageDesc* sd = p.table ? p.table + cs : &inl;
-            const int U = sd->units;
-            const int gi = ct / U, u = ct - gi * U;
-            const int nv = min(min(B::kNsb, U - u), ct1 - ct);
-            const int slot = issued % D;
+            const int nv = min(min(B::kNsb, cU - cu), ct1 - ct);
             if (lane == 0) {
-                int seg, row, nrows;
-                group_at(sd, cg, gi, seg, row, nrows);
                 fence_proxy_async_smem();   // this warp's reads of the buffer come before the copy's writes
-                mbar_arrive_expect_tx(&full[slot], B::kCopy);
-                tma_load_2d(ring + (size_t)slot * B::kTile, &sd->maps[seg], &full[slot], u * B::kElems, row);
+                mbar_arrive_expect_tx(&full[islot], B::kCopy);
+                tma_load_2d(ring + (size_t)islot * B::kTile, &csd->maps[cseg], &full[islot], cu * B::kElems, crow);
             }
             ct += nv;
-            ++issued;
+            cu += nv;
+            if (cu == cU && ct < ct1) {   // next group of this run
+                cu = 0;
+                ++cgi;
+                int nrows;
+                group_at(csd, cg, cgi, cseg, crow, nrows);
+            }
+            ++inflight;
+            if (++islot == D) islot = 0;
         }
     };
     refill();
+    int cslot = 0;          // ring slot of the next copy to consume
+    uint32_t cphase = 0;    // its barrier phase
 
     for (int s = 0; s < p.nstages; ++s) {
         const StageDesc* sd = p.table ? p.table + s : &inl;
@@ -389,8 +404,8 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 if (cur >= 0) flush(cur);
                 cur = gi;
             }
-            const int slot = consumed % D;
-            wait_full(&full[slot], (uint32_t)(consumed / D) & 1u, p.status);
+            wait_full(&full[cslot], cphase, p.status);
+            const int slot = cslot;
             const uint8_t* rowp = ring + (size_t)slot * B::kTile + r * B::kRow;
 #pragma unroll
             for (int j = 0; j < B::kNsb; ++j) {
@@ -408,7 +423,11 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 }
             }
             __syncwarp();   // every lane is done with the buffer
-            ++consumed;
+            if (++cslot == D) {
+                cslot = 0;
+                cphase ^= 1u;
+            }
+            --inflight;
             refill();
             t += nv;
             u += nv;

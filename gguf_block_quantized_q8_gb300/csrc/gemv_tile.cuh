@@ -104,19 +104,35 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
     constexpr uint64_t kHi0 = 0x000000F0000000F0ull, kHi1 = 0x0000F0000000F000ull, kHi2 = 0x00F0000000F00000ull;
     float a_lo[R], a_hi[R], b_lo[R], b_hi[R];
     uint64_t wp[R][4];   // word pairs (0,1) (2,3) (4,5) (6,7) of the chunk
+    // 6-bit scales and mins of sub-blocks 2c, 2c+1 (bytes jl, jh of the words
+    // below).  Sub-blocks 0-3: the low 6 bits of scale bytes 0-3 / 4-7; 4-7: a
+    // low nibble of bytes 8-11 plus the top 2 bits of bytes 0-3 / 4-7.  The
+    // masks depend on c only, so they are worked out once per lane.
     const int jl = (2 * c) & 3, jh = (2 * c + 1) & 3;
+    const bool upper = c >= 2;
+    const uint32_t m1 = upper ? 0x0F0F0F0Fu : 0x3F3F3F3Fu, m2 = upper ? 0x30303030u : 0u;
+    const uint32_t sel_lo = 0x7650u | (uint32_t)jl, sel_hi = 0x7650u | (uint32_t)jh;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const uint8_t* row = rp + r * rstride;
         const uint4 h = *reinterpret_cast<const uint4*>(row);
         const float d96 = half_bits_to_float(h.x) * kTwo96;
         const float dmin = half_bits_to_float(h.x >> 16);
-        const uint32_t scw = c < 2 ? (h.y & 0x3F3F3F3Fu) : ((h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u));
-        const uint32_t mw = c < 2 ? (h.z & 0x3F3F3F3Fu) : (((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u));
-        a_lo[r] = d96 * byte_to_float(scw, jl);
-        a_hi[r] = d96 * byte_to_float(scw, jh);
-        b_lo[r] = dmin * byte_to_float(mw, jl);
-        b_hi[r] = dmin * byte_to_float(mw, jh);
+        const uint32_t scw = ((upper ? h.w : h.y) & m1) | ((h.y >> 2) & m2);
+        const uint32_t mw = ((upper ? (h.w >> 4) : h.z) & m1) | ((h.z >> 2) & m2);
+        // 0x4B0000 | byte is the float 2^23 + byte
+        const float2 sc = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(scw, 0x4B000000u, sel_lo)),
+                                                 __uint_as_float(__byte_perm(scw, 0x4B000000u, sel_hi))),
+                                     make_float2(-8388608.0f, -8388608.0f));
+        const float2 mn = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(mw, 0x4B000000u, sel_lo)),
+                                                 __uint_as_float(__byte_perm(mw, 0x4B000000u, sel_hi))),
+                                     make_float2(-8388608.0f, -8388608.0f));
+        const float2 a = __fmul2_rn(sc, make_float2(d96, d96));
+        const float2 bb = __fmul2_rn(mn, make_float2(dmin, dmin));
+        a_lo[r] = a.x;
+        a_hi[r] = a.y;
+        b_lo[r] = bb.x;
+        b_hi[r] = bb.y;
         const ulonglong2 q0 = *reinterpret_cast<const ulonglong2*>(row + 16 + 32 * c);
         const ulonglong2 q1 = *reinterpret_cast<const ulonglong2*>(row + 32 + 32 * c);
         wp[r][0] = q0.x; wp[r][1] = q0.y; wp[r][2] = q1.x; wp[r][3] = q1.y;

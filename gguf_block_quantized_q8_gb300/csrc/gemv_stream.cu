@@ -167,11 +167,17 @@ struct Groups {
     int first[kMaxSeg];    // index of the first group of each matrix
 };
 
+__device__ __forceinline__ int cta_row(int R, int b, int nb) {
+    // R * b / nb; 32-bit division whenever the product fits (every realistic stage)
+    if ((unsigned)R <= 0xFFFFFFFFu / (unsigned)nb) return (int)((unsigned)R * (unsigned)b / (unsigned)nb);
+    return (int)((long long)R * b / nb);
+}
+
 __device__ __forceinline__ Groups cta_groups(const StageDesc* sd, int b, int nb) {
     Groups G;
-    const long long R = sd->row0[sd->nseg];
-    G.r0 = (int)(R * b / nb);
-    G.r1 = (int)(R * (b + 1) / nb);
+    const int R = sd->row0[sd->nseg];
+    G.r0 = cta_row(R, b, nb);
+    G.r1 = cta_row(R, b + 1, nb);
     int n = 0;
 #pragma unroll
     for (int s = 0; s < kMaxSeg; ++s) {
@@ -197,11 +203,14 @@ __device__ __forceinline__ void group_at(const StageDesc* sd, const Groups& G, i
     nrows = min(kGroupRows, hi - g0);
 }
 
-// The tile run [t0, t1) of warp w (of nw): tile t = group * U + SB.
-__device__ __forceinline__ void warp_run(const Groups& G, int U, int w, int nw, int& t0, int& t1) {
-    const long long T = (long long)G.n * U;
-    t0 = (int)(T * w / nw);
-    t1 = (int)(T * (w + 1) / nw);
+// The tile run [t0, t1) of warp w (of NW): tile t = group * U + SB.  A CTA
+// holds fewer than 2^28 tiles (the stage holds fewer than 2^31 SBs and a CTA
+// at most 1/G of its rows plus one group per matrix), so T * w fits 32 bits.
+template <int NW>
+__device__ __forceinline__ void warp_run(const Groups& G, int U, int w, int& t0, int& t1) {
+    const unsigned T = (unsigned)G.n * (unsigned)U;
+    t0 = (int)(T * (unsigned)w / NW);
+    t1 = (int)(T * (unsigned)(w + 1) / NW);
 }
 
 template <bool Q4K, int MMAX, int W>
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     if (++cs == p.nstages) break;
                     csd = p.table ? p.table + cs : &inl;
                     cg = cta_groups(csd, blockIdx.x, gridDim.x);
-                    warp_run(cg, csd->units, warp, W, ct, ct1);
+                    warp_run<W>(cg, csd->units, warp, ct, ct1);
                 }
                 if (cs >= p.nstages) break;
                 cU = csd->units;
@@ -272,6 +281,25 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         }
     };
     refill();
+
+    // x' placement of the lane's 4 consecutive columns 4l .. 4l+3 of a
+    // 128-column half of an SB (the other half adds 136 floats).  Q4_K: chunk
+    // l/16 (68 floats each), low or high nibbles ((l/8) odd: high), byte
+    // positions b = 0..3 of word l%8 at q4k_xslot, stride 8.  Q8_0: byte
+    // positions of the period, 34 per block of 32 after its 2-byte scale.
+    int xoff;
+    float4 xsc;
+    {
+        const int hi = (lane >> 3) & 1;
+        if (Q4K) {
+            xoff = (lane >> 4) * 68 + 32 * hi + (lane & 7);
+            const int k = 4 * lane;
+            xsc = make_float4(q4k_xscale(k), q4k_xscale(k + 1), q4k_xscale(k + 2), q4k_xscale(k + 3));
+        } else {
+            xoff = 34 * (lane >> 3) + 2 + 4 * (lane & 7);
+            xsc = make_float4(q8_xscale(xoff), q8_xscale(xoff + 1), q8_xscale(xoff + 2), q8_xscale(xoff + 3));
+        }
+    }
     int cslot = 0;          // ring slot of the next copy to consume
     uint32_t cphase = 0;    // its barrier phase
 
@@ -281,7 +309,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         // worked out before the stage barrier
         const Groups G = cta_groups(sd, blockIdx.x, gridDim.x);
         int t0, t1;
-        warp_run(G, sd->units, warp, W, t0, t1);
+        warp_run<W>(G, sd->units, warp, t0, t1);
         if (s == 0) {
             pdl_wait();   // x may come from the previous kernel in the stream
         } else {
@@ -299,12 +327,15 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         {
             // Lane l of a warp step takes 4 consecutive values (one float4) of x:
             // 8 lanes cover a 32-column sub-block, whose sum takes 3 shuffles.
+            // A warp step covers 128 columns of one activation row (cols is a
+            // multiple of 256), half of an SB: the lane's place in it and the
+            // scales of its 4 values are the lane constants xoff and xsc.
             // Every load of a batch is issued before any is used (one L2 round
             // trip per batch of kBatch float4 per lane).
             constexpr int kBatch = 8;
-            const int n4 = p.M * cols / 4;   // float4 of x (cols % 256 == 0)
+            const int c4 = cols / 4;          // float4 per activation row
+            const int n4 = p.M * c4;
             const float4* x4 = reinterpret_cast<const float4*>(sd->x);
-            const int a = lane & 7;          // float4 index inside the sub-block
             for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
                 float4 v[kBatch];
 #pragma unroll
@@ -314,29 +345,29 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 }
 #pragma unroll
                 for (int i = 0; i < kBatch; ++i) {
-                    const int qb = q0 + i * kThreads;   // warp-uniform: 4 sub-blocks of x
+                    const int qb = q0 + i * kThreads;   // warp-uniform, a multiple of 32
                     if (qb >= n4) break;
                     float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
                     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
                     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
                     sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                    const int k = 4 * (qb + lane);      // first of the lane's 4 columns
-                    const int m = k / cols, kc = k - m * cols;
-                    const int u = kc >> 8, kk = kc & 255, sb = kk >> 5;
-                    float* xm = xp + (size_t)m * xs + u * 272;
-                    const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                    const int m = MMAX == 1 ? 0 : qb / c4;
+                    const int h = qb - m * c4;          // first float4 of the step within the row
+                    const int u = h >> 6;               // SB
+                    float* dst = xp + (size_t)m * xs + u * 272 + ((h & 32) ? 136 : 0) + xoff;
+                    const float4 e = make_float4(v[i].x * xsc.x, v[i].y * xsc.y, v[i].z * xsc.z, v[i].w * xsc.w);
                     if (Q4K) {
-                        // q4k_xslot(kk + b) = (kk & ~31) | (b << 3) | a, chunk padded to 68
-                        float* dst = xm + (kk >> 6) * 68 + (kk & 32) + a;
-#pragma unroll
-                        for (int bb = 0; bb < 4; ++bb) dst[8 * bb] = e[bb] * q4k_xscale(kk + bb);
-                        if (a == 0) sums[m * nsub + u * 8 + sb] = sum;
+                        dst[0] = e.x;
+                        dst[8] = e.y;
+                        dst[16] = e.z;
+                        dst[24] = e.w;
                     } else {
-                        const int pos = 34 * sb + 2 + (kk & 31);   // byte position in the period
-#pragma unroll
-                        for (int bb = 0; bb < 4; ++bb) xm[pos + bb] = e[bb] * q8_xscale(pos + bb);
-                        if (a == 0) sums[m * nsub + u * 8 + sb] = 128.0f * sum;
+                        dst[0] = e.x;
+                        dst[1] = e.y;
+                        dst[2] = e.z;
+                        dst[3] = e.w;
                     }
+                    if ((lane & 7) == 0) sums[m * nsub + u * 8 + ((h & 32) >> 3) + (lane >> 3)] = Q4K ? sum : 128.0f * sum;
                 }
             }
         }
@@ -450,7 +481,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             // empty run are skipped) while their part of a started group is this one
             for (int w2 = warp + 1; w2 < W; ++w2) {
                 int a2, b2;
-                warp_run(G, U, w2, W, a2, b2);
+                warp_run<W>(G, U, w2, a2, b2);
                 if (a2 == b2) continue;
                 if (cut_grp[w2] != gi) break;
 #pragma unroll

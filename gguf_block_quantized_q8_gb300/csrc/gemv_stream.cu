@@ -35,6 +35,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstddef>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -56,9 +57,10 @@ constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kRowsPerLane = 2;                 // rows r and r + 8 of a group
 constexpr int kGroupRows = 8 * kRowsPerLane;
 
-// One stage of a chain (device-visible: kernel parameter or global table).
-struct StageDesc {
-    CUtensorMap maps[kMaxSeg];  // per matrix: 8-byte elements, box of 16 rows x (NSB SBs + pad)
+// The fields of a stage other than its tensor maps.  A CTA copies them to
+// shared memory one stage ahead: read from global memory after a stage
+// barrier (whose acquire leaves the L1 cold) each would wait an L2 round trip.
+struct StageInfo {
     float* y[kMaxSeg];          // [M][rows]
     const float* x;             // [M][cols]
     int rows[kMaxSeg];
@@ -66,7 +68,17 @@ struct StageDesc {
     int nseg;
     int cols;
     int units;                  // U = cols / 256
+    int pad[2];
 };
+constexpr int kInfoVec = sizeof(StageInfo) / 16;   // 16-byte pieces
+static_assert(sizeof(StageInfo) % 16 == 0, "StageInfo is copied in 16-byte pieces");
+
+// One stage of a chain (device-visible: kernel parameter or global table).
+struct StageDesc {
+    CUtensorMap maps[kMaxSeg];  // per matrix: 8-byte elements, box of 16 rows x (NSB SBs + pad)
+    StageInfo info;
+};
+static_assert(offsetof(StageDesc, info) % 16 == 0, "StageInfo is copied in 16-byte pieces");
 
 struct ChainParams {
     const StageDesc* table;     // the stages in device memory, or null: the inline stage only
@@ -173,7 +185,7 @@ __device__ __forceinline__ int cta_row(int R, int b, int nb) {
     return (int)((long long)R * b / nb);
 }
 
-__device__ __forceinline__ Groups cta_groups(const StageDesc* sd, int b, int nb) {
+__device__ __forceinline__ Groups cta_groups(const StageInfo* sd, int b, int nb) {
     Groups G;
     const int R = sd->row0[sd->nseg];
     G.r0 = cta_row(R, b, nb);
@@ -192,7 +204,7 @@ __device__ __forceinline__ Groups cta_groups(const StageDesc* sd, int b, int nb)
 }
 
 // Group gi: matrix, first row (in the matrix), rows in the group.
-__device__ __forceinline__ void group_at(const StageDesc* sd, const Groups& G, int gi, int& seg, int& row, int& nrows) {
+__device__ __forceinline__ void group_at(const StageInfo* sd, const Groups& G, int gi, int& seg, int& row, int& nrows) {
     seg = 0;
 #pragma unroll
     for (int s = 1; s < kMaxSeg; ++s)
@@ -222,9 +234,10 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     const int r = lane >> 2, c = lane & 3;   // row of the group, chunk of the SB
     const int D = p.ring;
 
-    // shared memory: [warp rings][x'][sums][cut-group parts][barriers]
+    // shared memory: [warp rings][stage info x2][x'][sums][cut-group parts][barriers]
     uint8_t* ring = smem + (size_t)warp * D * B::kTile;
-    float* xp = reinterpret_cast<float*>(smem + (size_t)W * D * B::kTile);
+    StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)W * D * B::kTile);   // stage s in slot s & 1
+    float* xp = reinterpret_cast<float*>(infos + 2);
     float* sums = xp + (size_t)MMAX * p.xs;
     float* cut_val = sums + (size_t)MMAX * p.nsub;                                // [2][W][8][MMAX]
     int* cut_grp = reinterpret_cast<int*>(cut_val + 2 * W * kGroupRows * MMAX);   // [2][W]
@@ -234,7 +247,9 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         for (int i = 0; i < D; ++i) mbar_init(&full[i], 1);
         fence_mbar_init();
     }
-    __syncwarp();
+    if (warp == 0 && lane < kInfoVec)
+        reinterpret_cast<int4*>(infos)[lane] = reinterpret_cast<const int4*>(p.table ? &p.table->info : &inl.info)[lane];
+    __syncthreads();
     pdl_launch_dependents();
 
     // ---- copy cursor of this warp: its tiles of every stage, in order, one
@@ -252,15 +267,15 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 while (ct == ct1 && cs < p.nstages) {   // next stage in which this warp has tiles
                     if (++cs == p.nstages) break;
                     csd = p.table ? p.table + cs : &inl;
-                    cg = cta_groups(csd, blockIdx.x, gridDim.x);
-                    warp_run<W>(cg, csd->units, warp, ct, ct1);
+                    cg = cta_groups(&csd->info, blockIdx.x, gridDim.x);
+                    warp_run<W>(cg, csd->info.units, warp, ct, ct1);
                 }
                 if (cs >= p.nstages) break;
-                cU = csd->units;
+                cU = csd->info.units;
                 cgi = ct / cU;
                 cu = ct - cgi * cU;
                 int nrows;
-                group_at(csd, cg, cgi, cseg, crow, nrows);
+                group_at(&csd->info, cg, cgi, cseg, crow, nrows);
             }
             const int nv = min(min(B::kNsb, cU - cu), ct1 - ct);
             if (lane == 0) {
@@ -274,7 +289,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 cu = 0;
                 ++cgi;
                 int nrows;
-                group_at(csd, cg, cgi, cseg, crow, nrows);
+                group_at(&csd->info, cg, cgi, cseg, crow, nrows);
             }
             ++inflight;
             if (++islot == D) islot = 0;
@@ -304,12 +319,17 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     uint32_t cphase = 0;    // its barrier phase
 
     for (int s = 0; s < p.nstages; ++s) {
-        const StageDesc* sd = p.table ? p.table + s : &inl;
+        const StageInfo* sd = infos + (s & 1);
         // this CTA's row groups and this warp's tile run: independent of x, so
         // worked out before the stage barrier
         const Groups G = cta_groups(sd, blockIdx.x, gridDim.x);
         int t0, t1;
         warp_run<W>(G, sd->units, warp, t0, t1);
+        // the next stage's fields, to the other slot (free: every warp has
+        // passed the end of stage s-1); waited for before the end of stage s
+        if (s + 1 < p.nstages && warp == W - 1 && lane < kInfoVec)
+            cp_async_16(reinterpret_cast<int4*>(infos + ((s + 1) & 1)) + lane,
+                        reinterpret_cast<const int4*>(&p.table[s + 1].info) + lane);
         if (s == 0) {
             pdl_wait();   // x may come from the previous kernel in the stream
         } else {
@@ -502,6 +522,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         // warp's stores before thread 0's release); the last CTA of the chain
         // resets the counter for the next launch
         if (p.nstages > 1) {
+            if (warp == W - 1) cp_async_wait_all();
             __syncthreads();
             if (tid == 0) {
                 if (s + 1 < p.nstages) {
@@ -548,7 +569,8 @@ size_t rows_smem(bool q4k, int mmax, int ring, int64_t cols_max) {
     const int W = warps_of(q4k, mmax);
     const int64_t U = cols_max / 256;
     const size_t cut = (size_t)2 * W * kGroupRows * mmax * 4 + (size_t)2 * W * 4;
-    return (size_t)W * ring * tile_bytes(q4k) + (size_t)mmax * U * 272 * 4 + (size_t)mmax * U * 8 * 4 + cut +
+    return (size_t)W * ring * tile_bytes(q4k) + 2 * sizeof(StageInfo) + (size_t)mmax * U * 272 * 4 +
+           (size_t)mmax * U * 8 * 4 + cut +
            (size_t)W * ring * 8;
 }
 
@@ -597,16 +619,16 @@ int make_stage(int type, int n, const void* const* W, const int64_t* rows, int64
         const int64_t row_bytes = cols / 256 * (q4k ? 144 : 272);
         int rc = encode_map(&sd->maps[s], W[s], rows[s], row_bytes, q4k);
         if (rc) return rc;
-        sd->y[s] = y[s];
-        sd->rows[s] = (int)rows[s];
-        sd->row0[s] = r;
+        sd->info.y[s] = y[s];
+        sd->info.rows[s] = (int)rows[s];
+        sd->info.row0[s] = r;
         r += (int)rows[s];
     }
-    sd->row0[n] = r;
-    sd->nseg = n;
-    sd->x = x;
-    sd->cols = (int)cols;
-    sd->units = (int)(cols / 256);
+    sd->info.row0[n] = r;
+    sd->info.nseg = n;
+    sd->info.x = x;
+    sd->info.cols = (int)cols;
+    sd->info.units = (int)(cols / 256);
     return GGQ_OK;
 }
 

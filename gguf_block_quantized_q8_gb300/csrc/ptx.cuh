@@ -125,6 +125,13 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for all
+// of this thread's such copies.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (bulk copy / tensor core) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -497,15 +497,20 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             float tsum[MMAX];
 #pragma unroll
             for (int m = 0; m < MMAX; ++m) tsum[m] = cut_val[((W + warp) * kGroupRows + lane) * MMAX + m];
-            // the group goes on in the next warps that have tiles (warps with an
-            // empty run are skipped) while their part of a started group is this one
-            for (int w2 = warp + 1; w2 < W; ++w2) {
+            // the other parts: the later warps whose (non-empty) run starts
+            // inside this group, told from the run bounds alone so that every
+            // load is independent; added in warp order
+            const int g0 = gi * U, g1 = g0 + U;
+#pragma unroll
+            for (int w2 = 1; w2 < W; ++w2) {
                 int a2, b2;
                 warp_run<W>(G, U, w2, a2, b2);
-                if (a2 == b2) continue;
-                if (cut_grp[w2] != gi) break;
+                const bool part = w2 > warp && a2 < b2 && a2 > g0 && a2 < g1;
 #pragma unroll
-                for (int m = 0; m < MMAX; ++m) tsum[m] += cut_val[(w2 * kGroupRows + lane) * MMAX + m];
+                for (int m = 0; m < MMAX; ++m) {
+                    const float v = cut_val[(w2 * kGroupRows + lane) * MMAX + m];
+                    if (part) tsum[m] += v;
+                }
             }
             int seg, row, nrows;
             group_at(sd, G, gi, seg, row, nrows);

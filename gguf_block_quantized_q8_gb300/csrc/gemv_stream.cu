@@ -299,15 +299,15 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
 
     // x' placement of the lane's 4 consecutive columns 4l .. 4l+3 of a
     // 128-column half of an SB (the other half adds 136 floats).  Q4_K: chunk
-    // l/16 (68 floats each), low or high nibbles ((l/8) odd: high), byte
-    // positions b = 0..3 of word l%8 at q4k_xslot, stride 8.  Q8_0: byte
-    // positions of the period, 34 per block of 32 after its 2-byte scale.
+    // l/16 (68 floats each), byte positions b = 0..3 of word l%8, low or high
+    // nibble ((l/8) odd: high) at q4k_xslot, stride 16.  Q8_0: byte positions
+    // of the period, 34 per block of 32 after its 2-byte scale.
     int xoff;
     float4 xsc;
     {
         const int hi = (lane >> 3) & 1;
         if (Q4K) {
-            xoff = (lane >> 4) * 68 + 32 * hi + (lane & 7);
+            xoff = (lane >> 4) * 68 + 2 * (lane & 7) + hi;
             const int k = 4 * lane;
             xsc = make_float4(q4k_xscale(k), q4k_xscale(k + 1), q4k_xscale(k + 2), q4k_xscale(k + 3));
         } else {
@@ -378,9 +378,9 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     const float4 e = make_float4(v[i].x * xsc.x, v[i].y * xsc.y, v[i].z * xsc.z, v[i].w * xsc.w);
                     if (Q4K) {
                         dst[0] = e.x;
-                        dst[8] = e.y;
-                        dst[16] = e.z;
-                        dst[24] = e.w;
+                        dst[16] = e.y;
+                        dst[32] = e.z;
+                        dst[48] = e.w;
                     } else {
                         dst[0] = e.x;
                         dst[1] = e.y;
@@ -396,11 +396,15 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
 
         // ---- this warp's tiles
         constexpr int R = kRowsPerLane;
-        float acc[R][MMAX];   // rows r + 8i of the group
+        float acc[R][MMAX];     // rows r + 8i of the group
+        float2 acc2[R][MMAX];   // Q4_K: (low-nibble part, high-nibble part)
 #pragma unroll
         for (int i = 0; i < R; ++i)
 #pragma unroll
-            for (int m = 0; m < MMAX; ++m) acc[i][m] = 0.0f;
+            for (int m = 0; m < MMAX; ++m) {
+                acc[i][m] = 0.0f;
+                acc2[i][m] = make_float2(0.0f, 0.0f);
+            }
         int cur = -1;   // group being accumulated
 
         // finish group gi: add each row's four chunks, then store the group's
@@ -410,6 +414,10 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             for (int i = 0; i < R; ++i)
 #pragma unroll
                 for (int m = 0; m < MMAX; ++m) {
+                    if constexpr (Q4K) {
+                        acc[i][m] = acc2[i][m].x + acc2[i][m].y;
+                        acc2[i][m] = make_float2(0.0f, 0.0f);
+                    }
                     acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], 1);
                     acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], 2);
                 }
@@ -464,7 +472,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     const int uj = u + j;
                     if constexpr (Q4K) {
                         q4k_chunk_rows<MMAX, R>(rowp + j * B::kBytes, 8 * B::kRow, c, xp + uj * 272, xs,
-                                                sums + uj * 8, nsub, acc, 4, 1, 68);
+                                                sums + uj * 8, nsub, acc2, 68);
                     } else {
 #pragma unroll
                         for (int i = 0; i < R; ++i)

@@ -67,11 +67,12 @@ __device__ __forceinline__ float f2_sum(F2 a, F2 b) {
 }
 
 // Position of the x' value of weight k (natural order within a Q4_K
-// super-block) in the layout the tile code reads: [c][lo/hi][byte b][word w],
-// k = 64c + 32*hi + 4w + b.  x' values of words w and w+1 sit side by side, the
-// operand pair of one packed FMA over two qs words.
+// super-block) in the layout the tile code reads: [c][byte b][word w][lo/hi],
+// k = 64c + 32*hi + 4w + b.  The x' values of the low and the high nibble of
+// one byte sit side by side, the operand pair of one packed FMA over one qs
+// word; a float4 holds those of words w and w+1.
 __device__ __forceinline__ int q4k_xslot(int k) {
-    return (k & ~31) | ((k & 3) << 3) | ((k >> 2) & 7);
+    return (k & ~63) | ((k & 3) << 4) | (((k >> 2) & 7) << 1) | ((k >> 5) & 1);
 }
 
 __device__ __forceinline__ uint64_t and64(uint64_t a, uint64_t m) { return a & m; }
@@ -82,28 +83,36 @@ __device__ __forceinline__ void f2_fma64(F2& acc, uint64_t a, float b0, float b1
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc.v) : "l"(a), "l"(b));
 }
 
+// (w & m0, w & m1) as one register pair
+__device__ __forceinline__ uint64_t and_pair(uint32_t w, uint32_t m0, uint32_t m1) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 l, h;\n\tand.b32 l, %1, %2;\n\tand.b32 h, %1, %3;\n\tmov.b64 %0, {l, h};\n\t}"
+        : "=l"(r) : "r"(w), "r"(m0), "r"(m1));
+    return r;
+}
+
+// acc(2) += a(2) * b(2) on float2 values
+__device__ __forceinline__ void f2_fma(float2& acc, float2 a, float2 b) { acc = __ffma2_rn(a, b, acc); }
+
 // Chunk c (weights 64c .. 64c+63, sub-blocks 2c and 2c+1) of R rows of Q4_K
 // super-blocks per lane (rp: the lane's first row, `rstride` bytes to the next
 // of its rows) against x' of that super-block and the per-sub-block sums of x.
-// x' is read as float4 groups: slots 64c + 4q' .. +3 of the q4k_xslot layout
-// (group q' of chunk c) of activation row m at xu + m*xs + c*cs + q'*gs.
-// gs = 4, cs = 64: the 256 values contiguous; cs = 68: each chunk padded by 4
-// floats, so lanes reading different chunks of one super-block hit different
-// banks.  The sum of sub-block j of activation row m is su[m*ss + j*sj].
-// acc[r][m] += sum_{k in chunk c} w_r[k] * x[m][k].
+// x' of chunk c of activation row m starts at xu + m*xs + c*cs in the
+// q4k_xslot order (cs = 64: the 256 values contiguous; cs = 68: each chunk
+// padded by 4 floats, so lanes reading different chunks of one super-block
+// hit different banks).  The sums of sub-blocks 2c, 2c+1 of activation row m
+// are the float pair at su + m*ss + 2c.
+// acc[r][m].x + acc[r][m].y += sum_{k in chunk c} w_r[k] * x[m][k].
 //
-// Two consecutive qs words are handled as one 64-bit value: AND-ing it with a
-// mask repeated in both halves gives the bit patterns of the same nibble of
-// both words in one aligned register pair, the first operand of fma.f32x2.
+// Each qs word gives the bit patterns of its low and its high nibble at one
+// byte position in one aligned register pair (two ANDs), the first operand of
+// fma.f32x2; the accumulator pairs hold (low-nibble part, high-nibble part),
+// so the sub-block scales and mins apply as one packed FMA each.
 template <int MMAX, int R>
 __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, int c, const float* xu, int xs,
-                                               const float* su, int ss, float (&acc)[R][MMAX], int gs = 4,
-                                               int sj = 1, int cs = 64) {
-    // nibble masks (both halves): low nibble of bytes 0,1,2 in place, byte 3 after >> 8
-    constexpr uint64_t kLo0 = 0x0000000F0000000Full, kLo1 = 0x00000F0000000F00ull, kLo2 = 0x000F0000000F0000ull;
-    constexpr uint64_t kHi0 = 0x000000F0000000F0ull, kHi1 = 0x0000F0000000F000ull, kHi2 = 0x00F0000000F00000ull;
-    float a_lo[R], a_hi[R], b_lo[R], b_hi[R];
-    uint64_t wp[R][4];   // word pairs (0,1) (2,3) (4,5) (6,7) of the chunk
+                                               const float* su, int ss, float2 (&acc)[R][MMAX], int cs = 64) {
+    float2 a2[R], nb2[R];   // (d*sc, dmin*m) of sub-blocks 2c, 2c+1; the mins negated
+    uint32_t wd[R][8];      // the chunk's 8 qs words
     // 6-bit scales and mins of sub-blocks 2c, 2c+1 (bytes jl, jh of the words
     // below).  Sub-blocks 0-3: the low 6 bits of scale bytes 0-3 / 4-7; 4-7: a
     // low nibble of bytes 8-11 plus the top 2 bits of bytes 0-3 / 4-7.  The
@@ -117,7 +126,7 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
         const uint8_t* row = rp + r * rstride;
         const uint4 h = *reinterpret_cast<const uint4*>(row);
         const float d96 = half_bits_to_float(h.x) * kTwo96;
-        const float dmin = half_bits_to_float(h.x >> 16);
+        const float ndmin = -half_bits_to_float(h.x >> 16);
         const uint32_t scw = ((upper ? h.w : h.y) & m1) | ((h.y >> 2) & m2);
         const uint32_t mw = ((upper ? (h.w >> 4) : h.z) & m1) | ((h.z >> 2) & m2);
         // 0x4B0000 | byte is the float 2^23 + byte
@@ -127,69 +136,57 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
         const float2 mn = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(mw, 0x4B000000u, sel_lo)),
                                                  __uint_as_float(__byte_perm(mw, 0x4B000000u, sel_hi))),
                                      make_float2(-8388608.0f, -8388608.0f));
-        const float2 a = __fmul2_rn(sc, make_float2(d96, d96));
-        const float2 bb = __fmul2_rn(mn, make_float2(dmin, dmin));
-        a_lo[r] = a.x;
-        a_hi[r] = a.y;
-        b_lo[r] = bb.x;
-        b_hi[r] = bb.y;
-        const ulonglong2 q0 = *reinterpret_cast<const ulonglong2*>(row + 16 + 32 * c);
-        const ulonglong2 q1 = *reinterpret_cast<const ulonglong2*>(row + 32 + 32 * c);
-        wp[r][0] = q0.x; wp[r][1] = q0.y; wp[r][2] = q1.x; wp[r][3] = q1.y;
+        a2[r] = __fmul2_rn(sc, make_float2(d96, d96));
+        nb2[r] = __fmul2_rn(mn, make_float2(ndmin, ndmin));
+        const uint4 q0 = *reinterpret_cast<const uint4*>(row + 16 + 32 * c);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(row + 32 + 32 * c);
+        wd[r][0] = q0.x; wd[r][1] = q0.y; wd[r][2] = q0.z; wd[r][3] = q0.w;
+        wd[r][4] = q1.x; wd[r][5] = q1.y; wd[r][6] = q1.z; wd[r][7] = q1.w;
     }
-    // accumulator pairs per (low/high nibbles, byte position parity)
-    F2 lo[R][MMAX][2], hi[R][MMAX][2];
+    // two accumulator chains per (row, activation row): even and odd words
+    F2 t[R][MMAX][2];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int m = 0; m < MMAX; ++m)
-#pragma unroll
-            for (int b = 0; b < 2; ++b) lo[r][m][b] = hi[r][m][b] = f2_zero();
+        for (int m = 0; m < MMAX; ++m) t[r][m][0] = t[r][m][1] = f2_zero();
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-        // x' of byte position b for the 8 words: low nibbles, high nibbles
-        float4 xl[MMAX][2], xh[MMAX][2];
+        // nibble masks at byte position b (byte 3 is shifted down to byte 2)
+        const uint32_t ml = b == 0 ? 0x0000000Fu : b == 1 ? 0x00000F00u : 0x000F0000u;
+        const uint32_t mh = ml << 4;
+        // x' of byte position b: (w lo, w hi, w+1 lo, w+1 hi) for w = 0, 2, 4, 6
+        float4 xv[MMAX][4];
 #pragma unroll
-        for (int m = 0; m < MMAX; ++m) {
-            const float* xm = xu + m * xs + c * cs + 2 * b * gs;
-            xl[m][0] = *reinterpret_cast<const float4*>(xm);
-            xl[m][1] = *reinterpret_cast<const float4*>(xm + gs);
-            xh[m][0] = *reinterpret_cast<const float4*>(xm + 8 * gs);
-            xh[m][1] = *reinterpret_cast<const float4*>(xm + 9 * gs);
-        }
+        for (int m = 0; m < MMAX; ++m)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                xv[m][q] = *reinterpret_cast<const float4*>(xu + m * xs + c * cs + 16 * b + 4 * q);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
 #pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                const uint64_t v = b < 3 ? wp[r][pp] : (wp[r][pp] >> 8);
-                const uint64_t ml = b == 0 ? kLo0 : b == 1 ? kLo1 : kLo2;
-                const uint64_t mh = b == 0 ? kHi0 : b == 1 ? kHi1 : kHi2;
-                const uint64_t pl = and64(v, ml), ph = and64(v, mh);
+            for (int w = 0; w < 8; ++w) {
+                const uint32_t v = b < 3 ? wd[r][w] : (wd[r][w] >> 8);
+                const uint64_t pr = and_pair(v, ml, mh);
 #pragma unroll
                 for (int m = 0; m < MMAX; ++m) {
-                    const float4 a = xl[m][pp >> 1], e = xh[m][pp >> 1];
-                    if (pp & 1) {
-                        f2_fma64(lo[r][m][b & 1], pl, a.z, a.w);
-                        f2_fma64(hi[r][m][b & 1], ph, e.z, e.w);
-                    } else {
-                        f2_fma64(lo[r][m][b & 1], pl, a.x, a.y);
-                        f2_fma64(hi[r][m][b & 1], ph, e.x, e.y);
-                    }
+                    const float4 x4 = xv[m][w >> 1];
+                    if (w & 1) f2_fma64(t[r][m][1], pr, x4.z, x4.w);
+                    else f2_fma64(t[r][m][0], pr, x4.x, x4.y);
                 }
             }
         }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+    for (int m = 0; m < MMAX; ++m) {
+        const float2 s2 = *reinterpret_cast<const float2*>(su + m * ss + 2 * c);
 #pragma unroll
-        for (int m = 0; m < MMAX; ++m) {
-            const float* sm = su + m * ss;
-            float a = acc[r][m];
-            a = fmaf(a_lo[r], f2_sum(lo[r][m][0], lo[r][m][1]), a);
-            a = fmaf(-b_lo[r], sm[2 * c * sj], a);
-            a = fmaf(a_hi[r], f2_sum(hi[r][m][0], hi[r][m][1]), a);
-            a = fmaf(-b_hi[r], sm[(2 * c + 1) * sj], a);
-            acc[r][m] = a;
+        for (int r = 0; r < R; ++r) {
+            uint64_t sv;
+            asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sv) : "l"(t[r][m][0].v), "l"(t[r][m][1].v));
+            float2 pv;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(pv.x), "=f"(pv.y) : "l"(sv));
+            f2_fma(acc[r][m], a2[r], pv);
+            f2_fma(acc[r][m], nb2[r], s2);
         }
     }
 }
@@ -197,22 +194,21 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
 // All four chunks of R rows.
 template <int MMAX, int R>
 __device__ __forceinline__ void q4k_tile_rows(const uint8_t* rp, int rstride, const float* xu, int xs,
-                                              const float* su, int ss, float (&acc)[R][MMAX], int gs = 4,
-                                              int sj = 1, int cs = 64) {
+                                              const float* su, int ss, float2 (&acc)[R][MMAX], int cs = 64) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) q4k_chunk_rows<MMAX, R>(rp, rstride, c, xu, xs, su, ss, acc, gs, sj, cs);
+    for (int c = 0; c < 4; ++c) q4k_chunk_rows<MMAX, R>(rp, rstride, c, xu, xs, su, ss, acc, cs);
 }
 
-// One row (R = 1) of the above.
+// One row (R = 1) of the above into plain float accumulators.
 template <int MMAX>
 __device__ __forceinline__ void q4k_tile_row(const uint8_t* rp, const float* xu, int xs, const float* su, int ss,
                                              float (&acc)[MMAX]) {
-    float a[1][MMAX];
+    float2 a[1][MMAX];
 #pragma unroll
-    for (int m = 0; m < MMAX; ++m) a[0][m] = acc[m];
+    for (int m = 0; m < MMAX; ++m) a[0][m] = make_float2(acc[m], 0.0f);
     q4k_tile_rows<MMAX, 1>(rp, 0, xu, xs, su, ss, a);
 #pragma unroll
-    for (int m = 0; m < MMAX; ++m) acc[m] = a[0][m];
+    for (int m = 0; m < MMAX; ++m) acc[m] = a[0][m].x + a[0][m].y;
 }
 
 // One 8-block Q8_0 period of one row (rp: 272 bytes) against x' indexed by

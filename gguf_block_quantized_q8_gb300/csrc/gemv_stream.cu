@@ -57,9 +57,10 @@ constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kRowsPerLane = 2;                 // rows r and r + 8 of a group
 constexpr int kGroupRows = 8 * kRowsPerLane;
 
-// The fields of a stage other than its tensor maps.  A CTA copies them to
-// shared memory one stage ahead: read from global memory after a stage
-// barrier (whose acquire leaves the L1 cold) each would wait an L2 round trip.
+// The fields of a stage other than its tensor maps.  A CTA keeps those of the
+// next stages in shared memory (kInfoSlots slots, stage s in slot s mod
+// kInfoSlots): read from global memory after a stage barrier, whose acquire
+// leaves the L1 cold, each would wait an L2 round trip.
 struct StageInfo {
     float* y[kMaxSeg];          // [M][rows]
     const float* x;             // [M][cols]
@@ -71,6 +72,9 @@ struct StageInfo {
     int pad[2];
 };
 constexpr int kInfoVec = sizeof(StageInfo) / 16;   // 16-byte pieces
+// While stage s runs, slots hold stages s .. s + kInfoSlots - 2; stage
+// s + kInfoSlots - 1 is being fetched into the slot stage s - 1 used.
+constexpr int kInfoSlots = 8;
 static_assert(sizeof(StageInfo) % 16 == 0, "StageInfo is copied in 16-byte pieces");
 
 // One stage of a chain (device-visible: kernel parameter or global table).
@@ -234,10 +238,10 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     const int r = lane >> 2, c = lane & 3;   // row of the group, chunk of the SB
     const int D = p.ring;
 
-    // shared memory: [warp rings][stage info x2][x'][sums][cut-group parts][barriers]
+    // shared memory: [warp rings][stage info slots][x'][sums][cut-group parts][barriers]
     uint8_t* ring = smem + (size_t)warp * D * B::kTile;
-    StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)W * D * B::kTile);   // stage s in slot s & 1
-    float* xp = reinterpret_cast<float*>(infos + 2);
+    StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)W * D * B::kTile);
+    float* xp = reinterpret_cast<float*>(infos + kInfoSlots);
     float* sums = xp + (size_t)MMAX * p.xs;
     float* cut_val = sums + (size_t)MMAX * p.nsub;                                // [2][W][8][MMAX]
     int* cut_grp = reinterpret_cast<int*>(cut_val + 2 * W * kGroupRows * MMAX);   // [2][W]
@@ -247,8 +251,10 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         for (int i = 0; i < D; ++i) mbar_init(&full[i], 1);
         fence_mbar_init();
     }
-    if (warp == 0 && lane < kInfoVec)
-        reinterpret_cast<int4*>(infos)[lane] = reinterpret_cast<const int4*>(p.table ? &p.table->info : &inl.info)[lane];
+    // stages 0 .. kInfoSlots - 2
+    for (int i = tid; i < min(p.nstages, kInfoSlots - 1) * kInfoVec; i += kThreads)
+        reinterpret_cast<int4*>(infos)[i] =
+            reinterpret_cast<const int4*>(p.table ? &p.table[i / kInfoVec].info : &inl.info)[i % kInfoVec];
     __syncthreads();
     pdl_launch_dependents();
 
@@ -258,6 +264,8 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     // group's matrix and first row, advanced without dividing
     int cs = -1, ct = 0, ct1 = 0, cU = 1, cgi = 0, cu = 0, cseg = 0, crow = 0;
     const StageDesc* csd = &inl;
+    const StageInfo* cinf = infos;   // the fields of stage cs
+    int scur = 0;                    // stage the CTA is in: slots hold scur .. scur + kInfoSlots - 2
     Groups cg{};
     int inflight = 0;   // copies issued and not yet consumed
     int islot = 0;      // ring slot of the next copy
@@ -267,15 +275,16 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 while (ct == ct1 && cs < p.nstages) {   // next stage in which this warp has tiles
                     if (++cs == p.nstages) break;
                     csd = p.table ? p.table + cs : &inl;
-                    cg = cta_groups(&csd->info, blockIdx.x, gridDim.x);
-                    warp_run<W>(cg, csd->info.units, warp, ct, ct1);
+                    cinf = cs <= scur + kInfoSlots - 2 ? infos + cs % kInfoSlots : &csd->info;
+                    cg = cta_groups(cinf, blockIdx.x, gridDim.x);
+                    warp_run<W>(cg, cinf->units, warp, ct, ct1);
                 }
                 if (cs >= p.nstages) break;
-                cU = csd->info.units;
+                cU = cinf->units;
                 cgi = ct / cU;
                 cu = ct - cgi * cU;
                 int nrows;
-                group_at(&csd->info, cg, cgi, cseg, crow, nrows);
+                group_at(cinf, cg, cgi, cseg, crow, nrows);
             }
             const int nv = min(min(B::kNsb, cU - cu), ct1 - ct);
             if (lane == 0) {
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 cu = 0;
                 ++cgi;
                 int nrows;
-                group_at(&csd->info, cg, cgi, cseg, crow, nrows);
+                group_at(cinf, cg, cgi, cseg, crow, nrows);
             }
             ++inflight;
             if (++islot == D) islot = 0;
@@ -319,17 +328,19 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     uint32_t cphase = 0;    // its barrier phase
 
     for (int s = 0; s < p.nstages; ++s) {
-        const StageInfo* sd = infos + (s & 1);
+        const StageInfo* sd = infos + s % kInfoSlots;
+        scur = s;
         // this CTA's row groups and this warp's tile run: independent of x, so
         // worked out before the stage barrier
         const Groups G = cta_groups(sd, blockIdx.x, gridDim.x);
         int t0, t1;
         warp_run<W>(G, sd->units, warp, t0, t1);
-        // the next stage's fields, to the other slot (free: every warp has
-        // passed the end of stage s-1); waited for before the end of stage s
-        if (s + 1 < p.nstages && warp == W - 1 && lane < kInfoVec)
-            cp_async_16(reinterpret_cast<int4*>(infos + ((s + 1) & 1)) + lane,
-                        reinterpret_cast<const int4*>(&p.table[s + 1].info) + lane);
+        // the fields of stage s + kInfoSlots - 1, to the slot of stage s - 1
+        // (free: every warp has passed the end of stage s - 1, and copy
+        // cursors never go back); waited for before the end of stage s
+        if (s + kInfoSlots - 1 < p.nstages && warp == W - 1 && lane < kInfoVec)
+            cp_async_16(reinterpret_cast<int4*>(infos + (s + kInfoSlots - 1) % kInfoSlots) + lane,
+                        reinterpret_cast<const int4*>(&p.table[s + kInfoSlots - 1].info) + lane);
         if (s == 0) {
             pdl_wait();   // x may come from the previous kernel in the stream
         } else {
@@ -582,7 +593,7 @@ size_t rows_smem(bool q4k, int mmax, int ring, int64_t cols_max) {
     const int W = warps_of(q4k, mmax);
     const int64_t U = cols_max / 256;
     const size_t cut = (size_t)2 * W * kGroupRows * mmax * 4 + (size_t)2 * W * 4;
-    return (size_t)W * ring * tile_bytes(q4k) + 2 * sizeof(StageInfo) + (size_t)mmax * U * 272 * 4 +
+    return (size_t)W * ring * tile_bytes(q4k) + kInfoSlots * sizeof(StageInfo) + (size_t)mmax * U * 272 * 4 +
            (size_t)mmax * U * 8 * 4 + cut +
            (size_t)W * ring * 8;
 }

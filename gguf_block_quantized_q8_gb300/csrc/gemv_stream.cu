@@ -75,6 +75,9 @@ constexpr int kInfoVec = sizeof(StageInfo) / 16;   // 16-byte pieces
 // While stage s runs, slots hold stages s .. s + kInfoSlots - 2; stage
 // s + kInfoSlots - 1 is being fetched into the slot stage s - 1 used.
 constexpr int kInfoSlots = 8;
+// Row ranges of the CTA in the first kPartMax stages, worked out once at the
+// start of a launch (two integer divisions each) and kept in shared memory.
+constexpr int kPartMax = 128;
 static_assert(sizeof(StageInfo) % 16 == 0, "StageInfo is copied in 16-byte pieces");
 
 // One stage of a chain (device-visible: kernel parameter or global table).
@@ -185,15 +188,22 @@ struct Groups {
 
 __device__ __forceinline__ int cta_row(int R, int b, int nb) {
     // R * b / nb; 32-bit division whenever the product fits (every realistic stage)
-    if ((unsigned)R <= 0xFFFFFFFFu / (unsigned)nb) return (int)((unsigned)R * (unsigned)b / (unsigned)nb);
-    return (int)((long long)R * b / nb);
+    const unsigned long long rb = (unsigned long long)(unsigned)R * (unsigned)b;
+    if (rb <= 0xFFFFFFFFull) return (int)((unsigned)rb / (unsigned)nb);
+    return (int)(rb / (unsigned)nb);
 }
 
-__device__ __forceinline__ Groups cta_groups(const StageInfo* sd, int b, int nb) {
-    Groups G;
+// Rows [R*b/nb, R*(b+1)/nb) of CTA b in a stage of R rows
+__device__ __forceinline__ int2 cta_rows(const StageInfo* sd, int b, int nb) {
     const int R = sd->row0[sd->nseg];
-    G.r0 = cta_row(R, b, nb);
-    G.r1 = cta_row(R, b + 1, nb);
+    return make_int2(cta_row(R, b, nb), cta_row(R, b + 1, nb));
+}
+
+// This CTA's row groups in a stage, given its row range rr
+__device__ __forceinline__ Groups cta_groups(const StageInfo* sd, int2 rr) {
+    Groups G;
+    G.r0 = rr.x;
+    G.r1 = rr.y;
     int n = 0;
 #pragma unroll
     for (int s = 0; s < kMaxSeg; ++s) {
@@ -241,7 +251,8 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     // shared memory: [warp rings][stage info slots][x'][sums][cut-group parts][barriers]
     uint8_t* ring = smem + (size_t)warp * D * B::kTile;
     StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)W * D * B::kTile);
-    float* xp = reinterpret_cast<float*>(infos + kInfoSlots);
+    int2* part = reinterpret_cast<int2*>(infos + kInfoSlots);   // [kPartMax]
+    float* xp = reinterpret_cast<float*>(part + kPartMax);
     float* sums = xp + (size_t)MMAX * p.xs;
     float* cut_val = sums + (size_t)MMAX * p.nsub;                                // [2][W][8][MMAX]
     int* cut_grp = reinterpret_cast<int*>(cut_val + 2 * W * kGroupRows * MMAX);   // [2][W]
@@ -251,10 +262,12 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         for (int i = 0; i < D; ++i) mbar_init(&full[i], 1);
         fence_mbar_init();
     }
-    // stages 0 .. kInfoSlots - 2
+    // stages 0 .. kInfoSlots - 2, and the row ranges
     for (int i = tid; i < min(p.nstages, kInfoSlots - 1) * kInfoVec; i += kThreads)
         reinterpret_cast<int4*>(infos)[i] =
             reinterpret_cast<const int4*>(p.table ? &p.table[i / kInfoVec].info : &inl.info)[i % kInfoVec];
+    for (int i = tid; i < min(p.nstages, kPartMax); i += kThreads)
+        part[i] = cta_rows(p.table ? &p.table[i].info : &inl.info, blockIdx.x, gridDim.x);
     __syncthreads();
     pdl_launch_dependents();
 
@@ -276,7 +289,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     if (++cs == p.nstages) break;
                     csd = p.table ? p.table + cs : &inl;
                     cinf = cs <= scur + kInfoSlots - 2 ? infos + cs % kInfoSlots : &csd->info;
-                    cg = cta_groups(cinf, blockIdx.x, gridDim.x);
+                    cg = cta_groups(cinf, cs < kPartMax ? part[cs] : cta_rows(cinf, blockIdx.x, gridDim.x));
                     warp_run<W>(cg, cinf->units, warp, ct, ct1);
                 }
                 if (cs >= p.nstages) break;
@@ -332,7 +345,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         scur = s;
         // this CTA's row groups and this warp's tile run: independent of x, so
         // worked out before the stage barrier
-        const Groups G = cta_groups(sd, blockIdx.x, gridDim.x);
+        const Groups G = cta_groups(sd, s < kPartMax ? part[s] : cta_rows(sd, blockIdx.x, gridDim.x));
         int t0, t1;
         warp_run<W>(G, sd->units, warp, t0, t1);
         // the fields of stage s + kInfoSlots - 1, to the slot of stage s - 1
@@ -593,7 +606,7 @@ size_t rows_smem(bool q4k, int mmax, int ring, int64_t cols_max) {
     const int W = warps_of(q4k, mmax);
     const int64_t U = cols_max / 256;
     const size_t cut = (size_t)2 * W * kGroupRows * mmax * 4 + (size_t)2 * W * 4;
-    return (size_t)W * ring * tile_bytes(q4k) + kInfoSlots * sizeof(StageInfo) + (size_t)mmax * U * 272 * 4 +
+    return (size_t)W * ring * tile_bytes(q4k) + kInfoSlots * sizeof(StageInfo) + kPartMax * sizeof(int2) + (size_t)mmax * U * 272 * 4 +
            (size_t)mmax * U * 8 * 4 + cut +
            (size_t)W * ring * 8;
 }

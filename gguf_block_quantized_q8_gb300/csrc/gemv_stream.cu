@@ -8,12 +8,13 @@
 //
 // Work unit: one 256-column block of one row (SB) -- a Q4_K super-block
 // (144 B) or a Q8_0 period of 8 blocks (272 B) -- split into four 64-column
-// chunks.  The rows of a stage's matrices are numbered one after another.
+// chunks.  Each matrix's rows form groups of 16 (the last may be shorter),
+// numbered across the stage's matrices.
 //
-//   * CTA b (one per SM) owns rows [R*b/G, R*(b+1)/G): whole rows, so no output
-//     is ever split between CTAs and no cross-CTA reduction exists.
-//   * Its rows form groups of 16 (inside one matrix); the (group, SB) tiles are
-//     cut into W equal contiguous runs, one per warp.  A warp streams its run
+//   * CTA b (one per SM) owns groups [GT*b/G, GT*(b+1)/G) of the stage's GT:
+//     whole rows, so no output is ever split between CTAs and no cross-CTA
+//     reduction exists.
+//   * Its (group, SB) tiles are cut into W equal contiguous runs, one per warp.  A warp streams its run
 //     through its own ring of 2-D bulk tensor copies (16 rows x up to NSB SBs);
 //     weights do not depend on earlier stages, so the ring runs ahead into the
 //     next stages while the chain waits at a stage boundary.
@@ -65,7 +66,7 @@ struct StageInfo {
     float* y[kMaxSeg];          // [M][rows]
     const float* x;             // [M][cols]
     int rows[kMaxSeg];
-    int row0[kMaxSeg + 1];      // first row of each matrix in the stage's numbering; row0[nseg] = rows of the stage
+    int gstart[kMaxSeg + 1];    // first row group of each matrix in the stage's numbering; gstart[nseg] = groups
     int nseg;
     int cols;
     int units;                  // U = cols / 256
@@ -75,7 +76,7 @@ constexpr int kInfoVec = sizeof(StageInfo) / 16;   // 16-byte pieces
 // While stage s runs, slots hold stages s .. s + kInfoSlots - 2; stage
 // s + kInfoSlots - 1 is being fetched into the slot stage s - 1 used.
 constexpr int kInfoSlots = 8;
-// Row ranges of the CTA in the first kPartMax stages, worked out once at the
+// Group ranges of the CTA in the first kPartMax stages, worked out once at the
 // start of a launch (two integer divisions each) and kept in shared memory.
 constexpr int kPartMax = 128;
 static_assert(sizeof(StageInfo) % 16 == 0, "StageInfo is copied in 16-byte pieces");
@@ -178,60 +179,45 @@ __device__ __forceinline__ void wait_full(uint64_t* bar, uint32_t parity, int* s
     }
 }
 
-// Row groups of CTA b (of nb) in a stage: its rows [r0, r1) cut at matrix
-// boundaries, then into groups of up to 16 rows.
+// Row groups: each matrix's rows in groups of 16 (its last group may be
+// shorter), numbered across the stage's matrices.  CTA b (of nb) takes groups
+// [GT*b/nb, GT*(b+1)/nb) of the stage's GT: whole groups, so a CTA whose range
+// crosses a matrix boundary gets no extra partial group.
 struct Groups {
-    int r0, r1;
-    int n;                 // groups
-    int first[kMaxSeg];    // index of the first group of each matrix
+    int g0;   // first group (stage numbering)
+    int n;    // groups
 };
 
-__device__ __forceinline__ int cta_row(int R, int b, int nb) {
-    // R * b / nb; 32-bit division whenever the product fits (every realistic stage)
-    const unsigned long long rb = (unsigned long long)(unsigned)R * (unsigned)b;
-    if (rb <= 0xFFFFFFFFull) return (int)((unsigned)rb / (unsigned)nb);
-    return (int)(rb / (unsigned)nb);
+__device__ __forceinline__ int cta_part(int GT, int b, int nb) {
+    // GT * b / nb; 32-bit division whenever the product fits (every realistic stage)
+    const unsigned long long gb = (unsigned long long)(unsigned)GT * (unsigned)b;
+    if (gb <= 0xFFFFFFFFull) return (int)((unsigned)gb / (unsigned)nb);
+    return (int)(gb / (unsigned)nb);
 }
 
-// Rows [R*b/nb, R*(b+1)/nb) of CTA b in a stage of R rows
-__device__ __forceinline__ int2 cta_rows(const StageInfo* sd, int b, int nb) {
-    const int R = sd->row0[sd->nseg];
-    return make_int2(cta_row(R, b, nb), cta_row(R, b + 1, nb));
+// Groups [g0, g1) of CTA b in a stage
+__device__ __forceinline__ int2 cta_span(const StageInfo* sd, int b, int nb) {
+    const int GT = sd->gstart[sd->nseg];
+    return make_int2(cta_part(GT, b, nb), cta_part(GT, b + 1, nb));
 }
 
-// This CTA's row groups in a stage, given its row range rr
-__device__ __forceinline__ Groups cta_groups(const StageInfo* sd, int2 rr) {
-    Groups G;
-    G.r0 = rr.x;
-    G.r1 = rr.y;
-    int n = 0;
-#pragma unroll
-    for (int s = 0; s < kMaxSeg; ++s) {
-        G.first[s] = n;
-        if (s < sd->nseg) {
-            const int lo = max(G.r0, sd->row0[s]), hi = min(G.r1, sd->row0[s + 1]);
-            if (lo < hi) n += (hi - lo + kGroupRows - 1) / kGroupRows;
-        }
-    }
-    G.n = n;
-    return G;
-}
+__device__ __forceinline__ Groups cta_groups(int2 span) { return Groups{span.x, span.y - span.x}; }
 
-// Group gi: matrix, first row (in the matrix), rows in the group.
+// The CTA's group gi: matrix, first row (in the matrix), rows in the group.
 __device__ __forceinline__ void group_at(const StageInfo* sd, const Groups& G, int gi, int& seg, int& row, int& nrows) {
+    const int g = G.g0 + gi;
     seg = 0;
 #pragma unroll
     for (int s = 1; s < kMaxSeg; ++s)
-        if (s < sd->nseg && gi >= G.first[s]) seg = s;
-    const int lo = max(G.r0, sd->row0[seg]), hi = min(G.r1, sd->row0[seg + 1]);
-    const int g0 = lo + (gi - G.first[seg]) * kGroupRows;
-    row = g0 - sd->row0[seg];
-    nrows = min(kGroupRows, hi - g0);
+        if (s < sd->nseg && g >= sd->gstart[s]) seg = s;
+    row = (g - sd->gstart[seg]) * kGroupRows;
+    nrows = min(kGroupRows, sd->rows[seg] - row);
 }
 
 // The tile run [t0, t1) of warp w (of NW): tile t = group * U + SB.  A CTA
-// holds fewer than 2^28 tiles (the stage holds fewer than 2^31 SBs and a CTA
-// at most 1/G of its rows plus one group per matrix), so T * w fits 32 bits.
+// holds fewer than 2^28 tiles (the stage holds fewer than 2^31 SBs, so fewer
+// than 2^27 + 4U group-SBs, and a CTA at most all of them), so T * w fits 32
+// bits.
 template <int NW>
 __device__ __forceinline__ void warp_run(const Groups& G, int U, int w, int& t0, int& t1) {
     const unsigned T = (unsigned)G.n * (unsigned)U;
@@ -267,7 +253,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         reinterpret_cast<int4*>(infos)[i] =
             reinterpret_cast<const int4*>(p.table ? &p.table[i / kInfoVec].info : &inl.info)[i % kInfoVec];
     for (int i = tid; i < min(p.nstages, kPartMax); i += kThreads)
-        part[i] = cta_rows(p.table ? &p.table[i].info : &inl.info, blockIdx.x, gridDim.x);
+        part[i] = cta_span(p.table ? &p.table[i].info : &inl.info, blockIdx.x, gridDim.x);
     __syncthreads();
     pdl_launch_dependents();
 
@@ -289,7 +275,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     if (++cs == p.nstages) break;
                     csd = p.table ? p.table + cs : &inl;
                     cinf = cs <= scur + kInfoSlots - 2 ? infos + cs % kInfoSlots : &csd->info;
-                    cg = cta_groups(cinf, cs < kPartMax ? part[cs] : cta_rows(cinf, blockIdx.x, gridDim.x));
+                    cg = cta_groups(cs < kPartMax ? part[cs] : cta_span(cinf, blockIdx.x, gridDim.x));
                     warp_run<W>(cg, cinf->units, warp, ct, ct1);
                 }
                 if (cs >= p.nstages) break;
@@ -345,7 +331,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         scur = s;
         // this CTA's row groups and this warp's tile run: independent of x, so
         // worked out before the stage barrier
-        const Groups G = cta_groups(sd, s < kPartMax ? part[s] : cta_rows(sd, blockIdx.x, gridDim.x));
+        const Groups G = cta_groups(s < kPartMax ? part[s] : cta_span(sd, blockIdx.x, gridDim.x));
         int t0, t1;
         warp_run<W>(G, sd->units, warp, t0, t1);
         // the fields of stage s + kInfoSlots - 1, to the slot of stage s - 1
@@ -651,17 +637,17 @@ int make_stage(int type, int n, const void* const* W, const int64_t* rows, int64
                float* const* y, StageDesc* sd) {
     const bool q4k = type == GGQ_Q4_K;
     memset(sd, 0, sizeof(*sd));
-    int r = 0;
+    int g = 0;
     for (int s = 0; s < n; ++s) {
         const int64_t row_bytes = cols / 256 * (q4k ? 144 : 272);
         int rc = encode_map(&sd->maps[s], W[s], rows[s], row_bytes, q4k);
         if (rc) return rc;
         sd->info.y[s] = y[s];
         sd->info.rows[s] = (int)rows[s];
-        sd->info.row0[s] = r;
-        r += (int)rows[s];
+        sd->info.gstart[s] = g;
+        g += (int)((rows[s] + kGroupRows - 1) / kGroupRows);
     }
-    sd->info.row0[n] = r;
+    sd->info.gstart[n] = g;
     sd->info.nseg = n;
     sd->info.x = x;
     sd->info.cols = (int)cols;

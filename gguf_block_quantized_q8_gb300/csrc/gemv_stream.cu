@@ -581,7 +581,7 @@ int warps_of(bool q4k, int mmax) {
     }();
     if (env && mmax == 1) return env;
     (void)q4k;
-    return mmax == 4 ? 8 : 16;
+    return mmax == 4 ? 12 : 16;
 }
 
 constexpr int kMaxRing = 8;
@@ -711,7 +711,7 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
             return launch_t<true, 1, 16>(inl, p, stream, smem, coop);
         }
         if (mmax == 2) return launch_t<true, 2, 16>(inl, p, stream, smem, coop);
-        return launch_t<true, 4, 8>(inl, p, stream, smem, coop);
+        return launch_t<true, 4, 12>(inl, p, stream, smem, coop);
     }
     if (mmax == 1) {
         if (W == 8) return launch_t<false, 1, 8>(inl, p, stream, smem, coop);
@@ -719,7 +719,7 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
         return launch_t<false, 1, 16>(inl, p, stream, smem, coop);
     }
     if (mmax == 2) return launch_t<false, 2, 16>(inl, p, stream, smem, coop);
-    return launch_t<false, 4, 8>(inl, p, stream, smem, coop);
+    return launch_t<false, 4, 12>(inl, p, stream, smem, coop);
 }
 
 }  // namespace

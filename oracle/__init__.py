@@ -8,7 +8,9 @@ shares no code with it; the two meet only on input bytes from ``synth``.
 * ``ggq_oracle.c`` -- fp16 decode from IEEE-754, Q8_0 / Q4_K block decode to
   fp32, GEMV / GEMM with every product and sum in double (see its header for
   the passages followed);
-* ``gguf_reader.py`` -- a plain byte walk of GGUF v3.
+* ``gguf_reader.py`` -- a plain byte walk of GGUF v3;
+* ``layer_ops.py`` -- RMSNorm, SiLU(gate) * up and the residual add in float64,
+  the element-wise steps the chain fuses into its GEMV stages.
 
 Parity status: fp16 decode, Q8_0 decode, GEMV/GEMM and the GGUF reader are
 pinned by the tests in tests/test_oracle_pins.py.  Q4_K decode is pinned by

@@ -35,6 +35,14 @@ class ChainStage(ctypes.Structure):
                 ("cols", ctypes.c_int64), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p * 4)]
 
 
+X_PLAIN, X_RMSNORM, X_SILU_MUL = 0, 1, 2
+
+
+class ChainOps(ctypes.Structure):
+    _fields_ = [("x_op", ctypes.c_int), ("eps", ctypes.c_float), ("norm_w", ctypes.c_void_p),
+                ("up", ctypes.c_void_p), ("res", ctypes.c_void_p * 4)]
+
+
 def _bind(lib):
     vp, i64, u64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int32
     sig = {
@@ -57,6 +65,8 @@ def _bind(lib):
         "ggq_gemv_noalloc": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
         "ggq_chain_create": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ChainStage),
                               ctypes.POINTER(vp)], ctypes.c_int),
+        "ggq_chain_create_ops": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ChainStage),
+                                  ctypes.POINTER(ChainOps), ctypes.POINTER(vp)], ctypes.c_int),
         "ggq_chain_run": ([vp, vp], ctypes.c_int),
         "ggq_chain_reset": ([vp], ctypes.c_int),
         "ggq_chain_free": ([vp], None),
@@ -115,8 +125,10 @@ def ggq_gemv_multi(qtype: int, Ws, rows, cols: int, x: int, ys, M: int, stream: 
     return lib.ggq_gemv_multi(qtype, n, Wa, ra, cols, x, ya, M, stream)
 
 
-def ggq_chain_create(qtype: int, M: int, stages) -> tuple[int, int]:
-    """stages: sequence of (Ws, rows, cols, x, ys) with device pointers; returns (rc, handle)."""
+def ggq_chain_create(qtype: int, M: int, stages, ops=None) -> tuple[int, int]:
+    """stages: sequence of (Ws, rows, cols, x, ys) with device pointers; ops: None, or
+    per stage None or a dict with keys x_op, eps, norm_w, up, res (a list of up to 4
+    pointers or None), pointers as ints; returns (rc, handle)."""
     arr = (ChainStage * len(stages))()
     for i, (Ws, rows, cols, x, ys) in enumerate(stages):
         st = arr[i]
@@ -128,7 +140,20 @@ def ggq_chain_create(qtype: int, M: int, stages) -> tuple[int, int]:
         st.cols = cols
         st.x = x
     h = ctypes.c_void_p()
-    rc = lib.ggq_chain_create(qtype, M, len(stages), arr, ctypes.byref(h))
+    if ops is None:
+        rc = lib.ggq_chain_create(qtype, M, len(stages), arr, ctypes.byref(h))
+    else:
+        oa = (ChainOps * len(stages))()
+        for i, o in enumerate(ops):
+            if not o:
+                continue
+            oa[i].x_op = o.get("x_op", X_PLAIN)
+            oa[i].eps = o.get("eps", 0.0)
+            oa[i].norm_w = o.get("norm_w") or None
+            oa[i].up = o.get("up") or None
+            for j, r in enumerate((o.get("res") or [])[:4]):
+                oa[i].res[j] = r or None
+        rc = lib.ggq_chain_create_ops(qtype, M, len(stages), arr, oa, ctypes.byref(h))
     return rc, (h.value or 0)
 
 
@@ -276,16 +301,26 @@ class Chain:
     """A sequence of GEMV stages run as one launch (ggq_chain_create / ggq_chain_run).
 
     stages: sequence of (Ws, rows, cols, x, ys) with CUDA tensors; the chain keeps
-    references to them (their memory is bound at creation).
+    references to them (their memory is bound at creation).  ops: None, or per
+    stage None or a dict {x_op: X_RMSNORM / X_SILU_MUL, eps, norm_w, up, res: [..]}
+    with CUDA tensors (ggq_chain_create_ops).
     """
 
-    def __init__(self, qtype: int, M: int, stages):
+    def __init__(self, qtype: int, M: int, stages, ops=None):
         raw = [([w.data_ptr() for w in Ws], list(rows), cols, x.data_ptr(), [y.data_ptr() for y in ys])
                for (Ws, rows, cols, x, ys) in stages]
-        rc, h = ggq_chain_create(qtype, M, raw)
+        rops = None
+        if ops is not None:
+            def ptr(t):
+                return t.data_ptr() if t is not None else None
+            rops = [None if o is None else
+                    {"x_op": o.get("x_op", X_PLAIN), "eps": o.get("eps", 0.0), "norm_w": ptr(o.get("norm_w")),
+                     "up": ptr(o.get("up")), "res": [ptr(t) for t in (o.get("res") or [])]}
+                    for o in ops]
+        rc, h = ggq_chain_create(qtype, M, raw, rops)
         check(rc, "ggq_chain_create")
         self._h = h
-        self._keep = list(stages)
+        self._keep = list(stages) + ([ops] if ops is not None else [])
 
     def run(self, stream=None) -> None:
         check(ggq_chain_run(self._h, _stream_ptr(stream)), "ggq_chain_run")

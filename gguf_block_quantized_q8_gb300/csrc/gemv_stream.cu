@@ -37,6 +37,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstddef>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -65,12 +66,16 @@ constexpr int kGroupRows = 8 * kRowsPerLane;
 struct StageInfo {
     float* y[kMaxSeg];          // [M][rows]
     const float* x;             // [M][cols]
+    const float* norm_w;        // x_op RMSNORM: [cols]
+    const float* up;            // x_op SILU_MUL: [M][cols]
+    const float* res[kMaxSeg];  // null, or [M][rows]: added to y
     int rows[kMaxSeg];
     int gstart[kMaxSeg + 1];    // first row group of each matrix in the stage's numbering; gstart[nseg] = groups
     int nseg;
     int cols;
     int units;                  // U = cols / 256
-    int pad[2];
+    int x_op;                   // GGQ_X_PLAIN / RMSNORM / SILU_MUL
+    float eps;                  // RMSNORM
 };
 constexpr int kInfoVec = sizeof(StageInfo) / 16;   // 16-byte pieces
 // While stage s runs, slots hold stages s .. s + kInfoSlots - 2; stage
@@ -362,42 +367,109 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             // scales of its 4 values are the lane constants xoff and xsc.
             // Every load of a batch is issued before any is used (one L2 round
             // trip per batch of kBatch float4 per lane).
-            constexpr int kBatch = 8;
             const int c4 = cols / 4;          // float4 per activation row
             const int n4 = p.M * c4;
             const float4* x4 = reinterpret_cast<const float4*>(sd->x);
-            for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
-                float4 v[kBatch];
-#pragma unroll
-                for (int i = 0; i < kBatch; ++i) {
-                    const int q = q0 + i * kThreads + lane;
-                    v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            // place the float4 v of warp step qb (the lane's 4 columns): x', and
+            // the sub-block sum from 8 lanes
+            auto place = [&](int qb, float4 v) {
+                float sum = (v.x + v.y) + (v.z + v.w);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                const int m = MMAX == 1 ? 0 : qb / c4;
+                const int h = qb - m * c4;          // first float4 of the step within the row
+                const int u = h >> 6;               // SB
+                float* dst = xp + (size_t)m * xs + u * 272 + ((h & 32) ? 136 : 0) + xoff;
+                const float4 e = make_float4(v.x * xsc.x, v.y * xsc.y, v.z * xsc.z, v.w * xsc.w);
+                if (Q4K) {
+                    dst[0] = e.x;
+                    dst[16] = e.y;
+                    dst[32] = e.z;
+                    dst[48] = e.w;
+                } else {
+                    dst[0] = e.x;
+                    dst[1] = e.y;
+                    dst[2] = e.z;
+                    dst[3] = e.w;
                 }
+                if ((lane & 7) == 0) sums[m * nsub + u * 8 + ((h & 32) >> 3) + (lane >> 3)] = Q4K ? sum : 128.0f * sum;
+            };
+            const int xop = sd->x_op;
+            if (xop == GGQ_X_PLAIN) {
+                constexpr int kBatch = 8;
+                for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                    float4 v[kBatch];
 #pragma unroll
-                for (int i = 0; i < kBatch; ++i) {
-                    const int qb = q0 + i * kThreads;   // warp-uniform, a multiple of 32
-                    if (qb >= n4) break;
-                    float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                    const int m = MMAX == 1 ? 0 : qb / c4;
-                    const int h = qb - m * c4;          // first float4 of the step within the row
-                    const int u = h >> 6;               // SB
-                    float* dst = xp + (size_t)m * xs + u * 272 + ((h & 32) ? 136 : 0) + xoff;
-                    const float4 e = make_float4(v[i].x * xsc.x, v[i].y * xsc.y, v[i].z * xsc.z, v[i].w * xsc.w);
-                    if (Q4K) {
-                        dst[0] = e.x;
-                        dst[16] = e.y;
-                        dst[32] = e.z;
-                        dst[48] = e.w;
-                    } else {
-                        dst[0] = e.x;
-                        dst[1] = e.y;
-                        dst[2] = e.z;
-                        dst[3] = e.w;
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int q = q0 + i * kThreads + lane;
+                        v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    if ((lane & 7) == 0) sums[m * nsub + u * 8 + ((h & 32) >> 3) + (lane >> 3)] = Q4K ? sum : 128.0f * sum;
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int qb = q0 + i * kThreads;   // warp-uniform, a multiple of 32
+                        if (qb >= n4) break;
+                        place(qb, v[i]);
+                    }
+                }
+            } else {
+                // fused step on x ("GGUF Inferencer in R" section 4).  RMSNORM: the
+                // sum of squares of each activation row first (a CTA reduction
+                // through the cut-group scratch, free until the tiles), then
+                // norm_w * x / sqrt(mean + eps).  SILU_MUL: silu(x) * up.
+                float rs[MMAX];
+                if (xop == GGQ_X_RMSNORM) {
+                    float* red = cut_val;   // [W][MMAX]
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m) {
+                        float ss = 0.0f;
+                        if (m < p.M) {
+#pragma unroll 4
+                            for (int q = tid; q < c4; q += kThreads) {
+                                const float4 v = __ldcg(x4 + (size_t)m * c4 + q);
+                                ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+                            }
+                        }
+                        ss = warp_sum(ss);
+                        if (lane == 0) red[warp * MMAX + m] = ss;
+                    }
+                    __syncthreads();
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m) {
+                        float t = 0.0f;
+                        for (int w2 = 0; w2 < W; ++w2) t += red[w2 * MMAX + m];   // same order in every thread
+                        rs[m] = 1.0f / sqrtf(t / (float)cols + sd->eps);
+                    }
+                }
+                const float4* o4 = reinterpret_cast<const float4*>(xop == GGQ_X_RMSNORM ? sd->norm_w : sd->up);
+                constexpr int kBatch = 4;   // two float4 a step: x and norm_w / up
+                for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                    float4 v[kBatch], o[kBatch];
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int q = q0 + i * kThreads + lane;
+                        const int qb = q0 + i * kThreads;
+                        const int m = MMAX == 1 ? 0 : qb / c4;
+                        v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        o[i] = q < n4 ? __ldcg(o4 + (xop == GGQ_X_RMSNORM ? q - m * c4 : q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int qb = q0 + i * kThreads;
+                        if (qb >= n4) break;
+                        float4 t = v[i];
+                        if (xop == GGQ_X_RMSNORM) {
+                            float r = rs[0];
+#pragma unroll
+                            for (int m = 1; m < MMAX; ++m)
+                                if (qb >= m * c4) r = rs[m];
+                            t = make_float4(o[i].x * (t.x * r), o[i].y * (t.y * r), o[i].z * (t.z * r), o[i].w * (t.w * r));
+                        } else {
+                            t = make_float4(t.x / (1.0f + expf(-t.x)) * o[i].x, t.y / (1.0f + expf(-t.y)) * o[i].y,
+                                            t.z / (1.0f + expf(-t.z)) * o[i].z, t.w / (1.0f + expf(-t.w)) * o[i].w);
+                        }
+                        place(qb, t);
+                    }
                 }
             }
         }
@@ -416,6 +488,27 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 acc2[i][m] = make_float2(0.0f, 0.0f);
             }
         int cur = -1;   // group being accumulated
+        // the residual of the group's rows (lanes c == 0), read when the warp
+        // starts a group whose first tile is in its run: that warp's part of
+        // the group is the one that carries it (deterministic sum order)
+        float resv[R][MMAX];
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int m = 0; m < MMAX; ++m) resv[i][m] = 0.0f;
+        auto load_res = [&](int gi) {
+            if (c != 0 || gi * U < t0) return;
+            int seg, row, nrows;
+            group_at(sd, G, gi, seg, row, nrows);
+            const float* rp = sd->res[seg];
+            if (!rp) return;
+            const int rows = sd->rows[seg];
+#pragma unroll
+            for (int i = 0; i < R; ++i)
+#pragma unroll
+                for (int m = 0; m < MMAX; ++m)
+                    resv[i][m] = (r + 8 * i < nrows && m < p.M) ? __ldcg(rp + (int64_t)m * rows + row + r + 8 * i) : 0.0f;
+        };
 
         // finish group gi: add each row's four chunks, then store the group's
         // rows if this warp saw all of its SBs, else keep this warp's part
@@ -433,6 +526,15 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 }
             const bool started = gi * U >= t0;
             const bool whole = started && (gi + 1) * U <= t1;
+            if (started && c == 0) {
+#pragma unroll
+                for (int i = 0; i < R; ++i)
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m) {
+                        acc[i][m] += resv[i][m];
+                        resv[i][m] = 0.0f;
+                    }
+            }
             if (whole) {
                 int seg, row, nrows;
                 group_at(sd, G, gi, seg, row, nrows);
@@ -471,6 +573,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             const int nv = min(min(B::kNsb, U - u), t1 - t);
             if (gi != cur) {
                 if (cur >= 0) flush(cur);
+                load_res(gi);
                 cur = gi;
             }
             wait_full(&full[cslot], cphase, p.status);
@@ -759,6 +862,11 @@ struct ggq_chain {
 };
 
 extern "C" int ggq_chain_create(int type, int M, int nstages, const ggq_chain_stage* stages, ggq_chain** out) {
+    return ggq_chain_create_ops(type, M, nstages, stages, nullptr, out);
+}
+
+extern "C" int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chain_stage* stages,
+                                    const ggq_chain_ops* ops, ggq_chain** out) {
     clear_error();
     if (!out) return fail(GGQ_EINVAL, "ggq_chain_create: out is NULL");
     *out = nullptr;
@@ -780,6 +888,23 @@ extern "C" int ggq_chain_create(int type, int M, int nstages, const ggq_chain_st
         }
         if (!stream_gemv_supported(type, st.cols, M, st.n, st.rows))
             return fail(GGQ_EINVAL, "ggq_chain_create: stage %d shape unsupported (cols %% 256, size)", s);
+        if (ops) {
+            const ggq_chain_ops& o = ops[s];
+            if (o.x_op == GGQ_X_RMSNORM) {
+                if (!o.norm_w || (reinterpret_cast<uintptr_t>(o.norm_w) & 15) != 0)
+                    return fail(GGQ_EINVAL, "ggq_chain_create: stage %d norm_w missing or not 16-byte aligned", s);
+                if (!(o.eps >= 0.0f) || !(o.eps < INFINITY))
+                    return fail(GGQ_EINVAL, "ggq_chain_create: stage %d eps must be finite and >= 0", s);
+            } else if (o.x_op == GGQ_X_SILU_MUL) {
+                if (!o.up || (reinterpret_cast<uintptr_t>(o.up) & 15) != 0)
+                    return fail(GGQ_EINVAL, "ggq_chain_create: stage %d up missing or not 16-byte aligned", s);
+            } else if (o.x_op != GGQ_X_PLAIN) {
+                return fail(GGQ_EINVAL, "ggq_chain_create: stage %d x_op %d unknown", s, o.x_op);
+            }
+            for (int i = 0; i < st.n; ++i)
+                if ((reinterpret_cast<uintptr_t>(o.res[i]) & 3) != 0)
+                    return fail(GGQ_EINVAL, "ggq_chain_create: stage %d res[%d] misaligned", s, i);
+        }
         cols_max = std::max<int64_t>(cols_max, st.cols);
     }
     if (rows_ring(type == GGQ_Q4_K, mmax_of(M), cols_max) == 0)
@@ -788,6 +913,14 @@ extern "C" int ggq_chain_create(int type, int M, int nstages, const ggq_chain_st
         const ggq_chain_stage& st = stages[s];
         int rc = make_stage(type, st.n, st.W, st.rows, st.cols, st.x, st.y, &host[(size_t)s]);
         if (rc) return rc;
+        if (ops) {
+            StageInfo& si = host[(size_t)s].info;
+            si.x_op = ops[s].x_op;
+            si.eps = ops[s].eps;
+            si.norm_w = ops[s].norm_w;
+            si.up = ops[s].up;
+            for (int i = 0; i < st.n; ++i) si.res[i] = ops[s].res[i];
+        }
     }
     ggq_chain* c = new (std::nothrow) ggq_chain();
     if (!c) return fail(GGQ_ENOMEM, "host allocation failed");

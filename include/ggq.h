@@ -220,6 +220,50 @@ typedef struct ggq_chain ggq_chain;
 int ggq_chain_create(int type, int M, int nstages, const ggq_chain_stage* stages, ggq_chain** out);
 
 /*
+ * Element-wise steps fused into a chain stage.  "GGUF Inferencer in R" section
+ * 4 walks a layer: the input is RMS-normalized ("Normalize Input", before the
+ * q/k/v and again before the gate/up projections), the gate projection goes
+ * through SiLU and multiplies the up projection ("Activate Weights", before
+ * the down projection), and the o and down projections are added to the
+ * layer's input ("Add to Input").  The C++ engine post (culpeo.ws) lists the
+ * same steps as the kernels rmsnorm, silu_mul and add.  A chain applies them
+ * while it reads a stage's x and while it stores its y: no launch and no
+ * extra pass over memory of their own.
+ *
+ *   x_op     GGQ_X_PLAIN     the stage multiplies x as given;
+ *            GGQ_X_RMSNORM   ... norm_w[k] * x[m,k] / sqrt(mean_k x[m,k]^2 + eps)
+ *                            (norm_w: device fp32 [cols], 16-byte aligned;
+ *                            eps finite, >= 0; the mean over the stage's cols);
+ *            GGQ_X_SILU_MUL  ... silu(x[m,k]) * up[m,k], silu(v) = v / (1 + e^-v)
+ *                            (up: device fp32 [M, cols], 16-byte aligned).
+ *   res[i]   NULL, or device fp32 [M, rows[i]], 4-byte aligned:
+ *            y[i] = W_i x' + res[i] (res[i] may be the stage's own y[i]: the
+ *            add happens as y[i] is written, after res[i] was read).
+ * x, norm_w, up and res are only read; each may be an output of an earlier
+ * stage of the chain (it is read after that stage's outputs are written).
+ * Arithmetic is fp32: the sum of squares, 1 / sqrt by the IEEE square root and
+ * division, SiLU with expf and an IEEE division.
+ */
+enum { GGQ_X_PLAIN = 0, GGQ_X_RMSNORM = 1, GGQ_X_SILU_MUL = 2 };
+
+typedef struct {
+    int x_op;
+    float eps;
+    const float* norm_w;
+    const float* up;
+    const float* res[4];
+} ggq_chain_ops;
+
+/*
+ * ggq_chain_create_ops -- ggq_chain_create with the fused steps of each stage:
+ * ops[s] for stage s (ops may be NULL: no fused steps anywhere).  Errors as for
+ * ggq_chain_create; a bad x_op, a missing or misaligned norm_w / up / res, or a
+ * negative or non-finite eps is GGQ_EINVAL naming the stage.  Synchronous.
+ */
+int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chain_stage* stages, const ggq_chain_ops* ops,
+                         ggq_chain** out);
+
+/*
  * ggq_chain_run -- run every stage of the chain, in order, as one cooperative
  * launch (every CTA resident at once, one per SM) on `stream` (cudaStream_t)
  * on the device the chain was created on.  The chain's stage counter lives in

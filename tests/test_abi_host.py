@@ -192,3 +192,25 @@ def test_chain_create_validates_stages(ggq):
     assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([16] * 5, [64] * 5, 256, 16, [16] * 5)])[0] == -1   # n = 5
     assert ggq.ggq_chain_run(0, 0) == -1
     ggq.ggq_chain_free(0)
+
+
+def test_chain_create_ops_validates_fused_steps(ggq):
+    """ggq_chain_create_ops rejects malformed fused steps before touching the device."""
+    ok = ([16], [64], 2048, 16, [16])
+
+    def rc(op, stages=None):
+        stages = stages or [ok, ok]
+        return ggq.ggq_chain_create(ggq.Q4_K, 1, stages, [None, op])[0]
+
+    assert rc({"x_op": ggq.X_RMSNORM, "eps": 1e-6, "norm_w": 0}) == -1             # norm_w missing
+    assert "stage 1" in ggq.lib.ggq_last_error().decode()
+    assert rc({"x_op": ggq.X_RMSNORM, "eps": 1e-6, "norm_w": 24}) == -1            # norm_w misaligned
+    assert rc({"x_op": ggq.X_RMSNORM, "eps": -1.0, "norm_w": 32}) == -1            # eps < 0
+    assert rc({"x_op": ggq.X_RMSNORM, "eps": float("nan"), "norm_w": 32}) == -1    # eps NaN
+    assert rc({"x_op": ggq.X_RMSNORM, "eps": float("inf"), "norm_w": 32}) == -1    # eps infinite
+    assert rc({"x_op": ggq.X_SILU_MUL, "up": 0}) == -1                             # up missing
+    assert rc({"x_op": ggq.X_SILU_MUL, "up": 8}) == -1                             # up misaligned
+    assert rc({"x_op": 7}) == -1                                                   # unknown step
+    assert "x_op 7" in ggq.lib.ggq_last_error().decode()
+    assert rc({"res": [6]}) == -1                                                  # residual misaligned
+    assert "res[0]" in ggq.lib.ggq_last_error().decode()

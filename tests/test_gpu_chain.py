@@ -171,3 +171,130 @@ def test_chain_in_cuda_graph(env):
     assert ggq.device_status() == 0
     out = {n: y.cpu().numpy() for n, y in net.y.items()}
     net.check(x1, out)
+
+
+# ---- fused steps: RMSNorm / SiLU(gate)*up on x, residual add on y -----------
+
+from oracle import layer_ops  # noqa: E402
+
+
+def _fused_layers(torch, ggq, qtype, M, H, KV, F, layers, seed):
+    """A residual stream through `layers` Llama-style layers as one fused chain:
+    [q,k,v](rmsnorm(h)), [o](q) + h, [gate,up](rmsnorm(h2)), [down](silu(gate)*up) + h2.
+    Returns the chain, the buffers and, per stage, what the oracle needs."""
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()   # noqa: E731
+    h0 = torch.empty((M, H), dtype=torch.float32, device="cuda")
+    stages, ops, plan = [], [], []
+    h = h0
+    for l in range(layers):
+        W = {}
+        for j, (name, r, c) in enumerate([("q", H, H), ("k", KV, H), ("v", KV, H), ("o", H, H),
+                                          ("gate", F, H), ("up", F, H), ("down", H, F)]):
+            W[name] = (synth.weight_rows(qtype, 300 + 31 * seed + 10 * l + j, r, c), r, c)
+        Wd = {n: dev(w) for n, (w, _, _) in W.items()}
+        y = {n: torch.full((M, r), float("nan"), dtype=torch.float32, device="cuda") for n, (_, r, _) in W.items()}
+        g_attn = (1.0 + 0.1 * synth.normal_f32(H, 400 + 7 * seed + 2 * l)).astype(np.float32)
+        g_ffn = (1.0 + 0.1 * synth.normal_f32(H, 401 + 7 * seed + 2 * l)).astype(np.float32)
+        ga, gf = dev(g_attn), dev(g_ffn)
+        eps = 1e-6
+        stages += [([Wd["q"], Wd["k"], Wd["v"]], [H, KV, KV], H, h, [y["q"], y["k"], y["v"]]),
+                   ([Wd["o"]], [H], H, y["q"], [y["o"]]),
+                   ([Wd["gate"], Wd["up"]], [F, F], H, y["o"], [y["gate"], y["up"]]),
+                   ([Wd["down"]], [H], F, y["gate"], [y["down"]])]
+        ops += [{"x_op": ggq.X_RMSNORM, "eps": eps, "norm_w": ga},
+                {"res": [h]},
+                {"x_op": ggq.X_RMSNORM, "eps": eps, "norm_w": gf},
+                {"x_op": ggq.X_SILU_MUL, "up": y["up"], "res": [y["o"]]}]
+        plan += [(["q", "k", "v"], W, y, ("rms", h, g_attn, eps), None),
+                 (["o"], W, y, ("plain", y["q"]), h),
+                 (["gate", "up"], W, y, ("rms", y["o"], g_ffn, eps), None),
+                 (["down"], W, y, ("silu", y["gate"], y["up"]), y["o"])]
+        h = y["down"]
+    chain = ggq.Chain(qtype, M, stages, ops)
+    return chain, h0, plan, (stages, ops)
+
+
+def _check_fused(qtype, plan):
+    worst = 0.0
+    for names, W, y, xin, res in plan:
+        xa = xin[1].cpu().numpy().astype(np.float64)          # what the stage read
+        if xin[0] == "rms":
+            xr = layer_ops.rmsnorm(xa, xin[2], xin[3])
+        elif xin[0] == "silu":
+            xr = layer_ops.silu_mul(xa, xin[2].cpu().numpy().astype(np.float64))
+        else:
+            xr = xa
+        assert np.isfinite(xr).all()
+        for n in names:
+            w, rows, cols = W[n]
+            wd = oracle.dequantize(qtype, w, rows, cols).astype(np.float64)   # exact decoded weights
+            y_ref = xr @ wd.T
+            a_ref = np.abs(xr) @ np.abs(wd).T
+            if res is not None:
+                r = res.cpu().numpy().astype(np.float64)
+                y_ref = layer_ops.add(y_ref, r)
+                a_ref = a_ref + np.abs(r)
+            ok, wr = oracle.tolerance_ok(y[n].cpu().numpy(), y_ref, a_ref, REL, ABS)
+            assert ok, f"{n}: worst error / bound = {wr:.3g}"
+            worst = max(worst, wr)
+    return worst
+
+
+@pytest.mark.parametrize("qtype,M", [(12, 1), (12, 2), (12, 3), (8, 1), (8, 4)])
+def test_chain_fused_layers(env, qtype, M):
+    """Two fused layers (RMSNorm before q/k/v and gate/up, SiLU(gate)*up into down,
+    residual adds after o and down) against the oracle's layer steps + GEMV,
+    each stage fed with what it actually read on the GPU."""
+    torch, ggq = env
+    chain, h0, plan, _ = _fused_layers(torch, ggq, qtype, M, 1280, 256, 2816, 2, seed=qtype + M)
+    for run in range(2):
+        h0.copy_(torch.from_numpy((3.0 * synth.normal_f32(M * 1280, 500 + run)).reshape(M, 1280)))
+        chain.run()
+        torch.cuda.synchronize()
+        assert ggq.device_status() == 0
+        _check_fused(qtype, plan)
+
+
+def test_chain_fused_residual_into_own_output(env):
+    """res may be the stage's own y: y = W x + y_before."""
+    torch, ggq = env
+    rows, cols = 3000, 2048
+    W = synth.weight_rows(12, 610, rows, cols)
+    x = synth.normal_f32(cols, 611).reshape(1, cols)
+    y0 = synth.normal_f32(rows, 612).reshape(1, rows)
+    Wd, xd = _dev(torch, W), _dev(torch, x)
+    yd = _dev(torch, y0)
+    ch = ggq.Chain(12, 1, [([Wd], [rows], cols, xd, [yd])], [{"res": [yd]}])
+    ch.run()
+    torch.cuda.synchronize()
+    assert ggq.device_status() == 0
+    wd = oracle.dequantize(12, W, rows, cols).astype(np.float64)
+    y_ref = x.astype(np.float64) @ wd.T + y0
+    a_ref = np.abs(x.astype(np.float64)) @ np.abs(wd).T + np.abs(y0)
+    ok, wr = oracle.tolerance_ok(yd.cpu().numpy(), y_ref, a_ref, REL, ABS)
+    assert ok, wr
+
+
+def test_chain_fused_rmsnorm_spiky_and_zero_rows(env):
+    """RMSNorm on activation rows of very different scale, one of them all zero
+    (eps keeps it finite: its normalized x is 0)."""
+    torch, ggq = env
+    M, rows, cols = 3, 1500, 4096
+    W = synth.weight_rows(12, 620, rows, cols)
+    x = synth.normal_f32(M * cols, 621).reshape(M, cols).astype(np.float64)
+    x[0] *= 1e-4
+    x[1] = 0.0
+    x[2, 17] = 5e4    # one spike
+    x = x.astype(np.float32)
+    g = (1.0 + 0.1 * synth.normal_f32(cols, 622)).astype(np.float32)
+    Wd, xd, gd = _dev(torch, W), _dev(torch, x), _dev(torch, g)
+    yd = torch.full((M, rows), float("nan"), dtype=torch.float32, device="cuda")
+    ch = ggq.Chain(12, M, [([Wd], [rows], cols, xd, [yd])], [{"x_op": ggq.X_RMSNORM, "eps": 1e-5, "norm_w": gd}])
+    ch.run()
+    torch.cuda.synchronize()
+    assert ggq.device_status() == 0
+    xr = layer_ops.rmsnorm(x.astype(np.float64), g, 1e-5)
+    wd = oracle.dequantize(12, W, rows, cols).astype(np.float64)
+    ok, wr = oracle.tolerance_ok(yd.cpu().numpy(), xr @ wd.T, np.abs(xr) @ np.abs(wd).T, REL, ABS)
+    assert ok, wr
+    assert np.array_equal(yd.cpu().numpy()[1], np.zeros(rows, dtype=np.float32))

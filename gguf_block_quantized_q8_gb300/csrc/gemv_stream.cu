@@ -417,21 +417,27 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 // sum of squares of each activation row first (a CTA reduction
                 // through the cut-group scratch, free until the tiles), then
                 // norm_w * x / sqrt(mean + eps).  SILU_MUL: silu(x) * up.
+                const float4* o4 = reinterpret_cast<const float4*>(xop == GGQ_X_RMSNORM ? sd->norm_w : sd->up);
+                constexpr int kBatch = 4;   // two float4 a step: x and norm_w / up
+                float* red = cut_val;       // [W][MMAX]: per-warp sums of squares
                 float rs[MMAX];
-                if (xop == GGQ_X_RMSNORM) {
-                    float* red = cut_val;   // [W][MMAX]
+                auto load2 = [&](int q0, float4 (&v)[kBatch], float4 (&o)[kBatch]) {
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int q = q0 + i * kThreads + lane;
+                        const int qb = q0 + i * kThreads;
+                        const int m = MMAX == 1 ? 0 : qb / c4;
+                        v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        o[i] = q < n4 ? __ldcg(o4 + (xop == GGQ_X_RMSNORM ? q - m * c4 : q))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                };
+                // sums of squares per activation row (ss from this thread) -> rs
+                auto reduce_rs = [&](float (&ss)[MMAX]) {
 #pragma unroll
                     for (int m = 0; m < MMAX; ++m) {
-                        float ss = 0.0f;
-                        if (m < p.M) {
-#pragma unroll 4
-                            for (int q = tid; q < c4; q += kThreads) {
-                                const float4 v = __ldcg(x4 + (size_t)m * c4 + q);
-                                ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-                            }
-                        }
-                        ss = warp_sum(ss);
-                        if (lane == 0) red[warp * MMAX + m] = ss;
+                        const float t = warp_sum(ss[m]);
+                        if (lane == 0) red[warp * MMAX + m] = t;
                     }
                     __syncthreads();
 #pragma unroll
@@ -440,35 +446,69 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                         for (int w2 = 0; w2 < W; ++w2) t += red[w2 * MMAX + m];   // same order in every thread
                         rs[m] = 1.0f / sqrtf(t / (float)cols + sd->eps);
                     }
-                }
-                const float4* o4 = reinterpret_cast<const float4*>(xop == GGQ_X_RMSNORM ? sd->norm_w : sd->up);
-                constexpr int kBatch = 4;   // two float4 a step: x and norm_w / up
-                for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                };
+                auto transform = [&](int qb, float4 t, float4 o) {
+                    if (xop == GGQ_X_RMSNORM) {
+                        float r = rs[0];
+#pragma unroll
+                        for (int m = 1; m < MMAX; ++m)
+                            if (qb >= m * c4) r = rs[m];
+                        return make_float4(o.x * (t.x * r), o.y * (t.y * r), o.z * (t.z * r), o.w * (t.w * r));
+                    }
+                    return make_float4(t.x / (1.0f + expf(-t.x)) * o.x, t.y / (1.0f + expf(-t.y)) * o.y,
+                                       t.z / (1.0f + expf(-t.z)) * o.z, t.w / (1.0f + expf(-t.w)) * o.w);
+                };
+                if (MMAX <= 2 && xop == GGQ_X_RMSNORM && n4 <= kThreads * kBatch) {
+                    // one batch a thread: the squares come from the registers the
+                    // values are placed from (one L2 round trip; up to 2 activation
+                    // rows, where the registers allow it)
                     float4 v[kBatch], o[kBatch];
+                    const int q0 = warp * 32;
+                    load2(q0, v, o);
+                    float ss[MMAX];
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m) ss[m] = 0.0f;
 #pragma unroll
                     for (int i = 0; i < kBatch; ++i) {
-                        const int q = q0 + i * kThreads + lane;
                         const int qb = q0 + i * kThreads;
-                        const int m = MMAX == 1 ? 0 : qb / c4;
-                        v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        o[i] = q < n4 ? __ldcg(o4 + (xop == GGQ_X_RMSNORM ? q - m * c4 : q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float e = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, v[i].w * v[i].w)));
+#pragma unroll
+                        for (int m = 0; m < MMAX; ++m)
+                            if (qb >= m * c4 && qb < (m + 1) * c4) ss[m] += e;   // zero beyond n4
                     }
+                    reduce_rs(ss);
 #pragma unroll
                     for (int i = 0; i < kBatch; ++i) {
                         const int qb = q0 + i * kThreads;
                         if (qb >= n4) break;
-                        float4 t = v[i];
-                        if (xop == GGQ_X_RMSNORM) {
-                            float r = rs[0];
+                        place(qb, transform(qb, v[i], o[i]));
+                    }
+                } else {
+                    if (xop == GGQ_X_RMSNORM) {
+                        // x too long for one batch: a first pass for the squares
+                        float ss[MMAX];
 #pragma unroll
-                            for (int m = 1; m < MMAX; ++m)
-                                if (qb >= m * c4) r = rs[m];
-                            t = make_float4(o[i].x * (t.x * r), o[i].y * (t.y * r), o[i].z * (t.z * r), o[i].w * (t.w * r));
-                        } else {
-                            t = make_float4(t.x / (1.0f + expf(-t.x)) * o[i].x, t.y / (1.0f + expf(-t.y)) * o[i].y,
-                                            t.z / (1.0f + expf(-t.z)) * o[i].z, t.w / (1.0f + expf(-t.w)) * o[i].w);
+                        for (int m = 0; m < MMAX; ++m) {
+                            ss[m] = 0.0f;
+                            if (m < p.M) {
+#pragma unroll 4
+                                for (int q = tid; q < c4; q += kThreads) {
+                                    const float4 v = __ldcg(x4 + (size_t)m * c4 + q);
+                                    ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
+                                }
+                            }
                         }
-                        place(qb, t);
+                        reduce_rs(ss);
+                    }
+                    for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                        float4 v[kBatch], o[kBatch];
+                        load2(q0, v, o);
+#pragma unroll
+                        for (int i = 0; i < kBatch; ++i) {
+                            const int qb = q0 + i * kThreads;
+                            if (qb >= n4) break;
+                            place(qb, transform(qb, v[i], o[i]));
+                        }
                     }
                 }
             }

@@ -224,10 +224,12 @@ class DecodePass:
 
     def fused_pass(self, synth):
         """The same weights as a real layer data flow, every element-wise step fused
-        into the chain (ggq_chain_create_ops): per layer h -> [q,k,v](rmsnorm(h)),
-        [o](q) + h = h2, [gate,up](rmsnorm(h2)), [down](silu(gate) * up) + h2;
-        then the head on rmsnorm(h) as a one-stage Q8_0 chain.  Returns a
-        callable running the pass (2 launches) and the objects it keeps."""
+        into the chain (ggq_chain_create_ops): h = the embedding row of one token
+        (ggq_embed; the Q8_0 head matrix read as a tied embedding table), then per
+        layer h -> [q,k,v](rmsnorm(h)), [o](q) + h = h2, [gate,up](rmsnorm(h2)),
+        [down](silu(gate) * up) + h2; then the head on rmsnorm(h) as a one-stage
+        Q8_0 chain.  Returns a callable running the pass (3 launches) and the
+        objects it keeps."""
         torch, ggq = self.torch, self.ggq
         q4 = self.q4
         assert len(q4) % 4 == 0 and len(self.rest) == 1
@@ -258,7 +260,13 @@ class DecodePass:
                                         [{"x_op": ggq.X_RMSNORM, "eps": 1e-5, "norm_w": norm_w(7999)}])
         ggq.check(rc, "ggq_chain_create_ops")
 
+        tok = torch.tensor([1234], dtype=torch.int32, device="cuda")
+        norms.append(tok)
+        h_in = q4[0]["x"]
+
         def run(sp):
+            ggq.check(ggq.ggq_embed(hd["qtype"], hd["W"][0], hd["rows"][0], hd["cols"], tok.data_ptr(), 1, h_in, sp),
+                      "ggq_embed")
             ggq.check(ggq.ggq_chain_run(body, sp), "ggq_chain_run")
             ggq.check(ggq.ggq_chain_run(head, sp), "ggq_chain_run")
 
@@ -605,9 +613,9 @@ def main():
             raise SystemExit("device status set by the fused pass")
         ffree()
         extra["cfg3_fused_layer_pass"] = {
-            "ms": round(ms_f, 4), "GB_s": round(weight_bytes / (ms_f * 1e-3) / 1e9, 1), "launches": 2,
-            "fused": "rmsnorm into q/k/v and gate/up, silu(gate)*up into down, residual adds after o and down, "
-                     "final rmsnorm into the head"}
+            "ms": round(ms_f, 4), "GB_s": round(weight_bytes / (ms_f * 1e-3) / 1e9, 1), "launches": 3,
+            "fused": "token embedding row (ggq_embed), rmsnorm into q/k/v and gate/up, silu(gate)*up into down, "
+                     "residual adds after o and down, final rmsnorm into the head"}
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
 
     step_bytes = weight_bytes + dp.io_bytes

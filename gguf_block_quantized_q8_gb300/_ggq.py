@@ -68,6 +68,7 @@ def _bind(lib):
         "ggq_chain_create_ops": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ChainStage),
                                   ctypes.POINTER(ChainOps), ctypes.POINTER(vp)], ctypes.c_int),
         "ggq_chain_run": ([vp, vp], ctypes.c_int),
+        "ggq_embed": ([ctypes.c_int, vp, i64, i64, vp, ctypes.c_int, vp, vp], ctypes.c_int),
         "ggq_chain_reset": ([vp], ctypes.c_int),
         "ggq_chain_free": ([vp], None),
         "ggq_gemm_prefill": ([ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_int, vp], ctypes.c_int),
@@ -295,6 +296,21 @@ def gemv_multi(qtype: int, Ws, rows, cols: int, x, ys=None, stream=None):
     check(ggq_gemv_multi(qtype, [w.data_ptr() for w in Ws], list(rows), cols, x2.data_ptr(),
                          [y.data_ptr() for y in ys], M, _stream_ptr(stream)), "ggq_gemv_multi")
     return ys
+
+
+def ggq_embed(qtype: int, table: int, rows: int, cols: int, ids: int, n: int, out: int, stream: int) -> int:
+    return lib.ggq_embed(qtype, table, rows, cols, ids, n, out, stream)
+
+
+def embed(qtype: int, table, rows: int, cols: int, ids, out=None, stream=None):
+    """out[i] = row ids[i] of the block-quantized table, decoded to fp32 (CUDA tensors)."""
+    import torch
+    ids = ids.to(device=table.device, dtype=torch.int32).contiguous()
+    if out is None:
+        out = torch.empty((ids.numel(), cols), dtype=torch.float32, device=table.device)
+    check(ggq_embed(qtype, table.data_ptr(), rows, cols, ids.data_ptr(), ids.numel(), out.data_ptr(),
+                    _stream_ptr(stream)), "ggq_embed")
+    return out
 
 
 class Chain:

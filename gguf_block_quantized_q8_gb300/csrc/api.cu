@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "ggq_internal.h"
+#include "ptx.cuh"
 
 namespace ggq {
 
@@ -136,6 +137,19 @@ extern "C" int ggq_dequantize(int type, const void* W, int64_t rows, int64_t col
     return launch_dequantize(type, W, rows, cols, out, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int ggq_embed(int type, const void* table, int64_t rows, int64_t cols, const int32_t* ids, int n,
+                         float* out, void* stream) {
+    clear_error();
+    if (type != GGQ_Q8_0 && type != GGQ_Q4_K) return fail(GGQ_ETYPE, "ggq_embed: type %d not supported", type);
+    if (!table || !ids || !out) return fail(GGQ_EINVAL, "ggq_embed: NULL pointer");
+    const int64_t blk = type == GGQ_Q4_K ? 256 : 32;
+    if (rows < 1 || rows > 0x7fffffff || cols < 1 || cols % blk) return fail(GGQ_EINVAL, "ggq_embed: bad shape");
+    if (n < 1 || n > 65535) return fail(GGQ_EINVAL, "ggq_embed: n %d outside 1..65535", n);
+    if (!aligned(table, 2) || !aligned(ids, 4) || !aligned(out, 4))
+        return fail(GGQ_EINVAL, "ggq_embed: misaligned pointer");
+    return launch_embed(type, table, rows, cols, ids, n, out, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int ggq_device_status(void) {
     clear_error();
     cudaError_t e = cudaDeviceSynchronize();
@@ -143,7 +157,8 @@ extern "C" int ggq_device_status(void) {
     int v = 0;
     int rc = read_and_clear_status(&v);
     if (rc) return rc;
-    if (v & 1) return fail(GGQ_ETIMEOUT, "a kernel's bounded wait ran out");
+    if (v & kStatusTimeout) return fail(GGQ_ETIMEOUT, "a kernel's bounded wait ran out");
+    if (v & kStatusBadIndex) return fail(GGQ_EINVAL, "an embedding row id was outside the table");
     return GGQ_OK;
 }
 

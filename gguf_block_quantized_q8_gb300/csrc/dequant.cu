@@ -52,7 +52,62 @@ __global__ void dequant_q4k_kernel(const uint8_t* __restrict__ W, int64_t nsub, 
     for (int l = 0; l < 32; ++l) o[l] = fmaf(a, (float)((qs[l] >> shift) & 15), -bm);
 }
 
+// Token embedding rows ("GGUF Inferencer in R" section 4, "Input Embedding":
+// the token's row of the embedding table; the C++ engine post's embed(table,
+// token)): out[i, k] = w[ids[i], k].  One thread per output weight: the q
+// bytes and the writes are coalesced, the block's scale bytes come from cache.
+// An id outside [0, rows) gives a row of zeros and sets kStatusBadIndex.
+template <bool Q4K>
+__global__ void embed_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_t cols,
+                             const int32_t* __restrict__ ids, float* __restrict__ out, int* status) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int i = blockIdx.y;
+    if (k >= cols) return;
+    const int32_t id = ids[i];
+    float* o = out + (int64_t)i * cols + k;
+    if (id < 0 || id >= rows) {
+        *o = 0.0f;
+        if (k == 0) atomicOr(status, kStatusBadIndex);
+        return;
+    }
+    if constexpr (!Q4K) {
+        const uint8_t* blk = W + ((int64_t)id * (cols / 32) + k / 32) * 34;
+        const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+        *o = d * (float)(int8_t)blk[2 + (k & 31)];
+    } else {
+        const uint8_t* blk = W + ((int64_t)id * (cols / 256) + k / 256) * 144;
+        const int kk = (int)(k & 255), j = kk >> 5, l = kk & 31;
+        const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+        const float dmin = half_bits_to_float((uint32_t)blk[2] | ((uint32_t)blk[3] << 8));
+        const uint8_t* sc = blk + 4;
+        int s, m;
+        if (j < 4) {
+            s = sc[j] & 63;
+            m = sc[j + 4] & 63;
+        } else {
+            s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+            m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+        }
+        const int q = (blk[16 + 32 * (j >> 1) + l] >> ((j & 1) ? 4 : 0)) & 15;
+        *o = fmaf(d * (float)s, (float)q, -(dmin * (float)m));
+    }
+}
+
 }  // namespace
+
+int launch_embed(int type, const void* W, int64_t rows, int64_t cols, const int32_t* ids, int n, float* out,
+                 cudaStream_t stream) {
+    int* status = device_status_word();
+    if (!status) return fail(GGQ_ECUDA, "device status word unavailable");
+    const dim3 grid((unsigned)((cols + 255) / 256), (unsigned)n);
+    const uint8_t* w = static_cast<const uint8_t*>(W);
+    if (type == GGQ_Q8_0)
+        embed_kernel<false><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
+    else
+        embed_kernel<true><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GGQ_OK : cuda_fail(e, "embed launch");
+}
 
 int launch_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t stream) {
     const uint8_t* w = static_cast<const uint8_t*>(W);

@@ -9,7 +9,7 @@
 namespace ggq {
 
 // status bits written by kernels into the device status word
-enum : int { kStatusTimeout = 1 };
+enum : int { kStatusTimeout = 1, kStatusBadIndex = 2 };
 
 // Wall-clock limit of every spin-wait in this library's kernels.  A wait that
 // runs out records kStatusTimeout and the kernel carries on without the data.

@@ -331,10 +331,24 @@ int ggq_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* o
                    void* stream);
 
 /*
+ * ggq_embed -- token embedding lookup ("GGUF Inferencer in R" section 4, "Input
+ * Embedding": a token id selects one row of the embedding table; the C++
+ * engine post's embed(table, token)).  out[i*cols + k] = w[ids[i], k] as fp32,
+ * decoded exactly as ggq_dequantize does, for i < n.
+ *   type   GGQ_Q8_0 or GGQ_Q4_K; table device [rows, cols] blocks, 2-byte aligned
+ *   ids    device int32 [n], n in 1..65535; out device fp32 [n, cols], 4-byte aligned
+ * An id outside [0, rows) gives a row of zeros, and the next ggq_device_status
+ * returns GGQ_EINVAL.  Errors: GGQ_ETYPE, GGQ_EINVAL (NULL, shape, n,
+ * alignment), GGQ_ECUDA.  Allocates nothing.  Asynchronous.
+ */
+int ggq_embed(int type, const void* table, int64_t rows, int64_t cols, const int32_t* ids, int n, float* out,
+              void* stream);
+
+/*
  * ggq_device_status -- synchronise the current device, then return GGQ_ETIMEOUT
  * if any kernel of this library recorded a bounded-wait timeout since the last
- * call (and clear the record), GGQ_ECUDA if the device reports an error, else
- * GGQ_OK.  Outputs of the launch that timed out, and of launches made after it
+ * call (and clear the record), GGQ_EINVAL if ggq_embed met an id outside its
+ * table, GGQ_ECUDA if the device reports an error, else GGQ_OK.  Outputs of the launch that timed out, and of launches made after it
  * before this call, are undefined; a chain that timed out needs
  * ggq_chain_reset.  When one wait of a multi-CTA kernel runs out, the kernel's
  * other waits end within about a millisecond each, so the launch finishes

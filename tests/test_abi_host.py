@@ -214,3 +214,18 @@ def test_chain_create_ops_validates_fused_steps(ggq):
     assert "x_op 7" in ggq.lib.ggq_last_error().decode()
     assert rc({"res": [6]}) == -1                                                  # residual misaligned
     assert "res[0]" in ggq.lib.ggq_last_error().decode()
+
+
+def test_embed_validates_arguments(ggq):
+    """ggq_embed rejects bad arguments before any launch."""
+    assert ggq.ggq_embed(ggq.F32, 16, 4, 64, 16, 1, 16, 0) == -2          # type
+    assert ggq.ggq_embed(ggq.Q8_0, 0, 4, 64, 16, 1, 16, 0) == -1          # NULL table
+    assert ggq.ggq_embed(ggq.Q8_0, 16, 4, 64, 0, 1, 16, 0) == -1          # NULL ids
+    assert ggq.ggq_embed(ggq.Q8_0, 16, 4, 63, 16, 1, 16, 0) == -1         # cols % 32
+    assert ggq.ggq_embed(ggq.Q4_K, 16, 4, 288, 16, 1, 16, 0) == -1        # cols % 256
+    assert ggq.ggq_embed(ggq.Q8_0, 16, 0, 64, 16, 1, 16, 0) == -1         # rows = 0
+    assert ggq.ggq_embed(ggq.Q8_0, 16, 4, 64, 16, 0, 16, 0) == -1         # n = 0
+    assert ggq.ggq_embed(ggq.Q8_0, 16, 4, 64, 16, 65536, 16, 0) == -1     # n too large
+    assert ggq.ggq_embed(ggq.Q8_0, 17, 4, 64, 16, 1, 16, 0) == -1         # table misaligned
+    assert ggq.ggq_embed(ggq.Q8_0, 16, 4, 64, 18, 1, 16, 0) == -1         # ids misaligned
+    assert "misaligned" in ggq.lib.ggq_last_error().decode()

@@ -443,6 +443,16 @@ def extras(torch, ggq, synth, stream):
     t = kernel_time(torch, f5, stream, 8)
     flops = 2 * WL.CFG5_M * g.rows * g.cols
     out["cfg5_prefill_q4_k_512x14336x4096"] = {"us": round(t * 1e3, 2), "TFLOP_s": round(flops / t / 1e9, 1)}
+
+    # the same prefill with the Q8_0 14336x4096 matrix of cfg4
+    g8 = WL.CFG4
+    W8 = torch.from_numpy(synth.weight_rows(g8.qtype, g8.stream, g8.rows, g8.cols)).cuda()
+
+    def f5q8():
+        ggq.check(ggq.ggq_gemm_prefill(8, W8.data_ptr(), g8.rows, g8.cols, X.data_ptr(), Y.data_ptr(), WL.CFG5_M,
+                                       sp), "prefill")
+    t = kernel_time(torch, f5q8, stream, 8)
+    out["prefill_q8_0_512x14336x4096"] = {"us": round(t * 1e3, 2), "TFLOP_s": round(flops / t / 1e9, 1)}
     return out
 
 

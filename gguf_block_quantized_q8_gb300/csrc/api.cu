@@ -114,7 +114,8 @@ extern "C" int ggq_gemv_multi(int type, int n, const void* const* W, const int64
 extern "C" int ggq_gemm_prefill(int type, const void* W, int64_t rows, int64_t cols, const uint16_t* X, float* Y,
                                 int M, void* stream) {
     clear_error();
-    if (type != GGQ_Q4_K) return fail(GGQ_ETYPE, "ggq_gemm_prefill: type %d not supported", type);
+    if (type != GGQ_Q4_K && type != GGQ_Q8_0)
+        return fail(GGQ_ETYPE, "ggq_gemm_prefill: type %d not supported", type);
     if (!W || !X || !Y) return fail(GGQ_EINVAL, "ggq_gemm_prefill: NULL pointer");
     if (rows < 128 || rows % 128 || rows > 0x7fffffff)
         return fail(GGQ_EINVAL, "ggq_gemm_prefill: rows %lld not a positive multiple of 128", (long long)rows);

@@ -1,7 +1,7 @@
 // Fused dequantize + GEMV / small-batch GEMM for Q8_0 and Q4_K weights.
 //
 //   y[m][r] = sum_c w[r][c] * x[m][c]      (matvec of the culpeo.ws kernel list;
-//                                           "GGUF Inferencer in R" 5.2: Q = NormIn %*% t(W))
+//                                           "GGUF Inferencer in R" 5.2: normalized input times transposed weight)
 //
 // Q8_0 ("GGUF: The File Format...", "How a Q8_0 block is stored"): 32 weights per
 // 34-byte block, fp16 d then 32 signed bytes q, w = d*q.

@@ -1,9 +1,11 @@
 // Prefill dequant-GEMM on the tcgen05 tensor cores:  Y[M, rows] = X[M, cols] * W^T.
 //
-// "GGUF Inferencer in R" section 4: prefill runs the whole prompt through the same
-// weights "at once with big matrix multiplications".  W is Q4_K ("GGUF: The File
+// "GGUF Inferencer in R" section 4: prefill takes the whole prompt through each
+// weight matrix as one large matrix product.  W is Q4_K ("GGUF: The File
 // Format...", k-quant paragraph of "How a Q8_0 block is stored"): 256 weights per
-// 144-byte super-block, w = d*sc_j*q - dmin*m_j.  X is bf16.
+// 144-byte super-block, w = d*sc_j*q - dmin*m_j; or Q8_0 (same section): 34-byte
+// blocks of an fp16 d and 32 int8 q, w = d*q, staged 8 blocks (272 bytes, 256
+// columns) at a time like a super-block.  X is bf16.
 //
 // One CTA computes a 128 (W rows) x 256 (tokens) tile of Y^T in tensor memory:
 //   warp 0      TMA producer: raw Q4_K super-blocks [128 rows x 144 B] and X tiles
@@ -37,7 +39,12 @@ constexpr int kTileTok = 256;         // UMMA N (tokens)
 constexpr int kKStage = 64;           // k per stage: one 128-byte swizzle row of bf16
 constexpr int kStages = 3;
 constexpr int kRawStages = 2;
-constexpr int kRawBytes = kTileRows * 144;              // one super-block column
+template <bool Q4K>
+struct Raw {   // one 256-column block column of a 128-row tile: Q4_K super-blocks or Q8_0 periods
+    static constexpr int kRowBytes = Q4K ? 144 : 272;
+    static constexpr int kBytes = kTileRows * kRowBytes;
+};
+constexpr int kRawBytes = Raw<false>::kBytes;            // the larger of the two: the ring's slot
 constexpr int kABytes = kTileRows * kKStage * 2;        // 16 KB
 constexpr int kBBytes = kTileTok * kKStage * 2;         // 32 KB
 constexpr int kThreads = 192;
@@ -138,9 +145,11 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
 
 // ------------------------------------------------------------------- kernel
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                                  const __grid_constant__ CUtensorMap xmap,
-                                                                  const PrefillParams p) {
+template <bool Q4K>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                              const __grid_constant__ CUtensorMap xmap,
+                                                              const PrefillParams p) {
+    using RB = Raw<Q4K>;
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_tile = blockIdx.x / p.tok_tiles;
@@ -194,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_q4k_kernel(const __grid_c
                 if ((ks & 3) == 0) {
                     const int sb = ks >> 2, r = sb % kRawStages;
                     mbar_wait(&empty_raw[r], ((sb / kRawStages) & 1) ^ 1, p.status);
-                    mbar_arrive_expect_tx(&full_raw[r], kRawBytes);
-                    tma_load_2d(sRaw + (size_t)r * kRawBytes, &wmap, &full_raw[r], sb * 144, row0);
+                    mbar_arrive_expect_tx(&full_raw[r], RB::kBytes);
+                    // Q4_K map: 1-byte elements; Q8_0 map: 2-byte elements (136 a period)
+                    tma_load_2d(sRaw + (size_t)r * kRawBytes, &wmap, &full_raw[r], sb * (Q4K ? 144 : 136), row0);
                 }
                 const int s = ks % kStages;
                 mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
@@ -231,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_q4k_kernel(const __grid_c
         for (int sb = 0; sb < nsb; ++sb) {
             const int r = sb % kRawStages;
             mbar_wait(&full_raw[r], (sb / kRawStages) & 1, p.status);
-            const uint8_t* rp = sRaw + (size_t)r * kRawBytes + (size_t)t * 144;
+            const uint8_t* rp = sRaw + (size_t)r * kRawBytes + (size_t)t * RB::kRowBytes;
+            if constexpr (Q4K) {
             const uint4 h = *reinterpret_cast<const uint4*>(rp);
             const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
 #pragma unroll 1
@@ -274,6 +285,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_q4k_kernel(const __grid_c
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&full_a[s]);
+            }
+            } else {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                // Q8_0: stage c holds blocks 2c (k = 0..31) and 2c+1 (k = 32..63) of
+                // the row's 272-byte period, each an fp16 d and 32 int8 q; w = d*q
+                // is exact in fp32, then rounded to bf16
+                const int ks = sb * 4 + c;
+                const int s = ks % kStages;
+                uint32_t u[2][8];   // the 32 q bytes of each block, four a word
+                float d[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int off = 34 * (2 * c + h2);   // 2-byte aligned; q bytes at off + 2
+                    d[h2] = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rp + off));
+                    const int qo = off + 2;
+                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rp + (qo & ~3));
+                    const int sh = 8 * (qo & 3);        // 0 or 16
+                    uint32_t v[9];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = wp[i];
+                    v[8] = sh ? wp[8] : 0u;             // only a misaligned start reaches a ninth word
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) u[h2][i] = __funnelshift_r(v[i], v[i + 1], sh);
+                }
+                mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
+                uint8_t* arow = sA + (size_t)s * kABytes + (size_t)t * 128;
+                const int sw = t & 7;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {   // chunk j: k = 8j..8j+7 (block 2c + j/4)
+                    const int h2 = j >> 2;
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t w = u[h2][2 * (j & 3) + (e >> 1)];
+                        const int b0 = 2 * (e & 1);
+                        const float f0 = d[h2] * (float)(int8_t)(w >> (8 * b0));
+                        const float f1 = d[h2] * (float)(int8_t)(w >> (8 * (b0 + 1)));
+                        o[e] = pack_bf16x2(f0, f1);
+                    }
+                    *reinterpret_cast<uint4*>(arow + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&full_a[s]);
+            }
             }
             mbar_arrive(&empty_raw[r]);
         }
@@ -318,18 +374,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 }  // namespace
 
-int launch_prefill(int /*type*/, const void* W, int64_t rows, int64_t cols, const uint16_t* X, float* Y, int M,
+int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const uint16_t* X, float* Y, int M,
                    cudaStream_t stream) {
+    const bool q4k = type == GGQ_Q4_K;
     auto enc = encoder();
     if (!enc) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled unavailable");
     CUtensorMap wmap, xmap;
     {
-        const int64_t rb = cols / 256 * 144;
-        cuuint64_t dims[2] = {(cuuint64_t)rb, (cuuint64_t)rows};
+        // Q4_K: 144-byte super-blocks as bytes; Q8_0: 272-byte periods of 8 blocks
+        // as 2-byte elements (136 a period)
+        const int64_t rb = cols / 256 * (q4k ? 144 : 272);
+        cuuint64_t dims[2] = {(cuuint64_t)(q4k ? rb : rb / 2), (cuuint64_t)rows};
         cuuint64_t strides[1] = {(cuuint64_t)rb};
-        cuuint32_t box[2] = {144, kTileRows};
+        cuuint32_t box[2] = {(cuuint32_t)(q4k ? 144 : 136), kTileRows};
         cuuint32_t es[2] = {1, 1};
-        CUresult r = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, es,
+        CUresult r = enc(&wmap, q4k ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                         const_cast<void*>(W), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(GGQ_ECUDA, "tensor map (W) failed (%d)", (int)r);
@@ -353,8 +413,8 @@ int launch_prefill(int /*type*/, const void* W, int64_t rows, int64_t cols, cons
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
 
-    cudaError_t e = cudaFuncSetAttribute(prefill_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    auto kernel = q4k ? prefill_kernel<true> : prefill_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((rows / kTileRows) * p.tok_tiles));
@@ -366,7 +426,7 @@ int launch_prefill(int /*type*/, const void* W, int64_t rows, int64_t cols, cons
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_q4k_kernel, wmap, xmap, p);
+    e = cudaLaunchKernelEx(&cfg, kernel, wmap, xmap, p);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return GGQ_OK;
 }

@@ -5,8 +5,8 @@
  * copy its tensor payloads to device memory unchanged, and multiply
  * block-quantized weight matrices (Q8_0, Q4_K) by activation vectors with the
  * blocks decoded in registers.  Conventions follow the kernel list of the
- * culpeo.ws C++ engine blog ("none of these allocate, the memory for the output
- * will always be provided by the caller"): every compute entry point writes into
+ * culpeo.ws C++ engine blog, whose kernels never allocate and leave the output
+ * memory to the caller: every compute entry point writes into
  * caller-provided device memory and enqueues its work on the caller's CUDA
  * stream without synchronising it.
  *
@@ -44,9 +44,9 @@ extern "C" {
 #define GGQ_ENOTFOUND (-8) /* no tensor / metadata key with that name */
 
 /* ---------------------------------------------------- tensor type ids
- * F32 = 0 ("GGUF: The File Format...", gguf_demo.py: "type F32=0") and
- * Q8_0 = 8 ("GGUF Inferencer in R" section 2.1: "Tensor Data Type = 8 (Q8_0)")
- * are on the pages; F16, Q4_0, Q4_K and Q6_K use the ggml ids of real files. */
+ * F32 = 0 (the gguf_demo.py listing of "GGUF: The File Format...") and Q8_0 = 8
+ * (the tensor-info example of "GGUF Inferencer in R" section 2.1) are on the
+ * pages; F16, Q4_0, Q4_K and Q6_K use the ggml ids of real files. */
 enum {
     GGQ_F32 = 0,
     GGQ_F16 = 1,
@@ -135,8 +135,9 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  *
  *   y[m*rows + r] = sum_c w[r, c] * x[m*cols + c],   m < M, r < rows
  *
- * This is the matvec of the culpeo.ws kernel list (matvec(w:[r,c], x:[c]) -> [r])
- * and of "GGUF Inferencer in R" section 5.2 (Q = NormIn %*% t(W)), with the
+ * This is the matrix-vector kernel of the culpeo.ws kernel list (an r x c
+ * weight times a c-vector gives an r-vector) and the product of the normalized
+ * input with the transposed weight in "GGUF Inferencer in R" section 5.2, with the
  * weights decoded on the fly: Q8_0 w = d*q ("GGUF: The File Format...", "How
  * a Q8_0 block is stored"), Q4_K w = d*sc_j*q - dmin*m_j (the k-quant paragraph
  * of the same section; byte layout: fp16 d, fp16 dmin, 12 bytes of packed
@@ -305,12 +306,14 @@ int ggq_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols, const 
 
 /*
  * ggq_gemm_prefill -- Y = X W^T for a whole prompt (M activation rows),
- * "GGUF Inferencer in R" section 4 (prefill runs the prompt "at once with big
- * matrix multiplications").  Q4_K weight tiles are decoded to bf16 in shared
- * memory and multiplied on the tcgen05 tensor cores with fp32 accumulation.
+ * "GGUF Inferencer in R" section 4 (prefill takes the whole prompt through each
+ * weight matrix as one large matrix product).  Weight tiles are decoded to bf16
+ * in shared memory (exact fp32 decode, then one rounding to bf16) and
+ * multiplied on the tcgen05 tensor cores with fp32 accumulation.
  *
- *   type   GGQ_Q4_K (cols % 256 == 0)
- *   W      device, rows x (cols/256*144) bytes, 16-byte aligned; rows % 128 == 0
+ *   type   GGQ_Q4_K or GGQ_Q8_0, cols % 256 == 0 for both
+ *   W      device, rows x (cols/256*144) (Q4_K) or rows x (cols/32*34) (Q8_0)
+ *          bytes, 16-byte aligned; rows % 128 == 0
  *   X      device, bf16 bit patterns [M, cols] row-major, 16-byte aligned
  *   Y      device, fp32 [M, rows] row-major; fully overwritten
  *   M      multiple of 128, 128..65536

@@ -27,8 +27,9 @@
  *      (sub-block 2c), weight 64c+32+l its high nibble (sub-block 2c+1), and
  *      w = d*sc_j*q - dmin*m_j.
  *   4. matvec -- culpeo.ws C++ engine blog, kernel list:
- *      matvec(w:[r,c], x:[c]) -> [r];  "GGUF Inferencer in R" section 5.2.1
- *      (Q = NormIn %*% t(W)): y[r] = sum_c w[r,c] * x[c].  For M activation
+ *      the matrix-vector kernel (an r x c weight and a c-vector give an
+ *      r-vector); "GGUF Inferencer in R" section 5.2.1 (the normalized input
+ *      times the transposed weight): y[r] = sum_c w[r,c] * x[c].  For M activation
  *      rows, y[m][r] = sum_c w[r,c] * x[m][c].  Every product and sum is taken
  *      in double, columns in order.
  *

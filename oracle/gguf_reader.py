@@ -16,7 +16,7 @@ Follows the layout the pages give:
 * tensor infos -- name, uint32 n_dims, n_dims x uint64 extents (fastest
   first: a 2x4 tensor is stored as dims (4, 2)), uint32 type, uint64 offset
   relative to the blob;
-* the blob starts at the next multiple of 32 ("pad to 32-byte alignment").
+* the blob starts at the next multiple of 32 (padding after the tensor infos).
 
 Payload sizes by type: F32 4 B, F16 2 B per value; Q8_0 34 B per 32 values;
 Q4_K 144 B per 256; Q4_0 18 B per 32; Q6_K 210 B per 256 (the lesson's bits/weight

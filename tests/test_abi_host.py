@@ -165,7 +165,9 @@ def test_compute_entry_points_validate_arguments(ggq):
     assert g(ggq.Q8_0, 16, 4, 64, 8, 16, 1, 0) == -1                 # x misaligned
     assert g(ggq.F32, 16, 4, 64, 16, 16, 1, 0) == -2                 # type
     p = ggq.ggq_gemm_prefill
-    assert p(ggq.Q8_0, 16, 128, 256, 16, 16, 128, 0) == -2
+    assert p(ggq.F16, 16, 128, 256, 16, 16, 128, 0) == -2
+    assert p(ggq.Q8_0, 16, 100, 256, 16, 16, 128, 0) == -1           # Q8_0 too: rows % 128
+    assert p(ggq.Q8_0, 16, 128, 224, 16, 16, 128, 0) == -1           # cols % 256
     assert p(ggq.Q4_K, 16, 100, 256, 16, 16, 128, 0) == -1           # rows % 128
     assert p(ggq.Q4_K, 16, 128, 256, 16, 16, 100, 0) == -1           # M % 128
     assert p(ggq.Q4_K, 16, 128, 256, 8, 16, 128, 0) == -1            # X misaligned

@@ -1,6 +1,6 @@
 """GPU parity of the tcgen05 prefill dequant-GEMM (ggq_gemm_prefill) against the oracle.
 
-Y[M, rows] = X[M, cols] W^T with W Q4_K and X bf16.  The GPU decodes W to bf16
+Y[M, rows] = X[M, cols] W^T with W Q4_K or Q8_0 and X bf16.  The GPU decodes W to bf16
 in shared memory; the oracle uses the exact fp32 weights.  Bar:
 |Y - Y_ref| <= 1e-3 * sum_c |w x| + 1e-6.  Integer-valued cases whose weights
 are exact in bf16 must match exactly; one-hot rows of X return bf16(w) exactly.
@@ -25,7 +25,7 @@ def env():
     return torch, ggq
 
 
-def gpu_prefill(env, W, rows, cols, X_bits):
+def gpu_prefill(env, W, rows, cols, X_bits, qtype=12):
     torch, ggq = env
     M = X_bits.shape[0]
     Wd = torch.from_numpy(np.ascontiguousarray(W)).cuda()
@@ -33,7 +33,7 @@ def gpu_prefill(env, W, rows, cols, X_bits):
     guard = 256
     buf = torch.full((M * rows + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
     Y = buf[guard:guard + M * rows]
-    ggq.check(ggq.ggq_gemm_prefill(ggq.Q4_K, Wd.data_ptr(), rows, cols, Xd.data_ptr(), Y.data_ptr(), M,
+    ggq.check(ggq.ggq_gemm_prefill(qtype, Wd.data_ptr(), rows, cols, Xd.data_ptr(), Y.data_ptr(), M,
                                    torch.cuda.current_stream().cuda_stream), "ggq_gemm_prefill")
     torch.cuda.synchronize()
     assert ggq.device_status() == 0, "a bounded wait timed out"
@@ -71,24 +71,47 @@ def test_prefill_integer_exact(env, rows, cols, M):
     assert np.array_equal(Y.astype(np.int64), X.astype(np.int64) @ w.T)
 
 
-def test_prefill_one_hot_rows(env):
+def int_q8_0(rng, rows, cols):
+    """Q8_0 blocks with d = 1 and q in [-127, 127]: every weight an integer, exact in bf16."""
+    q = rng.integers(-127, 128, size=(rows, cols))
+    blocks = q.reshape(rows, cols // 32, 32).astype(np.int8)
+    W = np.empty((rows, cols // 32, 34), np.uint8)
+    W[:, :, 0:2] = np.frombuffer(np.uint16(0x3C00).tobytes(), np.uint8)   # fp16 1.0
+    W[:, :, 2:] = blocks.view(np.uint8)
+    return W.reshape(-1).copy(), q
+
+
+@pytest.mark.parametrize("rows,cols,M", [(128, 256, 128), (256, 1024, 256), (128, 2304, 384)])
+def test_prefill_q8_0_integer_exact(env, rows, cols, M):
+    """Q8_0 with d = 1: |w| <= 127 and X in [-8, 8] are exact in bf16; every sum is exact."""
+    rng = np.random.default_rng(rows + cols + M + 1)
+    W, w = int_q8_0(rng, rows, cols)
+    X = rng.integers(-8, 9, size=(M, cols)).astype(np.float32)
+    bits = (X.view(np.uint32) >> 16).astype(np.uint16)
+    Y = gpu_prefill(env, W, rows, cols, bits, qtype=8)
+    assert np.array_equal(Y.astype(np.int64), X.astype(np.int64) @ w.T)
+
+
+@pytest.mark.parametrize("qtype", [12, 8])
+def test_prefill_one_hot_rows(env, qtype):
     rows, cols, M = 256, 1024, 256
-    W = synth.weight_rows(12, 61, rows, cols)
-    wb = bf16_round(oracle.dequantize(12, W, rows, cols))
+    W = synth.weight_rows(qtype, 61, rows, cols)
+    wb = bf16_round(oracle.dequantize(qtype, W, rows, cols))
     X = np.zeros((M, cols), np.float32)
     cs = (np.arange(M) * 37) % cols
     X[np.arange(M), cs] = 1.0
     bits = (X.view(np.uint32) >> 16).astype(np.uint16)
-    Y = gpu_prefill(env, W, rows, cols, bits)
+    Y = gpu_prefill(env, W, rows, cols, bits, qtype=qtype)
     assert np.array_equal(Y, wb[:, cs].T)
 
 
+@pytest.mark.parametrize("qtype", [12, 8])
 @pytest.mark.parametrize("rows,cols,M", [(128, 256, 128), (256, 4096, 256), (512, 2304, 512)])
-def test_prefill_random(env, rows, cols, M):
-    W = synth.weight_rows(12, 62, rows, cols)
+def test_prefill_random(env, qtype, rows, cols, M):
+    W = synth.weight_rows(qtype, 62, rows, cols)
     X = synth.normal_bf16(M * cols, 63).reshape(M, cols)
-    Y = gpu_prefill(env, W, rows, cols, X)
-    Y_ref, A_ref = oracle.gemm_bf16(12, W, rows, cols, X)
+    Y = gpu_prefill(env, W, rows, cols, X, qtype=qtype)
+    Y_ref, A_ref = oracle.gemm_bf16(qtype, W, rows, cols, X)
     ok, worst = oracle.tolerance_ok(Y, Y_ref, A_ref)
     assert ok, f"worst error / bound = {worst:.3g}"
 

@@ -158,7 +158,10 @@ extern "C" int ggq_device_status(void) {
     int v = 0;
     int rc = read_and_clear_status(&v);
     if (rc) return rc;
-    if (v & kStatusTimeout) return fail(GGQ_ETIMEOUT, "a kernel's bounded wait ran out");
+    if (v & kStatusTimeout) {
+        reset_prefill_sync();   // nothing runs now: the next prefill starts from clean sync words
+        return fail(GGQ_ETIMEOUT, "a kernel's bounded wait ran out");
+    }
     if (v & kStatusBadIndex) return fail(GGQ_EINVAL, "an embedding row id was outside the table");
     return GGQ_OK;
 }

@@ -66,6 +66,7 @@ int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const ui
 // device-side status word (bounded-wait timeouts); see ggq_device_status
 int* device_status_word();       // device pointer for the current device (lazily zeroed)
 int read_and_clear_status(int* status);
+int reset_prefill_sync();   // after a timeout: zero the prefill split-tile sync words
 int launch_embed(int type, const void* W, int64_t rows, int64_t cols, const int32_t* ids, int n, float* out,
                  cudaStream_t stream);
 

@@ -7,7 +7,9 @@
 // blocks of an fp16 d and 32 int8 q, w = d*q, staged 8 blocks (272 bytes, 256
 // columns) at a time like a super-block.  X is bf16.
 //
-// One CTA computes a 128 (W rows) x 256 (tokens) tile of Y^T in tensor memory:
+// One CTA computes a 128 (W rows) x 256 (tokens) tile of Y^T in tensor memory
+// (tiles of the last, partly filled wave as two halves along K, see
+// g_split_sync):
 //   warp 0      TMA producer: raw Q4_K super-blocks [128 rows x 144 B] and X tiles
 //               [256 tokens x 64 k] (128-byte swizzle) into shared-memory rings;
 //   warp 1      allocates 256 TMEM columns; one thread issues tcgen05.mma
@@ -53,8 +55,19 @@ constexpr int kTmemCols = 256;
 constexpr size_t kSmemPayload = (size_t)kStages * (kABytes + kBBytes) + (size_t)kRawStages * kRawBytes;
 constexpr size_t kSmemBytes = kSmemPayload + 1024 /* alignment */ + 256 /* barriers */;
 
+// The last, partly filled wave of tiles is split in two along K (whole
+// super-block columns): two CTAs compute halves of one tile.  The first to
+// finish stores its half and raises the tile's flag; the second waits for the
+// flag (its partner is already storing), adds its half to Y and resets the
+// tile's counter and flag for the next launch.  Two terms: the same fp32 sum
+// whichever finishes first.
+constexpr int kMaxSplit = 256;
+__device__ int g_split_sync[2 * kMaxSplit];   // [counter, flag] per split tile, zero between launches
+
 struct PrefillParams {
     float* Y;
+    int* split;      // g_split_sync
+    int full_tiles;  // tiles computed whole (CTAs 0 .. full_tiles-1); the rest as halves
     int rows;        // W rows (Y columns)
     int cols;        // K
     int M;           // tokens
@@ -145,6 +158,31 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
 
 // ------------------------------------------------------------------- kernel
 
+__device__ __forceinline__ void st_relaxed_i32(int* p, int v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_add_i32(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_i32(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (bounded) until *flag != 0: the partner half of a split tile has stored.
+__device__ __forceinline__ void wait_flag(const int* flag, int* status) {
+    if (ld_acquire_i32(flag)) return;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ld_acquire_i32(flag)) return;
+        if ((it & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
 template <bool Q4K>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const __grid_constant__ CUtensorMap xmap,
@@ -152,12 +190,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     using RB = Raw<Q4K>;
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row_tile = blockIdx.x / p.tok_tiles;
-    const int tok_tile = blockIdx.x % p.tok_tiles;
+    // work item: a whole tile, or half of one (super-blocks [sb0, sb1))
+    const int nsb_all = p.cols / 256;
+    const bool split = (int)blockIdx.x >= p.full_tiles;
+    const int part = split ? ((int)blockIdx.x - p.full_tiles) & 1 : 0;
+    const int split_idx = split ? ((int)blockIdx.x - p.full_tiles) >> 1 : 0;
+    const int tile = split ? p.full_tiles + split_idx : (int)blockIdx.x;
+    const int sb0 = split && part ? nsb_all / 2 : 0;
+    const int sb1 = split && !part ? nsb_all / 2 : nsb_all;
+    const int row_tile = tile / p.tok_tiles;
+    const int tok_tile = tile % p.tok_tiles;
     const int row0 = row_tile * kTileRows;
     const int tok0 = tok_tile * kTileTok;
-    const int nks = p.cols / kKStage;     // k stages
-    const int nsb = p.cols / 256;         // super-blocks
+    const int ks0 = 4 * sb0;
+    const int nks = 4 * (sb1 - sb0);      // k stages of this item (local index i: global stage ks0 + i)
+    const int nsb = sb1 - sb0;            // super-blocks of this item
 
     // 1024-aligned carve-out
     const uint32_t base_u32 = smem_u32(smem_raw);
@@ -199,18 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (warp == 0) {
         if (lane == 0) {
             pdl_wait();   // X may come from the previous kernel in the stream
-            for (int ks = 0; ks < nks; ++ks) {
+            for (int ks = 0; ks < nks; ++ks) {   // local stage index
                 if ((ks & 3) == 0) {
                     const int sb = ks >> 2, r = sb % kRawStages;
                     mbar_wait(&empty_raw[r], ((sb / kRawStages) & 1) ^ 1, p.status);
                     mbar_arrive_expect_tx(&full_raw[r], RB::kBytes);
                     // Q4_K map: 1-byte elements; Q8_0 map: 2-byte elements (136 a period)
-                    tma_load_2d(sRaw + (size_t)r * kRawBytes, &wmap, &full_raw[r], sb * (Q4K ? 144 : 136), row0);
+                    tma_load_2d(sRaw + (size_t)r * kRawBytes, &wmap, &full_raw[r], (sb0 + sb) * (Q4K ? 144 : 136),
+                                row0);
                 }
                 const int s = ks % kStages;
                 mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
                 mbar_arrive_expect_tx(&full_b[s], kBBytes);
-                tma_load_2d(sB + (size_t)s * kBBytes, &xmap, &full_b[s], ks * kKStage, tok0);
+                tma_load_2d(sB + (size_t)s * kBBytes, &xmap, &full_b[s], (ks0 + ks) * kKStage, tok0);
             }
         }
         __syncwarp();
@@ -340,13 +388,50 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int q = warp & 3;                  // TMEM lane quarter of this warp
         const int row = row0 + 32 * q + lane;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+        // half of a split tile: the first half done stores, the second adds
+        // (after the first's stores are visible: flag, release / acquire)
+        bool add = false;
+        int* cnt = p.split + 2 * split_idx;
+        __shared__ int s_role;
+        if (split) {
+            if (threadIdx.x == 64) s_role = atomicAdd(cnt, 1);
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the 128 epilogue threads
+            add = s_role != 0;
+            if (add) {
+                if (threadIdx.x == 64) wait_flag(cnt + 1, p.status);
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+        }
         for (int col = 0; col < kTileTok; col += 16) {
             float v[16];
             tmem_ld16(taddr + (uint32_t)col, v);
+            if (add) {
+                // every old value of the 16 tokens is read before any is written
+                // (one L2 round trip a step, not one per token)
+                float old[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int tok = tok0 + col + i;
+                    old[i] = tok < p.M ? __ldcg(p.Y + (size_t)tok * p.rows + row) : 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] += old[i];
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int tok = tok0 + col + i;
                 if (tok < p.M) p.Y[(size_t)tok * p.rows + row] = v[i];
+            }
+        }
+        if (split) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (threadIdx.x == 64) {
+                if (add) {   // both halves done: reset for the next launch
+                    st_relaxed_i32(cnt, 0);
+                    st_relaxed_i32(cnt + 1, 0);
+                } else {
+                    red_release_add_i32(cnt + 1, 1);   // this half's stores, then the flag
+                }
             }
         }
     }
@@ -412,12 +497,27 @@ int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const ui
     p.tok_tiles = (M + kTileTok - 1) / kTileTok;
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
+    {
+        void* sp = nullptr;
+        cudaError_t e2 = cudaGetSymbolAddress(&sp, g_split_sync);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "split-tile sync words");
+        p.split = static_cast<int*>(sp);
+    }
+    // tiles in the last, partly filled wave (all tiles if they fill at most half
+    // of the SMs) are computed as two halves along K when the halves fit one wave
+    int dev = 0, nsm = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int T = (int)(rows / kTileRows) * p.tok_tiles;
+    const int R = T > nsm ? T % nsm : T;
+    const int nsplit = (R > 0 && 2 * R <= nsm && R <= kMaxSplit && cols >= 512) ? R : 0;
+    p.full_tiles = T - nsplit;
 
     auto kernel = q4k ? prefill_kernel<true> : prefill_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((rows / kTileRows) * p.tok_tiles));
+    cfg.gridDim = dim3((unsigned)(p.full_tiles + 2 * nsplit));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
@@ -429,6 +529,13 @@ int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const ui
     e = cudaLaunchKernelEx(&cfg, kernel, wmap, xmap, p);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return GGQ_OK;
+}
+
+// Zero the split-tile counters and flags (after a timeout left them set).
+int reset_prefill_sync() {
+    static const int zero[2 * kMaxSplit] = {};
+    cudaError_t e = cudaMemcpyToSymbol(g_split_sync, zero, sizeof(zero));
+    return e == cudaSuccess ? GGQ_OK : cuda_fail(e, "reset split-tile sync words");
 }
 
 }  // namespace ggq

@@ -319,8 +319,11 @@ int ggq_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols, const 
  *   M      multiple of 128, 128..65536
  *
  * Errors: GGQ_EINVAL, GGQ_ETYPE, GGQ_ECUDA.  The kernel's waits on its own
- * copies are bounded; if one runs out the kernel records it and
- * ggq_device_status reports GGQ_ETIMEOUT.  Asynchronous.
+ * copies (and, for a tile computed as two halves along K, on the other half)
+ * are bounded; if one runs out the kernel records it and ggq_device_status
+ * reports GGQ_ETIMEOUT.  Calls on one device must not run concurrently (they
+ * share the halves' sync words); calls on one stream may follow each other.
+ * Asynchronous.
  */
 int ggq_gemm_prefill(int type, const void* W, int64_t rows, int64_t cols,
                      const uint16_t* X, float* Y, int M, void* stream);

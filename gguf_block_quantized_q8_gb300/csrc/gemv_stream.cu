@@ -14,8 +14,9 @@
 //   * CTA b (one per SM) owns groups [GT*b/G, GT*(b+1)/G) of the stage's GT:
 //     whole rows, so no output is ever split between CTAs and no cross-CTA
 //     reduction exists.
-//   * Its (group, SB) tiles are cut into W equal contiguous runs, one per warp.  A warp streams its run
-//     through its own ring of 2-D bulk tensor copies (16 rows x up to NSB SBs);
+//   * Its (group, SB) tiles are cut into W equal contiguous runs, one per
+//     warp.  A warp streams its run through its own ring of 2-D bulk tensor
+//     copies (16 rows x up to NSB SBs);
 //     weights do not depend on earlier stages, so the ring runs ahead into the
 //     next stages while the chain waits at a stage boundary.
 //   * Lane (r, c) = (lane / 4, lane % 4) decodes chunk c of rows r and r + 8 of
@@ -30,6 +31,8 @@
 //   * Stage boundary: every CTA adds one to a device counter with release
 //     semantics after its outputs are stored; CTAs wait (acquire, bounded) for
 //     the count of all CTAs before reading the next stage's x.
+//   * Fused steps (optional, per stage): RMSNorm or SiLU(gate) * up applied to
+//     x while x' is built, a residual added as each output row is stored.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     const int r = lane >> 2, c = lane & 3;   // row of the group, chunk of the SB
     const int D = p.ring;
 
-    // shared memory: [warp rings][stage info slots][x'][sums][cut-group parts][barriers]
+    // shared memory: [warp rings][stage info slots][group ranges][x'][sums][cut-group parts][barriers]
     uint8_t* ring = smem + (size_t)warp * D * B::kTile;
     StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)W * D * B::kTile);
     int2* part = reinterpret_cast<int2*>(infos + kInfoSlots);   // [kPartMax]

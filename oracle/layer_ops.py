@@ -19,7 +19,7 @@ float64, one step per function in the order the pages give it.
 
 Rows of a [M, n] array are independent activation vectors (one per token).
 Parity status: pinned by closed forms and invariants in
-tests/test_oracle_pins.py (no page prints a numeric example of these steps).
+tests/test_oracle_layer_ops.py (no page prints a numeric example of these steps).
 """
 from __future__ import annotations
 

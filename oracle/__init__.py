@@ -5,7 +5,7 @@ TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and
 The CUDA library (``gguf_block_quantized_q8_gb300``) never imports it and
 shares no code with it; the two meet only on input bytes from ``synth``.
 
-* ``ggq_oracle.c`` -- fp16 decode from IEEE-754, Q8_0 / Q4_K block decode to
+* ``ggq_oracle.c`` -- fp16 decode from IEEE-754, Q8_0 / Q4_K / Q4_0 block decode to
   fp32, GEMV / GEMM with every product and sum in double (see its header for
   the passages followed);
 * ``gguf_reader.py`` -- a plain byte walk of GGUF v3;
@@ -16,7 +16,11 @@ Parity status: fp16 decode, Q8_0 decode, GEMV/GEMM and the GGUF reader are
 pinned by the tests in tests/test_oracle_pins.py.  Q4_K decode is pinned by
 closed-form hand-built super-blocks for the byte layout read here; no page
 prints a Q4_K block, so agreement with Q4_K files made by other tools is
-unpinned (the path and the oracle decode the same bytes either way).
+unpinned (the path and the oracle decode the same bytes either way).  Q4_0
+decode is pinned the same way and, beyond that, against the Q8_0 decode: a
+Q4_0 block and a Q8_0 block holding the same scale and the same integers
+decode to the same 32 values.  Which nibble holds which weight, and the offset
+of 8, are a reading of the format (real Q4_0 files), not on the pages.
 """
 from __future__ import annotations
 
@@ -35,7 +39,7 @@ _LIB = os.path.join(_HERE, "libggq_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, F16, Q8_0, Q4_K = 0, 1, 8, 12
+F32, F16, Q4_0, Q8_0, Q4_K = 0, 1, 2, 8, 12
 
 
 def compile_oracle(src: str, out: str) -> str:
@@ -71,6 +75,7 @@ class Oracle:
         lib.orc_bf16_value.restype = ctypes.c_double
         lib.orc_decode_q8_0_block.argtypes = [vp, vp]
         lib.orc_decode_q4_k_block.argtypes = [vp, vp]
+        lib.orc_decode_q4_0_block.argtypes = [vp, vp]
         lib.orc_row_bytes.argtypes = [ctypes.c_int, i64]
         lib.orc_row_bytes.restype = i64
         lib.orc_dequantize.argtypes = [ctypes.c_int, vp, i64, i64, vp]
@@ -142,6 +147,13 @@ class Oracle:
         self.lib.orc_decode_q4_k_block(b.ctypes.data, out.ctypes.data)
         return out
 
+    def decode_q4_0_block(self, blk: bytes) -> np.ndarray:
+        b = np.frombuffer(bytes(blk), dtype=np.uint8)
+        assert b.size == 18
+        out = np.empty(32, dtype=np.float32)
+        self.lib.orc_decode_q4_0_block(b.ctypes.data, out.ctypes.data)
+        return out
+
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=dtype)
@@ -186,6 +198,10 @@ def decode_q8_0_block(blk):
 
 def decode_q4_k_block(blk):
     return default().decode_q4_k_block(blk)
+
+
+def decode_q4_0_block(blk):
+    return default().decode_q4_0_block(blk)
 
 
 def tolerance_ok(y_dev: np.ndarray, y_ref: np.ndarray, abs_ref: np.ndarray,

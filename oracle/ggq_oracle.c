@@ -26,15 +26,25 @@
  *      weight 64c+l (c = 0..3, l = 0..31) is the low nibble of qs[32c+l]
  *      (sub-block 2c), weight 64c+32+l its high nibble (sub-block 2c+1), and
  *      w = d*sc_j*q - dmin*m_j.
- *   4. matvec -- culpeo.ws C++ engine blog, kernel list:
+ *   4. Q4_0 block decode -- "GGUF: The File Format...", "How a Q8_0 block is
+ *      stored": the Q8_0 layout with 4-bit integers, 2 + 16 = 18 bytes per 32
+ *      weights.  Which nibble holds which weight and how a 4-bit code becomes
+ *      a signed integer are not printed on the pages; the reading used here
+ *      (the layout of real Q4_0 files) is: bytes 0-1 d, 2-17 qs[0..15];
+ *      weight l (l < 16) is the low nibble of qs[l], weight 16+l its high
+ *      nibble, and a code u in 0..15 stands for the integer u - 8, so
+ *      w = d * (u - 8).
+ *   5. F32 rows -- "GGUF: The File Format...", the practice script's tensor
+ *      payload: little-endian fp32 values, row after row.
+ *   6. matvec -- culpeo.ws C++ engine blog, kernel list:
  *      the matrix-vector kernel (an r x c weight and a c-vector give an
  *      r-vector); "GGUF Inferencer in R" section 5.2.1 (the normalized input
  *      times the transposed weight): y[r] = sum_c w[r,c] * x[c].  For M activation
  *      rows, y[m][r] = sum_c w[r,c] * x[m][c].  Every product and sum is taken
  *      in double, columns in order.
  *
- * Decode produces fp32 exactly as the format defines it: the Q8_0 product
- * d*q and the Q4_K products d*sc*q and dmin*m are exact in fp32, so the only
+ * Decode produces fp32 exactly as the format defines it: the Q8_0 and Q4_0
+ * products d*q and the Q4_K products d*sc*q and dmin*m are exact in fp32, so the only
  * rounding is the final Q4_K subtraction (done here in double and rounded
  * once more to float, which gives the correctly rounded fp32 difference of two
  * fp32 values because 53 >= 2*24+2).
@@ -49,7 +59,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_Q8_0 = 8, ORC_Q4_K = 12 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_Q4_0 = 2, ORC_Q8_0 = 8, ORC_Q4_K = 12 };
 
 /* IEEE-754 binary16 value, from the definition */
 double orc_fp16_value(uint16_t h) {
@@ -83,6 +93,18 @@ void orc_decode_q8_0_block(const uint8_t* blk, float* out) {
     for (int i = 0; i < 32; ++i) {
         int q = (int8_t)blk[2 + i];
         out[i] = (float)(d * (double)q);
+    }
+}
+
+/* one Q4_0 block (18 bytes) -> 32 floats */
+void orc_decode_q4_0_block(const uint8_t* blk, float* out) {
+    double d = orc_fp16_value(rd16(blk));
+    const uint8_t* qs = blk + 2;
+    for (int l = 0; l < 16; ++l) {
+        int u_lo = qs[l] & 15;
+        int u_hi = qs[l] >> 4;
+        out[l] = (float)(d * (double)(u_lo - 8));
+        out[16 + l] = (float)(d * (double)(u_hi - 8));
     }
 }
 
@@ -122,6 +144,7 @@ int64_t orc_row_bytes(int type, int64_t cols) {
     case ORC_F32: return 4 * cols;
     case ORC_F16: return 2 * cols;
     case ORC_Q8_0: return cols % 32 ? 0 : cols / 32 * 34;
+    case ORC_Q4_0: return cols % 32 ? 0 : cols / 32 * 18;
     case ORC_Q4_K: return cols % 256 ? 0 : cols / 256 * 144;
     default: return 0;
     }
@@ -141,6 +164,9 @@ static int decode_row(int type, const uint8_t* row, int64_t cols, float* out) {
         return 0;
     case ORC_Q4_K:
         for (int64_t b = 0; b < cols / 256; ++b) orc_decode_q4_k_block(row + 144 * b, out + 256 * b);
+        return 0;
+    case ORC_Q4_0:
+        for (int64_t b = 0; b < cols / 32; ++b) orc_decode_q4_0_block(row + 18 * b, out + 32 * b);
         return 0;
     default:
         return -1;

@@ -16,6 +16,10 @@
  *     32 with 6-bit scale and min, fp16 d and dmin).  The pages give only the
  *     size (144 B) and the two-level idea ("What is quantization (in GGUF)");
  *     the byte layout is the de-facto one of real Q4_K files;
+ *   - a Q4_0 block encoder, the Q8_0 recipe on a 4-bit grid: d = fp16(absmax/7),
+ *     q = round-half-even(w / d) clipped to -8..7, stored as the code q + 8, the
+ *     code of weight l (l < 16) in the low nibble of byte l and that of weight
+ *     16 + l in its high nibble (the byte layout of real Q4_0 files);
  *   - fp32 -> fp16 / bf16 round-to-nearest-even conversions (bit manipulation).
  *
  * Determinism across machines: the generator uses only IEEE basic operations
@@ -160,6 +164,22 @@ static void encode_q8_0_block(const float* w, uint8_t* out) {
 
 static inline float clampf(float v, float lo, float hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
+/* Q4_0: 32 weights -> 18 bytes (fp16 d, 16 bytes of 4-bit codes) */
+static void encode_q4_0_block(const float* w, uint8_t* out) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) { float a = fabsf(w[i]); if (a > amax) amax = a; }
+    uint16_t dh = synth_f32_to_f16(amax / 7.0f);
+    float d = f16_to_f32_enc(dh);
+    out[0] = (uint8_t)(dh & 0xff);
+    out[1] = (uint8_t)(dh >> 8);
+    uint8_t code[32];
+    for (int i = 0; i < 32; ++i) {
+        float q = (d == 0.0f) ? 0.0f : clampf(rintf(w[i] / d), -8.0f, 7.0f);
+        code[i] = (uint8_t)((int)q + 8);
+    }
+    for (int l = 0; l < 16; ++l) out[2 + l] = (uint8_t)(code[l] | (code[16 + l] << 4));
+}
+
 /* Q4_K: 256 weights -> 144 bytes, round-to-nearest, no search */
 static void encode_q4_k_block(const float* w, uint8_t* out) {
     float s[8], mn[8], smax = 0.0f, mmax = 0.0f;
@@ -239,6 +259,11 @@ void synth_quantize_q8_0(const float* w, int64_t n, uint8_t* out) {
     for (int64_t b = 0; b < nb; ++b) encode_q8_0_block(w + 32 * b, out + 34 * b);
 }
 
+void synth_quantize_q4_0(const float* w, int64_t n, uint8_t* out) {
+    int64_t nb = n / 32;
+    for (int64_t b = 0; b < nb; ++b) encode_q4_0_block(w + 32 * b, out + 18 * b);
+}
+
 void synth_quantize_q4_k(const float* w, int64_t n, uint8_t* out) {
     int64_t nb = n / 256;
     for (int64_t b = 0; b < nb; ++b) encode_q4_k_block(w + 256 * b, out + 144 * b);
@@ -258,6 +283,36 @@ void synth_q8_0_rows(uint64_t seed, uint64_t stream, int64_t row0, int64_t nrows
             for (int i = 0; i < 32; ++i)
                 w[i] = (float)((double)sigma * normal_at(key, base + (uint64_t)(32 * b + i)));
             encode_q8_0_block(w, out + r * rb + 34 * b);
+        }
+    }
+}
+
+void synth_q4_0_rows(uint64_t seed, uint64_t stream, int64_t row0, int64_t nrows,
+                     int64_t cols, float sigma, uint8_t* out) {
+    uint64_t key = stream_key(seed, stream);
+    int64_t rb = cols / 32 * 18;
+    #pragma omp parallel for schedule(static) num_threads(nthreads()) if (nrows > 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        float w[32];
+        uint64_t base = (uint64_t)(row0 + r) * (uint64_t)cols;
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            for (int i = 0; i < 32; ++i)
+                w[i] = (float)((double)sigma * normal_at(key, base + (uint64_t)(32 * b + i)));
+            encode_q4_0_block(w, out + r * rb + 18 * b);
+        }
+    }
+}
+
+/* F32 rows: the same draws, stored as little-endian fp32 */
+void synth_f32_rows(uint64_t seed, uint64_t stream, int64_t row0, int64_t nrows,
+                    int64_t cols, float sigma, uint8_t* out) {
+    uint64_t key = stream_key(seed, stream);
+    #pragma omp parallel for schedule(static) num_threads(nthreads()) if (nrows > 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        uint64_t base = (uint64_t)(row0 + r) * (uint64_t)cols;
+        for (int64_t c = 0; c < cols; ++c) {
+            float v = (float)((double)sigma * normal_at(key, base + (uint64_t)c));
+            memcpy(out + (r * cols + c) * 4, &v, 4);
         }
     }
 }

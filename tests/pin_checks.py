@@ -12,7 +12,7 @@ import struct
 
 import numpy as np
 
-F32, F16, Q8_0, Q4_K = 0, 1, 8, 12
+F32, F16, Q4_0, Q8_0, Q4_K = 0, 1, 2, 8, 12
 
 
 # ------------------------------------------------------------ fp16 / bf16 ----
@@ -80,6 +80,43 @@ def check_q8_0_blocks(orc):
     # block byte size from bits/weight: 8.5 bits * 32 = 34 bytes
     assert orc.row_bytes(Q8_0, 32) == 34 and orc.row_bytes(Q8_0, 2048) == 64 * 34
     assert orc.row_bytes(Q8_0, 48) == 0  # not a whole number of blocks
+
+
+# ------------------------------------------------------------------- Q4_0 ----
+
+def check_q4_0_blocks(orc):
+    # Literal bytes, expected values worked out by hand for the reading (weight
+    # l: low nibble of byte l; weight 16 + l: its high nibble; code u -> u - 8).
+    # A: d = 1, byte l = l | (15 - l) << 4 -> weights -8..7, then 7..-8
+    blk = bytes([0x00, 0x3C]) + bytes([0xF0, 0xE1, 0xD2, 0xC3, 0xB4, 0xA5, 0x96, 0x87,
+                                       0x78, 0x69, 0x5A, 0x4B, 0x3C, 0x2D, 0x1E, 0x0F])
+    got = orc.decode_q4_0_block(blk)
+    assert got.tolist() == [float(v) for v in list(range(-8, 8)) + list(range(7, -9, -1))]
+    # B: d = 0.5, every byte 0x08: low code 8 -> 0, high code 0 -> -8 * 0.5
+    got = orc.decode_q4_0_block(bytes([0x00, 0x38]) + bytes([0x08] * 16))
+    assert got.tolist() == [0.0] * 16 + [-4.0] * 16
+    # C: d = -2, every byte 0xF0: low code 0 -> -8 * -2 = 16, high code 15 -> 7 * -2
+    got = orc.decode_q4_0_block(bytes([0x00, 0xC0]) + bytes([0xF0] * 16))
+    assert got.tolist() == [16.0] * 16 + [-14.0] * 16
+    # D: the Q8_0 layout with 4-bit integers: a Q4_0 block and a Q8_0 block with
+    # the same scale and the same integers decode alike (Q8_0 decode is pinned
+    # to the pages' own values)
+    rng = np.random.default_rng(3)
+    for d_bits in (0x3C00, 0x2E66, 0x8123, 0x0001, 0x7BFF):
+        codes = rng.integers(0, 16, 32)
+        qs = bytes(int(codes[l]) | (int(codes[16 + l]) << 4) for l in range(16))
+        q4 = orc.decode_q4_0_block(struct.pack("<H", d_bits) + qs)
+        q8 = orc.decode_q8_0_block(q8_block(d_bits, [int(u) - 8 for u in codes]))
+        assert np.array_equal(q4, q8), hex(d_bits)
+    # block byte size from bits/weight: 2 + 16 = 18 bytes, 4.5 bits per weight
+    assert orc.row_bytes(Q4_0, 32) == 18 and orc.row_bytes(Q4_0, 4096) == 128 * 18
+    assert orc.row_bytes(Q4_0, 48) == 0
+
+
+def q4_0_block(d_bits: int, codes) -> bytes:
+    """32 codes in weight order -> 18 bytes (reading: weight l low nibble of byte l)."""
+    assert len(codes) == 32
+    return struct.pack("<H", d_bits) + bytes(int(codes[l]) | (int(codes[16 + l]) << 4) for l in range(16))
 
 
 # ------------------------------------------------------------------- Q4_K ----
@@ -204,6 +241,22 @@ def check_one_hot(orc):
         j = k // 32
         assert y[0].tolist() == [float((j + 1 + r) * ((k + r) % 16) - (2 * b + j))
                                  for r in range(rows)], c
+    # Q4_0, cols 64: block (r, b) has d = 1 and code (i + 3r + 5b) % 16 for weight i
+    W = b"".join(q4_0_block(0x3C00, [(i + 3 * r + 5 * b) % 16 for i in range(32)])
+                 for r in range(rows) for b in range(2))
+    for c in (0, 15, 16, 31, 32, 47, 63):
+        x = np.zeros(64, dtype=np.float32)
+        x[c] = 1.0
+        y, _ = orc.gemv(Q4_0, np.frombuffer(W, np.uint8), rows, 64, x)
+        b, i = divmod(c, 32)
+        assert y[0].tolist() == [float((i + 3 * r + 5 * b) % 16 - 8) for r in range(rows)], c
+    # F32, cols 5 (no blocks): element (r, c) = 10r + c
+    Wf = np.array([[10.0 * r + c for c in range(5)] for r in range(rows)], dtype=np.float32)
+    for c in range(5):
+        x = np.zeros(5, dtype=np.float32)
+        x[c] = 1.0
+        y, _ = orc.gemv(F32, Wf.reshape(-1).view(np.uint8), rows, 5, x)
+        assert y[0].tolist() == [10.0 * r + c for r in range(rows)], c
 
 
 def check_integer_exact(orc):
@@ -230,6 +283,17 @@ def check_integer_exact(orc):
     w = sc[:, bidx, j] * qq - mm[:, bidx, j]
     y, _ = orc.gemv(Q4_K, np.frombuffer(W, np.uint8), rows, cols, x.astype(np.float32))
     assert np.array_equal(y, (x @ w.T).astype(np.float64))
+    # Q4_0 with d = 1: w = code - 8
+    u = rng.integers(0, 16, size=(rows, cols))
+    W = b"".join(q4_0_block(0x3C00, list(u[r, 32 * b: 32 * b + 32]))
+                 for r in range(rows) for b in range(cols // 32))
+    y, ay = orc.gemv(Q4_0, np.frombuffer(W, np.uint8), rows, cols, x.astype(np.float32))
+    assert np.array_equal(y, (x @ (u - 8).T).astype(np.float64))
+    assert np.array_equal(ay, (np.abs(x) @ np.abs(u - 8).T).astype(np.float64))
+    # F32 integer matrix
+    wi = rng.integers(-1000, 1001, size=(rows, cols))
+    y, _ = orc.gemv(F32, wi.astype(np.float32).reshape(-1).view(np.uint8), rows, cols, x.astype(np.float32))
+    assert np.array_equal(y, (x @ wi.T).astype(np.float64))
 
 
 def check_brute_force(orc):
@@ -269,6 +333,24 @@ def check_brute_force(orc):
         assert np.allclose(y, x.astype(np.float64) @ w.astype(np.float64).T, rtol=1e-12, atol=1e-15)
         Wd = orc.dequantize(Q4_K, np.frombuffer(W, np.uint8), rows, cols)
         assert np.array_equal(Wd, w)
+        # Q4_0 with random fp16 d, cols 96 (three blocks)
+        cols = 96
+        d = rng.uniform(1e-3, 1e-2, size=(rows, 3)).astype(np.float16)
+        u = rng.integers(0, 16, size=(rows, cols))
+        W = b"".join(q4_0_block(int(d[r, b].view(np.uint16)), list(u[r, 32 * b:32 * b + 32]))
+                     for r in range(rows) for b in range(3))
+        w = np.repeat(d.astype(np.float64), 32, axis=1) * (u - 8)
+        x = rng.standard_normal((3, cols)).astype(np.float32)
+        y, ay = orc.gemv(Q4_0, np.frombuffer(W, np.uint8), rows, cols, x)
+        assert np.allclose(y, x.astype(np.float64) @ w.T, rtol=1e-12, atol=1e-15)
+        assert np.allclose(ay, np.abs(x.astype(np.float64)) @ np.abs(w).T, rtol=1e-12)
+        assert np.array_equal(orc.dequantize(Q4_0, np.frombuffer(W, np.uint8), rows, cols),
+                              w.astype(np.float32))
+        # F32, cols 7
+        wf = rng.standard_normal((rows, 7)).astype(np.float32)
+        x = rng.standard_normal((2, 7)).astype(np.float32)
+        y, _ = orc.gemv(F32, wf.reshape(-1).view(np.uint8), rows, 7, x)
+        assert np.allclose(y, x.astype(np.float64) @ wf.astype(np.float64).T, rtol=1e-12, atol=1e-15)
 
 
 def check_gemm_bf16(orc):
@@ -287,5 +369,5 @@ def check_gemm_bf16(orc):
     assert np.array_equal(Y, y2)
 
 
-ALL_CHECKS = [check_fp16, check_bf16, check_q8_0_blocks, check_q4_k_blocks,
+ALL_CHECKS = [check_fp16, check_bf16, check_q8_0_blocks, check_q4_0_blocks, check_q4_k_blocks,
               check_one_hot, check_integer_exact, check_brute_force, check_gemm_bf16]

@@ -23,6 +23,14 @@ MUTANTS = {
     "q8_unsigned_bytes": ("int q = (int8_t)blk[2 + i];", "int q = blk[2 + i];"),
     "q8_block_stride": ("orc_decode_q8_0_block(row + 34 * b, out + 32 * b);",
                         "orc_decode_q8_0_block(row + 32 * b, out + 32 * b);"),
+    "q4_0_nibble_order": ("int u_lo = qs[l] & 15;", "int u_lo = qs[l] >> 4;"),
+    "q4_0_offset": ("(double)(u_hi - 8)", "(double)(u_hi - 7)"),
+    "q4_0_unsigned_codes": ("(double)(u_lo - 8)", "(double)u_lo"),
+    "q4_0_hi_weight_slot": ("out[16 + l] =", "out[15 + l] ="),
+    "q4_0_nibbles_at": ("const uint8_t* qs = blk + 2;", "const uint8_t* qs = blk + 1;"),
+    "q4_0_block_stride": ("orc_decode_q4_0_block(row + 18 * b", "orc_decode_q4_0_block(row + 16 * b"),
+    "q4_0_row_bytes": ("cols / 32 * 18;", "cols / 32 * 16;"),
+    "f32_row_stride": ("case ORC_F32: return 4 * cols;", "case ORC_F32: return 4 * cols + 4;"),
     "fp16_bias": ("expo - 25);", "expo - 24);"),
     "fp16_subnormal_scale": ("ldexp((double)frac, -24);", "ldexp((double)frac, -25);"),
     "bf16_widen": ("(uint32_t)b << 16;", "(uint32_t)b << 15;"),

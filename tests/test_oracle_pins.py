@@ -165,6 +165,21 @@ def test_practice_script_mean_error():
     assert f"{np.abs(back - w).mean():.5f}" == p["q8_mean_error"]
 
 
+def test_practice_script_mean_error_4bit():
+    """The same two blocks through a Q4_0 block (fp16 scale absmax/7, 4-bit codes
+    q + 8): 18 bytes per block, 4.5 bits per weight, mean error 0.00324 as the
+    practice script prints for its 4-bit block (same value mapping; only the
+    pairing of weights in a byte differs, which the mean error cannot see)."""
+    p = _lesson()["practice"]
+    rng = np.random.default_rng(p["seed"])
+    w = rng.normal(0, p["sigma"], size=p["n"]).astype(np.float32)
+    packed = synth.quantize_q4_0(w)
+    assert packed.size // (p["n"] // p["block"]) == p["q4_bytes_per_block"]
+    assert packed.size * 8 / p["n"] == p["q4_bits_per_weight"]
+    back = oracle.dequantize(2, packed, 1, p["n"]).reshape(-1)
+    assert f"{np.abs(back - w).mean():.5f}" == p["q4_mean_error"]
+
+
 def test_synth_rows_are_counter_based():
     """Any row range regenerates the same bytes (used for full-size spot checks)."""
     full = synth.weight_rows(12, 99, 8, 512)
@@ -173,6 +188,18 @@ def test_synth_rows_are_counter_based():
     assert np.array_equal(full[4 * rb:7 * rb], part)
     full8 = synth.weight_rows(8, 5, 6, 256)
     assert np.array_equal(full8[2 * 272:], synth.weight_rows(8, 5, 4, 256, row0=2))
+
+
+def test_synth_q4_0_roundtrip_error():
+    """Q4_0 of N(0, 0.02): every decoded weight within half a step (d / 2) of its
+    source, and the scale is absmax / 7 rounded to fp16."""
+    w = synth.normal_f32(32 * 64, 4, sigma=0.02)
+    packed = synth.quantize_q4_0(w)
+    back = oracle.dequantize(2, packed, 64, 32).reshape(64, 32)
+    d = packed.reshape(64, 18)[:, :2].copy().view(np.float16).astype(np.float64).reshape(64)
+    amax = np.abs(w.reshape(64, 32)).max(axis=1)
+    assert np.allclose(d, amax / 7, rtol=2 ** -10)
+    assert np.all(np.abs(back - w.reshape(64, 32)) <= d[:, None] / 2 * (1 + 2 ** -10))
 
 
 def test_synth_q4_k_roundtrip_error():

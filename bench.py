@@ -453,6 +453,31 @@ def extras(torch, ggq, synth, stream):
                                        sp), "prefill")
     t = kernel_time(torch, f5q8, stream, 8)
     out["prefill_q8_0_512x14336x4096"] = {"us": round(t * 1e3, 2), "TFLOP_s": round(flops / t / 1e9, 1)}
+    del W, W8, X, Y
+
+    # the cfg4 shape as Q4_0 (33 MB: 6 copies cycled, 198 MB) and as F32 (235 MB, one copy);
+    # Q4_0 14336x4128 runs on the warp-per-row kernel
+    for name, g, copies, Ms in [("q4_0_14336x4096", WL.Q40_GEMV, 6, (1, 2, 4, 8, 16)),
+                                ("q4_0_14336x4128_warp_per_row", WL.Q40_ODD_GEMV, 6, (1, 8)),
+                                ("f32_14336x4096", WL.F32_GEMV, 1, (1,))]:
+        W0 = torch.from_numpy(synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)).cuda()
+        Ws = [W0] + [W0.clone() for _ in range(copies - 1)]
+        nb = g.rows * synth.row_bytes(g.qtype, g.cols)
+        res = {}
+        for M in Ms:
+            x = torch.randn(M, g.cols, device="cuda")
+            y = torch.empty(M, g.rows, device="cuda")
+            k = [0]
+
+            def fx():
+                W = Ws[k[0] % len(Ws)]
+                k[0] += 1
+                ggq.check(ggq.ggq_gemv(g.qtype, W.data_ptr(), g.rows, g.cols, x.data_ptr(), y.data_ptr(), M, sp),
+                          "gemv")
+            t = kernel_time(torch, fx, stream, 12)
+            res[str(M)] = {"us": round(t * 1e3, 2), "GB_s": round(nb / t / 1e6, 1)}
+        out[name] = res
+        del Ws, W0
     return out
 
 

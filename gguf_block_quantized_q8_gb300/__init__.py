@@ -1,4 +1,4 @@
-"""ggq -- GB300-native block-quantized (Q8_0 / Q4_K) dequantize + GEMV.
+"""ggq -- GB300-native block-quantized (Q8_0 / Q4_K / Q4_0, and F32) dequantize + GEMV.
 
 The compute path is ``libggq.so`` (C ABI in ``include/ggq.h``), built in-tree for
 sm_103a by ``build.build()``.  This package is its thin Python binding.

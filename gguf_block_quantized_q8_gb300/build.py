@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libggq.so")
 
-SOURCES = ["api.cu", "gemv.cu", "gemv_stream.cu", "gemv_noalloc.cu", "smallm.cu", "dequant.cu", "prefill.cu",
+SOURCES = ["api.cu", "gemv.cu", "gemv_rows.cu", "gemv_stream.cu", "gemv_noalloc.cu", "smallm.cu", "dequant.cu", "prefill.cu",
            "gguf_loader.cpp"]
 HEADERS = ["ggq_internal.h", "ptx.cuh", "gemv_tile.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

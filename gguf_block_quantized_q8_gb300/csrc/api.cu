@@ -24,6 +24,17 @@ int* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// weights per block of the types the GEMV, decode and row-gather calls take; 0: none
+int64_t block_of(int type) {
+    switch (type) {
+    case GGQ_F32: return 1;
+    case GGQ_Q4_0:
+    case GGQ_Q8_0: return 32;
+    case GGQ_Q4_K: return 256;
+    default: return 0;
+    }
+}
 }  // namespace
 
 int fail(int code, const char* fmt, ...) {
@@ -72,10 +83,11 @@ using namespace ggq;
 extern "C" int ggq_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
                         void* stream) {
     clear_error();
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K) return fail(GGQ_ETYPE, "ggq_gemv: type %d not supported", type);
+    const int64_t blk = block_of(type);
+    if (blk == 0) return fail(GGQ_ETYPE, "ggq_gemv: type %d not supported", type);
     if (!W || !x || !y) return fail(GGQ_EINVAL, "ggq_gemv: NULL pointer");
     if (rows < 1 || rows > 0x7fffffff) return fail(GGQ_EINVAL, "ggq_gemv: rows %lld out of range", (long long)rows);
-    const int64_t blk = type == GGQ_Q4_K ? 256 : 32;
+    if (cols > (int64_t)1 << 40) return fail(GGQ_EINVAL, "ggq_gemv: cols %lld out of range", (long long)cols);
     if (cols < blk || cols % blk) return fail(GGQ_EINVAL, "ggq_gemv: cols %lld not a positive multiple of %lld",
                                               (long long)cols, (long long)blk);
     if (M < 1 || M > 16) return fail(GGQ_EINVAL, "ggq_gemv: M %d outside 1..16", M);
@@ -88,10 +100,11 @@ extern "C" int ggq_gemv(int type, const void* W, int64_t rows, int64_t cols, con
 extern "C" int ggq_gemv_multi(int type, int n, const void* const* W, const int64_t* rows, int64_t cols,
                               const float* x, float* const* y, int M, void* stream) {
     clear_error();
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K) return fail(GGQ_ETYPE, "ggq_gemv_multi: type %d not supported", type);
+    const int64_t blk = block_of(type);
+    if (blk == 0) return fail(GGQ_ETYPE, "ggq_gemv_multi: type %d not supported", type);
     if (n < 1 || n > 4) return fail(GGQ_EINVAL, "ggq_gemv_multi: n %d outside 1..4", n);
     if (!W || !rows || !y || !x) return fail(GGQ_EINVAL, "ggq_gemv_multi: NULL pointer");
-    const int64_t blk = type == GGQ_Q4_K ? 256 : 32;
+    if (cols > (int64_t)1 << 40) return fail(GGQ_EINVAL, "ggq_gemv_multi: cols %lld out of range", (long long)cols);
     if (cols < blk || cols % blk) return fail(GGQ_EINVAL, "ggq_gemv_multi: cols %lld not a positive multiple of %lld",
                                               (long long)cols, (long long)blk);
     if (M < 1 || M > 16) return fail(GGQ_EINVAL, "ggq_gemv_multi: M %d outside 1..16", M);
@@ -130,9 +143,9 @@ extern "C" int ggq_gemm_prefill(int type, const void* W, int64_t rows, int64_t c
 
 extern "C" int ggq_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out, void* stream) {
     clear_error();
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K) return fail(GGQ_ETYPE, "ggq_dequantize: type %d not supported", type);
+    const int64_t blk = block_of(type);
+    if (blk == 0) return fail(GGQ_ETYPE, "ggq_dequantize: type %d not supported", type);
     if (!W || !out) return fail(GGQ_EINVAL, "ggq_dequantize: NULL pointer");
-    const int64_t blk = type == GGQ_Q4_K ? 256 : 32;
     if (rows < 0 || cols < 0 || cols % blk) return fail(GGQ_EINVAL, "ggq_dequantize: bad shape");
     if (!aligned(W, 16) || !aligned(out, 4)) return fail(GGQ_EINVAL, "ggq_dequantize: misaligned pointer");
     return launch_dequantize(type, W, rows, cols, out, static_cast<cudaStream_t>(stream));
@@ -141,12 +154,12 @@ extern "C" int ggq_dequantize(int type, const void* W, int64_t rows, int64_t col
 extern "C" int ggq_embed(int type, const void* table, int64_t rows, int64_t cols, const int32_t* ids, int n,
                          float* out, void* stream) {
     clear_error();
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K) return fail(GGQ_ETYPE, "ggq_embed: type %d not supported", type);
+    const int64_t blk = block_of(type);
+    if (blk == 0) return fail(GGQ_ETYPE, "ggq_embed: type %d not supported", type);
     if (!table || !ids || !out) return fail(GGQ_EINVAL, "ggq_embed: NULL pointer");
-    const int64_t blk = type == GGQ_Q4_K ? 256 : 32;
     if (rows < 1 || rows > 0x7fffffff || cols < 1 || cols % blk) return fail(GGQ_EINVAL, "ggq_embed: bad shape");
     if (n < 1 || n > 65535) return fail(GGQ_EINVAL, "ggq_embed: n %d outside 1..65535", n);
-    if (!aligned(table, 2) || !aligned(ids, 4) || !aligned(out, 4))
+    if (!aligned(table, type == GGQ_F32 ? 4 : 2) || !aligned(ids, 4) || !aligned(out, 4))
         return fail(GGQ_EINVAL, "ggq_embed: misaligned pointer");
     return launch_embed(type, table, rows, cols, ids, n, out, static_cast<cudaStream_t>(stream));
 }

@@ -4,7 +4,10 @@
 // Q8_0 ("GGUF: The File Format...", "How a Q8_0 block is stored"): w = d * q.
 // Q4_K (same section, k-quant paragraph; byte layout fp16 d, fp16 dmin, 12 bytes of
 // packed 6-bit scales and mins, 128 bytes of nibbles): w = d*sc_j*q - dmin*m_j.
-// Both are exact in fp32 except the single rounding of the Q4_K subtraction.
+// Q4_0 (same section: the Q8_0 layout with 4-bit integers; byte layout fp16 d,
+// then byte l holding the codes of weights l (low nibble) and 16 + l (high)):
+// w = d * (code - 8).  F32 rows are copied as they are.
+// All are exact in fp32 except the single rounding of the Q4_K subtraction.
 #include <cuda_runtime.h>
 
 #include "ggq_internal.h"
@@ -23,6 +26,21 @@ __global__ void dequant_q8_kernel(const uint8_t* __restrict__ W, int64_t nblocks
     float* o = out + 32 * b;
 #pragma unroll 8
     for (int i = 0; i < 32; ++i) o[i] = d * (float)(int8_t)blk[2 + i];
+}
+
+// one thread per Q4_0 block; the 18-byte block starts on an even address
+__global__ void dequant_q40_kernel(const uint8_t* __restrict__ W, int64_t nblocks, float* __restrict__ out) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const uint8_t* blk = W + 18 * b;
+    const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+    float* o = out + 32 * b;
+#pragma unroll 4
+    for (int l = 0; l < 16; ++l) {
+        const int q = blk[2 + l];
+        o[l] = d * (float)((q & 15) - 8);
+        o[16 + l] = d * (float)((q >> 4) - 8);
+    }
 }
 
 // one thread per Q4_K sub-block (32 weights)
@@ -57,7 +75,7 @@ __global__ void dequant_q4k_kernel(const uint8_t* __restrict__ W, int64_t nsub, 
 // token)): out[i, k] = w[ids[i], k].  One thread per output weight: the q
 // bytes and the writes are coalesced, the block's scale bytes come from cache.
 // An id outside [0, rows) gives a row of zeros and sets kStatusBadIndex.
-template <bool Q4K>
+template <int TYPE>
 __global__ void embed_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_t cols,
                              const int32_t* __restrict__ ids, float* __restrict__ out, int* status) {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -70,10 +88,18 @@ __global__ void embed_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_
         if (k == 0) atomicOr(status, kStatusBadIndex);
         return;
     }
-    if constexpr (!Q4K) {
+    if constexpr (TYPE == GGQ_F32) {
+        *o = reinterpret_cast<const float*>(W)[(int64_t)id * cols + k];
+    } else if constexpr (TYPE == GGQ_Q8_0) {
         const uint8_t* blk = W + ((int64_t)id * (cols / 32) + k / 32) * 34;
         const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
         *o = d * (float)(int8_t)blk[2 + (k & 31)];
+    } else if constexpr (TYPE == GGQ_Q4_0) {
+        const uint8_t* blk = W + ((int64_t)id * (cols / 32) + k / 32) * 18;
+        const int l = (int)(k & 31);
+        const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+        const int q = (blk[2 + (l & 15)] >> (l >= 16 ? 4 : 0)) & 15;
+        *o = d * (float)(q - 8);
     } else {
         const uint8_t* blk = W + ((int64_t)id * (cols / 256) + k / 256) * 144;
         const int kk = (int)(k & 255), j = kk >> 5, l = kk & 31;
@@ -102,19 +128,31 @@ int launch_embed(int type, const void* W, int64_t rows, int64_t cols, const int3
     const dim3 grid((unsigned)((cols + 255) / 256), (unsigned)n);
     const uint8_t* w = static_cast<const uint8_t*>(W);
     if (type == GGQ_Q8_0)
-        embed_kernel<false><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
+        embed_kernel<GGQ_Q8_0><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
+    else if (type == GGQ_Q4_0)
+        embed_kernel<GGQ_Q4_0><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
+    else if (type == GGQ_F32)
+        embed_kernel<GGQ_F32><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
     else
-        embed_kernel<true><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
+        embed_kernel<GGQ_Q4_K><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GGQ_OK : cuda_fail(e, "embed launch");
 }
 
 int launch_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t stream) {
     const uint8_t* w = static_cast<const uint8_t*>(W);
-    if (type == GGQ_Q8_0) {
+    if (type == GGQ_F32) {
+        if (rows * cols == 0) return GGQ_OK;
+        cudaError_t e = cudaMemcpyAsync(out, W, (size_t)(rows * cols) * 4, cudaMemcpyDeviceToDevice, stream);
+        return e == cudaSuccess ? GGQ_OK : cuda_fail(e, "dequantize copy");
+    }
+    if (type == GGQ_Q8_0 || type == GGQ_Q4_0) {
         const int64_t nb = rows * (cols / 32);
         if (nb == 0) return GGQ_OK;
-        dequant_q8_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(w, nb, out);
+        if (type == GGQ_Q8_0)
+            dequant_q8_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(w, nb, out);
+        else
+            dequant_q40_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(w, nb, out);
     } else {
         const int64_t ns = rows * (cols / 256) * 8;
         if (ns == 0) return GGQ_OK;

@@ -418,6 +418,21 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
     p.M = M;
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
+    if (type == GGQ_F32 || type == GGQ_Q4_0) {
+        if (type == GGQ_Q4_0 && stream_gemv_supported(type, cols, std::min(M, 4), 1, &rows)) {
+            // the streaming kernel takes up to 4 activation rows; M 5..16 runs it
+            // once per group of up to 4 (x and y rows are contiguous)
+            for (int m0 = 0; m0 < M; m0 += 4) {
+                const void* Ws[1] = {W};
+                float* ys[1] = {y + (int64_t)m0 * rows};
+                const int rc = launch_gemv_stream(type, 1, Ws, &rows, cols, x + (int64_t)m0 * cols, ys,
+                                                  std::min(4, M - m0), stream);
+                if (rc) return rc;
+            }
+            return GGQ_OK;
+        }
+        return launch_gemv_rows(type, W, rows, cols, x, y, M, stream);
+    }
     if (type == GGQ_Q8_0 && cols % 256 != 0) {
         const int64_t grid = (rows + kWarps - 1) / kWarps;
         cudaLaunchConfig_t cfg = {};

@@ -7,8 +7,8 @@
 // one.  A single GEMV is a chain of one stage.
 //
 // Work unit: one 256-column block of one row (SB) -- a Q4_K super-block
-// (144 B) or a Q8_0 period of 8 blocks (272 B) -- split into four 64-column
-// chunks.  Each matrix's rows form groups of 16 (the last may be shorter),
+// (144 B), a Q8_0 period of 8 blocks (272 B) or a Q4_0 period of 8 blocks
+// (144 B) -- split into four 64-column chunks.  Each matrix's rows form groups of 16 (the last may be shorter),
 // numbered across the stage's matrices.
 //
 //   * CTA b (one per SM) owns groups [GT*b/G, GT*(b+1)/G) of the stage's GT:
@@ -101,24 +101,30 @@ struct ChainParams {
     int nstages;
     int M;
     int ring;                   // tiles per warp ring
-    int xs;                     // x' floats per activation row (272 per SB of the widest stage)
+    int xs;                     // x' floats per activation row (kXsb per SB of the widest stage)
     int nsub;                   // x sums per activation row (8 per SB of the widest stage)
     int* counter;               // stage counter (chains of > 1 stage); zero between launches
     int* status;
 };
 
+// Weight layouts the kernel streams: the copy geometry and the decode.
+enum Kind { kKQ8 = 0, kKQ4K = 1, kKQ40 = 2 };
+
 // Tile of one bulk tensor copy: 16 rows x NSB SBs, each row padded so that
 // rows r and r+1 of one chunk fall in different banks.  Copies of a few KB:
 // much smaller ones cost more per copy than the bytes they bring.
-template <bool Q4K>
+template <int K>
 struct Blk {
-    static constexpr int kBytes = Q4K ? 144 : 272;      // one SB
-    static constexpr int kElems = kBytes / 8;            // 8-byte elements per SB
-    static constexpr int kNsb = Q4K ? 2 : 1;             // SBs per copy
-    static constexpr int kPad = Q4K ? 2 : 0;             // elements of padding per row
+    static constexpr int kBytes = K == kKQ8 ? 272 : 144;     // one SB
+    static constexpr int kElems = kBytes / 8;                 // 8-byte elements per SB
+    static constexpr int kNsb = K == kKQ8 ? 1 : 2;            // SBs per copy
+    static constexpr int kPad = K == kKQ8 ? 0 : 2;            // elements of padding per row
     static constexpr int kRow = (kElems * kNsb + kPad) * 8;    // smem bytes per row: 304 / 272
     static constexpr int kCopy = kGroupRows * kRow;            // bytes per copy
     static constexpr int kTile = (kCopy + 127) / 128 * 128;    // smem stride: 128-byte aligned
+    // x' floats per SB: Q4_K four chunks of 64 padded to 68; Q8_0 one per byte
+    // of the period; Q4_0 two per byte of its four 36-byte chunks
+    static constexpr int kXsb = K == kKQ40 ? 288 : 272;
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -233,9 +239,10 @@ __device__ __forceinline__ void warp_run(const Groups& G, int U, int w, int& t0,
     t1 = (int)(T * (unsigned)(w + 1) / NW);
 }
 
-template <bool Q4K, int MMAX, int W>
+template <int K, int MMAX, int W>
 __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__ StageDesc inl, const ChainParams p) {
-    using B = Blk<Q4K>;
+    using B = Blk<K>;
+    constexpr bool Q4K = K == kKQ4K;
     constexpr int kThreads = 32 * W;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -314,10 +321,13 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     refill();
 
     // x' placement of the lane's 4 consecutive columns 4l .. 4l+3 of a
-    // 128-column half of an SB (the other half adds 136 floats).  Q4_K: chunk
-    // l/16 (68 floats each), byte positions b = 0..3 of word l%8, low or high
-    // nibble ((l/8) odd: high) at q4k_xslot, stride 16.  Q8_0: byte positions
-    // of the period, 34 per block of 32 after its 2-byte scale.
+    // 128-column half of an SB (the other half adds kXsb / 2 floats).  Q4_K:
+    // chunk l/16 (68 floats each), byte positions b = 0..3 of word l%8, low or
+    // high nibble ((l/8) odd: high) at q4k_xslot, stride 16.  Q8_0: byte
+    // positions of the period, 34 per block of 32 after its 2-byte scale.
+    // Q4_0: block l/8 of the half (chunk l/16, block (l/8)%2 of the chunk),
+    // weights 4(l%8) .. +3 of the block: byte positions 2 + 4(l%4) .. +3 after
+    // the block's start, high nibble when l%8 >= 4, at 2B + hi, stride 2.
     int xoff;
     float4 xsc;
     {
@@ -326,6 +336,10 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             xoff = (lane >> 4) * 68 + 2 * (lane & 7) + hi;
             const int k = 4 * lane;
             xsc = make_float4(q4k_xscale(k), q4k_xscale(k + 1), q4k_xscale(k + 2), q4k_xscale(k + 3));
+        } else if (K == kKQ40) {
+            const int b4 = lane >> 3;
+            xoff = (b4 >> 1) * 72 + 2 * (18 * (b4 & 1) + 2 + 4 * (lane & 3)) + ((lane >> 2) & 1);
+            xsc = make_float4(q40_xscale(xoff), q40_xscale(xoff + 2), q40_xscale(xoff + 4), q40_xscale(xoff + 6));
         } else {
             xoff = 34 * (lane >> 3) + 2 + 4 * (lane & 7);
             xsc = make_float4(q8_xscale(xoff), q8_xscale(xoff + 1), q8_xscale(xoff + 2), q8_xscale(xoff + 3));
@@ -358,10 +372,10 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         const int cols = sd->cols, U = sd->units;
         const int xs = p.xs, nsub = p.nsub;
 
-        // ---- x' and the 32-column sums of this stage: 272 floats per SB (Q4_K:
+        // ---- x' and the 32-column sums of this stage: kXsb floats per SB (Q4_K:
         // four chunks of 64 in the q4k_xslot order, each padded by 4; Q8_0: one
-        // float per byte position of the period).  x may have been written by
-        // other CTAs: read it from L2.
+        // float per byte position of the period; Q4_0: two per byte position).
+        // x may have been written by other CTAs: read it from L2.
         {
             // Lane l of a warp step takes 4 consecutive values (one float4) of x:
             // 8 lanes cover a 32-column sub-block, whose sum takes 3 shuffles.
@@ -383,20 +397,28 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 const int m = MMAX == 1 ? 0 : qb / c4;
                 const int h = qb - m * c4;          // first float4 of the step within the row
                 const int u = h >> 6;               // SB
-                float* dst = xp + (size_t)m * xs + u * 272 + ((h & 32) ? 136 : 0) + xoff;
+                float* dst = xp + (size_t)m * xs + u * B::kXsb + ((h & 32) ? B::kXsb / 2 : 0) + xoff;
                 const float4 e = make_float4(v.x * xsc.x, v.y * xsc.y, v.z * xsc.z, v.w * xsc.w);
                 if (Q4K) {
                     dst[0] = e.x;
                     dst[16] = e.y;
                     dst[32] = e.z;
                     dst[48] = e.w;
+                } else if (K == kKQ40) {
+                    dst[0] = e.x;
+                    dst[2] = e.y;
+                    dst[4] = e.z;
+                    dst[6] = e.w;
                 } else {
                     dst[0] = e.x;
                     dst[1] = e.y;
                     dst[2] = e.z;
                     dst[3] = e.w;
                 }
-                if ((lane & 7) == 0) sums[m * nsub + u * 8 + ((h & 32) >> 3) + (lane >> 3)] = Q4K ? sum : 128.0f * sum;
+                // the code offsets: Q8_0 bytes are stored XOR 0x80 (128), Q4_0 codes are q + 8
+                if ((lane & 7) == 0)
+                    sums[m * nsub + u * 8 + ((h & 32) >> 3) + (lane >> 3)] =
+                        Q4K ? sum : (K == kKQ40 ? 8.0f : 128.0f) * sum;
             };
             const int xop = sd->x_op;
             if (xop == GGQ_X_PLAIN) {
@@ -627,12 +649,15 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 if (j < nv) {
                     const int uj = u + j;
                     if constexpr (Q4K) {
-                        q4k_chunk_rows<MMAX, R>(rowp + j * B::kBytes, 8 * B::kRow, c, xp + uj * 272, xs,
+                        q4k_chunk_rows<MMAX, R>(rowp + j * B::kBytes, 8 * B::kRow, c, xp + uj * B::kXsb, xs,
                                                 sums + uj * 8, nsub, acc2, 68);
+                    } else if constexpr (K == kKQ40) {
+                        q40_chunk_rows<MMAX, R>(rowp + j * B::kBytes + 36 * c, 8 * B::kRow, xp + uj * B::kXsb + 72 * c,
+                                                xs, sums + uj * 8 + 2 * c, nsub, acc);
                     } else {
 #pragma unroll
                         for (int i = 0; i < R; ++i)
-                            q8_chunk<MMAX>(rowp + 8 * i * B::kRow + j * B::kBytes + 68 * c, xp + uj * 272 + 68 * c,
+                            q8_chunk<MMAX>(rowp + 8 * i * B::kRow + j * B::kBytes + 68 * c, xp + uj * B::kXsb + 68 * c,
                                            xs, sums + uj * 8 + 2 * c, nsub, acc[i]);
                     }
                 }
@@ -719,34 +744,43 @@ int mmax_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : 4; }
 
 // Warps per CTA.  GGQ_STREAM_WARPS=8|12|16 overrides the default for M = 1 (a
 // tuning aid; read once, so a chain keeps the layout it was created with).
-int warps_of(bool q4k, int mmax) {
+int warps_of(int mmax) {
     static const int env = [] {
         const char* v = getenv("GGQ_STREAM_WARPS");
         const int w = v ? atoi(v) : 0;
         return (w == 8 || w == 12 || w == 16) ? w : 0;
     }();
     if (env && mmax == 1) return env;
-    (void)q4k;
     return mmax == 4 ? 12 : 16;
 }
 
+int kind_of(int type) { return type == GGQ_Q4_K ? kKQ4K : type == GGQ_Q4_0 ? kKQ40 : kKQ8; }
+
 constexpr int kMaxRing = 8;
 
-size_t tile_bytes(bool q4k) { return q4k ? (size_t)Blk<true>::kTile : (size_t)Blk<false>::kTile; }
+size_t tile_bytes(int kind) {
+    return kind == kKQ8 ? (size_t)Blk<kKQ8>::kTile : kind == kKQ4K ? (size_t)Blk<kKQ4K>::kTile : (size_t)Blk<kKQ40>::kTile;
+}
+int row_box(int kind) {   // 8-byte elements per row of a copy box
+    return kind == kKQ8 ? Blk<kKQ8>::kRow / 8 : kind == kKQ4K ? Blk<kKQ4K>::kRow / 8 : Blk<kKQ40>::kRow / 8;
+}
+int xsb_of(int kind) { return kind == kKQ40 ? Blk<kKQ40>::kXsb : kind == kKQ4K ? Blk<kKQ4K>::kXsb : Blk<kKQ8>::kXsb; }
+int64_t sb_bytes(int kind) { return kind == kKQ8 ? 272 : 144; }
 
-size_t rows_smem(bool q4k, int mmax, int ring, int64_t cols_max) {
-    const int W = warps_of(q4k, mmax);
+size_t rows_smem(int kind, int mmax, int ring, int64_t cols_max) {
+    const int W = warps_of(mmax);
     const int64_t U = cols_max / 256;
     const size_t cut = (size_t)2 * W * kGroupRows * mmax * 4 + (size_t)2 * W * 4;
-    return (size_t)W * ring * tile_bytes(q4k) + kInfoSlots * sizeof(StageInfo) + kPartMax * sizeof(int2) + (size_t)mmax * U * 272 * 4 +
+    return (size_t)W * ring * tile_bytes(kind) + kInfoSlots * sizeof(StageInfo) + kPartMax * sizeof(int2) +
+           (size_t)mmax * U * xsb_of(kind) * 4 +
            (size_t)mmax * U * 8 * 4 + cut +
            (size_t)W * ring * 8;
 }
 
-int rows_ring(bool q4k, int mmax, int64_t cols_max) {
+int rows_ring(int kind, int mmax, int64_t cols_max) {
     int ring = kMaxRing;
-    while (ring > 1 && rows_smem(q4k, mmax, ring, cols_max) > kSmemLimit) --ring;
-    return rows_smem(q4k, mmax, ring, cols_max) <= kSmemLimit ? ring : 0;
+    while (ring > 1 && rows_smem(kind, mmax, ring, cols_max) > kSmemLimit) --ring;
+    return rows_smem(kind, mmax, ring, cols_max) <= kSmemLimit ? ring : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -765,12 +799,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // Tensor map of one matrix: rows of `row_bytes` as 8-byte elements, box of
 // 16 rows x (NSB SBs + pad).  Out-of-range parts of a box read as zeros.
-int encode_map(CUtensorMap* map, const void* W, int64_t rows, int64_t row_bytes, bool q4k) {
+int encode_map(CUtensorMap* map, const void* W, int64_t rows, int64_t row_bytes, int kind) {
     auto fn = tensor_map_encoder();
     if (!fn) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)(q4k ? Blk<true>::kRow / 8 : Blk<false>::kRow / 8), (cuuint32_t)kGroupRows};
+    cuuint32_t box[2] = {(cuuint32_t)row_box(kind), (cuuint32_t)kGroupRows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(W), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -781,12 +815,12 @@ int encode_map(CUtensorMap* map, const void* W, int64_t rows, int64_t row_bytes,
 
 int make_stage(int type, int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
                float* const* y, StageDesc* sd) {
-    const bool q4k = type == GGQ_Q4_K;
+    const int kind = kind_of(type);
     memset(sd, 0, sizeof(*sd));
     int g = 0;
     for (int s = 0; s < n; ++s) {
-        const int64_t row_bytes = cols / 256 * (q4k ? 144 : 272);
-        int rc = encode_map(&sd->maps[s], W[s], rows[s], row_bytes, q4k);
+        const int64_t row_bytes = cols / 256 * sb_bytes(kind);
+        int rc = encode_map(&sd->maps[s], W[s], rows[s], row_bytes, kind);
         if (rc) return rc;
         sd->info.y[s] = y[s];
         sd->info.rows[s] = (int)rows[s];
@@ -801,9 +835,9 @@ int make_stage(int type, int n, const void* const* W, const int64_t* rows, int64
     return GGQ_OK;
 }
 
-template <bool Q4K, int MMAX, int W>
+template <int K, int MMAX, int W>
 int launch_t(const StageDesc& inl, const ChainParams& p, cudaStream_t stream, size_t smem, bool cooperative) {
-    auto kernel = rows_kernel<Q4K, MMAX, W>;
+    auto kernel = rows_kernel<K, MMAX, W>;
     static int configured[64] = {};   // largest dynamic smem set so far, per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -834,50 +868,56 @@ int launch_t(const StageDesc& inl, const ChainParams& p, cudaStream_t stream, si
 // `inl` is the only stage.
 int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, int nstages, int64_t cols_max,
                 int* counter, cudaStream_t stream) {
-    const bool q4k = type == GGQ_Q4_K;
+    const int kind = kind_of(type);
     const int mmax = mmax_of(M);
-    const int W = warps_of(q4k, mmax);
+    const int W = warps_of(mmax);
     ChainParams p = {};
     p.table = table;
     p.nstages = nstages;
     p.M = M;
-    p.ring = rows_ring(q4k, mmax, cols_max);
+    p.ring = rows_ring(kind, mmax, cols_max);
     if (p.ring == 0) return fail(GGQ_EINVAL, "shape needs too much shared memory");
-    p.xs = (int)(cols_max / 256 * 272);
+    p.xs = (int)(cols_max / 256 * xsb_of(kind));
     p.nsub = (int)(cols_max / 32);
     p.counter = counter;
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
-    const size_t smem = rows_smem(q4k, mmax, p.ring, cols_max);
+    const size_t smem = rows_smem(kind, mmax, p.ring, cols_max);
     const bool coop = nstages > 1;
-    if (q4k) {
+    if (kind == kKQ4K) {
         if (mmax == 1) {
-            if (W == 8) return launch_t<true, 1, 8>(inl, p, stream, smem, coop);
-            if (W == 12) return launch_t<true, 1, 12>(inl, p, stream, smem, coop);
-            return launch_t<true, 1, 16>(inl, p, stream, smem, coop);
+            if (W == 8) return launch_t<kKQ4K, 1, 8>(inl, p, stream, smem, coop);
+            if (W == 12) return launch_t<kKQ4K, 1, 12>(inl, p, stream, smem, coop);
+            return launch_t<kKQ4K, 1, 16>(inl, p, stream, smem, coop);
         }
-        if (mmax == 2) return launch_t<true, 2, 16>(inl, p, stream, smem, coop);
-        return launch_t<true, 4, 12>(inl, p, stream, smem, coop);
+        if (mmax == 2) return launch_t<kKQ4K, 2, 16>(inl, p, stream, smem, coop);
+        return launch_t<kKQ4K, 4, 12>(inl, p, stream, smem, coop);
+    }
+    if (kind == kKQ40) {   // the warp-count override is not instantiated for Q4_0
+        if (mmax == 1) return launch_t<kKQ40, 1, 16>(inl, p, stream, smem, coop);
+        if (mmax == 2) return launch_t<kKQ40, 2, 16>(inl, p, stream, smem, coop);
+        return launch_t<kKQ40, 4, 12>(inl, p, stream, smem, coop);
     }
     if (mmax == 1) {
-        if (W == 8) return launch_t<false, 1, 8>(inl, p, stream, smem, coop);
-        if (W == 12) return launch_t<false, 1, 12>(inl, p, stream, smem, coop);
-        return launch_t<false, 1, 16>(inl, p, stream, smem, coop);
+        if (W == 8) return launch_t<kKQ8, 1, 8>(inl, p, stream, smem, coop);
+        if (W == 12) return launch_t<kKQ8, 1, 12>(inl, p, stream, smem, coop);
+        return launch_t<kKQ8, 1, 16>(inl, p, stream, smem, coop);
     }
-    if (mmax == 2) return launch_t<false, 2, 16>(inl, p, stream, smem, coop);
-    return launch_t<false, 4, 12>(inl, p, stream, smem, coop);
+    if (mmax == 2) return launch_t<kKQ8, 2, 16>(inl, p, stream, smem, coop);
+    return launch_t<kKQ8, 4, 12>(inl, p, stream, smem, coop);
 }
 
 }  // namespace
 
 bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_t* rows) {
     if (M > kMaxM || nseg < 1 || nseg > kMaxSeg || cols % 256 || cols > (1 << 20)) return false;
-    // a Q4_K copy box (2 SBs + pad) must not be wider than a row
-    if (type == GGQ_Q4_K && cols < 768) return false;
+    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0) return false;
+    // a Q4_K / Q4_0 copy box (2 SBs + pad) must not be wider than a row
+    if (type != GGQ_Q8_0 && cols < 768) return false;
     int64_t r = 0;
     for (int s = 0; s < nseg; ++s) r += rows[s];
     if (r * (cols / 256) >= (1ll << 31)) return false;   // SB indices are 32-bit
-    return rows_ring(type == GGQ_Q4_K, mmax_of(M), cols) > 0;
+    return rows_ring(kind_of(type), mmax_of(M), cols) > 0;
 }
 
 int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
@@ -913,7 +953,8 @@ extern "C" int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chai
     clear_error();
     if (!out) return fail(GGQ_EINVAL, "ggq_chain_create: out is NULL");
     *out = nullptr;
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K) return fail(GGQ_ETYPE, "ggq_chain_create: type %d not supported", type);
+    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0)
+        return fail(GGQ_ETYPE, "ggq_chain_create: type %d not supported", type);
     if (M < 1 || M > kMaxM) return fail(GGQ_EINVAL, "ggq_chain_create: M %d outside 1..%d", M, kMaxM);
     if (nstages < 1 || nstages > 65536 || !stages) return fail(GGQ_EINVAL, "ggq_chain_create: bad stage list");
     std::vector<StageDesc> host((size_t)nstages);
@@ -950,7 +991,7 @@ extern "C" int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chai
         }
         cols_max = std::max<int64_t>(cols_max, st.cols);
     }
-    if (rows_ring(type == GGQ_Q4_K, mmax_of(M), cols_max) == 0)
+    if (rows_ring(kind_of(type), mmax_of(M), cols_max) == 0)
         return fail(GGQ_EINVAL, "ggq_chain_create: widest stage needs too much shared memory");
     for (int s = 0; s < nstages; ++s) {   // all stages valid: encode them
         const ggq_chain_stage& st = stages[s];

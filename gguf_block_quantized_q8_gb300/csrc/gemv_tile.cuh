@@ -1,8 +1,9 @@
-// Per-lane decode + multiply of one weight tile row (one Q4_K super-block or one
-// 8-block Q8_0 period), shared by the GEMV kernels.
+// Per-lane decode + multiply of one weight tile row (one Q4_K super-block, one
+// 8-block Q8_0 period or a chunk of an 8-block Q4_0 period), shared by the
+// GEMV kernels.
 //
-// Decode trick (one AND per weight): a nibble (Q4_K) or an offset byte (Q8_0)
-// masked in place inside its 32-bit word is the float bit pattern
+// Decode trick (one AND per weight): a nibble (Q4_K, Q4_0) or an offset byte
+// (Q8_0) masked in place inside its 32-bit word is the float bit pattern
 // q * 2^(p - 149) for bit position p <= 20 -- a subnormal, or the first normal
 // binade, which continues the subnormals linearly.  The activations are stored
 // pre-scaled, x' = x * 2^(53 - p), so pattern * x' = q * x * 2^-96 exactly, and
@@ -258,6 +259,92 @@ __device__ __forceinline__ void q8_tile_row(const uint8_t* rp, const float* xu, 
                     }
                 }
             }
+        }
+    }
+}
+
+// Pre-scale factor of the x' value at slot e = 2B + hi of a Q4_0 chunk (B: the
+// byte position in the chunk, hi: 1 for the high nibble).  Chunks start on
+// 4-byte boundaries, so B mod 4 is the byte's position in its word; byte 3 is
+// shifted down to 2 before masking.
+__device__ __forceinline__ float q40_xscale(int e) {
+    const int pos = (e >> 1) & 3, hi = e & 1;
+    const int p = 8 * (pos < 2 ? pos : 2) + 4 * hi;   // bit position of the nibble
+    return p == 0 ? pow2f(53) : p == 4 ? pow2f(49) : p == 8 ? pow2f(45) : p == 12 ? pow2f(41)
+                              : p == 16 ? pow2f(37) : pow2f(33);
+}
+
+// Chunk c of a 144-byte Q4_0 period (blocks 2c and 2c+1: bytes 36c .. 36c+35,
+// nine 32-bit words; block 2c has d in bytes 0-1 and its codes in 2-17, block
+// 2c+1 has d in 18-19 and its codes in 20-35) for R rows per lane (rp: the
+// chunk in the lane's first row, 4-byte aligned; `rstride` bytes to the next).
+// The code of weight l (l < 16) of a block is the low nibble of its byte l,
+// that of weight 16 + l the high nibble; the weight is d * (code - 8).
+// x' of byte position B of the chunk sits at xu[2B] (low-nibble weight) and
+// xu[2B + 1] (high-nibble weight), 72 floats per chunk, activation row m at
+// xu + m*xs; 8 * sum(x) of blocks 2c, 2c+1 at su[m*ss + 0 / 1].
+// acc[r][m] += the chunk's 64 products.
+//
+// A qs word gives the patterns of the low and the high nibble of one byte as
+// one register pair (two ANDs), the first operand of fma.f32x2 against the
+// pair (x'_lo, x'_hi); both belong to the same block, so one accumulator pair
+// per block and the block's scale apply at the end.
+template <int MMAX, int R>
+__device__ __forceinline__ void q40_chunk_rows(const uint8_t* rp, int rstride, const float* xu, int xs,
+                                               const float* su, int ss, float (&acc)[R][MMAX]) {
+    uint32_t wd[R][9];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t* wp = reinterpret_cast<const uint32_t*>(rp + r * rstride);
+#pragma unroll
+        for (int i = 0; i < 9; ++i) wd[r][i] = wp[i];
+    }
+    F2 t[R][MMAX][2];   // [block of the chunk]
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) t[r][m][0] = t[r][m][1] = f2_zero();
+#pragma unroll
+    for (int wi = 0; wi < 9; ++wi) {
+        // byte positions of this word that hold codes, and their block
+        const int p0 = wi == 0 ? 2 : 0, p1 = wi == 4 ? 2 : 4;
+        const int blk = wi <= 4 ? 0 : 1;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {   // byte positions 2q, 2q + 1: one float4 of x' per activation row
+            if (2 * q + 1 < p0 || 2 * q >= p1) continue;
+            float4 xv[MMAX];
+#pragma unroll
+            for (int m = 0; m < MMAX; ++m) xv[m] = *reinterpret_cast<const float4*>(xu + m * xs + 8 * wi + 4 * q);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int pos = 2 * q + k;
+                if (pos < p0 || pos >= p1) continue;
+                const uint32_t ml = pos == 0 ? 0x0000000Fu : pos == 1 ? 0x00000F00u : 0x000F0000u;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t v = pos < 3 ? wd[r][wi] : (wd[r][wi] >> 8);
+                    const uint64_t pr = and_pair(v, ml, ml << 4);
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m) {
+                        if (k) f2_fma64(t[r][m][blk], pr, xv[m].z, xv[m].w);
+                        else f2_fma64(t[r][m][blk], pr, xv[m].x, xv[m].y);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float d0 = half_bits_to_float(wd[r][0]);
+        const float d1 = half_bits_to_float(wd[r][4] >> 16);
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) {
+            float p0x, p0y, p1x, p1y;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(p0x), "=f"(p0y) : "l"(t[r][m][0].v));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(p1x), "=f"(p1y) : "l"(t[r][m][1].v));
+            const float2 s2 = *reinterpret_cast<const float2*>(su + m * ss);
+            acc[r][m] = fmaf(d0, fmaf(p0x + p0y, kTwo96, -s2.x), acc[r][m]);
+            acc[r][m] = fmaf(d1, fmaf(p1x + p1y, kTwo96, -s2.y), acc[r][m]);
         }
     }
 }

@@ -141,10 +141,15 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  * weights decoded on the fly: Q8_0 w = d*q ("GGUF: The File Format...", "How
  * a Q8_0 block is stored"), Q4_K w = d*sc_j*q - dmin*m_j (the k-quant paragraph
  * of the same section; byte layout: fp16 d, fp16 dmin, 12 bytes of packed
- * 6-bit scales/mins, 128 bytes of nibbles).  Decoded weights are never written
- * to memory; products accumulate in fp32 (any order).
+ * 6-bit scales/mins, 128 bytes of nibbles), Q4_0 w = d*(u - 8) (the same
+ * section: the Q8_0 layout with 4-bit integers, 18 bytes per 32 weights; byte
+ * layout: fp16 d, then byte l holding the code u of weight l in its low nibble
+ * and that of weight 16 + l in its high nibble), F32 the fp32 values as
+ * stored.  Decoded weights are never written to memory; products accumulate
+ * in fp32 (any order).
  *
- *   type   GGQ_Q8_0 (cols % 32 == 0) or GGQ_Q4_K (cols % 256 == 0)
+ *   type   GGQ_Q8_0 or GGQ_Q4_0 (cols % 32 == 0), GGQ_Q4_K (cols % 256 == 0),
+ *          GGQ_F32 (any cols >= 1)
  *   W      device, rows x row-bytes, row-major, 16-byte aligned
  *   x      device, fp32 [M, cols] row-major, 16-byte aligned
  *   y      device, fp32 [M, rows] row-major, 4-byte aligned; fully overwritten
@@ -210,8 +215,9 @@ typedef struct {
 typedef struct ggq_chain ggq_chain;
 
 /*
- * ggq_chain_create -- validate `nstages` stages (1..65536) of type GGQ_Q8_0 or
- * GGQ_Q4_K for M activation rows (1..4), encode their copy descriptors and
+ * ggq_chain_create -- validate `nstages` stages (1..65536) of type GGQ_Q8_0,
+ * GGQ_Q4_K or GGQ_Q4_0 for M activation rows (1..4; Q4_K and Q4_0 stages need
+ * cols >= 768), encode their copy descriptors and
  * store them in device memory on the current device.  The pointers are bound
  * at creation: the chain reads and writes the same buffers on every run.  The
  * caller owns the returned chain and frees it with ggq_chain_free.  Errors:
@@ -296,8 +302,8 @@ void ggq_chain_free(ggq_chain* chain);
  * no cudaMalloc, cudaFree or other allocating routine.  Shapes that would need
  * another kernel fail instead of falling back.
  *
- * Arguments and result as for ggq_gemv, within these limits: type GGQ_Q8_0 or
- * GGQ_Q4_K, cols a multiple of 256, M in 1..4, x' of one activation row in
+ * Arguments and result as for ggq_gemv, within these limits: type GGQ_Q8_0,
+ * GGQ_Q4_K or GGQ_Q4_0 (the last two with cols >= 768), cols a multiple of 256, M in 1..4, x' of one activation row in
  * shared memory (cols up to about 40000 at M = 1); other shapes fail with
  * GGQ_EINVAL.  Calls may overlap on the GPU and may be captured into graphs.
  */
@@ -330,8 +336,10 @@ int ggq_gemm_prefill(int type, const void* W, int64_t rows, int64_t cols,
 
 /*
  * ggq_dequantize -- out[r*cols + c] = w[r, c] as fp32 (test and inspection
- * aid; the GEMV path never writes decoded weights).  Types GGQ_Q8_0, GGQ_Q4_K.
- * W 16-byte aligned, out 4-byte aligned.  Asynchronous.
+ * aid; the GEMV path never writes decoded weights).  Types GGQ_Q8_0, GGQ_Q4_K,
+ * GGQ_Q4_0 (decoded as in ggq_gemv) and GGQ_F32 (a device-to-device copy);
+ * cols a multiple of the type's block.  W 16-byte aligned, out 4-byte
+ * aligned.  Asynchronous.
  */
 int ggq_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out,
                    void* stream);
@@ -341,7 +349,8 @@ int ggq_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* o
  * Embedding": a token id selects one row of the embedding table; the C++
  * engine post's embed(table, token)).  out[i*cols + k] = w[ids[i], k] as fp32,
  * decoded exactly as ggq_dequantize does, for i < n.
- *   type   GGQ_Q8_0 or GGQ_Q4_K; table device [rows, cols] blocks, 2-byte aligned
+ *   type   GGQ_Q8_0, GGQ_Q4_K, GGQ_Q4_0 (table 2-byte aligned) or GGQ_F32
+ *          (4-byte aligned); table device [rows, cols] in the type's layout
  *   ids    device int32 [n], n in 1..65535; out device fp32 [n, cols], 4-byte aligned
  * An id outside [0, rows) gives a row of zeros, and the next ggq_device_status
  * returns GGQ_EINVAL.  Errors: GGQ_ETYPE, GGQ_EINVAL (NULL, shape, n,

@@ -8,7 +8,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-from . import TYPE_Q4_K, TYPE_Q8_0, stream_id
+from . import TYPE_F32, TYPE_Q4_0, TYPE_Q4_K, TYPE_Q8_0, stream_id
 
 W_SIGMA = 0.02
 X_SIGMA = 1.0
@@ -84,6 +84,13 @@ CFG4_M = (1, 2, 4, 8, 16)
 # prefill: Q4_K 14336 x 4096 times bf16 X [512, 4096]
 CFG5 = Gemv("cfg5.q4_k.weight", TYPE_Q4_K, 14336, 4096)
 CFG5_M = 512
+
+
+# the cfg4 shape in the other weight types the GEMV takes, M = 1 (and 2..8 for Q4_0)
+Q40_GEMV = Gemv("extra.q4_0.weight", TYPE_Q4_0, 14336, 4096)
+F32_GEMV = Gemv("extra.f32.weight", TYPE_F32, 14336, 4096)
+# a Q4_0 width that is not a multiple of 256 (the warp-per-row kernel)
+Q40_ODD_GEMV = Gemv("extra.q4_0_odd.weight", TYPE_Q4_0, 14336, 4128)
 
 
 def weight_bytes(gemvs) -> int:

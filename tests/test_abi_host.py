@@ -163,7 +163,15 @@ def test_compute_entry_points_validate_arguments(ggq):
     assert g(ggq.Q8_0, 8, 4, 64, 16, 16, 1, 0) == -1                 # W misaligned
     assert g(ggq.Q8_0, 16, 0, 64, 16, 16, 1, 0) == -1                # rows = 0
     assert g(ggq.Q8_0, 16, 4, 64, 8, 16, 1, 0) == -1                 # x misaligned
-    assert g(ggq.F32, 16, 4, 64, 16, 16, 1, 0) == -2                 # type
+    assert g(ggq.F16, 16, 4, 64, 16, 16, 1, 0) == -2                 # type
+    assert g(ggq.Q6_K, 16, 4, 256, 16, 16, 1, 0) == -2
+    assert g(ggq.Q4_0, 16, 4, 48, 16, 16, 1, 0) == -1                # Q4_0: cols % 32
+    assert g(ggq.Q4_0, 16, 4, 64, 16, 16, 17, 0) == -1
+    assert g(ggq.F32, 16, 4, 0, 16, 16, 1, 0) == -1                  # F32: cols >= 1
+    assert g(ggq.F32, 8, 4, 5, 16, 16, 1, 0) == -1                   # F32: W misaligned
+    n = ggq.ggq_gemv_noalloc
+    assert n(ggq.Q4_0, 16, 4, 512, 16, 16, 1, 0) == -1               # Q4_0 stream kernel: cols >= 768
+    assert n(ggq.F32, 16, 4, 1024, 16, 16, 1, 0) == -2               # F32 has no allocation-free kernel
     p = ggq.ggq_gemm_prefill
     assert p(ggq.F16, 16, 128, 256, 16, 16, 128, 0) == -2
     assert p(ggq.Q8_0, 16, 100, 256, 16, 16, 128, 0) == -1           # Q8_0 too: rows % 128
@@ -174,6 +182,7 @@ def test_compute_entry_points_validate_arguments(ggq):
     d = ggq.ggq_dequantize
     assert d(ggq.Q4_K, 16, 2, 100, 16, 0) == -1
     assert d(ggq.F16, 16, 2, 256, 16, 0) == -2
+    assert d(ggq.Q4_0, 16, 2, 40, 16, 0) == -1                       # cols % 32
     assert g(ggq.Q8_0, 16, 4, 64, 16, 16, 17, 0) == -1
     assert "M 17 outside 1..16" in ggq.lib.ggq_last_error().decode()
 
@@ -192,6 +201,8 @@ def test_chain_create_validates_stages(ggq):
     assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([16], [0], 256, 16, [16])])[0] == -1          # rows = 0
     assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([16], [64], 320, 16, [16])])[0] == -1         # cols % 256
     assert ggq.ggq_chain_create(ggq.Q4_K, 1, [([16] * 5, [64] * 5, 256, 16, [16] * 5)])[0] == -1   # n = 5
+    assert ggq.ggq_chain_create(ggq.Q4_0, 1, [([16], [64], 512, 16, [16])])[0] == -1         # Q4_0: cols >= 768
+    assert ggq.ggq_chain_create(ggq.Q4_0, 1, [([16], [64], 800, 16, [16])])[0] == -1         # Q4_0: cols % 256
     assert ggq.ggq_chain_run(0, 0) == -1
     ggq.ggq_chain_free(0)
 
@@ -220,7 +231,9 @@ def test_chain_create_ops_validates_fused_steps(ggq):
 
 def test_embed_validates_arguments(ggq):
     """ggq_embed rejects bad arguments before any launch."""
-    assert ggq.ggq_embed(ggq.F32, 16, 4, 64, 16, 1, 16, 0) == -2          # type
+    assert ggq.ggq_embed(ggq.F16, 16, 4, 64, 16, 1, 16, 0) == -2          # type
+    assert ggq.ggq_embed(ggq.Q4_0, 16, 4, 40, 16, 1, 16, 0) == -1         # Q4_0: cols % 32
+    assert ggq.ggq_embed(ggq.F32, 18, 4, 5, 16, 1, 16, 0) == -1           # F32 table: 4-byte aligned
     assert ggq.ggq_embed(ggq.Q8_0, 0, 4, 64, 16, 1, 16, 0) == -1          # NULL table
     assert ggq.ggq_embed(ggq.Q8_0, 16, 4, 64, 0, 1, 16, 0) == -1          # NULL ids
     assert ggq.ggq_embed(ggq.Q8_0, 16, 4, 63, 16, 1, 16, 0) == -1         # cols % 32

@@ -89,7 +89,7 @@ def _layer(prefix, hidden, kv, ffn, src):
     ]
 
 
-@pytest.mark.parametrize("qtype,M", [(12, 1), (12, 2), (12, 3), (8, 1), (8, 4)])
+@pytest.mark.parametrize("qtype,M", [(12, 1), (12, 2), (12, 3), (8, 1), (8, 4), (2, 1), (2, 3)])
 def test_chain_two_layers(env, qtype, M):
     """Two small layers: every stage after the first reads the previous stage's y."""
     stages = _layer("a.", 1280, 256, 2816, "x0") + _layer("b.", 1280, 256, 2816, "a.down")
@@ -240,7 +240,7 @@ def _check_fused(qtype, plan):
     return worst
 
 
-@pytest.mark.parametrize("qtype,M", [(12, 1), (12, 2), (12, 3), (8, 1), (8, 4)])
+@pytest.mark.parametrize("qtype,M", [(12, 1), (12, 2), (12, 3), (8, 1), (8, 4), (2, 1), (2, 2), (2, 4)])
 def test_chain_fused_layers(env, qtype, M):
     """Two fused layers (RMSNorm before q/k/v and gate/up, SiLU(gate)*up into down,
     residual adds after o and down) against the oracle's layer steps + GEMV,

@@ -27,7 +27,7 @@ def env():
 
 
 @pytest.mark.parametrize("qtype,rows,cols,M", [(12, 4096, 4096, 1), (12, 1000, 11008, 2), (8, 2048, 2048, 1),
-                                               (8, 777, 4096, 3)])
+                                               (8, 777, 4096, 3), (2, 3000, 4096, 1), (2, 500, 1024, 4)])
 def test_noalloc_matches_gemv_twice(env, qtype, rows, cols, M):
     torch, ggq = env
     W = synth.weight_rows(qtype, 70 + qtype, rows, cols)

@@ -5,7 +5,7 @@ TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and
 The CUDA library (``gguf_block_quantized_q8_gb300``) never imports it and
 shares no code with it; the two meet only on input bytes from ``synth``.
 
-* ``ggq_oracle.c`` -- fp16 decode from IEEE-754, Q8_0 / Q4_K / Q4_0 block decode to
+* ``ggq_oracle.c`` -- fp16 decode from IEEE-754, Q8_0 / Q4_K / Q4_0 / Q6_K block decode to
   fp32, GEMV / GEMM with every product and sum in double (see its header for
   the passages followed);
 * ``gguf_reader.py`` -- a plain byte walk of GGUF v3;
@@ -20,7 +20,11 @@ unpinned (the path and the oracle decode the same bytes either way).  Q4_0
 decode is pinned the same way and, beyond that, against the Q8_0 decode: a
 Q4_0 block and a Q8_0 block holding the same scale and the same integers
 decode to the same 32 values.  Which nibble holds which weight, and the offset
-of 8, are a reading of the format (real Q4_0 files), not on the pages.
+of 8, are a reading of the format (real Q4_0 files), not on the pages.  Q6_K:
+only the size (210 bytes per 256 weights) and the k-quant idea are on the pages;
+its byte layout is a reading (real Q6_K files), pinned by hand-built
+super-blocks and against the Q8_0 decode (a Q6_K super-block with unit
+sub-block scales equals eight Q8_0 blocks of the same scale and integers).
 """
 from __future__ import annotations
 
@@ -39,7 +43,7 @@ _LIB = os.path.join(_HERE, "libggq_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, F16, Q4_0, Q8_0, Q4_K = 0, 1, 2, 8, 12
+F32, F16, Q4_0, Q8_0, Q4_K, Q6_K = 0, 1, 2, 8, 12, 14
 
 
 def compile_oracle(src: str, out: str) -> str:
@@ -76,6 +80,7 @@ class Oracle:
         lib.orc_decode_q8_0_block.argtypes = [vp, vp]
         lib.orc_decode_q4_k_block.argtypes = [vp, vp]
         lib.orc_decode_q4_0_block.argtypes = [vp, vp]
+        lib.orc_decode_q6_k_block.argtypes = [vp, vp]
         lib.orc_row_bytes.argtypes = [ctypes.c_int, i64]
         lib.orc_row_bytes.restype = i64
         lib.orc_dequantize.argtypes = [ctypes.c_int, vp, i64, i64, vp]
@@ -147,6 +152,13 @@ class Oracle:
         self.lib.orc_decode_q4_k_block(b.ctypes.data, out.ctypes.data)
         return out
 
+    def decode_q6_k_block(self, blk: bytes) -> np.ndarray:
+        b = np.frombuffer(bytes(blk), dtype=np.uint8)
+        assert b.size == 210
+        out = np.empty(256, dtype=np.float32)
+        self.lib.orc_decode_q6_k_block(b.ctypes.data, out.ctypes.data)
+        return out
+
     def decode_q4_0_block(self, blk: bytes) -> np.ndarray:
         b = np.frombuffer(bytes(blk), dtype=np.uint8)
         assert b.size == 18
@@ -202,6 +214,10 @@ def decode_q4_k_block(blk):
 
 def decode_q4_0_block(blk):
     return default().decode_q4_0_block(blk)
+
+
+def decode_q6_k_block(blk):
+    return default().decode_q6_k_block(blk)
 
 
 def tolerance_ok(y_dev: np.ndarray, y_ref: np.ndarray, abs_ref: np.ndarray,

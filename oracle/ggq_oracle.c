@@ -34,9 +34,22 @@
  *      weight l (l < 16) is the low nibble of qs[l], weight 16+l its high
  *      nibble, and a code u in 0..15 stands for the integer u - 8, so
  *      w = d * (u - 8).
- *   5. F32 rows -- "GGUF: The File Format...", the practice script's tensor
+ *   5. Q6_K super-block decode -- "GGUF: The File Format...", "How a Q8_0
+ *      block is stored" (k-quant paragraph: 256-weight super-blocks split into
+ *      sub-blocks with their own scales under one 16-bit scale; the bits/weight
+ *      loop: 210 bytes per 256 weights) and "Understanding quantization names
+ *      like Q4_K_M" (Q4_K_M files hold some tensors as Q6_K).  The byte layout
+ *      is not printed on the pages; the reading used here (the layout of real
+ *      Q6_K files) is: bytes 0-127 ql (low 4 bits), 128-191 qh (high 2 bits),
+ *      192-207 sixteen signed 8-bit sub-block scales sc[0..15] (one per 16
+ *      weights), 208-209 d (fp16).  Weight k = 128h + 32g + l (h = 0..1,
+ *      g = 0..3, l = 0..31) has the 6-bit code
+ *        u = ((ql[64h + 32(g & 1) + l] >> 4(g >> 1)) & 15)
+ *            | (((qh[32h + l] >> 2g) & 3) << 4)
+ *      and w = d * sc[8h + 2g + l/16] * (u - 32).
+ *   6. F32 rows -- "GGUF: The File Format...", the practice script's tensor
  *      payload: little-endian fp32 values, row after row.
- *   6. matvec -- culpeo.ws C++ engine blog, kernel list:
+ *   7. matvec -- culpeo.ws C++ engine blog, kernel list:
  *      the matrix-vector kernel (an r x c weight and a c-vector give an
  *      r-vector); "GGUF Inferencer in R" section 5.2.1 (the normalized input
  *      times the transposed weight): y[r] = sum_c w[r,c] * x[c].  For M activation
@@ -44,7 +57,8 @@
  *      in double, columns in order.
  *
  * Decode produces fp32 exactly as the format defines it: the Q8_0 and Q4_0
- * products d*q and the Q4_K products d*sc*q and dmin*m are exact in fp32, so the only
+ * products d*q, the Q6_K product d*sc*(u-32) (11 + 7 + 6 significant bits:
+ * exact in fp32) and the Q4_K products d*sc*q and dmin*m are exact in fp32, so the only
  * rounding is the final Q4_K subtraction (done here in double and rounded
  * once more to float, which gives the correctly rounded fp32 difference of two
  * fp32 values because 53 >= 2*24+2).
@@ -59,7 +73,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_Q4_0 = 2, ORC_Q8_0 = 8, ORC_Q4_K = 12 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_Q4_0 = 2, ORC_Q8_0 = 8, ORC_Q4_K = 12, ORC_Q6_K = 14 };
 
 /* IEEE-754 binary16 value, from the definition */
 double orc_fp16_value(uint16_t h) {
@@ -138,6 +152,25 @@ void orc_decode_q4_k_block(const uint8_t* blk, float* out) {
     }
 }
 
+/* one Q6_K super-block (210 bytes) -> 256 floats */
+void orc_decode_q6_k_block(const uint8_t* blk, float* out) {
+    const uint8_t* ql = blk;
+    const uint8_t* qh = blk + 128;
+    const int8_t* sc = (const int8_t*)(blk + 192);
+    double d = orc_fp16_value(rd16(blk + 208));
+    for (int h = 0; h < 2; ++h) {
+        for (int g = 0; g < 4; ++g) {
+            for (int l = 0; l < 32; ++l) {
+                int lo = (ql[64 * h + 32 * (g & 1) + l] >> (4 * (g >> 1))) & 15;
+                int hi = (qh[32 * h + l] >> (2 * g)) & 3;
+                int u = lo | (hi << 4);
+                int scale = sc[8 * h + 2 * g + l / 16];
+                out[128 * h + 32 * g + l] = (float)(d * (double)scale * (double)(u - 32));
+            }
+        }
+    }
+}
+
 /* bytes of one row of `cols` weights; 0 if the type or shape is not supported */
 int64_t orc_row_bytes(int type, int64_t cols) {
     switch (type) {
@@ -146,6 +179,7 @@ int64_t orc_row_bytes(int type, int64_t cols) {
     case ORC_Q8_0: return cols % 32 ? 0 : cols / 32 * 34;
     case ORC_Q4_0: return cols % 32 ? 0 : cols / 32 * 18;
     case ORC_Q4_K: return cols % 256 ? 0 : cols / 256 * 144;
+    case ORC_Q6_K: return cols % 256 ? 0 : cols / 256 * 210;
     default: return 0;
     }
 }
@@ -167,6 +201,9 @@ static int decode_row(int type, const uint8_t* row, int64_t cols, float* out) {
         return 0;
     case ORC_Q4_0:
         for (int64_t b = 0; b < cols / 32; ++b) orc_decode_q4_0_block(row + 18 * b, out + 32 * b);
+        return 0;
+    case ORC_Q6_K:
+        for (int64_t b = 0; b < cols / 256; ++b) orc_decode_q6_k_block(row + 210 * b, out + 256 * b);
         return 0;
     default:
         return -1;

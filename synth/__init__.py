@@ -4,10 +4,10 @@ Holds input generation only (no decode, no dot products):
 
 * ``normal_f32`` / ``normal_bf16`` -- counter-based N(0, sigma) draws;
 * ``weight_rows`` -- rows of a seeded weight tensor, encoded to Q8_0 (34 B /
-  32 weights), Q4_K (144 B / 256 weights) or Q4_0 (18 B / 32 weights) bytes,
-  or stored as F32;
-* ``quantize_q8_0`` / ``quantize_q4_k`` / ``quantize_q4_0`` -- the same
-  encoders on given floats;
+  32 weights), Q4_K (144 B / 256 weights), Q4_0 (18 B / 32 weights) or Q6_K
+  (210 B / 256 weights) bytes, or stored as F32;
+* ``quantize_q8_0`` / ``quantize_q4_k`` / ``quantize_q4_0`` /
+  ``quantize_q6_k`` -- the same encoders on given floats;
 * ``write_gguf`` -- a GGUF v3 writer (header, typed KVs, tensor-info table,
   32-byte padding, 32-byte-aligned payloads), laid out as in "GGUF: The File
   Format..." (section "What is stored inside a GGUF file") and the byte
@@ -61,6 +61,8 @@ def _load():
         lib.synth_quantize_q8_0.argtypes = [vp, i64, vp]
         lib.synth_quantize_q4_k.argtypes = [vp, i64, vp]
         lib.synth_quantize_q4_0.argtypes = [vp, i64, vp]
+        lib.synth_quantize_q6_k.argtypes = [vp, i64, vp]
+        lib.synth_q6_k_rows.argtypes = [u64, u64, i64, i64, i64, f32, vp]
         lib.synth_q8_0_rows.argtypes = [u64, u64, i64, i64, i64, f32, vp]
         lib.synth_q4_k_rows.argtypes = [u64, u64, i64, i64, i64, f32, vp]
         lib.synth_q4_0_rows.argtypes = [u64, u64, i64, i64, i64, f32, vp]
@@ -92,6 +94,7 @@ def _ptr(a: np.ndarray) -> int:
 QK8_0, Q8_0_BYTES = 32, 34
 QK_K, Q4_K_BYTES = 256, 144
 QK4_0, Q4_0_BYTES = 32, 18
+Q6_K_BYTES = 210
 TYPE_F32, TYPE_F16, TYPE_Q4_0, TYPE_Q8_0, TYPE_Q4_K, TYPE_Q6_K = 0, 1, 2, 8, 12, 14
 
 
@@ -102,6 +105,8 @@ def row_bytes(qtype: int, cols: int) -> int:
         return cols // QK_K * Q4_K_BYTES
     if qtype == TYPE_Q4_0:
         return cols // QK4_0 * Q4_0_BYTES
+    if qtype == TYPE_Q6_K:
+        return cols // QK_K * Q6_K_BYTES
     if qtype == TYPE_F32:
         return cols * 4
     raise ValueError(f"unsupported type {qtype}")
@@ -146,6 +151,14 @@ def quantize_q4_0(w: np.ndarray) -> np.ndarray:
     return out
 
 
+def quantize_q6_k(w: np.ndarray) -> np.ndarray:
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    assert w.size % QK_K == 0
+    out = np.empty(w.size // QK_K * Q6_K_BYTES, dtype=np.uint8)
+    _load().synth_quantize_q6_k(_ptr(w), w.size, _ptr(out))
+    return out
+
+
 def weight_rows(qtype: int, stream: int, rows: int, cols: int, row0: int = 0,
                 sigma: float = 0.02, seed: int = BASE_SEED,
                 out: np.ndarray | None = None) -> np.ndarray:
@@ -161,6 +174,8 @@ def weight_rows(qtype: int, stream: int, rows: int, cols: int, row0: int = 0,
         lib.synth_q4_k_rows(seed, stream, row0, rows, cols, sigma, _ptr(out))
     elif qtype == TYPE_Q4_0:
         lib.synth_q4_0_rows(seed, stream, row0, rows, cols, sigma, _ptr(out))
+    elif qtype == TYPE_Q6_K:
+        lib.synth_q6_k_rows(seed, stream, row0, rows, cols, sigma, _ptr(out))
     elif qtype == TYPE_F32:
         lib.synth_f32_rows(seed, stream, row0, rows, cols, sigma, _ptr(out))
     else:

@@ -20,6 +20,11 @@
  *     q = round-half-even(w / d) clipped to -8..7, stored as the code q + 8, the
  *     code of weight l (l < 16) in the low nibble of byte l and that of weight
  *     16 + l in its high nibble (the byte layout of real Q4_0 files);
+ *   - a round-to-nearest Q6_K super-block encoder (256 weights, 16 sub-blocks of
+ *     16 with a signed 8-bit scale each under an fp16 d; 6-bit codes q + 32 split
+ *     into 4 low bits (ql) and 2 high bits (qh)).  The pages give only the size
+ *     (210 B) and the k-quant idea; the byte layout is the de-facto one of real
+ *     Q6_K files;
  *   - fp32 -> fp16 / bf16 round-to-nearest-even conversions (bit manipulation).
  *
  * Determinism across machines: the generator uses only IEEE basic operations
@@ -226,6 +231,37 @@ static void encode_q4_k_block(const float* w, uint8_t* out) {
             qs[32 * c + l] = (uint8_t)(q[64 * c + l] | (q[64 * c + 32 + l] << 4));
 }
 
+/* Q6_K: 256 weights -> 210 bytes, round-to-nearest, no search.  Sub-block j
+ * (weights 16j .. 16j+15) gets the scale amax_j / 31; d = fp16(max scale / 127),
+ * sc_j = round(scale_j / d) in 0..127, q = round(w / (d * sc_j)) in -32..31. */
+static void encode_q6_k_block(const float* w, uint8_t* out) {
+    float s[16], smax = 0.0f;
+    for (int j = 0; j < 16; ++j) {
+        float amax = 0.0f;
+        for (int i = 0; i < 16; ++i) { float a = fabsf(w[16 * j + i]); if (a > amax) amax = a; }
+        s[j] = amax / 31.0f;
+        if (s[j] > smax) smax = s[j];
+    }
+    uint16_t dh = synth_f32_to_f16(smax / 127.0f);
+    float d = f16_to_f32_enc(dh);
+    int sc[16];
+    for (int j = 0; j < 16; ++j) sc[j] = (d == 0.0f) ? 0 : (int)clampf(rintf(s[j] / d), 0.0f, 127.0f);
+    uint8_t* ql = out;
+    uint8_t* qh = out + 128;
+    memset(out, 0, 192);
+    for (int k = 0; k < 256; ++k) {
+        float a = d * (float)sc[k / 16];
+        int q = (a == 0.0f) ? 0 : (int)clampf(rintf(w[k] / a), -32.0f, 31.0f);
+        int u = q + 32;
+        int h = k / 128, g = (k % 128) / 32, l = k % 32;
+        ql[64 * h + 32 * (g & 1) + l] |= (uint8_t)((u & 15) << (4 * (g >> 1)));
+        qh[32 * h + l] |= (uint8_t)((u >> 4) << (2 * g));
+    }
+    for (int j = 0; j < 16; ++j) out[192 + j] = (uint8_t)(int8_t)sc[j];
+    out[208] = (uint8_t)(dh & 0xff);
+    out[209] = (uint8_t)(dh >> 8);
+}
+
 /* ------------------------------------------------------------- API ---- */
 
 static int g_threads = 0;
@@ -264,6 +300,11 @@ void synth_quantize_q4_0(const float* w, int64_t n, uint8_t* out) {
     for (int64_t b = 0; b < nb; ++b) encode_q4_0_block(w + 32 * b, out + 18 * b);
 }
 
+void synth_quantize_q6_k(const float* w, int64_t n, uint8_t* out) {
+    int64_t nb = n / 256;
+    for (int64_t b = 0; b < nb; ++b) encode_q6_k_block(w + 256 * b, out + 210 * b);
+}
+
 void synth_quantize_q4_k(const float* w, int64_t n, uint8_t* out) {
     int64_t nb = n / 256;
     for (int64_t b = 0; b < nb; ++b) encode_q4_k_block(w + 256 * b, out + 144 * b);
@@ -299,6 +340,22 @@ void synth_q4_0_rows(uint64_t seed, uint64_t stream, int64_t row0, int64_t nrows
             for (int i = 0; i < 32; ++i)
                 w[i] = (float)((double)sigma * normal_at(key, base + (uint64_t)(32 * b + i)));
             encode_q4_0_block(w, out + r * rb + 18 * b);
+        }
+    }
+}
+
+void synth_q6_k_rows(uint64_t seed, uint64_t stream, int64_t row0, int64_t nrows,
+                     int64_t cols, float sigma, uint8_t* out) {
+    uint64_t key = stream_key(seed, stream);
+    int64_t rb = cols / 256 * 210;
+    #pragma omp parallel for schedule(static) num_threads(nthreads()) if (nrows > 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        float w[256];
+        uint64_t base = (uint64_t)(row0 + r) * (uint64_t)cols;
+        for (int64_t b = 0; b < cols / 256; ++b) {
+            for (int i = 0; i < 256; ++i)
+                w[i] = (float)((double)sigma * normal_at(key, base + (uint64_t)(256 * b + i)));
+            encode_q6_k_block(w, out + r * rb + 210 * b);
         }
     }
 }

@@ -12,7 +12,7 @@ import struct
 
 import numpy as np
 
-F32, F16, Q4_0, Q8_0, Q4_K = 0, 1, 2, 8, 12
+F32, F16, Q4_0, Q8_0, Q4_K, Q6_K = 0, 1, 2, 8, 12, 14
 
 
 # ------------------------------------------------------------ fp16 / bf16 ----
@@ -117,6 +117,76 @@ def q4_0_block(d_bits: int, codes) -> bytes:
     """32 codes in weight order -> 18 bytes (reading: weight l low nibble of byte l)."""
     assert len(codes) == 32
     return struct.pack("<H", d_bits) + bytes(int(codes[l]) | (int(codes[16 + l]) << 4) for l in range(16))
+
+
+# ------------------------------------------------------------------- Q6_K ----
+
+def q6k_raw(ql, qh, sc, d_bits) -> bytes:
+    assert len(ql) == 128 and len(qh) == 64 and len(sc) == 16
+    return bytes(ql) + bytes(qh) + bytes(v & 0xFF for v in sc) + struct.pack("<H", d_bits)
+
+
+def q6k_block(d_bits: int, sc, codes) -> bytes:
+    """256 six-bit codes in weight order + 16 signed scales -> 210 bytes, for the
+    reading's bit placement: weight 128h + 32g + l keeps its low 4 bits in ql byte
+    64h + 32(g % 2) + l (low nibble for g < 2, high nibble for g >= 2) and its high
+    2 bits in qh byte 32h + l at bit 2g."""
+    ql, qh = [0] * 128, [0] * 64
+    for k, u in enumerate(codes):
+        h, g, l = k // 128, (k % 128) // 32, k % 32
+        ql[64 * h + 32 * (g % 2) + l] |= (int(u) & 15) << (4 * (g // 2))
+        qh[32 * h + l] |= (int(u) >> 4) << (2 * g)
+    return q6k_raw(ql, qh, sc, d_bits)
+
+
+def check_q6_k_blocks(orc):
+    ones = [1] * 16
+    # all codes 0: every weight is (0 - 32) * d * 1
+    got = orc.decode_q6_k_block(q6k_raw([0] * 128, [0] * 64, ones, 0x3C00))
+    assert got.tolist() == [-32.0] * 256
+    # every 2-bit high field 1 (qh bytes 0x55), low bits 0: codes 16 -> -16 * sc;
+    # sub-block scales in natural order: weight k uses scale k // 16, signed
+    sc = [1, -1, 2, -2, 3, -3, 4, -4, 5, -5, 6, -6, 7, -7, 127, -128]
+    got = orc.decode_q6_k_block(q6k_raw([0] * 128, [0x55] * 64, sc, 0x3C00))
+    assert got.tolist() == [-16.0 * sc[k // 16] for k in range(256)]
+    # d = 0.5 (0x3800), all bits set: codes 63 -> 31 * 0.5 * sc
+    got = orc.decode_q6_k_block(q6k_raw([0xFF] * 128, [0xFF] * 64, sc, 0x3800))
+    assert got.tolist() == [15.5 * sc[k // 16] for k in range(256)]
+    # one set nibble of ql byte b: its low nibble is weight 128(b // 64) + b % 64,
+    # its high nibble the weight 64 after it; every other weight stays -32
+    for b in (0, 1, 31, 32, 63, 64, 100, 127):
+        ql = [0] * 128
+        ql[b] = 0x0F
+        got = orc.decode_q6_k_block(q6k_raw(ql, [0] * 64, ones, 0x3C00))
+        want = [-32.0] * 256
+        want[128 * (b // 64) + b % 64] = -17.0
+        assert got.tolist() == want, b
+        ql[b] = 0xF0
+        got = orc.decode_q6_k_block(q6k_raw(ql, [0] * 64, ones, 0x3C00))
+        want = [-32.0] * 256
+        want[128 * (b // 64) + b % 64 + 64] = -17.0
+        assert got.tolist() == want, b
+    # one 2-bit field g of qh byte b is weight 128(b // 32) + 32g + b % 32
+    for b in (0, 5, 31, 32, 63):
+        for g in range(4):
+            qh = [0] * 64
+            qh[b] = 3 << (2 * g)
+            got = orc.decode_q6_k_block(q6k_raw([0] * 128, qh, ones, 0x3C00))
+            want = [-32.0] * 256
+            want[128 * (b // 32) + 32 * g + b % 32] = 16.0
+            assert got.tolist() == want, (b, g)
+    # unit scales: a Q6_K super-block equals eight Q8_0 blocks with the same d
+    # and the integers u - 32 (Q8_0 decode is pinned to the pages' own values)
+    rng = np.random.default_rng(6)
+    for d_bits in (0x3C00, 0x2E66, 0x8123, 0x0001):
+        codes = rng.integers(0, 64, 256)
+        q6 = orc.decode_q6_k_block(q6k_block(d_bits, ones, codes))
+        q8 = np.concatenate([orc.decode_q8_0_block(q8_block(d_bits, [int(u) - 32 for u in codes[32 * i:32 * i + 32]]))
+                             for i in range(8)])
+        assert np.array_equal(q6, q8), hex(d_bits)
+    # block byte size from bits/weight: 6.5625 bits * 256 = 210 bytes
+    assert orc.row_bytes(Q6_K, 256) == 210 and orc.row_bytes(Q6_K, 4096) == 16 * 210
+    assert orc.row_bytes(Q6_K, 288) == 0
 
 
 # ------------------------------------------------------------------- Q4_K ----
@@ -250,6 +320,15 @@ def check_one_hot(orc):
         y, _ = orc.gemv(Q4_0, np.frombuffer(W, np.uint8), rows, 64, x)
         b, i = divmod(c, 32)
         assert y[0].tolist() == [float((i + 3 * r + 5 * b) % 16 - 8) for r in range(rows)], c
+    # Q6_K, cols 512: super-block (r, b) has d = 1, sc_j = j - 8 + r, code (k + 3r + b) % 64
+    W = b"".join(q6k_block(0x3C00, [j - 8 + r for j in range(16)], [(k + 3 * r + b) % 64 for k in range(256)])
+                 for r in range(rows) for b in range(2))
+    for c in (0, 15, 16, 100, 255, 256, 300, 511):
+        x = np.zeros(512, dtype=np.float32)
+        x[c] = 1.0
+        y, _ = orc.gemv(Q6_K, np.frombuffer(W, np.uint8), rows, 512, x)
+        b, k = divmod(c, 256)
+        assert y[0].tolist() == [float((k // 16 - 8 + r) * ((k + 3 * r + b) % 64 - 32)) for r in range(rows)], c
     # F32, cols 5 (no blocks): element (r, c) = 10r + c
     Wf = np.array([[10.0 * r + c for c in range(5)] for r in range(rows)], dtype=np.float32)
     for c in range(5):
@@ -290,6 +369,15 @@ def check_integer_exact(orc):
     y, ay = orc.gemv(Q4_0, np.frombuffer(W, np.uint8), rows, cols, x.astype(np.float32))
     assert np.array_equal(y, (x @ (u - 8).T).astype(np.float64))
     assert np.array_equal(ay, (np.abs(x) @ np.abs(u - 8).T).astype(np.float64))
+    # Q6_K with d = 1: w = sc[k // 16] * (code - 32)
+    sc = rng.integers(-128, 128, size=(rows, cols // 256, 16))
+    u = rng.integers(0, 64, size=(rows, cols))
+    W = b"".join(q6k_block(0x3C00, list(sc[r, b]), list(u[r, 256 * b:256 * b + 256]))
+                 for r in range(rows) for b in range(cols // 256))
+    w = sc[:, np.arange(cols) // 256, (np.arange(cols) % 256) // 16] * (u - 32)
+    y, ay = orc.gemv(Q6_K, np.frombuffer(W, np.uint8), rows, cols, x.astype(np.float32))
+    assert np.array_equal(y, (x @ w.T).astype(np.float64))
+    assert np.array_equal(ay, (np.abs(x) @ np.abs(w).T).astype(np.float64))
     # F32 integer matrix
     wi = rng.integers(-1000, 1001, size=(rows, cols))
     y, _ = orc.gemv(F32, wi.astype(np.float32).reshape(-1).view(np.uint8), rows, cols, x.astype(np.float32))
@@ -346,6 +434,19 @@ def check_brute_force(orc):
         assert np.allclose(ay, np.abs(x.astype(np.float64)) @ np.abs(w).T, rtol=1e-12)
         assert np.array_equal(orc.dequantize(Q4_0, np.frombuffer(W, np.uint8), rows, cols),
                               w.astype(np.float32))
+        # Q6_K with random fp16 d and signed scales, cols 512
+        cols = 512
+        d = rng.uniform(1e-5, 1e-4, size=(rows, 2)).astype(np.float16)
+        sc = rng.integers(-128, 128, size=(rows, 2, 16))
+        u = rng.integers(0, 64, size=(rows, cols))
+        W = b"".join(q6k_block(int(d[r, b].view(np.uint16)), list(sc[r, b]), list(u[r, 256 * b:256 * b + 256]))
+                     for r in range(rows) for b in range(2))
+        bi, j = np.arange(cols) // 256, (np.arange(cols) % 256) // 16
+        w = d.astype(np.float64)[:, bi] * sc[:, bi, j] * (u - 32)
+        x = rng.standard_normal((2, cols)).astype(np.float32)
+        y, _ = orc.gemv(Q6_K, np.frombuffer(W, np.uint8), rows, cols, x)
+        assert np.allclose(y, x.astype(np.float64) @ w.T, rtol=1e-12, atol=1e-15)
+        assert np.array_equal(orc.dequantize(Q6_K, np.frombuffer(W, np.uint8), rows, cols), w.astype(np.float32))
         # F32, cols 7
         wf = rng.standard_normal((rows, 7)).astype(np.float32)
         x = rng.standard_normal((2, 7)).astype(np.float32)
@@ -369,5 +470,5 @@ def check_gemm_bf16(orc):
     assert np.array_equal(Y, y2)
 
 
-ALL_CHECKS = [check_fp16, check_bf16, check_q8_0_blocks, check_q4_0_blocks, check_q4_k_blocks,
+ALL_CHECKS = [check_fp16, check_bf16, check_q8_0_blocks, check_q4_0_blocks, check_q6_k_blocks, check_q4_k_blocks,
               check_one_hot, check_integer_exact, check_brute_force, check_gemm_bf16]

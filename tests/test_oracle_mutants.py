@@ -30,6 +30,15 @@ MUTANTS = {
     "q4_0_nibbles_at": ("const uint8_t* qs = blk + 2;", "const uint8_t* qs = blk + 1;"),
     "q4_0_block_stride": ("orc_decode_q4_0_block(row + 18 * b", "orc_decode_q4_0_block(row + 16 * b"),
     "q4_0_row_bytes": ("cols / 32 * 18;", "cols / 32 * 16;"),
+    "q6k_qh_shift": ("(qh[32 * h + l] >> (2 * g)) & 3", "(qh[32 * h + l] >> g) & 3"),
+    "q6k_ql_half": ("ql[64 * h + 32 * (g & 1) + l]", "ql[64 * h + 32 * (g >> 1) + l]"),
+    "q6k_nibble_shift": (">> (4 * (g >> 1))) & 15", ">> (4 * (g & 1))) & 15"),
+    "q6k_offset": ("(double)(u - 32)", "(double)(u - 31)"),
+    "q6k_unsigned_scales": ("const int8_t* sc = (const int8_t*)(blk + 192);", "const uint8_t* sc = blk + 192;"),
+    "q6k_scale_index": ("sc[8 * h + 2 * g + l / 16]", "sc[8 * h + g + l / 16]"),
+    "q6k_d_at": ("rd16(blk + 208)", "rd16(blk + 206)"),
+    "q6k_high_bits_at": ("const uint8_t* qh = blk + 128;", "const uint8_t* qh = blk + 127;"),
+    "q6k_row_bytes": ("cols / 256 * 210;", "cols / 256 * 208;"),
     "f32_row_stride": ("case ORC_F32: return 4 * cols;", "case ORC_F32: return 4 * cols + 4;"),
     "fp16_bias": ("expo - 25);", "expo - 24);"),
     "fp16_subnormal_scale": ("ldexp((double)frac, -24);", "ldexp((double)frac, -25);"),

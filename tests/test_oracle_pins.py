@@ -202,6 +202,19 @@ def test_synth_q4_0_roundtrip_error():
     assert np.all(np.abs(back - w.reshape(64, 32)) <= d[:, None] / 2 * (1 + 2 ** -10))
 
 
+def test_synth_q6_k_roundtrip_error():
+    """Q6_K of N(0, 0.02): every decoded weight within half a step (d * sc / 2)
+    of its source; scales are non-negative and d = fp16(max scale / 127)."""
+    w = synth.normal_f32(256 * 32, 5, sigma=0.02)
+    packed = synth.quantize_q6_k(w).reshape(32, 210)
+    back = oracle.dequantize(14, packed.reshape(-1), 32, 256)
+    d = packed[:, 208:210].copy().view(np.float16).astype(np.float64).reshape(32)
+    sc = packed[:, 192:208].view(np.int8).astype(np.float64)
+    assert (sc >= 0).all() and (sc.max(axis=1) >= 126).all()
+    step = d[:, None] * np.repeat(sc, 16, axis=1)
+    assert np.all(np.abs(back - w.reshape(32, 256)) <= step / 2 * (1 + 2 ** -10) + 1e-12)
+
+
 def test_synth_q4_k_roundtrip_error():
     """RTN Q4_K of N(0, 0.02): decoded weights stay within one step of the grid."""
     w = synth.normal_f32(256 * 64, 3, sigma=0.02)

@@ -456,10 +456,12 @@ def extras(torch, ggq, synth, stream):
     del W, W8, X, Y
 
     # the cfg4 shape as Q4_0 (33 MB: 6 copies cycled, 198 MB) and as F32 (235 MB, one copy);
-    # Q4_0 14336x4128 runs on the warp-per-row kernel
+    # Q4_0 14336x4128 runs on the warp-per-row kernel; Q6_K (48.2 MB: 4 copies) too
     for name, g, copies, Ms in [("q4_0_14336x4096", WL.Q40_GEMV, 6, (1, 2, 4, 8, 16)),
                                 ("q4_0_14336x4128_warp_per_row", WL.Q40_ODD_GEMV, 6, (1, 8)),
-                                ("f32_14336x4096", WL.F32_GEMV, 1, (1,))]:
+                                ("f32_14336x4096", WL.F32_GEMV, 1, (1,)),
+                                ("q6_k_14336x4096", WL.Q6K_GEMV, 4, (1, 2, 8)),
+                                ("q6_k_4096x14336", WL.Q6K_DOWN_GEMV, 4, (1,))]:
         W0 = torch.from_numpy(synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)).cuda()
         Ws = [W0] + [W0.clone() for _ in range(copies - 1)]
         nb = g.rows * synth.row_bytes(g.qtype, g.cols)

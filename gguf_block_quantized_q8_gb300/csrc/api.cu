@@ -31,7 +31,8 @@ int64_t block_of(int type) {
     case GGQ_F32: return 1;
     case GGQ_Q4_0:
     case GGQ_Q8_0: return 32;
-    case GGQ_Q4_K: return 256;
+    case GGQ_Q4_K:
+    case GGQ_Q6_K: return 256;
     default: return 0;
     }
 }

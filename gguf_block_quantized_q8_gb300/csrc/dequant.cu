@@ -6,7 +6,9 @@
 // packed 6-bit scales and mins, 128 bytes of nibbles): w = d*sc_j*q - dmin*m_j.
 // Q4_0 (same section: the Q8_0 layout with 4-bit integers; byte layout fp16 d,
 // then byte l holding the codes of weights l (low nibble) and 16 + l (high)):
-// w = d * (code - 8).  F32 rows are copied as they are.
+// w = d * (code - 8).  Q6_K (same section; layout of real files: ql[128] low
+// 4 bits, qh[64] high 2 bits, 16 signed 8-bit sub-block scales, fp16 d):
+// w = d * sc[k/16] * (u - 32).  F32 rows are copied as they are.
 // All are exact in fp32 except the single rounding of the Q4_K subtraction.
 #include <cuda_runtime.h>
 
@@ -41,6 +43,28 @@ __global__ void dequant_q40_kernel(const uint8_t* __restrict__ W, int64_t nblock
         o[l] = d * (float)((q & 15) - 8);
         o[16 + l] = d * (float)((q >> 4) - 8);
     }
+}
+
+// the 6-bit code of weight k of a Q6_K super-block
+__device__ __forceinline__ int q6k_code(const uint8_t* blk, int k) {
+    const int h = k >> 7, g = (k >> 5) & 3, l = k & 31;
+    const int lo = (blk[64 * h + 32 * (g & 1) + l] >> (4 * (g >> 1))) & 15;
+    const int hi = (blk[128 + 32 * h + l] >> (2 * g)) & 3;
+    return lo | (hi << 4);
+}
+
+// one thread per Q6_K sub-block (16 weights sharing a scale)
+__global__ void dequant_q6k_kernel(const uint8_t* __restrict__ W, int64_t nsub, float* __restrict__ out) {
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= nsub) return;
+    const int64_t sb = g >> 4;
+    const int j = (int)(g & 15);
+    const uint8_t* blk = W + 210 * sb;
+    const float d = half_bits_to_float((uint32_t)blk[208] | ((uint32_t)blk[209] << 8));
+    const float a = d * (float)(int8_t)blk[192 + j];
+    float* o = out + 256 * sb + 16 * j;
+#pragma unroll 4
+    for (int l = 0; l < 16; ++l) o[l] = a * (float)(q6k_code(blk, 16 * j + l) - 32);
 }
 
 // one thread per Q4_K sub-block (32 weights)
@@ -94,6 +118,11 @@ __global__ void embed_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_
         const uint8_t* blk = W + ((int64_t)id * (cols / 32) + k / 32) * 34;
         const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
         *o = d * (float)(int8_t)blk[2 + (k & 31)];
+    } else if constexpr (TYPE == GGQ_Q6_K) {
+        const uint8_t* blk = W + ((int64_t)id * (cols / 256) + k / 256) * 210;
+        const int kk = (int)(k & 255);
+        const float d = half_bits_to_float((uint32_t)blk[208] | ((uint32_t)blk[209] << 8));
+        *o = d * (float)(int8_t)blk[192 + kk / 16] * (float)(q6k_code(blk, kk) - 32);
     } else if constexpr (TYPE == GGQ_Q4_0) {
         const uint8_t* blk = W + ((int64_t)id * (cols / 32) + k / 32) * 18;
         const int l = (int)(k & 31);
@@ -131,6 +160,8 @@ int launch_embed(int type, const void* W, int64_t rows, int64_t cols, const int3
         embed_kernel<GGQ_Q8_0><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
     else if (type == GGQ_Q4_0)
         embed_kernel<GGQ_Q4_0><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
+    else if (type == GGQ_Q6_K)
+        embed_kernel<GGQ_Q6_K><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
     else if (type == GGQ_F32)
         embed_kernel<GGQ_F32><<<grid, 256, 0, stream>>>(w, rows, cols, ids, out, status);
     else
@@ -153,6 +184,10 @@ int launch_dequantize(int type, const void* W, int64_t rows, int64_t cols, float
             dequant_q8_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(w, nb, out);
         else
             dequant_q40_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(w, nb, out);
+    } else if (type == GGQ_Q6_K) {
+        const int64_t ns = rows * (cols / 256) * 16;
+        if (ns == 0) return GGQ_OK;
+        dequant_q6k_kernel<<<(unsigned)((ns + 255) / 256), 256, 0, stream>>>(w, ns, out);
     } else {
         const int64_t ns = rows * (cols / 256) * 8;
         if (ns == 0) return GGQ_OK;

@@ -1,6 +1,6 @@
-// Warp-per-row GEMV for F32 weights and for the Q4_0 shapes the streaming
-// kernel does not take (cols % 256 != 0, cols < 768, x' of an activation row
-// too wide for its shared memory); M up to 16.
+// Warp-per-row GEMV for F32 and Q6_K weights and for the Q4_0 shapes the
+// streaming kernel does not take (cols % 256 != 0, cols < 768, x' of an
+// activation row too wide for its shared memory); M up to 16.
 //
 //   y[m][r] = sum_c w[r][c] * x[m][c]      (matvec of the culpeo.ws kernel list)
 //
@@ -10,6 +10,12 @@
 // integers, 18 bytes per 32 weights): fp16 d, then 16 bytes of 4-bit codes;
 // weight l (l < 16) is the low nibble of byte l, weight 16 + l its high
 // nibble, and w = d * (code - 8) (the layout of real Q4_0 files).
+// Q6_K (same page: the k-quant paragraph and the bits/weight loop, 210 bytes
+// per 256 weights; "Understanding quantization names like Q4_K_M": Q4_K_M
+// files hold some tensors as Q6_K): ql[128] low 4 bits, qh[64] high 2 bits,
+// 16 signed 8-bit sub-block scales, fp16 d; weight k = 128h + 32g + l has the
+// code u = ql[64h + 32(g%2) + l] >> 4(g/2) & 15 | (qh[32h + l] >> 2g & 3) << 4
+// and w = d * sc[k/16] * (u - 32) (the layout of real Q6_K files).
 //
 // One warp owns a row at a time (grid-stride over rows), lanes split the row's
 // columns, a shuffle tree adds the lanes: every output is written by exactly
@@ -141,6 +147,65 @@ __global__ void __launch_bounds__(kThreads) gemv_q40_rows_kernel(const uint8_t* 
     }
 }
 
+// Q6_K: a warp step is one 256-weight super-block of the row.  Lane (h, i) =
+// (lane / 16, lane % 16) takes columns l = 2i, 2i+1 of half h in all four
+// quarters g (weights 128h + 32g + l): the ql bytes 64h + l (g = 0 low nibble,
+// g = 2 high) and 64h + 32 + l (g = 1, 3), and the qh bytes 32h + l (2 bits per
+// g).  Each of the three is one 16-bit load covering both columns, and the 16
+// lanes of a half read 32 contiguous bytes of each.  The 6-bit codes of a
+// quarter are assembled two at a time in one register; 0x4B000000 | u is the
+// float 2^23 + u, so u - 32 is one subtraction.  Weight k uses sub-block scale
+// k / 16 = 8h + 2g + i / 8.  The super-block starts on an even address (W is
+// 16-byte aligned, 210 is even).
+template <int MMAX>
+__global__ void __launch_bounds__(kThreads) gemv_q6k_rows_kernel(const uint8_t* __restrict__ W,
+                                                                 const float* __restrict__ x, float* __restrict__ y,
+                                                                 int64_t rows, int64_t cols, int M) {
+    const int lane = threadIdx.x & 31, h = lane >> 4, i = lane & 15;
+    const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+    const int64_t ns = cols / 256;
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int64_t row = warp0; row < rows; row += nwarps) {
+        float acc[MMAX];
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
+        const uint8_t* rp = W + row * ns * 210;
+#pragma unroll 2
+        for (int64_t u = 0; u < ns; ++u) {
+            const uint8_t* sb = rp + 210 * u;
+            const unsigned short* sb16 = reinterpret_cast<const unsigned short*>(sb);
+            const uint32_t a = __ldcs(sb16 + 32 * h + i);         // ql 64h + 2i, +1
+            const uint32_t b = __ldcs(sb16 + 32 * h + 16 + i);    // ql 64h + 32 + 2i, +1
+            const uint32_t c = __ldcs(sb16 + 64 + 16 * h + i);    // qh 32h + 2i, +1
+            const float d = half_bits_to_float(__ldcs(sb16 + 104));
+            const signed char* sc = reinterpret_cast<const signed char*>(sb + 192 + 8 * h + (i >> 3));
+            // codes of columns 2i (byte 0) and 2i + 1 (byte 1) in quarter g
+            const uint32_t q[4] = {(a & 0x0F0Fu) | ((c << 4) & 0x3030u), (b & 0x0F0Fu) | ((c << 2) & 0x3030u),
+                                   ((a >> 4) & 0x0F0Fu) | (c & 0x3030u), ((b >> 4) & 0x0F0Fu) | ((c >> 2) & 0x3030u)};
+            float w0[4], w1[4], ds[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                w0[g] = __uint_as_float(0x4B000000u | (q[g] & 0xFFu)) - 8388640.0f;
+                w1[g] = __uint_as_float(0x4B000000u | (q[g] >> 8)) - 8388640.0f;
+                ds[g] = d * (float)__ldcs(sc + 2 * g);
+            }
+#pragma unroll
+            for (int m = 0; m < MMAX; ++m) {
+                if (m >= M) continue;
+                const float* xb = x + m * cols + 256 * u + 128 * h + 2 * i;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const float2 xv = __ldg(reinterpret_cast<const float2*>(xb + 32 * g));
+                    acc[m] = fmaf(ds[g], fmaf(w0[g], xv.x, w1[g] * xv.y), acc[m]);
+                }
+            }
+        }
+        store_row<MMAX>(acc, y, rows, row, M, lane);
+    }
+}
+
 template <typename Kernel, typename WT>
 int launch(Kernel kernel, const WT* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
            cudaStream_t stream) {
@@ -170,6 +235,8 @@ int launch_mmax(int type, const void* W, int64_t rows, int64_t cols, const float
         if (cols % 4 == 0) return launch(gemv_f32_kernel<MMAX, true>, w, rows, cols, x, y, M, stream);
         return launch(gemv_f32_kernel<MMAX, false>, w, rows, cols, x, y, M, stream);
     }
+    if (type == GGQ_Q6_K)
+        return launch(gemv_q6k_rows_kernel<MMAX>, static_cast<const uint8_t*>(W), rows, cols, x, y, M, stream);
     return launch(gemv_q40_rows_kernel<MMAX>, static_cast<const uint8_t*>(W), rows, cols, x, y, M, stream);
 }
 
@@ -177,7 +244,8 @@ int launch_mmax(int type, const void* W, int64_t rows, int64_t cols, const float
 
 int launch_gemv_rows(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
                      cudaStream_t stream) {
-    if (type != GGQ_F32 && type != GGQ_Q4_0) return fail(GGQ_ETYPE, "gemv: type %d has no warp-per-row kernel", type);
+    if (type != GGQ_F32 && type != GGQ_Q4_0 && type != GGQ_Q6_K)
+        return fail(GGQ_ETYPE, "gemv: type %d has no warp-per-row kernel", type);
     if (M <= 1) return launch_mmax<1>(type, W, rows, cols, x, y, M, stream);
     if (M <= 2) return launch_mmax<2>(type, W, rows, cols, x, y, M, stream);
     if (M <= 4) return launch_mmax<4>(type, W, rows, cols, x, y, M, stream);

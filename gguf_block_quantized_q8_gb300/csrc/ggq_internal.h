@@ -52,7 +52,8 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
 bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_t* rows);
 int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* rows, int64_t cols,
                        const float* x, float* const* y, int M, cudaStream_t stream);
-// warp-per-row GEMV for F32 (any cols) and Q4_0 (cols % 32 == 0), M up to 16
+// warp-per-row GEMV for F32 (any cols), Q4_0 (cols % 32 == 0) and Q6_K
+// (cols % 256 == 0), M up to 16
 int launch_gemv_rows(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
                      cudaStream_t stream);
 // small-batch dequant-GEMM on the tensor cores (M up to 16, cols % 256 == 0);

@@ -144,12 +144,16 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  * 6-bit scales/mins, 128 bytes of nibbles), Q4_0 w = d*(u - 8) (the same
  * section: the Q8_0 layout with 4-bit integers, 18 bytes per 32 weights; byte
  * layout: fp16 d, then byte l holding the code u of weight l in its low nibble
- * and that of weight 16 + l in its high nibble), F32 the fp32 values as
- * stored.  Decoded weights are never written to memory; products accumulate
- * in fp32 (any order).
+ * and that of weight 16 + l in its high nibble), Q6_K w = d*sc[k/16]*(u - 32)
+ * (the k-quant paragraph and the bits/weight loop of the same page, 210 bytes
+ * per 256 weights; byte layout of real files: ql[128] low 4 bits, qh[64] high
+ * 2 bits, 16 signed 8-bit sub-block scales, fp16 d; weight 128h + 32g + l has
+ * the low bits in ql[64h + 32(g%2) + l] at bit 4(g/2) and the high bits in
+ * qh[32h + l] at bit 2g), F32 the fp32 values as stored.  Decoded weights are
+ * never written to memory; products accumulate in fp32 (any order).
  *
- *   type   GGQ_Q8_0 or GGQ_Q4_0 (cols % 32 == 0), GGQ_Q4_K (cols % 256 == 0),
- *          GGQ_F32 (any cols >= 1)
+ *   type   GGQ_Q8_0 or GGQ_Q4_0 (cols % 32 == 0), GGQ_Q4_K or GGQ_Q6_K
+ *          (cols % 256 == 0), GGQ_F32 (any cols >= 1)
  *   W      device, rows x row-bytes, row-major, 16-byte aligned
  *   x      device, fp32 [M, cols] row-major, 16-byte aligned
  *   y      device, fp32 [M, rows] row-major, 4-byte aligned; fully overwritten
@@ -337,7 +341,8 @@ int ggq_gemm_prefill(int type, const void* W, int64_t rows, int64_t cols,
 /*
  * ggq_dequantize -- out[r*cols + c] = w[r, c] as fp32 (test and inspection
  * aid; the GEMV path never writes decoded weights).  Types GGQ_Q8_0, GGQ_Q4_K,
- * GGQ_Q4_0 (decoded as in ggq_gemv) and GGQ_F32 (a device-to-device copy);
+ * GGQ_Q4_0, GGQ_Q6_K (decoded as in ggq_gemv) and GGQ_F32 (a device-to-device
+ * copy);
  * cols a multiple of the type's block.  W 16-byte aligned, out 4-byte
  * aligned.  Asynchronous.
  */
@@ -349,7 +354,7 @@ int ggq_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* o
  * Embedding": a token id selects one row of the embedding table; the C++
  * engine post's embed(table, token)).  out[i*cols + k] = w[ids[i], k] as fp32,
  * decoded exactly as ggq_dequantize does, for i < n.
- *   type   GGQ_Q8_0, GGQ_Q4_K, GGQ_Q4_0 (table 2-byte aligned) or GGQ_F32
+ *   type   GGQ_Q8_0, GGQ_Q4_K, GGQ_Q4_0, GGQ_Q6_K (table 2-byte aligned) or GGQ_F32
  *          (4-byte aligned); table device [rows, cols] in the type's layout
  *   ids    device int32 [n], n in 1..65535; out device fp32 [n, cols], 4-byte aligned
  * An id outside [0, rows) gives a row of zeros, and the next ggq_device_status

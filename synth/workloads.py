@@ -8,7 +8,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-from . import TYPE_F32, TYPE_Q4_0, TYPE_Q4_K, TYPE_Q8_0, stream_id
+from . import TYPE_F32, TYPE_Q4_0, TYPE_Q4_K, TYPE_Q6_K, TYPE_Q8_0, stream_id
 
 W_SIGMA = 0.02
 X_SIGMA = 1.0
@@ -91,6 +91,9 @@ Q40_GEMV = Gemv("extra.q4_0.weight", TYPE_Q4_0, 14336, 4096)
 F32_GEMV = Gemv("extra.f32.weight", TYPE_F32, 14336, 4096)
 # a Q4_0 width that is not a multiple of 256 (the warp-per-row kernel)
 Q40_ODD_GEMV = Gemv("extra.q4_0_odd.weight", TYPE_Q4_0, 14336, 4128)
+# Q6_K in the shapes a Q4_K_M file gives it (ffn_down 4096 x 14336) and the cfg4 shape
+Q6K_GEMV = Gemv("extra.q6_k.weight", TYPE_Q6_K, 14336, 4096)
+Q6K_DOWN_GEMV = Gemv("extra.q6_k_down.weight", TYPE_Q6_K, 4096, 14336)
 
 
 def weight_bytes(gemvs) -> int:

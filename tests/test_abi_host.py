@@ -164,7 +164,8 @@ def test_compute_entry_points_validate_arguments(ggq):
     assert g(ggq.Q8_0, 16, 0, 64, 16, 16, 1, 0) == -1                # rows = 0
     assert g(ggq.Q8_0, 16, 4, 64, 8, 16, 1, 0) == -1                 # x misaligned
     assert g(ggq.F16, 16, 4, 64, 16, 16, 1, 0) == -2                 # type
-    assert g(ggq.Q6_K, 16, 4, 256, 16, 16, 1, 0) == -2
+    assert g(ggq.Q6_K, 16, 4, 288, 16, 16, 1, 0) == -1                # Q6_K: cols % 256
+    assert g(ggq.Q6_K, 16, 4, 256, 16, 16, 17, 0) == -1
     assert g(ggq.Q4_0, 16, 4, 48, 16, 16, 1, 0) == -1                # Q4_0: cols % 32
     assert g(ggq.Q4_0, 16, 4, 64, 16, 16, 17, 0) == -1
     assert g(ggq.F32, 16, 4, 0, 16, 16, 1, 0) == -1                  # F32: cols >= 1
@@ -183,6 +184,9 @@ def test_compute_entry_points_validate_arguments(ggq):
     assert d(ggq.Q4_K, 16, 2, 100, 16, 0) == -1
     assert d(ggq.F16, 16, 2, 256, 16, 0) == -2
     assert d(ggq.Q4_0, 16, 2, 40, 16, 0) == -1                       # cols % 32
+    assert d(ggq.Q6_K, 16, 2, 100, 16, 0) == -1                      # cols % 256
+    assert ggq.ggq_chain_create(ggq.Q6_K, 1, [([16], [64], 2048, 16, [16])])[0] == -2   # no Q6_K chains
+    assert ggq.ggq_gemv_noalloc(ggq.Q6_K, 16, 4, 1024, 16, 16, 1, 0) == -2
     assert g(ggq.Q8_0, 16, 4, 64, 16, 16, 17, 0) == -1
     assert "M 17 outside 1..16" in ggq.lib.ggq_last_error().decode()
 
@@ -233,6 +237,7 @@ def test_embed_validates_arguments(ggq):
     """ggq_embed rejects bad arguments before any launch."""
     assert ggq.ggq_embed(ggq.F16, 16, 4, 64, 16, 1, 16, 0) == -2          # type
     assert ggq.ggq_embed(ggq.Q4_0, 16, 4, 40, 16, 1, 16, 0) == -1         # Q4_0: cols % 32
+    assert ggq.ggq_embed(ggq.Q6_K, 16, 4, 320, 16, 1, 16, 0) == -1        # Q6_K: cols % 256
     assert ggq.ggq_embed(ggq.F32, 18, 4, 5, 16, 1, 16, 0) == -1           # F32 table: 4-byte aligned
     assert ggq.ggq_embed(ggq.Q8_0, 0, 4, 64, 16, 1, 16, 0) == -1          # NULL table
     assert ggq.ggq_embed(ggq.Q8_0, 16, 4, 64, 0, 1, 16, 0) == -1          # NULL ids

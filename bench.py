@@ -282,6 +282,139 @@ class DecodePass:
             self.chain = 0
 
 
+# ----------------------------------------------- a pass planned from a file ----
+
+# the GEMV stages of a layer in dependency order, by GGUF tensor name
+LAYER_STAGES = (("attn_q", "attn_k", "attn_v"), ("attn_output",), ("ffn_gate", "ffn_up"), ("ffn_down",))
+CHAIN_TYPES = (2, 8, 12)   # the types the chain kernel streams: Q4_0, Q8_0, Q4_K
+
+
+def plan_from_table(model, layers: int):
+    """The decode pass of a loaded file from its tensor table alone: per layer
+    the stages [q,k,v], [o], [gate,up], [down], then the head.  A stage whose
+    matrices differ in type is split by type, in order.  Returns a list of
+    (type, [tensor info])."""
+    stages = []
+    for L in range(layers):
+        for names in LAYER_STAGES:
+            groups = {}
+            for n in names:
+                t = model.find(f"blk.{L}.{n}.weight")
+                groups.setdefault(t["type"], []).append(t)
+            stages += list(groups.items())
+    head = model.find("output.weight")
+    stages.append((head["type"], [head]))
+    return stages
+
+
+def segments(types):
+    """Launches for stages of the given types, in order: each run of
+    consecutive stages of one type the chain kernel streams is one chain
+    launch, every other stage a launch of its own.  Returns [(start, end,
+    is_chain)] over stage indices."""
+    out, i = [], 0
+    while i < len(types):
+        if types[i] in CHAIN_TYPES:
+            j = i
+            while j < len(types) and types[j] == types[i]:
+                j += 1
+            out.append((i, j, True))
+            i = j
+        else:
+            out.append((i, i + 1, False))
+            i += 1
+    return out
+
+
+class FilePass:
+    """A decode pass planned from a loaded file (plan_from_table): each run of
+    consecutive stages of one type the chain kernel streams is ONE ggq_chain
+    launch; every other stage (Q6_K, F32) is one ggq_gemv / ggq_gemv_multi
+    launch.  Every stage reads its own seeded x (as in DecodePass)."""
+
+    def __init__(self, model, layers, torch, ggq, synth, x_stream0=9000):
+        self.torch, self.ggq = torch, ggq
+        self.plan, self.keep = [], []
+        self.weight_bytes = 0
+        self.type_bytes = {}   # weight bytes per tensor type
+        for si, (qtype, ts) in enumerate(plan_from_table(model, layers)):
+            cols = ts[0]["ne"][0]
+            rows = [t["ne"][1] for t in ts]
+            x = torch.from_numpy(synth.normal_f32(cols, x_stream0 + si)).cuda()
+            ys = [torch.full((r,), float("nan"), device="cuda") for r in rows]
+            self.keep += [x] + ys
+            self.weight_bytes += sum(t["nbytes"] for t in ts)
+            self.type_bytes[qtype] = self.type_bytes.get(qtype, 0) + sum(t["nbytes"] for t in ts)
+            self.plan.append(dict(qtype=qtype, W=[t["data"] for t in ts], rows=rows, cols=cols, x=x, ys=ys,
+                                  names=[t["name"] for t in ts], x_stream=x_stream0 + si))
+        self.calls, self.chains = [], []
+        for i, j, is_chain in segments([p["qtype"] for p in self.plan]):
+            if is_chain:
+                rc, h = ggq.ggq_chain_create(self.plan[i]["qtype"], 1,
+                                             [(q["W"], q["rows"], q["cols"], q["x"].data_ptr(),
+                                               [y.data_ptr() for y in q["ys"]]) for q in self.plan[i:j]])
+                ggq.check(rc, "ggq_chain_create")
+                self.chains.append(h)
+                self.calls.append(("chain", h))
+            else:
+                self.calls.append(("stage", self.plan[i]))
+
+    def run(self, sp):
+        ggq = self.ggq
+        for kind, c in self.calls:
+            if kind == "chain":
+                ggq.check(ggq.ggq_chain_run(c, sp), "ggq_chain_run")
+            elif len(c["W"]) == 1:
+                ggq.check(ggq.ggq_gemv(c["qtype"], c["W"][0], c["rows"][0], c["cols"], c["x"].data_ptr(),
+                                       c["ys"][0].data_ptr(), 1, sp), "ggq_gemv")
+            else:
+                ggq.check(ggq.ggq_gemv_multi(c["qtype"], c["W"], c["rows"], c["cols"], c["x"].data_ptr(),
+                                             [y.data_ptr() for y in c["ys"]], 1, sp), "ggq_gemv_multi")
+
+    def close(self):
+        for h in self.chains:
+            self.ggq.ggq_chain_free(h)
+        self.chains = []
+
+
+def q4km_file_pass(torch, ggq, synth, stream, steps: int = 20, layers: int = 32):
+    """The mixed-type pass of a Q4_K_M-style file: write it (synth.workloads.
+    write_q4km_file, 4.9 GB), load it with ggq_load, plan the pass from the tensor
+    table (FilePass) and time it as a CUDA graph.  The weights exceed L2."""
+    from synth import workloads as WL
+    shm = "/dev/shm" if os.path.isdir("/dev/shm") else tempfile.gettempdir()
+    path = os.path.join(shm, f"ggq_q4km_{os.getpid()}.gguf")
+    t0 = time.perf_counter()
+    try:
+        WL.write_q4km_file(path, layers)
+        t_gen = time.perf_counter() - t0
+        file_bytes = os.path.getsize(path)
+        model = ggq.Model.load(path)
+    finally:
+        if os.path.exists(path):
+            os.remove(path)
+    fp = FilePass(model, layers, torch, ggq, synth)
+    sp = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        fp.run(sp)
+    torch.cuda.synchronize()
+    g = capture(torch, lambda: fp.run(sp), stream)
+    time_graph(torch, g, stream, 3)
+    ms = time_graph(torch, g, stream, steps)
+    rc = ggq.device_status()
+    out = {"ms": round(ms, 4), "GB_s": round(fp.weight_bytes / ms / 1e6, 1), "launches": len(fp.calls),
+           "chain_launches": len(fp.chains), "weight_bytes_per_pass": fp.weight_bytes,
+           "q6_k_bytes_per_pass": fp.type_bytes.get(14, 0), "file_bytes": file_bytes,
+           "generate_s": round(t_gen, 2), "status": rc,
+           "plan": "per layer [q,k,v] [o] [gate,up] [down], split by type; runs of Q4_K stages as one chain "
+                   "launch each, Q6_K stages as their own launches; attn_v and ffn_down Q6_K in odd layers, "
+                   "Q6_K head"}
+    del g
+    fp.close()
+    model.close()
+    return out
+
+
 def time_graph(torch, graph, stream, steps):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -638,6 +771,8 @@ def main():
         raise SystemExit(f"device status {rc} after the timed region")
 
     extra = {} if a.no_extras else extras(torch, ggq, synth, stream)
+    if not a.no_extras:
+        extra["q4_k_m_file_pass_llama8b"] = q4km_file_pass(torch, ggq, synth, stream)
     if not a.no_extras and len(dp.rest) == 1:
         # the pass with the layer's element-wise steps fused in (real data flow)
         frun, ffree, _norms = dp.fused_pass(synth)

@@ -153,66 +153,107 @@ __global__ void __launch_bounds__(kThreads) gemv_q40_rows_kernel(const uint8_t* 
 // g = 2 high) and 64h + 32 + l (g = 1, 3), and the qh bytes 32h + l (2 bits per
 // g).  Each of the three is one 16-bit load covering both columns, and the 16
 // lanes of a half read 32 contiguous bytes of each.  The 6-bit codes of a
-// quarter are assembled two at a time in one register; 0x4B000000 | u is the
-// float 2^23 + u, so u - 32 is one subtraction.  Weight k uses sub-block scale
-// k / 16 = 8h + 2g + i / 8.  The super-block starts on an even address (W is
-// 16-byte aligned, 210 is even).
-template <int MMAX>
-__global__ void __launch_bounds__(kThreads) gemv_q6k_rows_kernel(const uint8_t* __restrict__ W,
+// quarter are assembled two at a time in one register; a byte permute puts a
+// code under 0x4B0000 (the float 2^23 + u), so u - 32 is one packed
+// subtraction.  Weight k uses sub-block scale k / 16 = 8h + 2g + i / 8: lane j
+// converts scale j % 16 (d * sc, no int-to-float instruction) and the lanes
+// that need it read it by shuffle.  The super-block starts on an even address
+// (W is 16-byte aligned, 210 is even).
+//
+// Rows with few super-blocks in flight per SM (few rows) are shared: P = 1, 2,
+// 4 or 8 warps of a CTA take one row, each a contiguous range of its
+// super-blocks, and add their parts in shared memory in warp order.
+//
+// MINB: CTAs per SM the registers must allow.  With one warp per row (P = 1)
+// and M = 1, 6 (48 warps per SM, 40 registers) measured faster; where rows are
+// shared (P > 1), 4 (up to 64 registers) did (14336x4096: 27.6 vs 33.3 us; the
+// 4096x14336 ffn_down shape, P = 2: 41.4 vs 37.3 us).
+template <int MMAX, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) gemv_q6k_rows_kernel(const uint8_t* __restrict__ W,
                                                                  const float* __restrict__ x, float* __restrict__ y,
-                                                                 int64_t rows, int64_t cols, int M) {
-    const int lane = threadIdx.x & 31, h = lane >> 4, i = lane & 15;
-    const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+                                                                 int64_t rows, int64_t cols, int M, int P) {
+    __shared__ float red[kWarps][MMAX];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, h = lane >> 4, i = lane & 15;
+    const int rpc = kWarps / P, slot = warp / P, part = warp - slot * P;   // rows per CTA step
     const int64_t ns = cols / 256;
+    const int64_t u0 = ns * part / P, u1 = ns * (part + 1) / P;
     pdl_launch_dependents();
     pdl_wait();
-    for (int64_t row = warp0; row < rows; row += nwarps) {
-        float acc[MMAX];
+    for (int64_t base = (int64_t)blockIdx.x * rpc; base < rows; base += (int64_t)gridDim.x * rpc) {
+        const int64_t row = base + slot;
+        float2 acc[MMAX];
 #pragma unroll
-        for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
-        const uint8_t* rp = W + row * ns * 210;
-#pragma unroll 2
-        for (int64_t u = 0; u < ns; ++u) {
-            const uint8_t* sb = rp + 210 * u;
-            const unsigned short* sb16 = reinterpret_cast<const unsigned short*>(sb);
-            const uint32_t a = __ldcs(sb16 + 32 * h + i);         // ql 64h + 2i, +1
-            const uint32_t b = __ldcs(sb16 + 32 * h + 16 + i);    // ql 64h + 32 + 2i, +1
-            const uint32_t c = __ldcs(sb16 + 64 + 16 * h + i);    // qh 32h + 2i, +1
-            const float d = half_bits_to_float(__ldcs(sb16 + 104));
-            const signed char* sc = reinterpret_cast<const signed char*>(sb + 192 + 8 * h + (i >> 3));
-            // codes of columns 2i (byte 0) and 2i + 1 (byte 1) in quarter g
-            const uint32_t q[4] = {(a & 0x0F0Fu) | ((c << 4) & 0x3030u), (b & 0x0F0Fu) | ((c << 2) & 0x3030u),
-                                   ((a >> 4) & 0x0F0Fu) | (c & 0x3030u), ((b >> 4) & 0x0F0Fu) | ((c >> 2) & 0x3030u)};
-            float w0[4], w1[4], ds[4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                w0[g] = __uint_as_float(0x4B000000u | (q[g] & 0xFFu)) - 8388640.0f;
-                w1[g] = __uint_as_float(0x4B000000u | (q[g] >> 8)) - 8388640.0f;
-                ds[g] = d * (float)__ldcs(sc + 2 * g);
-            }
-#pragma unroll
-            for (int m = 0; m < MMAX; ++m) {
-                if (m >= M) continue;
-                const float* xb = x + m * cols + 256 * u + 128 * h + 2 * i;
+        for (int m = 0; m < MMAX; ++m) acc[m] = make_float2(0.0f, 0.0f);
+        if (row < rows) {
+            const uint8_t* rp = W + row * ns * 210;
+            // super-blocks in flight per warp: more where the registers allow
+            constexpr int kUnroll = MMAX <= 4 ? 2 : 1;
+#pragma unroll kUnroll
+            for (int64_t u = u0; u < u1; ++u) {
+                const uint8_t* sb = rp + 210 * u;
+                const unsigned short* sb16 = reinterpret_cast<const unsigned short*>(sb);
+                const uint32_t a = __ldcs(sb16 + 32 * h + i);         // ql 64h + 2i, +1
+                const uint32_t b = __ldcs(sb16 + 32 * h + 16 + i);    // ql 64h + 32 + 2i, +1
+                const uint32_t c = __ldcs(sb16 + 64 + 16 * h + i);    // qh 32h + 2i, +1
+                const float d = half_bits_to_float(__ldcs(sb16 + 104));
+                // scale (lane % 16) as a float: (sc + 128) under 0x4B0000, minus 2^23 + 128
+                const uint32_t ub = __ldcs(sb + 192 + (lane & 15));
+                const float dsl = d * (__uint_as_float(0x4B000000u | (ub ^ 0x80u)) - 8388736.0f);
+                // codes of columns 2i (byte 0) and 2i + 1 (byte 1) in quarter g
+                const uint32_t q[4] = {(a & 0x0F0Fu) | ((c << 4) & 0x3030u), (b & 0x0F0Fu) | ((c << 2) & 0x3030u),
+                                       ((a >> 4) & 0x0F0Fu) | (c & 0x3030u), ((b >> 4) & 0x0F0Fu) | ((c >> 2) & 0x3030u)};
+                float2 w[4];
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    const float2 xv = __ldg(reinterpret_cast<const float2*>(xb + 32 * g));
-                    acc[m] = fmaf(ds[g], fmaf(w0[g], xv.x, w1[g] * xv.y), acc[m]);
+                    const float ds = __shfl_sync(0xffffffffu, dsl, 8 * h + 2 * g + (i >> 3));
+                    const float2 f = make_float2(__uint_as_float(__byte_perm(q[g], 0x4B000000u, 0x7440)),
+                                                 __uint_as_float(__byte_perm(q[g], 0x4B000000u, 0x7441)));
+                    w[g] = __fmul2_rn(__fadd2_rn(f, make_float2(-8388640.0f, -8388640.0f)), make_float2(ds, ds));
+                }
+#pragma unroll
+                for (int m = 0; m < MMAX; ++m) {
+                    if (m >= M) continue;
+                    const float* xb = x + m * cols + 256 * u + 128 * h + 2 * i;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        acc[m] = __ffma2_rn(w[g], __ldg(reinterpret_cast<const float2*>(xb + 32 * g)), acc[m]);
                 }
             }
         }
-        store_row<MMAX>(acc, y, rows, row, M, lane);
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) {
+            if (m >= M) continue;
+            const float v = warp_sum(acc[m].x + acc[m].y);
+            if (P == 1) {
+                if (lane == 0 && row < rows) y[(int64_t)m * rows + row] = v;
+            } else if (lane == 0) {
+                red[warp][m] = v;
+            }
+        }
+        if (P > 1) {
+            __syncthreads();
+            if (part == 0 && lane < M && lane < MMAX && row < rows) {
+                float v = 0.0f;
+                for (int p2 = 0; p2 < P; ++p2) v += red[warp + p2][lane];
+                y[(int64_t)lane * rows + row] = v;
+            }
+            __syncthreads();   // red is reused by the next step
+        }
     }
 }
 
-template <typename Kernel, typename WT>
-int launch(Kernel kernel, const WT* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
-           cudaStream_t stream) {
+int num_sms() {
     int dev = 0, sms = 1;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t want = (rows + kWarps - 1) / kWarps;
+    return sms > 0 ? sms : 1;
+}
+
+template <typename Kernel, typename WT, typename... Extra>
+int launch(Kernel kernel, const WT* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
+           cudaStream_t stream, int rows_per_cta = kWarps, Extra... extra) {
+    const int sms = num_sms();
+    const int64_t want = (rows + rows_per_cta - 1) / rows_per_cta;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)std::max(sms, 1) * 8));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -223,7 +264,7 @@ int launch(Kernel kernel, const WT* W, int64_t rows, int64_t cols, const float* 
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, W, x, y, rows, cols, M);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, W, x, y, rows, cols, M, extra...);
     return e == cudaSuccess ? GGQ_OK : cuda_fail(e, "gemv launch");
 }
 
@@ -235,8 +276,20 @@ int launch_mmax(int type, const void* W, int64_t rows, int64_t cols, const float
         if (cols % 4 == 0) return launch(gemv_f32_kernel<MMAX, true>, w, rows, cols, x, y, M, stream);
         return launch(gemv_f32_kernel<MMAX, false>, w, rows, cols, x, y, M, stream);
     }
-    if (type == GGQ_Q6_K)
-        return launch(gemv_q6k_rows_kernel<MMAX>, static_cast<const uint8_t*>(W), rows, cols, x, y, M, stream);
+    if (type == GGQ_Q6_K) {
+        // warps per row: enough rows in flight for about 48 warps per SM
+        const int64_t target = (int64_t)num_sms() * 48;
+        int P = 1;
+        while (P < kWarps && rows * P < target && cols / 256 >= 2 * P) P *= 2;
+        if constexpr (MMAX == 1) {
+            if (P == 1)
+                return launch(gemv_q6k_rows_kernel<1, 6>, static_cast<const uint8_t*>(W), rows, cols, x, y, M, stream,
+                              kWarps, 1);
+        }
+        constexpr int kMinB = MMAX <= 2 ? 4 : MMAX == 8 ? 3 : 2;   // the registers the build needs, no spills
+        return launch(gemv_q6k_rows_kernel<MMAX, kMinB>, static_cast<const uint8_t*>(W), rows, cols, x, y, M, stream,
+                      kWarps / P, P);
+    }
     return launch(gemv_q40_rows_kernel<MMAX>, static_cast<const uint8_t*>(W), rows, cols, x, y, M, stream);
 }
 

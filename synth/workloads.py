@@ -96,6 +96,50 @@ Q6K_GEMV = Gemv("extra.q6_k.weight", TYPE_Q6_K, 14336, 4096)
 Q6K_DOWN_GEMV = Gemv("extra.q6_k_down.weight", TYPE_Q6_K, 4096, 14336)
 
 
+def q6k_layer(L: int) -> bool:
+    """Layers whose attn_v and ffn_down are Q6_K in the Q4_K_M-style mixture:
+    every other layer (the pages say only "part of" those tensors)."""
+    return L % 2 == 1
+
+
+def llama8b_q4km_tensors(n_layers: int = 32, vocab: int = 128256):
+    """Every tensor of a Llama-8B-shaped file in a Q4_K_M-style mixture, in file
+    order: token_embd (Q4_K), per layer attn_norm (F32), q, k, v, o, ffn_norm
+    (F32), gate, up, down, then output_norm (F32) and the output head.  attn_v
+    and ffn_down are Q6_K in the layers q6k_layer picks, the head is Q6_K (as in
+    real Q4_K_M files), every other matrix Q4_K: 4.9 GB for 32 layers, the size
+    the pages give for an 8B model in Q4_K_M.  Norms are rows = 1."""
+    out = [Gemv("token_embd.weight", TYPE_Q4_K, vocab, 4096)]
+    for L in range(n_layers):
+        p = f"blk.{L}"
+        six = TYPE_Q6_K if q6k_layer(L) else TYPE_Q4_K
+        out += [Gemv(f"{p}.attn_norm.weight", TYPE_F32, 1, 4096),
+                Gemv(f"{p}.attn_q.weight", TYPE_Q4_K, 4096, 4096),
+                Gemv(f"{p}.attn_k.weight", TYPE_Q4_K, 1024, 4096),
+                Gemv(f"{p}.attn_v.weight", six, 1024, 4096),
+                Gemv(f"{p}.attn_output.weight", TYPE_Q4_K, 4096, 4096),
+                Gemv(f"{p}.ffn_norm.weight", TYPE_F32, 1, 4096),
+                Gemv(f"{p}.ffn_gate.weight", TYPE_Q4_K, 14336, 4096),
+                Gemv(f"{p}.ffn_up.weight", TYPE_Q4_K, 14336, 4096),
+                Gemv(f"{p}.ffn_down.weight", six, 4096, 14336)]
+    out += [Gemv("output_norm.weight", TYPE_F32, 1, 4096), Gemv("output.weight", TYPE_Q6_K, vocab, 4096)]
+    return out
+
+
+def write_q4km_file(path: str, n_layers: int = 32, vocab: int = 128256):
+    """Write llama8b_q4km_tensors as a GGUF v3 file (seeded payloads); returns
+    the tensor list."""
+    from . import weight_rows, write_gguf
+    ts = llama8b_q4km_tensors(n_layers, vocab)
+    kvs = [("general.architecture", 8, "llama"), ("general.name", 8, "synthetic-llama8b-q4_k_m-shape"),
+           ("llama.block_count", 4, n_layers), ("llama.embedding_length", 4, 4096),
+           ("llama.feed_forward_length", 4, 14336), ("llama.attention.head_count", 4, 32),
+           ("llama.attention.head_count_kv", 4, 8)]
+    tensors = [(g.name, [g.cols] if g.rows == 1 else [g.cols, g.rows], g.qtype) for g in ts]
+    write_gguf(path, kvs, tensors, (weight_rows(g.qtype, g.stream, g.rows, g.cols) for g in ts))
+    return ts
+
+
 def weight_bytes(gemvs) -> int:
     from . import row_bytes
     return sum(g.rows * row_bytes(g.qtype, g.cols) for g in gemvs)

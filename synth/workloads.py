@@ -98,7 +98,7 @@ Q6K_DOWN_GEMV = Gemv("extra.q6_k_down.weight", TYPE_Q6_K, 4096, 14336)
 
 def q6k_layer(L: int) -> bool:
     """Layers whose attn_v and ffn_down are Q6_K in the Q4_K_M-style mixture:
-    every other layer (the pages say only "part of" those tensors)."""
+    every other layer (the pages name only some of those tensors as Q6_K)."""
     return L % 2 == 1
 
 

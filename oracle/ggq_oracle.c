@@ -57,16 +57,20 @@
  *      in double, columns in order.
  *
  * Decode produces fp32 exactly as the format defines it: the Q8_0 and Q4_0
- * products d*q, the Q6_K product d*sc*(u-32) (11 + 7 + 6 significant bits:
- * exact in fp32) and the Q4_K products d*sc*q and dmin*m are exact in fp32, so the only
- * rounding is the final Q4_K subtraction (done here in double and rounded
- * once more to float, which gives the correctly rounded fp32 difference of two
- * fp32 values because 53 >= 2*24+2).
+ * products d*q, the Q6_K product d*sc*(u-32) (11 + 7 + 6 significant bits) and
+ * the Q4_K products d*sc*q and dmin*m are exact in fp32, so the only rounding
+ * is the final Q4_K subtraction (done here in double and rounded once more to
+ * float, which gives the correctly rounded fp32 difference of two fp32 values
+ * because 53 >= 2*24+2).
  *
- * Pins (tests/test_oracle_pins.py): closed-form values of hand-built blocks,
- * IEEE binary16 special values, one-hot x (exact columns), integer-valued
- * inputs (exact sums), brute force against a library matmul on tiny shapes,
- * and the pages' printed byte counts / offsets for the GGUF reader.
+ * Pins (tests/test_oracle_pins.py, tests/pin_checks.py): closed-form values of
+ * hand-built blocks, IEEE binary16 special values, one-hot x (exact columns),
+ * integer-valued inputs (exact sums), brute force against a library matmul on
+ * tiny shapes, the pages' printed byte counts / offsets for the GGUF reader,
+ * the practice script's printed mean errors (Q8_0 and its 4-bit block, through
+ * the synth encoders), and Q4_0 / Q6_K blocks decoding like the Q8_0 blocks
+ * of the same scale and integers.  tests/test_oracle_mutants.py plants slips
+ * in copies of this file and checks that a pin fails for each.
  */
 #include <stdint.h>
 #include <math.h>

@@ -162,9 +162,10 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  *   stream cudaStream_t
  *
  * Finite inputs with |x| < 2^70 are supported.  Errors: GGQ_EINVAL (NULL
- * pointer, rows < 1, cols not a multiple of the block, M outside 1..16, W not
- * 16-byte aligned, x not 16-byte or y not 4-byte aligned), GGQ_ETYPE, GGQ_ECUDA (launch
- * failure).  Asynchronous: returns after the launch.
+ * pointer, rows outside 1..2^31-1, cols not a positive multiple of the block
+ * or above 2^40, M outside 1..16, W not 16-byte aligned, x not 16-byte or y not
+ * 4-byte aligned), GGQ_ETYPE (F16 or a type id not listed above), GGQ_ECUDA
+ * (launch failure).  Asynchronous: returns after the launch.
  *
  * The call allocates no device memory and may be captured into a CUDA graph.
  * Calls on one stream run in stream order.

@@ -222,3 +222,21 @@ def test_synth_q4_k_roundtrip_error():
     back = oracle.dequantize(12, packed, 64, 256).reshape(-1)
     err = np.abs(back - w)
     assert err.mean() < 0.0025 and err.max() < 0.01
+
+
+def test_synth_encoders_edge_blocks():
+    """Encoder edge cases (the inputs both sides read): an all-zero block has
+    scale 0 and decodes to zeros; the largest magnitude of a block lands on the
+    end of its grid (Q4_0: code 8 + 7 or 8 - 7; Q6_K: 32 + 31 or 32 - 31)."""
+    z = np.zeros(256, np.float32)
+    assert not oracle.dequantize(2, synth.quantize_q4_0(z), 1, 256).any()
+    assert not oracle.dequantize(14, synth.quantize_q6_k(z), 1, 256).any()
+    w = synth.normal_f32(256, 9, sigma=0.02)
+    w[37] = 0.5                       # the largest magnitude, positive
+    w[200] = -0.5
+    q4 = synth.quantize_q4_0(w).reshape(8, 18)
+    assert (q4[1, 2 + 5] & 15) == 15          # weight 37 = block 1, weight 5: low nibble, code 15
+    assert (q4[6, 2 + 8] & 15) == 1           # weight 200 = block 6, weight 8: low nibble, code 1
+    q6 = synth.quantize_q6_k(w)
+    back = oracle.dequantize(14, q6, 1, 256).reshape(-1)
+    assert abs(back[37] - 0.5) <= 0.5 / 31 / 2 * 1.01 and abs(back[200] + 0.5) <= 0.5 / 31 / 2 * 1.01

@@ -720,7 +720,7 @@ def main():
 
     clocks = ClockSampler(dev)
     clocks.start()
-    # ---- warm-up (also sets up the stream's workspace), then capture one pass
+    # ---- warm-up (kernel attributes are set on first launch), then capture one pass
     with torch.cuda.stream(stream):
         for _ in range(max(1, a.warmup)):
             dp.run(sp)

@@ -155,12 +155,17 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const __grid_constan
     for (int r0 = 0; r0 < S; r0 += p.rbuf, ++round) {
         const int n = min(p.rbuf, S - r0);
         if (tid == 0) {
+            if (round == 0) {
+                // warm L2 only; every copy waits for the previous kernel in the
+                // stream, which may still be writing x (or W)
+                for (int u = 0; u < n; ++u) tma_prefetch_2d(&wmap, (u0 + r0 + u) * kQ4kRowBytes, rb * kRows);
+                pdl_wait();
+            }
             for (int u = 0; u < n; ++u) {
                 mbar_arrive_expect_tx(&s.bars[u], kQ4kTile);
                 tma_load_2d(s.tiles + (size_t)u * kQ4kTile, &wmap, &s.bars[u], (u0 + r0 + u) * kQ4kRowBytes,
                             rb * kRows);
             }
-            if (round == 0) pdl_wait();  // x may come from the previous kernel in the stream
             mbar_arrive_expect_tx(s.xbar, (uint32_t)(p.M * n * 1024));
             for (int m = 0; m < p.M; ++m)
                 for (int u = 0; u < n; ++u)
@@ -234,13 +239,17 @@ __global__ void __launch_bounds__(kThreads) gemv_q8_kernel(const __grid_constant
     for (int r0 = 0; r0 < S; r0 += p.rbuf, ++round) {
         const int n = min(p.rbuf, S - r0);
         if (tid == 0) {
+            if (round == 0) {
+                // warm L2 only; every copy waits for the previous kernel in the stream
+                for (int u = 0; u < n; ++u) tma_prefetch_2d(&wmap, (u0 + r0 + u) * (kQ8RowBytes / 2), rb * kRows);
+                pdl_wait();
+            }
             for (int u = 0; u < n; ++u) {
                 mbar_arrive_expect_tx(&s.bars[u], kQ8Tile);
                 // the map's elements are 2 bytes: 136 per 272-byte period
                 tma_load_2d(s.tiles + (size_t)u * kQ8Tile, &wmap, &s.bars[u], (u0 + r0 + u) * (kQ8RowBytes / 2),
                             rb * kRows);
             }
-            if (round == 0) pdl_wait();
             // raw x of unit u lands at float 16 of its 272-float region
             mbar_arrive_expect_tx(s.xbar, (uint32_t)(p.M * n * 1024));
             for (int m = 0; m < p.M; ++m)

@@ -38,6 +38,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstddef>
 #include <cmath>
@@ -318,6 +319,25 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             if (++islot == D) islot = 0;
         }
     };
+    // The previous kernel in the stream may still be writing what this one
+    // reads (x, and W too if a caller rewrites weights in place), so every copy
+    // is issued after the wait.  Before it, only L2 is warmed with this warp's
+    // first tiles of stage 0 (a prefetch never decides what a copy reads).
+    if (lane == 0) {
+        const StageDesc* d0 = p.table ? p.table : &inl;
+        const Groups g0 = cta_groups(part[0]);
+        const int U0 = infos[0].units;
+        int t, tend;
+        warp_run<W>(g0, U0, warp, t, tend);
+        for (int k = 0; k < D && t < tend; ++k) {
+            const int gi = t / U0, u = t - gi * U0;
+            int seg, row, nrows;
+            group_at(&infos[0], g0, gi, seg, row, nrows);
+            tma_prefetch_2d(&d0->maps[seg], u * B::kElems, row);
+            t += min(min(B::kNsb, U0 - u), tend - t);
+        }
+    }
+    pdl_wait();
     refill();
 
     // x' placement of the lane's 4 consecutive columns 4l .. 4l+3 of a
@@ -362,9 +382,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         if (s + kInfoSlots - 1 < p.nstages && warp == W - 1 && lane < kInfoVec)
             cp_async_16(reinterpret_cast<int4*>(infos + (s + kInfoSlots - 1) % kInfoSlots) + lane,
                         reinterpret_cast<const int4*>(&p.table[s + kInfoSlots - 1].info) + lane);
-        if (s == 0) {
-            pdl_wait();   // x may come from the previous kernel in the stream
-        } else {
+        if (s > 0) {
             // every CTA has finished stage s-1 (its outputs are visible)
             if (tid == 0) wait_count(p.counter, s * (int)gridDim.x, p.status);
             __syncthreads();
@@ -732,12 +750,16 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
 // ------------------------------------------------------------------ host ----
 
 int num_sms() {
-    static int sms[64] = {};
+    static std::atomic<int> sms[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 1;
-    if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    return sms[dev] > 0 ? sms[dev] : 1;
+    int n = sms[dev].load(std::memory_order_relaxed);
+    if (!n) {
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        sms[dev].store(n, std::memory_order_relaxed);
+    }
+    return n > 0 ? n : 1;
 }
 
 int mmax_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : 4; }
@@ -838,14 +860,20 @@ int make_stage(int type, int n, const void* const* W, const int64_t* rows, int64
 template <int K, int MMAX, int W>
 int launch_t(const StageDesc& inl, const ChainParams& p, cudaStream_t stream, size_t smem, bool cooperative) {
     auto kernel = rows_kernel<K, MMAX, W>;
-    static int configured[64] = {};   // largest dynamic smem set so far, per device
+    // largest dynamic smem set so far, per device; host threads may launch
+    // concurrently, so the check is atomic and the update serialised
+    static std::atomic<int> configured[64] = {};
+    static std::mutex update;
     int dev = 0;
     cudaGetDevice(&dev);
     cudaError_t e = cudaSuccess;
-    if (dev < 0 || dev >= 64 || configured[dev] < (int)smem) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        if (dev >= 0 && dev < 64) configured[dev] = (int)smem;
+    if (dev < 0 || dev >= 64 || configured[dev].load(std::memory_order_acquire) < (int)smem) {
+        std::lock_guard<std::mutex> lock(update);
+        if (dev < 0 || dev >= 64 || configured[dev].load(std::memory_order_relaxed) < (int)smem) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            if (dev >= 0 && dev < 64) configured[dev].store((int)smem, std::memory_order_release);
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)num_sms());
@@ -1040,9 +1068,22 @@ extern "C" int ggq_chain_run(const ggq_chain* c, void* stream) {
 extern "C" int ggq_chain_reset(ggq_chain* c) {
     clear_error();
     if (!c) return fail(GGQ_EINVAL, "ggq_chain_reset: NULL chain");
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (c->device >= 0 && c->device != prev) {
+        cudaError_t e = cudaSetDevice(c->device);
+        if (e != cudaSuccess) return cuda_fail(e, "ggq_chain_reset: set device");
+    }
+    // the counter, and the device status word: while it is set, every bounded
+    // wait of this device gives up after a few polls, so a run after a reset
+    // that left it set would read stage inputs before they are written
+    int rc = GGQ_OK;
     cudaError_t e = cudaMemset(c->counter, 0, sizeof(int));
-    if (e != cudaSuccess) return cuda_fail(e, "ggq_chain_reset");
-    return GGQ_OK;
+    if (e != cudaSuccess) rc = cuda_fail(e, "ggq_chain_reset");
+    int status = 0;
+    if (rc == GGQ_OK) rc = read_and_clear_status(&status);
+    if (c->device >= 0 && c->device != prev && prev >= 0) cudaSetDevice(prev);
+    return rc;
 }
 
 extern "C" void ggq_chain_free(ggq_chain* c) {

@@ -243,10 +243,14 @@ int payload_bytes(int32_t type, uint64_t ne0, uint64_t n, uint64_t* out) {
     switch (type) {
     case GGQ_F32: bytes = 4; break;
     case GGQ_F16: bytes = 2; break;
-    case GGQ_Q4_0: per = 32; bytes = 18; break;    // "Q4_0 ... 2 + 16 = 18 bytes"
-    case GGQ_Q8_0: per = 32; bytes = 34; break;    // "2 + 32 = 34 bytes per 32 weights"
-    case GGQ_Q4_K: per = 256; bytes = 144; break;  // "Q4_K costs 144 bytes per 256 weights"
-    case GGQ_Q6_K: per = 256; bytes = 210; break;  // bits/weight table: 210 B / 256
+    // block sizes from "GGUF: The File Format Powering Local LLM Inference",
+    // "What is quantization (in GGUF)" and its bits-per-weight table: an fp16
+    // scale plus 32 one-byte codes (Q8_0) or 16 bytes of nibbles (Q4_0); 4.5
+    // bits a weight for Q4_K and 6.5625 for Q6_K over 256-weight super-blocks
+    case GGQ_Q4_0: per = 32; bytes = 18; break;
+    case GGQ_Q8_0: per = 32; bytes = 34; break;
+    case GGQ_Q4_K: per = 256; bytes = 144; break;
+    case GGQ_Q6_K: per = 256; bytes = 210; break;
     default: *out = 0; return GGQ_ETYPE;
     }
     if (ne0 % per) { *out = 0; return GGQ_EFORMAT; }

@@ -18,6 +18,7 @@
 //               reaches only its own quarter of the 128 TMEM lanes) and store Y.
 // Every wait is bounded (ptx.cuh: mbar_wait); a timeout is recorded in the device
 // status word and the kernel runs to completion without the data.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -180,8 +181,13 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
     pdl_launch_dependents();
 
     if (warp == 0) {
-        // weights do not depend on the previous kernel: no wait before streaming them
         if (lane == 0) {
+            // the previous kernel in the stream may still be writing W (a caller
+            // that rewrites weights in place): warm L2 with the first raw stages,
+            // then wait before any copy
+            for (int sb = 0; sb < nsb && sb < kRawStages; ++sb)
+                tma_prefetch_2d(&wmap, sb * (Q4K ? 144 : 136), row0);
+            pdl_wait();
             for (int sb = 0; sb < nsb; ++sb) {
                 const int r = sb % kRawStages;
                 mbar_wait(&empty_raw[r], ((sb / kRawStages) & 1) ^ 1, p.status);
@@ -356,14 +362,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 template <bool Q4K>
 int launch_t(const CUtensorMap& wmap, const SmallParams& p, cudaStream_t stream) {
-    static int configured[64] = {};
+    static std::atomic<int> configured[64] = {};   // set once per device; the value set never changes
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(smallm_kernel<Q4K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        if (dev >= 0 && dev < 64) configured[dev] = 1;
+        if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((p.rows + kTileRows - 1) / kTileRows));

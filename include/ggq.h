@@ -287,8 +287,11 @@ int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chain_stage* st
  */
 int ggq_chain_run(const ggq_chain* chain, void* stream);
 
-/* ggq_chain_reset -- zero the chain's stage counter (after a run that timed
- * out).  Synchronous. */
+/* ggq_chain_reset -- after a run that timed out: zero the chain's stage
+ * counter and clear the device status word of the chain's device (read
+ * ggq_device_status first to learn what happened; while the status word is
+ * set, every bounded wait on that device gives up after a few polls).  No run
+ * may be pending on the device.  Synchronous. */
 int ggq_chain_reset(ggq_chain* chain);
 
 /* ggq_chain_free -- release a chain (NULL is ignored).  No run may be pending. */
@@ -310,7 +313,7 @@ void ggq_chain_free(ggq_chain* chain);
  * Arguments and result as for ggq_gemv, within these limits: type GGQ_Q8_0,
  * GGQ_Q4_K or GGQ_Q4_0 (the last two with cols >= 768), cols a multiple of 256, M in 1..4, x' of one activation row in
  * shared memory (cols up to about 40000 at M = 1); other shapes fail with
- * GGQ_EINVAL.  Calls may overlap on the GPU and may be captured into graphs.
+ * GGQ_EINVAL.  Calls may overlap on the GPU: they share no device memory.
  */
 int ggq_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
                      void* stream);

@@ -222,9 +222,12 @@ def decode_q6_k_block(blk):
 
 def tolerance_ok(y_dev: np.ndarray, y_ref: np.ndarray, abs_ref: np.ndarray,
                  rel: float = 1e-3, abs_: float = 1e-6):
-    """|y - y_ref| <= rel * sum|w x| + abs_, elementwise. Returns (ok, worst ratio)."""
+    """|y - y_ref| <= rel * sum|w x| + abs_, elementwise. Returns (ok, worst ratio).
+
+    Every element must be within its bound; a NaN or inf anywhere in y_dev
+    fails, and the worst ratio is then NaN or inf too (never hidden)."""
     err = np.abs(np.asarray(y_dev, dtype=np.float64) - y_ref)
     bound = rel * abs_ref + abs_
     ratio = err / bound
-    worst = float(np.nanmax(ratio)) if ratio.size else 0.0
+    worst = float(np.max(ratio)) if ratio.size else 0.0
     return bool(np.all(err <= bound)), worst

@@ -320,9 +320,8 @@ def test_load_file_to_device_and_multiply(env, tmp_path):
 @pytest.mark.parametrize("qtype,rows,cols,M", [(12, 33, 4096, 1), (8, 100, 2048, 1), (12, 1000, 11008, 2),
                                                (8, 4000, 4096, 4)])
 def test_gemv_repeated_calls_are_bit_identical(env, qtype, rows, cols, M):
-    """Row blocks split between warps are finished through a workspace whose
-    counters must be back at zero after every launch: repeated calls agree bit
-    for bit."""
+    """Groups of rows cut between warps are added in a fixed warp order, so
+    repeated calls agree bit for bit (and with the oracle within the bound)."""
     torch, ggq = env
     W = weights(qtype, rows, cols, stream=50)
     x = xs(M, cols, stream=51)
@@ -345,7 +344,7 @@ def test_gemv_in_cuda_graph(env):
     y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        ggq.gemv(12, Wd, rows, cols, xd, y)       # first call on this stream sets up its workspace
+        ggq.gemv(12, Wd, rows, cols, xd, y)       # outside capture first: kernel attributes are set once
     s.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
@@ -355,3 +354,37 @@ def test_gemv_in_cuda_graph(env):
         g.replay()
         torch.cuda.synchronize()
         assert_close(y.cpu().numpy(), y_ref, a_ref, "graph replay")
+
+
+@pytest.mark.parametrize("qtype,rows,cols,M", [(12, 4096, 4096, 1), (8, 2048, 4096, 3), (12, 300, 512, 2),
+                                               (8, 1024, 4096, 8), (12, 1024, 4096, 16)])
+def test_gemv_reads_weights_written_by_the_previous_kernel(env, qtype, rows, cols, M):
+    """A device kernel (an element-wise OR, not a copy) rewrites W on the same
+    stream right before the GEMV: the GEMV must read the new weights.  The
+    shapes reach the streaming kernel (M <= 4), the narrow-shape cluster
+    kernel and the tensor-core small-batch kernel (M 8, 16)."""
+    torch, ggq = env
+    W_old = weights(qtype, rows, cols, stream=60)
+    W_new = weights(qtype, rows, cols, stream=61)
+    x = xs(M, cols, stream=62)
+    y_ref, a_ref = oracle.gemv(qtype, W_new, rows, cols, x)
+    Wd = _dev(torch, W_old)
+    W_src = _dev(torch, W_new)
+    zero = torch.zeros((), dtype=torch.uint8, device="cuda")
+    xd = _dev(torch, x)
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        Wd.copy_(_dev(torch, W_old))
+        y = torch.full((M, rows), float("nan"), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        torch.bitwise_or(W_src, zero, out=Wd)      # a kernel writes W
+        if call == 0:
+            rc = ggq.ggq_gemv(qtype, Wd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr(), M, stream)
+        elif M <= 4 and cols % 256 == 0 and cols >= 768:
+            rc = ggq.ggq_gemv_noalloc(qtype, Wd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr(), M, stream)
+        else:
+            continue
+        ggq.check(rc, "gemv after a kernel wrote W")
+        torch.cuda.synchronize()
+        assert ggq.device_status() == 0
+        assert_close(y.cpu().numpy(), y_ref, a_ref, f"call {call}")

@@ -284,97 +284,35 @@ class DecodePass:
 
 # ----------------------------------------------- a pass planned from a file ----
 
-# the GEMV stages of a layer in dependency order, by GGUF tensor name
-LAYER_STAGES = (("attn_q", "attn_k", "attn_v"), ("attn_output",), ("ffn_gate", "ffn_up"), ("ffn_down",))
-CHAIN_TYPES = (2, 8, 12)   # the types the chain kernel streams: Q4_0, Q8_0, Q4_K
-
-
-def plan_from_table(model, layers: int):
-    """The decode pass of a loaded file from its tensor table alone: per layer
-    the stages [q,k,v], [o], [gate,up], [down], then the head.  A stage whose
-    matrices differ in type is split by type, in order.  Returns a list of
-    (type, [tensor info])."""
-    stages = []
-    for L in range(layers):
-        for names in LAYER_STAGES:
-            groups = {}
-            for n in names:
-                t = model.find(f"blk.{L}.{n}.weight")
-                groups.setdefault(t["type"], []).append(t)
-            stages += list(groups.items())
-    head = model.find("output.weight")
-    stages.append((head["type"], [head]))
-    return stages
-
-
-def segments(types):
-    """Launches for stages of the given types, in order: each run of
-    consecutive stages of one type the chain kernel streams is one chain
-    launch, every other stage a launch of its own.  Returns [(start, end,
-    is_chain)] over stage indices."""
-    out, i = [], 0
-    while i < len(types):
-        if types[i] in CHAIN_TYPES:
-            j = i
-            while j < len(types) and types[j] == types[i]:
-                j += 1
-            out.append((i, j, True))
-            i = j
-        else:
-            out.append((i, i + 1, False))
-            i += 1
-    return out
-
-
 class FilePass:
-    """A decode pass planned from a loaded file (plan_from_table): each run of
-    consecutive stages of one type the chain kernel streams is ONE ggq_chain
-    launch; every other stage (Q6_K, F32) is one ggq_gemv / ggq_gemv_multi
-    launch.  Every stage reads its own seeded x (as in DecodePass)."""
+    """The library's planned pass (gguf_block_quantized_q8_gb300.plan) of a loaded
+    file, every stage reading its own seeded x (as in DecodePass) and writing
+    NaN-initialised outputs."""
 
     def __init__(self, model, layers, torch, ggq, synth, x_stream0=9000):
-        self.torch, self.ggq = torch, ggq
-        self.plan, self.keep = [], []
-        self.weight_bytes = 0
+        from gguf_block_quantized_q8_gb300 import plan as P
+        stages = P.plan_from_table(model, layers)
+        self.plan, xs, ys = [], [], []
         self.type_bytes = {}   # weight bytes per tensor type
-        for si, (qtype, ts) in enumerate(plan_from_table(model, layers)):
+        for si, (qtype, ts) in enumerate(stages):
             cols = ts[0]["ne"][0]
             rows = [t["ne"][1] for t in ts]
             x = torch.from_numpy(synth.normal_f32(cols, x_stream0 + si)).cuda()
-            ys = [torch.full((r,), float("nan"), device="cuda") for r in rows]
-            self.keep += [x] + ys
-            self.weight_bytes += sum(t["nbytes"] for t in ts)
+            y = [torch.full((r,), float("nan"), device="cuda") for r in rows]
+            xs.append(x)
+            ys.append(y)
             self.type_bytes[qtype] = self.type_bytes.get(qtype, 0) + sum(t["nbytes"] for t in ts)
-            self.plan.append(dict(qtype=qtype, W=[t["data"] for t in ts], rows=rows, cols=cols, x=x, ys=ys,
-                                  names=[t["name"] for t in ts], x_stream=x_stream0 + si))
-        self.calls, self.chains = [], []
-        for i, j, is_chain in segments([p["qtype"] for p in self.plan]):
-            if is_chain:
-                rc, h = ggq.ggq_chain_create(self.plan[i]["qtype"], 1,
-                                             [(q["W"], q["rows"], q["cols"], q["x"].data_ptr(),
-                                               [y.data_ptr() for y in q["ys"]]) for q in self.plan[i:j]])
-                ggq.check(rc, "ggq_chain_create")
-                self.chains.append(h)
-                self.calls.append(("chain", h))
-            else:
-                self.calls.append(("stage", self.plan[i]))
+            self.plan.append(dict(qtype=qtype, rows=rows, cols=cols, x=x, ys=y, names=[t["name"] for t in ts],
+                                  x_stream=x_stream0 + si))
+        self.dp = P.DecodePass(stages, xs, ys)
+        self.weight_bytes = self.dp.weight_bytes
+        self.calls, self.chains = self.dp.calls, self.dp.chains
 
     def run(self, sp):
-        ggq = self.ggq
-        for kind, c in self.calls:
-            if kind == "chain":
-                ggq.check(ggq.ggq_chain_run(c, sp), "ggq_chain_run")
-            elif len(c["W"]) == 1:
-                ggq.check(ggq.ggq_gemv(c["qtype"], c["W"][0], c["rows"][0], c["cols"], c["x"].data_ptr(),
-                                       c["ys"][0].data_ptr(), 1, sp), "ggq_gemv")
-            else:
-                ggq.check(ggq.ggq_gemv_multi(c["qtype"], c["W"], c["rows"], c["cols"], c["x"].data_ptr(),
-                                             [y.data_ptr() for y in c["ys"]], 1, sp), "ggq_gemv_multi")
+        self.dp.run(sp)
 
     def close(self):
-        for h in self.chains:
-            self.ggq.ggq_chain_free(h)
-        self.chains = []
+        self.dp.close()
 
 
 def q4km_file_pass(torch, ggq, synth, stream, steps: int = 20, layers: int = 32):

@@ -278,42 +278,52 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     // stage, next tile, end of the run; (group, SB) of the next tile and the
     // group's matrix and first row, advanced without dividing
     int cs = -1, ct = 0, ct1 = 0, cU = 1, cgi = 0, cu = 0, cseg = 0, crow = 0;
+    int cnext = 0;                   // first local group of matrix cseg + 1 (groups advance by one)
     const StageDesc* csd = &inl;
     const StageInfo* cinf = infos;   // the fields of stage cs
     int scur = 0;                    // stage the CTA is in: slots hold scur .. scur + kInfoSlots - 2
     Groups cg{};
     int inflight = 0;   // copies issued and not yet consumed
     int islot = 0;      // ring slot of the next copy
+    const uint64_t wpol = l2_evict_first_policy();   // weights are read once per pass
+    auto next_seg_start = [&]() {
+        return cseg + 1 < cinf->nseg ? cinf->gstart[cseg + 1] - cg.g0 : 0x7fffffff;
+    };
+    // the next stage in which this warp has tiles; false past the last
+    auto next_stage = [&]() {
+        while (ct == ct1) {
+            if (++cs >= p.nstages) return false;
+            csd = p.table ? p.table + cs : &inl;
+            cinf = cs <= scur + kInfoSlots - 2 ? infos + cs % kInfoSlots : &csd->info;
+            cg = cta_groups(cs < kPartMax ? part[cs] : cta_span(cinf, blockIdx.x, gridDim.x));
+            warp_run<W>(cg, cinf->units, warp, ct, ct1);
+        }
+        cU = cinf->units;
+        cgi = ct / cU;
+        cu = ct - cgi * cU;
+        int nrows;
+        group_at(cinf, cg, cgi, cseg, crow, nrows);
+        cnext = next_seg_start();
+        return true;
+    };
     auto refill = [&]() {   // keep up to D copies in flight or resident
         while (inflight < D) {
-            if (ct == ct1) {
-                while (ct == ct1 && cs < p.nstages) {   // next stage in which this warp has tiles
-                    if (++cs == p.nstages) break;
-                    csd = p.table ? p.table + cs : &inl;
-                    cinf = cs <= scur + kInfoSlots - 2 ? infos + cs % kInfoSlots : &csd->info;
-                    cg = cta_groups(cs < kPartMax ? part[cs] : cta_span(cinf, blockIdx.x, gridDim.x));
-                    warp_run<W>(cg, cinf->units, warp, ct, ct1);
-                }
-                if (cs >= p.nstages) break;
-                cU = cinf->units;
-                cgi = ct / cU;
-                cu = ct - cgi * cU;
-                int nrows;
-                group_at(cinf, cg, cgi, cseg, crow, nrows);
-            }
+            if (ct == ct1 && !next_stage()) break;
             const int nv = min(min(B::kNsb, cU - cu), ct1 - ct);
-            if (lane == 0) {
-                fence_proxy_async_smem();   // this warp's reads of the buffer come before the copy's writes
-                mbar_arrive_expect_tx(&full[islot], B::kCopy);
-                tma_load_2d(ring + (size_t)islot * B::kTile, &csd->maps[cseg], &full[islot], cu * B::kElems, crow);
-            }
+            tma_issue_2d(lane == 0, ring + (size_t)islot * B::kTile, &csd->maps[cseg], &full[islot], cu * B::kElems,
+                         crow, B::kCopy, wpol);
             ct += nv;
             cu += nv;
-            if (cu == cU && ct < ct1) {   // next group of this run
+            if (cu == cU && ct < ct1) {   // next group of this run: same matrix, 16 rows on, or the next matrix
                 cu = 0;
                 ++cgi;
-                int nrows;
-                group_at(cinf, cg, cgi, cseg, crow, nrows);
+                if (cgi == cnext) {
+                    ++cseg;
+                    crow = 0;
+                    cnext = next_seg_start();
+                } else {
+                    crow += kGroupRows;
+                }
             }
             ++inflight;
             if (++islot == D) islot = 0;

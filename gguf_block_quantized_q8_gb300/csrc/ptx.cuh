@@ -82,6 +82,43 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// An L2 cache policy that evicts the lines a copy brings in first: for data
+// streamed once (weights), so that it does not push out data read again soon
+// (activations).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_2d with an L2 cache policy (l2_evict_first_policy).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// One 2-D tile copy issued by the lanes with `issue` set (normally one lane of
+// a warp), as a single predicated block so the warp never branches around it:
+// order this thread's earlier generic reads of the destination before the
+// copy's writes, arm `bar` with the copy's bytes, start the copy (L2 policy
+// `policy`).
+__device__ __forceinline__ void tma_issue_2d(bool issue, void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                             uint32_t bytes, uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+        "@p fence.proxy.async.shared::cta;\n\t"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%2], %6;\n\t"
+        "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%1], [%3, {%4, %5}], [%2], %7;\n\t}" ::"r"((uint32_t)issue),
+        "r"(smem_u32(dst)), "r"(smem_u32(bar)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bytes),
+        "l"(policy)
+        : "memory");
+}
+
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -220,6 +220,52 @@ def decode_q6_k_block(blk):
     return default().decode_q6_k_block(blk)
 
 
+def _widen_bf16(X_bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64, exactly (the pattern is the top half of an
+    IEEE binary32)."""
+    b = np.ascontiguousarray(X_bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def gemv_dense(qtype, W, rows, cols, x, chunk=16384):
+    """The same quantities as gemv -- y[m, r] = sum_c w[r, c] x[m, c] and
+    sum_c |w[r, c] x[m, c]| in float64 -- for full-size matrices: the weights
+    decoded exactly by the oracle (dequantize), widened to float64, then one
+    float64 matrix product per block of rows (the plain definition y = W x,
+    in another summation order than gemv's column loop)."""
+    W = _c(W, np.uint8).reshape(-1)
+    x64 = _c(x, np.float32).reshape(-1, cols).astype(np.float64)
+    M = x64.shape[0]
+    rb = row_bytes(qtype, cols)
+    y = np.empty((M, rows), dtype=np.float64)
+    ay = np.empty((M, rows), dtype=np.float64)
+    ax = np.abs(x64)
+    for r0 in range(0, rows, chunk):
+        n = min(chunk, rows - r0)
+        w = dequantize(qtype, W[r0 * rb:(r0 + n) * rb], n, cols).astype(np.float64)
+        y[:, r0:r0 + n] = x64 @ w.T
+        ay[:, r0:r0 + n] = ax @ np.abs(w).T
+    return y, ay
+
+
+def gemm_bf16_dense(qtype, W, rows, cols, X_bits, chunk=8192):
+    """gemm_bf16 for full-size matrices, as gemv_dense: decoded weights times
+    the exactly widened bf16 activations, in float64."""
+    W = _c(W, np.uint8).reshape(-1)
+    X64 = _widen_bf16(np.asarray(X_bits).reshape(-1, cols))
+    M = X64.shape[0]
+    rb = row_bytes(qtype, cols)
+    Y = np.empty((M, rows), dtype=np.float64)
+    aY = np.empty((M, rows), dtype=np.float64)
+    aX = np.abs(X64)
+    for r0 in range(0, rows, chunk):
+        n = min(chunk, rows - r0)
+        w = dequantize(qtype, W[r0 * rb:(r0 + n) * rb], n, cols).astype(np.float64)
+        Y[:, r0:r0 + n] = X64 @ w.T
+        aY[:, r0:r0 + n] = aX @ np.abs(w).T
+    return Y, aY
+
+
 def tolerance_ok(y_dev: np.ndarray, y_ref: np.ndarray, abs_ref: np.ndarray,
                  rel: float = 1e-3, abs_: float = 1e-6):
     """|y - y_ref| <= rel * sum|w x| + abs_, elementwise. Returns (ok, worst ratio).

@@ -1,19 +1,16 @@
-"""bench.py's pass planner on the CPU: the stages a file's tensor table gives
-(split by type in order) and the launches they make (runs of chain-kernel
+"""The library's pass planner (gguf_block_quantized_q8_gb300.plan) on the CPU:
+the stages a file's tensor table gives (split by type in order), the layer
+count from the metadata, and the launches they make (runs of chain-kernel
 types as one chain launch, every other stage on its own)."""
-import importlib.util
-import os
+import pytest
 
+import synth
 from synth import workloads as WL
-
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _bench():
-    spec = importlib.util.spec_from_file_location("bench_plan", os.path.join(ROOT, "bench.py"))
-    mod = importlib.util.module_from_spec(spec)
-    spec.loader.exec_module(mod)
-    return mod
+    from gguf_block_quantized_q8_gb300 import plan
+    return plan
 
 
 class FakeModel:
@@ -25,6 +22,12 @@ class FakeModel:
 
     def find(self, name):
         return self.t[name]
+
+    def tensors(self):
+        return list(self.t.values())
+
+    def kvs(self):
+        return [("general.architecture", 8, b"llama")]
 
 
 def test_plan_splits_stages_by_type_in_order():
@@ -55,3 +58,26 @@ def test_q4km_file_size_matches_the_pages():
     assert 4.85e9 < total < 4.95e9
     plan_types = [g.qtype for g in ts if g.rows > 1 and g.name != "token_embd.weight"]
     assert plan_types.count(14) == 16 * 2 + 1
+
+
+def test_block_count_from_metadata_and_table(tmp_path):
+    import gguf_block_quantized_q8_gb300 as ggq
+    from gguf_block_quantized_q8_gb300 import plan
+    # from the table alone
+    assert plan.block_count(FakeModel(3, 100)) == 3
+    # from the <arch>.block_count key of a real file (metadata-only load)
+    q4 = synth.weight_rows(12, 5, 2, 256)
+    head, offs, end = synth.gguf_header([("general.architecture", 8, "llama"), ("llama.block_count", 4, 7)],
+                                        [("blk.0.attn_q.weight", [256, 2], 12)])
+    blob = bytearray(end)
+    blob[offs[0]:offs[0] + q4.nbytes] = q4.tobytes()
+    with ggq.Model.from_bytes(head + bytes(blob), metadata_only=True) as m:
+        assert plan.block_count(m) == 7
+
+
+def test_decode_pass_checks_its_arguments():
+    from gguf_block_quantized_q8_gb300 import plan
+    with pytest.raises(ValueError):
+        plan.DecodePass([], [], [], M=5)
+    with pytest.raises(ValueError):
+        plan.DecodePass([(12, [dict(ne=[256, 2], data=0, nbytes=0)])], [], [])

@@ -1,11 +1,9 @@
 """GPU parity for a mixed-type decode pass planned from a file's tensor table:
 a 2-layer Q4_K_M-style GGUF (Q4_K matrices, Q6_K attn_v / ffn_down in layer 1,
 F32 norms, a Q6_K head of 32000 rows) written, loaded with ggq_load, planned by
-bench.py's FilePass (Q4_K runs as chain launches, Q6_K stages on their own) and
-run once; every stage's outputs checked on sampled rows against the oracle."""
-import importlib.util
-import os
-
+the library's planner (gguf_block_quantized_q8_gb300.plan: Q4_K runs as chain
+launches, Q6_K stages on their own) and run twice; every output row of every
+stage checked against the oracle."""
 import numpy as np
 import pytest
 
@@ -14,7 +12,6 @@ import synth
 from synth import workloads as WL
 
 pytestmark = pytest.mark.gpu
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module")
@@ -28,30 +25,31 @@ def env():
 
 def test_q4km_file_pass(env, tmp_path):
     torch, ggq = env
-    spec = importlib.util.spec_from_file_location("bench_fp", os.path.join(ROOT, "bench.py"))
-    bench = importlib.util.module_from_spec(spec)
-    spec.loader.exec_module(bench)
+    from gguf_block_quantized_q8_gb300 import plan as P
     layers, vocab = 2, 32000
     path = str(tmp_path / "q4km.gguf")
     ts = WL.write_q4km_file(path, layers, vocab)
     byname = {g.name: g for g in ts}
     with ggq.Model.load(path) as model:
-        fp = bench.FilePass(model, layers, torch, ggq, synth)
-        assert len(fp.chains) == 2 and len(fp.calls) == 5   # chain, v, chain, down, head
-        for _ in range(2):                                    # twice: chains reset their counters
-            fp.run(torch.cuda.current_stream().cuda_stream)
+        assert P.block_count(model) == layers
+        stages = P.plan_from_table(model)
+        xs, ys = [], []
+        for si, (qtype, tl) in enumerate(stages):
+            xs.append(torch.from_numpy(synth.normal_f32(tl[0]["ne"][0], 9000 + si)).cuda())
+            ys.append([torch.full((t["ne"][1],), float("nan"), device="cuda") for t in tl])
+        dp = P.DecodePass(stages, xs, ys)
+        assert len(dp.chains) == 2 and dp.launches == 5   # chain, v, chain, down, head
+        for _ in range(2):                                  # twice: chains reset their counters
+            dp.run()
             torch.cuda.synchronize()
             assert ggq.device_status() == 0
-        rng = np.random.default_rng(3)
-        for p in fp.plan:
-            x = synth.normal_f32(p["cols"], p["x_stream"]).reshape(1, -1)
-            for name, rows, y in zip(p["names"], p["rows"], p["ys"]):
-                g = byname[name]
-                assert g.qtype == p["qtype"] and g.rows == rows and g.cols == p["cols"]
-                rs = np.unique(np.r_[0, rows - 1, rng.integers(0, rows, 40)])
-                W = np.concatenate([synth.weight_rows(g.qtype, g.stream, 1, g.cols, row0=int(r)) for r in rs])
-                y_ref, a_ref = oracle.gemv(g.qtype, W, len(rs), g.cols, x)
-                got = y.cpu().numpy()[rs].reshape(1, -1)
-                ok, worst = oracle.tolerance_ok(got, y_ref, a_ref)
-                assert ok, f"{name}: worst error / bound {worst:.3g}"
-        fp.close()
+        for si, (qtype, tl) in enumerate(stages):
+            x = xs[si].cpu().numpy().reshape(1, -1)
+            for t, y in zip(tl, ys[si]):
+                g = byname[t["name"]]
+                assert g.qtype == qtype and g.rows == t["ne"][1] and g.cols == t["ne"][0]
+                W = synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)
+                y_ref, a_ref = oracle.gemv_dense(g.qtype, W, g.rows, g.cols, x)
+                ok, worst = oracle.tolerance_ok(y.cpu().numpy().reshape(1, -1), y_ref, a_ref)
+                assert ok, f"{t['name']}: worst error / bound {worst:.3g}"
+        dp.close()

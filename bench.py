@@ -45,7 +45,52 @@ def args_parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-config kernel timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES),
+                    help="run one configuration's GEMV a few times and exit (a small command to profile)")
+    ap.add_argument("--M", type=int, default=1, help="activation rows for --kernel")
     return ap.parse_args()
+
+
+# one GEMV configuration each: (workload attribute, description)
+KERNEL_SHAPES = {
+    "q8_0_head": ("HEAD", "Q8_0 4096 -> 128256 output head of the Llama-8B-shaped pass"),
+    "q6_k_14336x4096": ("Q6K_GEMV", "Q6_K 14336 x 4096"),
+    "q6_k_4096x14336": ("Q6K_DOWN_GEMV", "Q6_K 4096 x 14336 (ffn_down shape)"),
+    "q8_0_14336x4096": ("CFG4", "Q8_0 14336 x 4096"),
+    "q4_0_14336x4096": ("Q40_GEMV", "Q4_0 14336 x 4096"),
+}
+
+
+def run_kernel(a):
+    """Five launches of one configuration's ggq_gemv (seeded weights, random x)
+    after one warm-up; prints the per-launch time of the last five."""
+    import torch
+    import gguf_block_quantized_q8_gb300 as ggq
+    import synth
+    from synth import workloads as WL
+    attr, desc = KERNEL_SHAPES[a.kernel]
+    g = WL.llama8b_pass(1)[-1] if attr == "HEAD" else getattr(WL, attr)
+    torch.cuda.set_device(0)
+    W = torch.from_numpy(synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)).cuda()
+    x = torch.randn(a.M, g.cols, device="cuda")
+    y = torch.empty(a.M, g.rows, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+
+    def once():
+        ggq.check(ggq.ggq_gemv(g.qtype, W.data_ptr(), g.rows, g.cols, x.data_ptr(), y.data_ptr(), a.M, s), "gemv")
+    once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / 5
+    nb = g.rows * synth.row_bytes(g.qtype, g.cols)
+    print(json.dumps({"kernel": a.kernel, "desc": desc, "M": a.M, "us": round(us, 2),
+                      "GB_s": round(nb / us / 1e3, 1), "status": ggq.device_status()}))
+    return 0
 
 
 # ------------------------------------------------------------ distributed ----
@@ -197,6 +242,9 @@ class DecodePass:
         rc, self.chain = ggq.ggq_chain_create(12, 1, [(s["W"], s["rows"], s["cols"], s["x"], s["y"]) for s in self.q4])
         ggq.check(rc, "ggq_chain_create")
         self.q4_bytes = sum(s["nbytes"] + s["io_bytes"] for s in self.q4)
+        # the pass's result: the output head's logits (the last stage's y)
+        self.head_rows = self.stages[-1]["rows"][0]
+        self.head_y = self.y_dev[ny - self.head_rows:]
 
     def launch_stage(self, st, stream_ptr):
         ggq = self.ggq
@@ -384,89 +432,217 @@ def roofline_chain(torch, dp, stream, steps):
     return dp.q4_bytes, ms * 1e-3
 
 
-def cpu_oracle_sample(budget_s: float, layers: int = 32):
-    """The oracle on a bounded sample of the decode pass: whole rows drawn from
-    every tensor of the stack in turn (regenerated from their counters) until the
-    time budget is spent.  Returns (GB/s of weight bytes, description, seconds)."""
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _on_threads(calls, threads: int) -> float:
+    """Run the oracle calls (callables) on `threads` Python threads -- the
+    oracle's C functions release the interpreter lock -- and return the wall
+    seconds."""
+    import concurrent.futures as cf
+    t0 = time.perf_counter()
+    if threads <= 1:
+        for c in calls:
+            c()
+    else:
+        with cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda c: c(), calls))
+    return time.perf_counter() - t0
+
+
+def _row_jobs(qtype, W, rows, cols, x, pieces, gemm=False):
+    """The oracle over `rows` rows of W as `pieces` calls on contiguous row blocks."""
+    import oracle
+    rb = oracle.row_bytes(qtype, cols)
+    jobs = []
+    for k in range(pieces):
+        r0, r1 = rows * k // pieces, rows * (k + 1) // pieces
+        if r1 > r0:
+            Wk = W[r0 * rb:r1 * rb]
+            if gemm:
+                jobs.append(lambda Wk=Wk, n=r1 - r0: oracle.gemm_bf16(qtype, Wk, n, cols, x))
+            else:
+                jobs.append(lambda Wk=Wk, n=r1 - r0: oracle.gemv(qtype, Wk, n, cols, x))
+    return jobs
+
+
+def cpu_oracle_jobs(budget_s: float, layers: int = 32):
+    """A bounded sample of the decode pass for the oracle: whole rows drawn
+    from every tensor of the stack in turn (regenerated from their counters),
+    64 rows per tensor, about budget_s of single-thread oracle work.  Returns
+    (oracle calls, weight bytes, description)."""
     import numpy as np
     import oracle
     import synth
     from synth import workloads as WL
     gem = WL.llama8b_pass(layers)
     rng = np.random.default_rng(0)
-    done_bytes, t_used, n_rows, n_tensors = 0, 0.0, 0, 0
-    i = 0
-    t_start = time.perf_counter()
-    while t_used < budget_s and time.perf_counter() - t_start < 3 * budget_s:
+    budget_bytes = budget_s * 0.4e9   # the oracle's single-thread rate, about 0.4 GB/s of weights
+    jobs, done_bytes, n_rows, i = [], 0, 0, 0
+    while done_bytes < budget_bytes:
         g = gem[i % len(gem)]
         i += 1
-        rows = 8
+        rows = 64
         r0 = int(rng.integers(0, g.rows - rows + 1))
         W = synth.weight_rows(g.qtype, g.stream, rows, g.cols, row0=r0)
         x = synth.normal_f32(g.cols, g.x_stream).reshape(1, -1)
-        t0 = time.perf_counter()
-        oracle.gemv(g.qtype, W, rows, g.cols, x)
-        t_used += time.perf_counter() - t0
+        jobs.append(lambda W=W, g=g, x=x, rows=rows: oracle.gemv(g.qtype, W, rows, g.cols, x))
         done_bytes += W.nbytes
         n_rows += rows
-        n_tensors += 1
-    desc = (f"{n_rows} whole rows ({done_bytes / 1e6:.1f} MB of Q4_K/Q8_0 weights) sampled 8 at a time from "
-            f"{n_tensors} tensors of the {layers}-layer pass, oracle decode + fp64 dot products, one thread")
-    return done_bytes / t_used / 1e9, desc, t_used
+    desc = (f"{n_rows} whole rows ({done_bytes / 1e6:.1f} MB of Q4_K/Q8_0 weights) sampled 64 at a time from "
+            f"{i} tensors of the {layers}-layer pass, oracle decode + fp64 dot products (generation not timed)")
+    return jobs, done_bytes, desc
+
+
+def cpu_oracle_sample(budget_s: float, layers: int = 32, threads: int = 1):
+    """The oracle on a bounded sample of the pass (cpu_oracle_jobs) on
+    `threads` threads.  Returns (GB/s of weight bytes, description, seconds)."""
+    jobs, nbytes, desc = cpu_oracle_jobs(budget_s, layers)
+    used = _on_threads(jobs, threads)
+    return nbytes / used / 1e9, f"{desc}, {threads} thread(s)", used
+
+
+def cpu_oracle_configs(threads: int):
+    """The oracle per configuration, single-threaded and on `threads` threads
+    (row blocks of the same matrices): cfg1 and cfg2 whole, cfg4 on 1024 of its
+    14336 rows at every M, cfg5 on 16 of its 14336 rows for all 512 tokens.
+    GB/s of weight bytes (TFLOP/s for cfg5).  Generation is not timed."""
+    import numpy as np
+    import synth
+    from synth import workloads as WL
+    out = {}
+
+    def both(name, qtype, W, rows, cols, x, work, unit, gemm=False):
+        r = {}
+        for n in (1, threads):
+            t = _on_threads(_row_jobs(qtype, W, rows, cols, x, max(n, 1) * (4 if n > 1 else 1), gemm), n)
+            r["threads_%d" % n] = round(work / t / (1e12 if unit == "TFLOP/s" else 1e9), 6 if unit == "TFLOP/s" else 4)
+        r["unit"] = unit
+        out[name] = r
+
+    g = WL.CFG1[0]
+    W = synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)
+    both("cfg1_q8_0_2048x2048", g.qtype, W, g.rows, g.cols, synth.normal_f32(g.cols, g.x_stream).reshape(1, -1),
+         W.nbytes, "GB/s")
+    # cfg2: the 7 projections one after another
+    tot, t1, tn = 0, 0.0, 0.0
+    for g in WL.CFG2:
+        W = synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)
+        x = synth.normal_f32(g.cols, g.x_stream).reshape(1, -1)
+        t1 += _on_threads(_row_jobs(g.qtype, W, g.rows, g.cols, x, 1), 1)
+        tn += _on_threads(_row_jobs(g.qtype, W, g.rows, g.cols, x, 4 * threads), threads)
+        tot += W.nbytes
+    out["cfg2_smollm3_layer_q4_k"] = {"threads_1": round(tot / t1 / 1e9, 4),
+                                      "threads_%d" % threads: round(tot / tn / 1e9, 4), "unit": "GB/s"}
+    g = WL.CFG4
+    rows = 1024
+    W = synth.weight_rows(g.qtype, g.stream, rows, g.cols)
+    res = {}
+    for M in WL.CFG4_M:
+        x = synth.normal_f32(M * g.cols, g.x_stream).reshape(M, -1)
+        r = {}
+        for n in (1, threads):
+            t = _on_threads(_row_jobs(g.qtype, W, rows, g.cols, x, 4 * n if n > 1 else 1), n)
+            r["threads_%d" % n] = round(W.nbytes / t / 1e9, 4)
+        res[str(M)] = r
+    out["cfg4_q8_0_14336x4096"] = {"rows_sampled": rows, "unit": "GB/s", **res}
+    g = WL.CFG5
+    rows = 16
+    W = synth.weight_rows(g.qtype, g.stream, rows, g.cols)
+    X = synth.normal_bf16(WL.CFG5_M * g.cols, g.x_stream).reshape(WL.CFG5_M, g.cols)
+    both("cfg5_prefill_q4_k_512x14336x4096", g.qtype, W, rows, g.cols, X, 2.0 * WL.CFG5_M * rows * g.cols,
+         "TFLOP/s", gemm=True)
+    out["cfg5_prefill_q4_k_512x14336x4096"]["rows_sampled"] = rows
+    del np
+    return out
 
 
 # -------------------------------------------------------------- extras ----
 
-def kernel_time(torch, fn, stream, iters):
-    """Per-launch time of fn (a C-ABI call on `stream`) from a CUDA graph of
-    `iters` launches."""
+L2_BYTES = 129 * 1000 * 1000          # GB300 L2
+ROTATE_BYTES = 4 * L2_BYTES           # distinct weight bytes cycled through between reuses
+MIN_LAUNCHES = 200
+
+
+def copies_for(nbytes: int, cap: int = 160) -> int:
+    """Weight copies to cycle so that one pass over them moves at least
+    4 x L2 of distinct bytes (each launch reads its weights cold)."""
+    return max(1, min(cap, -(-ROTATE_BYTES // max(1, nbytes))))
+
+
+def kernel_time(torch, fn, stream, per_graph, min_launches=MIN_LAUNCHES, min_replays=5):
+    """Per-launch time of fn (a C-ABI call on `stream`): a CUDA graph of
+    `per_graph` launches (fn cycles its weight copies), replayed until at
+    least `min_launches` launches and `min_replays` replays; each replay timed
+    with CUDA events on the stream.  Returns (median seconds per launch over
+    the replays, launches timed)."""
     fn()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for _ in range(iters):
+        for _ in range(per_graph):
             fn()
-    g.replay()
+    with torch.cuda.stream(stream):
+        g.replay()
     torch.cuda.synchronize()
-    return time_graph(torch, g, stream, 3) / iters
+    replays = max(min_replays, -(-min_launches // per_graph))
+    e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in e:
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    per = sorted(e0.elapsed_time(e1) * 1e-3 / per_graph for e0, e1 in e)
+    return per[len(per) // 2], replays * per_graph
 
 
 def extras(torch, ggq, synth, stream):
-    """Kernel timings for the other configurations (cold-L2 by rotating weight
-    copies for the small ones)."""
+    """Kernel timings for the other configurations: weights cycled through
+    copies totalling at least 4 x L2 (cold reads), the median over replays of
+    a graph, at least 200 launches each."""
     import numpy as np
     from synth import workloads as WL
     out = {}
     sp = stream.cuda_stream
 
-    def rotating(gs, copies):
-        Ws = []
-        for _ in range(copies):
-            Ws.append([torch.from_numpy(synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)).cuda() for g in gs])
-        return Ws
+    def rotating(gs):
+        base = [torch.from_numpy(synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)).cuda() for g in gs]
+        n = copies_for(sum(int(b.numel()) for b in base))
+        return [base] + [[b.clone() for b in base] for _ in range(n - 1)]
 
-    # cfg1: Q8_0 2048x2048, M=1; 32 weight copies (143 MB > L2) cycled
+    def timing(t, launches, copies, nbytes, **kw):
+        return {"us": round(t * 1e6, 2), "GB_s": round(nbytes / t / 1e9, 1), **kw,
+                "launches": launches, "weight_copies": copies,
+                "rotated_MB": round(copies * nbytes / 1e6, 1)}
+
+    # cfg1: Q8_0 2048x2048, M=1
     g = WL.CFG1[0]
-    Ws = rotating([g], 32)
+    Ws = rotating([g])
     x = torch.randn(g.cols, device="cuda")
     y = torch.empty(g.rows, device="cuda")
+    nb = g.rows * synth.row_bytes(g.qtype, g.cols)
     k = [0]
 
     def f1():
         W = Ws[k[0] % len(Ws)][0]
         k[0] += 1
         ggq.check(ggq.ggq_gemv(g.qtype, W.data_ptr(), g.rows, g.cols, x.data_ptr(), y.data_ptr(), 1, sp), "gemv")
-    t = kernel_time(torch, f1, stream, 64)
-    nb = g.rows * synth.row_bytes(g.qtype, g.cols)
-    out["cfg1_q8_0_2048x2048"] = {"us": round(t * 1e3, 2), "GB_s": round(nb / t / 1e6, 1)}
+    t, n = kernel_time(torch, f1, stream, len(Ws))
+    out["cfg1_q8_0_2048x2048"] = timing(t, n, len(Ws), nb)
     del Ws
 
-    # cfg2: one SmolLM3 layer, 7 Q4_K GEMVs in 4 launches; 4 layer copies cycled (176 MB)
+    # cfg2: one SmolLM3 layer, 7 Q4_K GEMVs in 4 launches ([q,k,v], [o], [gate,up], [down])
     gs = WL.CFG2
-    Ws = rotating(gs, 4)
+    Ws = rotating(gs)
     xs = {c: torch.randn(c, device="cuda") for c in (2048, 11008)}
     ys = [torch.empty(gg.rows, device="cuda") for gg in gs]
     groups = [[0, 1, 2], [3], [4, 5], [6]]
+    nb = sum(gg.rows * synth.row_bytes(gg.qtype, gg.cols) for gg in gs)
     k = [0]
 
     def f2():
@@ -476,14 +652,13 @@ def extras(torch, ggq, synth, stream):
             ggq.check(ggq.ggq_gemv_multi(12, [Wc[i].data_ptr() for i in grp], [gs[i].rows for i in grp],
                                          gs[grp[0]].cols, xs[gs[grp[0]].cols].data_ptr(),
                                          [ys[i].data_ptr() for i in grp], 1, sp), "gemv")
-    t = kernel_time(torch, f2, stream, 16)
-    nb = sum(gg.rows * synth.row_bytes(gg.qtype, gg.cols) for gg in gs)
-    out["cfg2_smollm3_layer_q4_k"] = {"us": round(t * 1e3, 2), "GB_s": round(nb / t / 1e6, 1)}
+    t, n = kernel_time(torch, f2, stream, len(Ws), min_launches=MIN_LAUNCHES // 4)
+    out["cfg2_smollm3_layer_q4_k"] = timing(t, 4 * n, len(Ws), nb, launches_per_layer=4)
     del Ws
 
-    # cfg4: Q8_0 14336x4096, M in 1..16; 4 weight copies cycled (250 MB)
+    # cfg4: Q8_0 14336x4096, M in 1..16
     g = WL.CFG4
-    Ws = rotating([g], 4)
+    Ws = rotating([g])
     nb = g.rows * synth.row_bytes(g.qtype, g.cols)
     res = {}
     for M in WL.CFG4_M:
@@ -496,45 +671,40 @@ def extras(torch, ggq, synth, stream):
             k[0] += 1
             ggq.check(ggq.ggq_gemv(g.qtype, W.data_ptr(), g.rows, g.cols, x.data_ptr(), y.data_ptr(), M, sp),
                       "gemv")
-        t = kernel_time(torch, f4, stream, 16)
-        res[str(M)] = {"us": round(t * 1e3, 2), "GB_s": round(nb / t / 1e6, 1),
-                       "TFLOP_s": round(2 * M * g.rows * g.cols / t / 1e9, 2)}
+        t, n = kernel_time(torch, f4, stream, len(Ws))
+        res[str(M)] = timing(t, n, len(Ws), nb, TFLOP_s=round(2 * M * g.rows * g.cols / t / 1e12, 2))
     out["cfg4_q8_0_14336x4096"] = res
     del Ws
 
-    # cfg5: prefill Q4_K 14336x4096 x bf16 X 512x4096
+    # cfg5: prefill Q4_K 14336x4096 x bf16 X 512x4096 (compute-bound), and the
+    # same with the Q8_0 14336x4096 matrix of cfg4
     g = WL.CFG5
-    W = torch.from_numpy(synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)).cuda()
     X = torch.from_numpy(synth.normal_bf16(WL.CFG5_M * g.cols, g.x_stream).view(np.int16)).cuda()
     Y = torch.empty(WL.CFG5_M, g.rows, device="cuda")
-
-    def f5():
-        ggq.check(ggq.ggq_gemm_prefill(12, W.data_ptr(), g.rows, g.cols, X.data_ptr(), Y.data_ptr(), WL.CFG5_M,
-                                       sp), "prefill")
-    t = kernel_time(torch, f5, stream, 8)
     flops = 2 * WL.CFG5_M * g.rows * g.cols
-    out["cfg5_prefill_q4_k_512x14336x4096"] = {"us": round(t * 1e3, 2), "TFLOP_s": round(flops / t / 1e9, 1)}
+    for name, gq in (("cfg5_prefill_q4_k_512x14336x4096", g), ("prefill_q8_0_512x14336x4096", WL.CFG4)):
+        Ws = rotating([gq])
+        k = [0]
 
-    # the same prefill with the Q8_0 14336x4096 matrix of cfg4
-    g8 = WL.CFG4
-    W8 = torch.from_numpy(synth.weight_rows(g8.qtype, g8.stream, g8.rows, g8.cols)).cuda()
+        def f5():
+            W = Ws[k[0] % len(Ws)][0]
+            k[0] += 1
+            ggq.check(ggq.ggq_gemm_prefill(gq.qtype, W.data_ptr(), gq.rows, gq.cols, X.data_ptr(), Y.data_ptr(),
+                                           WL.CFG5_M, sp), "prefill")
+        t, n = kernel_time(torch, f5, stream, len(Ws))
+        out[name] = {"us": round(t * 1e6, 2), "TFLOP_s": round(flops / t / 1e12, 1), "launches": n,
+                     "weight_copies": len(Ws)}
+        del Ws
+    del X, Y
 
-    def f5q8():
-        ggq.check(ggq.ggq_gemm_prefill(8, W8.data_ptr(), g8.rows, g8.cols, X.data_ptr(), Y.data_ptr(), WL.CFG5_M,
-                                       sp), "prefill")
-    t = kernel_time(torch, f5q8, stream, 8)
-    out["prefill_q8_0_512x14336x4096"] = {"us": round(t * 1e3, 2), "TFLOP_s": round(flops / t / 1e9, 1)}
-    del W, W8, X, Y
-
-    # the cfg4 shape as Q4_0 (33 MB: 6 copies cycled, 198 MB) and as F32 (235 MB, one copy);
-    # Q4_0 14336x4128 runs on the warp-per-row kernel; Q6_K (48.2 MB: 4 copies) too
-    for name, g, copies, Ms in [("q4_0_14336x4096", WL.Q40_GEMV, 6, (1, 2, 4, 8, 16)),
-                                ("q4_0_14336x4128_warp_per_row", WL.Q40_ODD_GEMV, 6, (1, 8)),
-                                ("f32_14336x4096", WL.F32_GEMV, 1, (1,)),
-                                ("q6_k_14336x4096", WL.Q6K_GEMV, 4, (1, 2, 8)),
-                                ("q6_k_4096x14336", WL.Q6K_DOWN_GEMV, 4, (1,))]:
-        W0 = torch.from_numpy(synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)).cuda()
-        Ws = [W0] + [W0.clone() for _ in range(copies - 1)]
+    # the cfg4 shape as Q4_0, as F32 and as Q6_K; Q4_0 14336x4128 (warp-per-row
+    # kernel); the Q6_K ffn_down shape
+    for name, g, Ms in [("q4_0_14336x4096", WL.Q40_GEMV, (1, 2, 4, 8, 16)),
+                        ("q4_0_14336x4128_warp_per_row", WL.Q40_ODD_GEMV, (1, 8)),
+                        ("f32_14336x4096", WL.F32_GEMV, (1,)),
+                        ("q6_k_14336x4096", WL.Q6K_GEMV, (1, 2, 8)),
+                        ("q6_k_4096x14336", WL.Q6K_DOWN_GEMV, (1,))]:
+        Ws = rotating([g])
         nb = g.rows * synth.row_bytes(g.qtype, g.cols)
         res = {}
         for M in Ms:
@@ -543,14 +713,14 @@ def extras(torch, ggq, synth, stream):
             k = [0]
 
             def fx():
-                W = Ws[k[0] % len(Ws)]
+                W = Ws[k[0] % len(Ws)][0]
                 k[0] += 1
                 ggq.check(ggq.ggq_gemv(g.qtype, W.data_ptr(), g.rows, g.cols, x.data_ptr(), y.data_ptr(), M, sp),
                           "gemv")
-            t = kernel_time(torch, fx, stream, 12)
-            res[str(M)] = {"us": round(t * 1e3, 2), "GB_s": round(nb / t / 1e6, 1)}
+            t, n = kernel_time(torch, fx, stream, len(Ws))
+            res[str(M)] = timing(t, n, len(Ws), nb)
         out[name] = res
-        del Ws, W0
+        del Ws
     return out
 
 
@@ -596,16 +766,19 @@ def run_reference(a, ws, rank):
         return 0
     import multiprocessing
     steps = max(1, a.steps)
-    per = max(0.05, min(a.cpu_seconds, 120.0 / (steps + a.warmup)))
+    threads = host_threads()
+    # one sample of about `per` seconds of single-thread oracle work, generated
+    # once; each step runs the oracle over all of it on every host thread
+    per = max(0.05, min(a.cpu_seconds / 6, 120.0 * threads / (steps + a.warmup)))
+    jobs, nbytes, desc = cpu_oracle_jobs(per, a.layers)
+    desc = f"{desc}, {threads} threads"
     for _ in range(a.warmup):
-        cpu_oracle_sample(per, a.layers)
+        _on_threads(jobs, threads)
     vals, walls = [], []
-    desc = ""
     for _ in range(steps):
-        t0 = time.perf_counter()
-        v, desc, _ = cpu_oracle_sample(per, a.layers)
-        walls.append(time.perf_counter() - t0)
-        vals.append(v)
+        t = _on_threads(jobs, threads)
+        walls.append(t)
+        vals.append(nbytes / t / 1e9)
     value = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
@@ -613,7 +786,7 @@ def run_reference(a, ws, rank):
         "ms_per_step": round(1e3 * statistics.median(walls), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "layers": a.layers, "sampled": True},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"per step: {desc}", "host_cpus": multiprocessing.cpu_count()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -623,6 +796,8 @@ def run_reference(a, ws, rank):
 
 def main():
     a = args_parse()
+    if a.kernel:
+        return run_kernel(a)
     ws, rank, local = dist_setup()
     if a.impl == "reference":
         return run_reference(a, ws, rank)
@@ -680,21 +855,56 @@ def main():
     dist_barrier(ws)
     ms = dist_max(ms, ws, device="cuda")
 
-    # ---- end to end through the C ABI with host buffers: H2D of every stage's
-    # x, the pass, D2H of every stage's y, all inside the timed region (the x
-    # and y of all stages are contiguous: one copy each way)
+    # ---- end to end through the C ABI with host buffers: every step uploads
+    # the x of all its stages from pinned memory (one copy: they are
+    # contiguous) and reads back its result, the head's logits, all inside the
+    # timed region.  Two device buffer sets (a second pass bound to them):
+    # step k+1's upload runs on a copy stream while step k computes, and step
+    # k's logits come back while step k+1 computes.
+    dp2 = DecodePass(model, stage_plan(a.layers), torch, ggq, synth)
+    with torch.cuda.stream(stream):
+        dp2.run(sp)
+    torch.cuda.synchronize()
+    graph2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph2, stream=stream):
+        dp2.run(sp)
+    passes = [(dp, graph), (dp2, graph2)]
+    head_host = torch.empty(dp.head_rows, dtype=torch.float32).pin_memory()
+    cstream = torch.cuda.Stream()
     e2e_steps = max(3, min(a.steps, 50))
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            dp.x_dev.copy_(dp.x_host, non_blocking=True)
-            graph.replay()
-            dp.y_host.copy_(dp.y_dev, non_blocking=True)
-        e1.record(stream)
+    e0.record(stream)
+    cstream.wait_event(e0)
+    with torch.cuda.stream(cstream):
+        passes[0][0].x_dev.copy_(dp.x_host, non_blocking=True)
+        ev_up[0].record(cstream)
+    for k in range(e2e_steps):
+        b = k % 2
+        pk, gk = passes[b]
+        stream.wait_event(ev_up[b])
+        with torch.cuda.stream(stream):
+            gk.replay()
+        ev_done[b].record(stream)
+        with torch.cuda.stream(cstream):
+            if k + 1 < e2e_steps:
+                nb_ = (k + 1) % 2
+                if k >= 1:
+                    cstream.wait_event(ev_free[nb_])   # step k-1 read its x and its logits are home
+                passes[nb_][0].x_dev.copy_(dp.x_host, non_blocking=True)
+                ev_up[nb_].record(cstream)
+            cstream.wait_event(ev_done[b])
+            head_host.copy_(pk.head_y, non_blocking=True)
+            ev_free[b].record(cstream)
+    stream.wait_stream(cstream)
+    e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = dist_max(e0.elapsed_time(e1) / e2e_steps, ws, device="cuda")
+    del graph2
+    dp2.close()
 
     # ---- roofline of the dominant kernel (Q4_K GEMV launches)
     r_steps = max(3, min(a.steps, 20))
@@ -753,8 +963,11 @@ def main():
         "frac_of_8tbs": round(value / 8000.0, 4),
         "frac_of_measured_hbm": round(value / hbm_peak, 4),
         "e2e": {"value": round(step_bytes * ws / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "h2d_bytes_per_step": dp.x_bytes, "d2h_bytes_per_step": dp.y_bytes,
-                "ms_per_step": round(ms_e2e, 4)},
+                "h2d_bytes_per_step": dp.x_bytes, "d2h_bytes_per_step": 4 * dp.head_rows,
+                "ms_per_step": round(ms_e2e, 4),
+                "how": "per step: every stage's x uploaded from pinned host memory (one copy), the pass, the "
+                       "head's logits read back to pinned memory; two device buffer sets, step k+1's upload and "
+                       "step k's read-back on a copy stream overlapping the passes"},
         "gpu_launches": dp.launches * a.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": roofline_traffic(int(per_launch_bytes)),
@@ -769,11 +982,16 @@ def main():
         "configs": extra,
     }
     if not a.no_cpu_baseline and rank == 0 and ws == 1:
-        v, desc, used = cpu_oracle_sample(a.cpu_seconds, a.layers)
         import multiprocessing
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": desc, "seconds": round(used, 2),
-                                "host_cpus": multiprocessing.cpu_count()}
+        threads = host_threads()
+        jobs, nbytes, desc = cpu_oracle_jobs(a.cpu_seconds / 6, a.layers)
+        used1 = _on_threads(jobs, 1)
+        used = _on_threads(jobs, threads)
+        line["cpu_baseline"] = {"value": round(nbytes / used / 1e9, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": f"{desc}, {threads} threads", "seconds": round(used, 2),
+                                "single_thread": {"value": round(nbytes / used1 / 1e9, 4), "seconds": round(used1, 2)},
+                                "host_cpus": multiprocessing.cpu_count(),
+                                "configs": cpu_oracle_configs(threads)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     dp.close()

@@ -269,6 +269,9 @@ class Model:
 # -------------------------------------------------------------- torch helpers
 
 def _stream_ptr(stream) -> int:
+    """A torch stream, a raw cudaStream_t value (int), or None (the current stream)."""
+    if isinstance(stream, int):
+        return stream
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(s.cuda_stream)

@@ -122,6 +122,8 @@ class DecodePass:
         return len(self.calls)
 
     def run(self, stream=None) -> None:
+        """Launch the pass on `stream` (a torch stream, a cudaStream_t value or
+        None: the current stream); asynchronous."""
         sp = _ggq._stream_ptr(stream)
         for kind, c in self.calls:
             if kind == "chain":

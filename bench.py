@@ -58,6 +58,8 @@ KERNEL_SHAPES = {
     "q6_k_4096x14336": ("Q6K_DOWN_GEMV", "Q6_K 4096 x 14336 (ffn_down shape)"),
     "q8_0_14336x4096": ("CFG4", "Q8_0 14336 x 4096"),
     "q4_0_14336x4096": ("Q40_GEMV", "Q4_0 14336 x 4096"),
+    "prefill_q4_k_512x14336x4096": ("CFG5", "prefill: Q4_K 14336 x 4096 times bf16 X 512 x 4096"),
+    "prefill_q8_0_512x14336x4096": ("CFG4", "prefill: Q8_0 14336 x 4096 times bf16 X 512 x 4096"),
 }
 
 
@@ -72,12 +74,22 @@ def run_kernel(a):
     g = WL.llama8b_pass(1)[-1] if attr == "HEAD" else getattr(WL, attr)
     torch.cuda.set_device(0)
     W = torch.from_numpy(synth.weight_rows(g.qtype, g.stream, g.rows, g.cols)).cuda()
-    x = torch.randn(a.M, g.cols, device="cuda")
-    y = torch.empty(a.M, g.rows, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
+    if a.kernel.startswith("prefill"):
+        import numpy as np
+        a.M = WL.CFG5_M
+        x = torch.from_numpy(synth.normal_bf16(a.M * g.cols, WL.CFG5.x_stream).view(np.int16)).cuda()
+    else:
+        x = torch.randn(a.M, g.cols, device="cuda")
+    y = torch.empty(a.M, g.rows, device="cuda")
 
     def once():
-        ggq.check(ggq.ggq_gemv(g.qtype, W.data_ptr(), g.rows, g.cols, x.data_ptr(), y.data_ptr(), a.M, s), "gemv")
+        if a.kernel.startswith("prefill"):
+            ggq.check(ggq.ggq_gemm_prefill(g.qtype, W.data_ptr(), g.rows, g.cols, x.data_ptr(), y.data_ptr(), a.M,
+                                           s), "prefill")
+        else:
+            ggq.check(ggq.ggq_gemv(g.qtype, W.data_ptr(), g.rows, g.cols, x.data_ptr(), y.data_ptr(), a.M, s),
+                      "gemv")
     once()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -89,7 +101,8 @@ def run_kernel(a):
     us = e0.elapsed_time(e1) * 1e3 / 5
     nb = g.rows * synth.row_bytes(g.qtype, g.cols)
     print(json.dumps({"kernel": a.kernel, "desc": desc, "M": a.M, "us": round(us, 2),
-                      "GB_s": round(nb / us / 1e3, 1), "status": ggq.device_status()}))
+                      "GB_s": round(nb / us / 1e3, 1), "TFLOP_s": round(2 * a.M * g.rows * g.cols / us / 1e6, 1),
+                      "status": ggq.device_status()}))
     return 0
 
 

@@ -7,19 +7,23 @@
 // blocks of an fp16 d and 32 int8 q, w = d*q, staged 8 blocks (272 bytes, 256
 // columns) at a time like a super-block.  X is bf16.
 //
-// One CTA computes a 128 (W rows) x 256 (tokens) tile of Y^T in tensor memory
+// One CTA computes a 128 (W rows) x 256 TH (tokens) tile of Y^T in tensor
+// memory, TH = 2 for Q4_K when M is a multiple of 512 (each decoded W tile then
+// feeds both token halves: every weight is decoded once for 512 tokens), else 1
 // (tiles of the last, partly filled wave as two halves along K, see
 // g_split_sync):
 //   warp 0      TMA producer: raw Q4_K super-blocks [128 rows x 144 B] and X tiles
-//               [256 tokens x 64 k] (128-byte swizzle) into shared-memory rings;
-//   warp 1      allocates 256 TMEM columns; one thread issues tcgen05.mma
+//               [256 tokens x 64 k] per token half (128-byte swizzle) into
+//               shared-memory rings;
+//   warp 1      allocates 256 TH TMEM columns; one thread issues tcgen05.mma
 //               (kind::f16, bf16 x bf16 -> fp32, M=128, N=256, K=16) per 16 k and
-//               commits each stage back to its "empty" barrier;
-//   warps 2..5  decoders: thread = W row; each 64-k stage decodes 64 weights exactly
-//               in fp32, rounds them to bf16 and writes the row in the canonical
-//               K-major 128-byte-swizzle layout the MMA reads; afterwards the same
-//               warps read the accumulator (tcgen05.ld) and store Y (each warp may
-//               only reach its own quarter of the 128 TMEM lanes).
+//               token half, and commits each stage back to its "empty" barrier;
+//   warps 2..   decoders (4 or 8 warps, see Dec): one or two threads per W row;
+//               each 64-k stage decodes the row's weights exactly in fp32,
+//               rounds them to bf16 and writes them in the canonical K-major
+//               128-byte-swizzle layout the MMA reads; afterwards the same warps
+//               read the accumulator (tcgen05.ld) and store Y (each warp may only
+//               reach its own quarter of the 128 TMEM lanes).
 // Every wait is bounded (ptx.cuh: mbar_wait); a timeout is recorded in the device
 // status word and the kernel runs to completion without the data.
 #include <cuda.h>
@@ -37,9 +41,8 @@ namespace ggq {
 namespace {
 
 constexpr int kTileRows = 128;        // UMMA M (W rows)
-constexpr int kTileTok = 256;         // UMMA N (tokens)
-constexpr int kKStage = 64;           // k per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 3;
+constexpr int kTileTok = 256;         // UMMA N (tokens): one token half of a tile
+constexpr int kKStage = 64;           // k per stage of one-half tiles: one 128-byte swizzle row of bf16
 constexpr int kRawStages = 2;
 template <bool Q4K>
 struct Raw {   // one 256-column block column of a 128-row tile: Q4_K super-blocks or Q8_0 periods
@@ -47,13 +50,42 @@ struct Raw {   // one 256-column block column of a 128-row tile: Q4_K super-bloc
     static constexpr int kBytes = kTileRows * kRowBytes;
 };
 constexpr int kRawBytes = Raw<false>::kBytes;            // the larger of the two: the ring's slot
-constexpr int kABytes = kTileRows * kKStage * 2;        // 16 KB
-constexpr int kBBytes = kTileTok * kKStage * 2;         // 32 KB
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;
+// Decoder warps 2 .. 2 + kDecWarps - 1: kParts threads per W row, each
+// decoding its share of a stage's 64 k (kParts = 2: the low- or high-nibble
+// half of Q4_K, one of the two Q8_0 blocks), then reading their TMEM lane
+// quarter's share of the accumulator columns in the epilogue.  Eight warps
+// where the decode sets the pace (Q8_0; tiles of 256 tokens), four for Q4_K
+// tiles of 512 tokens (measured faster there).
+template <bool Q4K, int TH>
+struct Dec {
+    static constexpr int kDecWarps = Q4K && TH == 2 ? 4 : 8;
+    static constexpr int kDecoders = 32 * kDecWarps;
+    static constexpr int kParts = kDecWarps / 4;
+    static constexpr int kThreads = 64 + kDecoders;
+};
 
-constexpr size_t kSmemPayload = (size_t)kStages * (kABytes + kBBytes) + (size_t)kRawStages * kRawBytes;
-constexpr size_t kSmemBytes = kSmemPayload + 1024 /* alignment */ + 256 /* barriers */;
+// A tile is 128 W rows x TH token halves of 256 (TH = 1 or 2).  With TH = 2
+// each decoded W tile feeds two MMAs (one per half) into a 512-column TMEM
+// accumulator: every weight is decoded once for 512 tokens.  Its B stages take
+// 64 KB, so the ring is two stages deep (three for TH = 1); the raw weight
+// ring holds Q4_K super-blocks (18 KB a slot), so TH = 2 is for Q4_K (Q8_0's
+// 34 KB periods leave no room: it keeps TH = 1).
+template <bool Q4K, int TH>
+struct Tile {
+    static constexpr int kTok = kTileTok * TH;
+    static constexpr int kKS = kKStage;                      // k per stage
+    static constexpr int kSPS = 256 / kKS;                   // stages per 256-column block
+    static constexpr int kRowB = kKS * 2;                    // bytes of a swizzled A / B row
+    static constexpr int kStages = TH == 2 ? 2 : 3;
+    static constexpr int kABytes = kTileRows * kRowB;
+    static constexpr int kHalfBBytes = kTileTok * kRowB;
+    static constexpr int kBBytes = kHalfBBytes * TH;
+    static constexpr int kTmemCols = kTileTok * TH;
+    static constexpr int kRawSlot = TH == 2 ? Raw<true>::kBytes : kRawBytes;
+    static constexpr size_t kSmemBytes = (size_t)kStages * (kABytes + kBBytes) + (size_t)kRawStages * kRawSlot +
+                                         1024 /* alignment */ + 256 /* barriers */;
+};
+static_assert(Tile<true, 2>::kSmemBytes <= 227 * 1024, "two-half Q4_K tiles fit shared memory");
 
 // The last, partly filled wave of tiles is split in two along K (whole
 // super-block columns): two CTAs compute halves of one tile.  The first to
@@ -71,7 +103,7 @@ struct PrefillParams {
     int rows;        // W rows (Y columns)
     int cols;        // K
     int M;           // tokens
-    int tok_tiles;   // M / 256 (rounded up)
+    int tok_tiles;   // M / (256 * TH) (rounded up)
     int* status;
 };
 
@@ -183,11 +215,20 @@ __device__ __forceinline__ void wait_flag(const int* flag, int* status) {
     }
 }
 
-template <bool Q4K>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap wmap,
+template <bool Q4K, int TH>
+__global__ void __launch_bounds__(Dec<Q4K, TH>::kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const __grid_constant__ CUtensorMap xmap,
                                                               const PrefillParams p) {
     using RB = Raw<Q4K>;
+    using TL = Tile<Q4K, TH>;
+    constexpr int kDecoders = Dec<Q4K, TH>::kDecoders, kParts = Dec<Q4K, TH>::kParts;
+    static_assert(Q4K || TH == 1, "two token halves per tile for Q4_K only");
+    constexpr int kRawSlot = TL::kRawSlot;
+    constexpr int kKS = TL::kKS, kSPS = TL::kSPS, kABytes = TL::kABytes, kHalfBBytes = TL::kHalfBBytes;
+    auto desc = [](uint32_t addr) { return sw128_desc(addr); };
+    constexpr int kStages = TL::kStages;
+    constexpr int kBBytes = TL::kBBytes;
+    constexpr int kTmemCols = TL::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // work item: a whole tile, or half of one (super-blocks [sb0, sb1))
@@ -201,18 +242,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int row_tile = tile / p.tok_tiles;
     const int tok_tile = tile % p.tok_tiles;
     const int row0 = row_tile * kTileRows;
-    const int tok0 = tok_tile * kTileTok;
-    const int ks0 = 4 * sb0;
-    const int nks = 4 * (sb1 - sb0);      // k stages of this item (local index i: global stage ks0 + i)
+    const int tok0 = tok_tile * TL::kTok;
+    const int ks0 = kSPS * sb0;
+    const int nks = kSPS * (sb1 - sb0);   // k stages of this item (local index i: global stage ks0 + i)
     const int nsb = sb1 - sb0;            // super-blocks of this item
 
     // 1024-aligned carve-out
     const uint32_t base_u32 = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
-    uint8_t* sB = base;                                      // kStages x 32 KB
-    uint8_t* sA = sB + (size_t)kStages * kBBytes;            // kStages x 16 KB
+    uint8_t* sB = base;                                      // kStages x TH x (16 or 32 KB)
+    uint8_t* sA = sB + (size_t)kStages * kBBytes;            // kStages x (8 or 16 KB)
     uint8_t* sRaw = sA + (size_t)kStages * kABytes;          // kRawStages x 18 KB
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + (size_t)kRawStages * kRawBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + (size_t)kRawStages * kRawSlot);
     uint64_t* full_b = bars;                     // [kStages]
     uint64_t* full_a = bars + kStages;           // [kStages]
     uint64_t* empty = bars + 2 * kStages;        // [kStages]
@@ -226,12 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         prefetch_tensormap(&xmap);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_b[s], 1);
-            mbar_init(&full_a[s], 128);
+            mbar_init(&full_a[s], kDecoders);
             mbar_init(&empty[s], 1);
         }
         for (int r = 0; r < kRawStages; ++r) {
             mbar_init(&full_raw[r], 1);
-            mbar_init(&empty_raw[r], 128);
+            mbar_init(&empty_raw[r], kDecoders);
         }
         mbar_init(acc_full, 1);
         fence_mbar_init();
@@ -247,18 +288,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (lane == 0) {
             pdl_wait();   // X may come from the previous kernel in the stream
             for (int ks = 0; ks < nks; ++ks) {   // local stage index
-                if ((ks & 3) == 0) {
-                    const int sb = ks >> 2, r = sb % kRawStages;
+                if (ks % kSPS == 0) {
+                    const int sb = ks / kSPS, r = sb % kRawStages;
                     mbar_wait(&empty_raw[r], ((sb / kRawStages) & 1) ^ 1, p.status);
                     mbar_arrive_expect_tx(&full_raw[r], RB::kBytes);
                     // Q4_K map: 1-byte elements; Q8_0 map: 2-byte elements (136 a period)
-                    tma_load_2d(sRaw + (size_t)r * kRawBytes, &wmap, &full_raw[r], (sb0 + sb) * (Q4K ? 144 : 136),
+                    tma_load_2d(sRaw + (size_t)r * kRawSlot, &wmap, &full_raw[r], (sb0 + sb) * (Q4K ? 144 : 136),
                                 row0);
                 }
                 const int s = ks % kStages;
                 mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
                 mbar_arrive_expect_tx(&full_b[s], kBBytes);
-                tma_load_2d(sB + (size_t)s * kBBytes, &xmap, &full_b[s], (ks0 + ks) * kKStage, tok0);
+#pragma unroll
+                for (int h = 0; h < TH; ++h)   // tokens beyond M read as zeros
+                    tma_load_2d(sB + (size_t)s * kBBytes + (size_t)h * kHalfBBytes, &xmap, &full_b[s],
+                                (ks0 + ks) * kKS, tok0 + h * kTileTok);
             }
         }
         __syncwarp();
@@ -273,10 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const uint32_t a_addr = smem_u32(sA + (size_t)s * kABytes);
                 const uint32_t b_addr = smem_u32(sB + (size_t)s * kBBytes);
 #pragma unroll
-                for (int kk = 0; kk < kKStage / 16; ++kk) {
-                    // 16 bf16 = 32 bytes further along the swizzled 128-byte rows
-                    umma_bf16(tmem, sw128_desc(a_addr + 32 * kk), sw128_desc(b_addr + 32 * kk), kIdesc,
-                              (ks | kk) != 0);
+                for (int kk = 0; kk < kKS / 16; ++kk) {
+                    // 16 bf16 = 32 bytes further along the swizzled rows; one MMA
+                    // per token half, accumulator columns 256 h ..
+#pragma unroll
+                    for (int h = 0; h < TH; ++h)
+                        umma_bf16(tmem + (uint32_t)(h * kTileTok), desc(a_addr + 32 * kk),
+                                  desc(b_addr + (uint32_t)(h * kHalfBBytes) + 32 * kk), kIdesc, (ks | kk) != 0);
                 }
                 umma_commit(&empty[s]);
             }
@@ -284,19 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ decoders (warps 2..5)
-        const int t = (warp - 2) * 32 + lane;   // W row within the tile
+        // ------------------------------------------------ decoders (warps 2..)
+        const int t = (threadIdx.x - 64) & (kTileRows - 1);   // W row within the tile
+        const int part = (threadIdx.x - 64) >> 7;             // share of the row's k (kParts > 1)
         for (int sb = 0; sb < nsb; ++sb) {
             const int r = sb % kRawStages;
             mbar_wait(&full_raw[r], (sb / kRawStages) & 1, p.status);
-            const uint8_t* rp = sRaw + (size_t)r * kRawBytes + (size_t)t * RB::kRowBytes;
+            const uint8_t* rp = sRaw + (size_t)r * kRawSlot + (size_t)t * RB::kRowBytes;
             if constexpr (Q4K) {
             const uint4 h = *reinterpret_cast<const uint4*>(rp);
             const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
-                const int ks = sb * 4 + c;
-                const int s = ks % kStages;
                 int sc_lo, m_lo, sc_hi, m_hi;
                 q4k_scale_min(h.y, h.z, h.w, 2 * c, sc_lo, m_lo);
                 q4k_scale_min(h.y, h.z, h.w, 2 * c + 1, sc_hi, m_hi);
@@ -305,13 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const uint4 q0 = *reinterpret_cast<const uint4*>(rp + 16 + 32 * c);
                 const uint4 q1 = *reinterpret_cast<const uint4*>(rp + 32 + 32 * c);
                 const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
-                uint8_t* arow = sA + (size_t)s * kABytes + (size_t)t * 128;
+                // chunk j (k = 8j .. 8j+7 of the 64): low nibbles, sub-block 2c;
+                // high nibbles, sub-block 2c+1, are k = 32 + 8j ..
+                uint32_t lo[4][4], hi[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    // chunk j: k = 8j..8j+7 (low nibbles, sub-block 2c);
-                    // chunk j+4: k = 32+8j..32+8j+7 (high nibbles, sub-block 2c+1)
-                    uint32_t lo[4], hi[4];
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const uint32_t w = qw[2 * j + half];
@@ -319,17 +363,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                         for (int b = 0; b < 4; ++b) {
                             const uint32_t byte = (w >> (8 * b)) & 0xFFu;
-                            fl[b] = fmaf(a_lo, __uint_as_float(0x4B000000u | (byte & 15u)) - 8388608.0f, -b_lo);
-                            fh[b] = fmaf(a_hi, __uint_as_float(0x4B000000u | (byte >> 4)) - 8388608.0f, -b_hi);
+                            if (kParts == 1 || part == 0)
+                                fl[b] = fmaf(a_lo, __uint_as_float(0x4B000000u | (byte & 15u)) - 8388608.0f, -b_lo);
+                            if (kParts == 1 || part == 1)
+                                fh[b] = fmaf(a_hi, __uint_as_float(0x4B000000u | (byte >> 4)) - 8388608.0f, -b_hi);
                         }
-                        lo[2 * half] = pack_bf16x2(fl[0], fl[1]);
-                        lo[2 * half + 1] = pack_bf16x2(fl[2], fl[3]);
-                        hi[2 * half] = pack_bf16x2(fh[0], fh[1]);
-                        hi[2 * half + 1] = pack_bf16x2(fh[2], fh[3]);
+                        lo[j][2 * half] = pack_bf16x2(fl[0], fl[1]);
+                        lo[j][2 * half + 1] = pack_bf16x2(fl[2], fl[3]);
+                        hi[j][2 * half] = pack_bf16x2(fh[0], fh[1]);
+                        hi[j][2 * half + 1] = pack_bf16x2(fh[2], fh[3]);
                     }
-                    const int sw = t & 7;
-                    *reinterpret_cast<uint4*>(arow + ((j ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    *reinterpret_cast<uint4*>(arow + (((j + 4) ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
+                // one 64-k stage: a 128-byte row, chunk position j ^ (row % 8)
+                const int ks = sb * 4 + c;
+                const int s = ks % kStages;
+                mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
+                uint8_t* arow = sA + (size_t)s * kABytes + (size_t)t * 128;
+                const int sw = t & 7;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (kParts == 1 || part == 0)
+                        *reinterpret_cast<uint4*>(arow + ((j ^ sw) << 4)) =
+                            make_uint4(lo[j][0], lo[j][1], lo[j][2], lo[j][3]);
+                    if (kParts == 1 || part == 1)
+                        *reinterpret_cast<uint4*>(arow + (((j + 4) ^ sw) << 4)) =
+                            make_uint4(hi[j][0], hi[j][1], hi[j][2], hi[j][3]);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&full_a[s]);
@@ -346,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 float d[2];
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
+                    if (kParts == 2 && h2 != part) continue;
                     const int off = 34 * (2 * c + h2);   // 2-byte aligned; q bytes at off + 2
                     d[h2] = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rp + off));
                     const int qo = off + 2;
@@ -364,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {   // chunk j: k = 8j..8j+7 (block 2c + j/4)
                     const int h2 = j >> 2;
+                    if (kParts == 2 && h2 != part) continue;
                     uint32_t o[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -386,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_wait(acc_full, 0, p.status);
         tc_fence_after();
         const int q = warp & 3;                  // TMEM lane quarter of this warp
+        constexpr int kCols = TL::kTok / kParts;  // accumulator columns this warp reads
+        const int col0 = ((warp - 2) >> 2) * kCols;
         const int row = row0 + 32 * q + lane;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
         // half of a split tile: the first half done stores, the second adds
@@ -395,14 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         __shared__ int s_role;
         if (split) {
             if (threadIdx.x == 64) s_role = atomicAdd(cnt, 1);
-            asm volatile("bar.sync 1, 128;" ::: "memory");   // the 128 epilogue threads
+            asm volatile("bar.sync 1, %0;" ::"n"(kDecoders) : "memory");   // the epilogue threads
             add = s_role != 0;
             if (add) {
                 if (threadIdx.x == 64) wait_flag(cnt + 1, p.status);
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                asm volatile("bar.sync 1, %0;" ::"n"(kDecoders) : "memory");
             }
         }
-        for (int col = 0; col < kTileTok; col += 16) {
+        for (int col = col0; col < col0 + kCols; col += 16) {
             float v[16];
             tmem_ld16(taddr + (uint32_t)col, v);
             if (add) {
@@ -424,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
         }
         if (split) {
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"n"(kDecoders) : "memory");
             if (threadIdx.x == 64) {
                 if (add) {   // both halves done: reset for the next launch
                     st_relaxed_i32(cnt, 0);
@@ -479,10 +541,13 @@ int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const ui
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(GGQ_ECUDA, "tensor map (W) failed (%d)", (int)r);
     }
+    // two token halves per tile (each weight decoded once for 512 tokens)
+    // when M is a multiple of 512, else one
+    const int th = q4k && M % (2 * kTileTok) == 0 ? 2 : 1;
     {
         cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)M};
         cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-        cuuint32_t box[2] = {kKStage, kTileTok};
+        cuuint32_t box[2] = {(cuuint32_t)kKStage, kTileTok};
         cuuint32_t es[2] = {1, 1};
         CUresult r = enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box,
                          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -494,7 +559,7 @@ int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const ui
     p.rows = (int)rows;
     p.cols = (int)cols;
     p.M = M;
-    p.tok_tiles = (M + kTileTok - 1) / kTileTok;
+    p.tok_tiles = (M + th * kTileTok - 1) / (th * kTileTok);
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
     {
@@ -513,13 +578,16 @@ int launch_prefill(int type, const void* W, int64_t rows, int64_t cols, const ui
     const int nsplit = (R > 0 && 2 * R <= nsm && R <= kMaxSplit && cols >= 512) ? R : 0;
     p.full_tiles = T - nsplit;
 
-    auto kernel = q4k ? prefill_kernel<true> : prefill_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto kernel = q4k ? (th == 2 ? prefill_kernel<true, 2> : prefill_kernel<true, 1>) : prefill_kernel<false, 1>;
+    const size_t smem = q4k ? (th == 2 ? Tile<true, 2>::kSmemBytes : Tile<true, 1>::kSmemBytes)
+                            : Tile<false, 1>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.full_tiles + 2 * nsplit));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(q4k && th == 2 ? Dec<true, 2>::kThreads : q4k ? Dec<true, 1>::kThreads
+                                                                     : Dec<false, 1>::kThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -60,7 +60,8 @@ def int_q4k(rng, rows, cols, sc_max=16, m_max=63):
     return W, sc[:, bi, j] * qq - mm[:, bi, j]
 
 
-@pytest.mark.parametrize("rows,cols,M", [(128, 256, 128), (256, 512, 256), (128, 2048, 512), (384, 1024, 384)])
+@pytest.mark.parametrize("rows,cols,M", [(128, 256, 128), (256, 512, 256), (128, 2048, 512), (384, 1024, 384),
+                                         (256, 768, 1024), (1280, 512, 512)])
 def test_prefill_integer_exact(env, rows, cols, M):
     """Weights |w| <= 240 and X in [-8, 8] are exact in bf16; every sum is exact."""
     rng = np.random.default_rng(rows + cols + M)
@@ -92,9 +93,9 @@ def test_prefill_q8_0_integer_exact(env, rows, cols, M):
     assert np.array_equal(Y.astype(np.int64), X.astype(np.int64) @ w.T)
 
 
-@pytest.mark.parametrize("qtype", [12, 8])
-def test_prefill_one_hot_rows(env, qtype):
-    rows, cols, M = 256, 1024, 256
+@pytest.mark.parametrize("qtype,M", [(12, 256), (8, 256), (12, 512)])
+def test_prefill_one_hot_rows(env, qtype, M):
+    rows, cols = 256, 1024
     W = synth.weight_rows(qtype, 61, rows, cols)
     wb = bf16_round(oracle.dequantize(qtype, W, rows, cols))
     X = np.zeros((M, cols), np.float32)
@@ -106,7 +107,8 @@ def test_prefill_one_hot_rows(env, qtype):
 
 
 @pytest.mark.parametrize("qtype", [12, 8])
-@pytest.mark.parametrize("rows,cols,M", [(128, 256, 128), (256, 4096, 256), (512, 2304, 512)])
+@pytest.mark.parametrize("rows,cols,M", [(128, 256, 128), (256, 4096, 256), (512, 2304, 512), (384, 1536, 1024),
+                                         (128, 1024, 1536), (20352, 512, 512)])
 def test_prefill_random(env, qtype, rows, cols, M):
     W = synth.weight_rows(qtype, 62, rows, cols)
     X = synth.normal_bf16(M * cols, 63).reshape(M, cols)

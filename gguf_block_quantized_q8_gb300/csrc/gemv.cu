@@ -428,7 +428,7 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
     if (type == GGQ_F32 || type == GGQ_Q4_0 || type == GGQ_Q6_K) {
-        if (type == GGQ_Q4_0 && stream_gemv_supported(type, cols, std::min(M, 4), 1, &rows)) {
+        if ((type == GGQ_Q4_0 || type == GGQ_Q6_K) && stream_gemv_supported(type, cols, std::min(M, 4), 1, &rows)) {
             // the streaming kernel takes up to 4 activation rows; M 5..16 runs it
             // once per group of up to 4 (x and y rows are contiguous)
             for (int m0 = 0; m0 < M; m0 += 4) {

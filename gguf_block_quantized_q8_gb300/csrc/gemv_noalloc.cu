@@ -26,7 +26,7 @@ using namespace ggq;
 extern "C" int ggq_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
                                 int M, void* stream) {
     clear_error();
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0)
+    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0 && type != GGQ_Q6_K)
         return fail(GGQ_ETYPE, "ggq_gemv_noalloc: type %d not supported", type);
     if (!W || !x || !y) return fail(GGQ_EINVAL, "ggq_gemv_noalloc: NULL pointer");
     if (rows < 1 || rows > 0x7fffffff) return fail(GGQ_EINVAL, "ggq_gemv_noalloc: rows %lld out of range", (long long)rows);

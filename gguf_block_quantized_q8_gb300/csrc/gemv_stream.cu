@@ -109,18 +109,25 @@ struct ChainParams {
 };
 
 // Weight layouts the kernel streams: the copy geometry and the decode.
-enum Kind { kKQ8 = 0, kKQ4K = 1, kKQ40 = 2 };
+enum Kind { kKQ8 = 0, kKQ4K = 1, kKQ40 = 2, kKQ6 = 3 };
 
 // Tile of one bulk tensor copy: 16 rows x NSB SBs, each row padded so that
 // rows r and r+1 of one chunk fall in different banks.  Copies of a few KB:
 // much smaller ones cost more per copy than the bytes they bring.
+// Q6_K: an SB is 210 bytes, so it starts on 16 bytes only every 8 SBs; its copy
+// starts at the 16-byte boundary below it and takes 240 bytes a row (224 cover
+// any start, 16 more stagger the rows across banks).
 template <int K>
 struct Blk {
-    static constexpr int kBytes = K == kKQ8 ? 272 : 144;     // one SB
-    static constexpr int kElems = kBytes / 8;                 // 8-byte elements per SB
-    static constexpr int kNsb = K == kKQ8 ? 1 : 2;            // SBs per copy
+    static constexpr int kBytes = K == kKQ8 ? 272 : K == kKQ6 ? 210 : 144;   // one SB
+    static constexpr int kElems = kBytes / 8;                 // 8-byte elements per SB (not Q6_K)
+    static constexpr int kNsb = (K == kKQ8 || K == kKQ6) ? 1 : 2;   // SBs per copy
     static constexpr int kPad = K == kKQ8 ? 0 : 2;            // elements of padding per row
-    static constexpr int kRow = (kElems * kNsb + kPad) * 8;    // smem bytes per row: 304 / 272
+    static constexpr int kRow = K == kKQ6 ? 240 : (kElems * kNsb + kPad) * 8;    // smem bytes per row
+    static constexpr int kSums = K == kKQ6 ? 16 : 8;          // x sums per SB (Q6_K: per 16 columns)
+    // first 8-byte element of the copy of SB u, and where the SB starts in it
+    __host__ __device__ static constexpr int coord(int u) { return K == kKQ6 ? ((210 * u) & ~15) / 8 : u * kElems; }
+    __host__ __device__ static constexpr int skew(int u) { return K == kKQ6 ? (210 * u) & 15 : 0; }
     static constexpr int kCopy = kGroupRows * kRow;            // bytes per copy
     static constexpr int kTile = (kCopy + 127) / 128 * 128;    // smem stride: 128-byte aligned
     // x' floats per SB: Q4_K four chunks of 64 padded to 68; Q8_0 one per byte
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         while (inflight < D) {
             if (ct == ct1 && !next_stage()) break;
             const int nv = min(min(B::kNsb, cU - cu), ct1 - ct);
-            tma_issue_2d(lane == 0, ring + (size_t)islot * B::kTile, &csd->maps[cseg], &full[islot], cu * B::kElems,
+            tma_issue_2d(lane == 0, ring + (size_t)islot * B::kTile, &csd->maps[cseg], &full[islot], B::coord(cu),
                          crow, B::kCopy, wpol);
             ct += nv;
             cu += nv;
@@ -343,7 +350,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             const int gi = t / U0, u = t - gi * U0;
             int seg, row, nrows;
             group_at(&infos[0], g0, gi, seg, row, nrows);
-            tma_prefetch_2d(&d0->maps[seg], u * B::kElems, row);
+            tma_prefetch_2d(&d0->maps[seg], B::coord(u), row);
             t += min(min(B::kNsb, U0 - u), tend - t);
         }
     }
@@ -366,6 +373,10 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             xoff = (lane >> 4) * 68 + 2 * (lane & 7) + hi;
             const int k = 4 * lane;
             xsc = make_float4(q4k_xscale(k), q4k_xscale(k + 1), q4k_xscale(k + 2), q4k_xscale(k + 3));
+        } else if (K == kKQ6) {
+            // chunk (h, gp) with gp = (l/8) % 2, pair slot l/16, word l % 8
+            xoff = ((lane >> 3) & 1) * 68 + 2 * (lane & 7) + (lane >> 4);
+            xsc = make_float4(pow2f(53), pow2f(45), pow2f(37), pow2f(37));
         } else if (K == kKQ40) {
             const int b4 = lane >> 3;
             xoff = (b4 >> 1) * 72 + 2 * (18 * (b4 & 1) + 2 + 4 * (lane & 3)) + ((lane >> 2) & 1);
@@ -421,13 +432,14 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 float sum = (v.x + v.y) + (v.z + v.w);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 1);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                const float sum16 = sum;   // Q6_K: 16 columns
                 sum += __shfl_xor_sync(0xffffffffu, sum, 4);
                 const int m = MMAX == 1 ? 0 : qb / c4;
                 const int h = qb - m * c4;          // first float4 of the step within the row
                 const int u = h >> 6;               // SB
                 float* dst = xp + (size_t)m * xs + u * B::kXsb + ((h & 32) ? B::kXsb / 2 : 0) + xoff;
                 const float4 e = make_float4(v.x * xsc.x, v.y * xsc.y, v.z * xsc.z, v.w * xsc.w);
-                if (Q4K) {
+                if (Q4K || K == kKQ6) {
                     dst[0] = e.x;
                     dst[16] = e.y;
                     dst[32] = e.z;
@@ -443,10 +455,16 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     dst[2] = e.z;
                     dst[3] = e.w;
                 }
-                // the code offsets: Q8_0 bytes are stored XOR 0x80 (128), Q4_0 codes are q + 8
-                if ((lane & 7) == 0)
+                // the code offsets: Q8_0 bytes are stored XOR 0x80 (128), Q4_0 codes are q + 8,
+                // Q6_K codes q + 32 (sums per 16 columns: slot 8 half + 4 gp + 2 (l >= 16) + g / 2)
+                if constexpr (K == kKQ6) {
+                    if ((lane & 3) == 0)
+                        sums[m * nsub + u * 16 + ((h & 32) >> 2) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) +
+                             (lane >> 4)] = 32.0f * sum16;
+                } else if ((lane & 7) == 0) {
                     sums[m * nsub + u * 8 + ((h & 32) >> 3) + (lane >> 3)] =
                         Q4K ? sum : (K == kKQ40 ? 8.0f : 128.0f) * sum;
+                }
             };
             const int xop = sd->x_op;
             if (xop == GGQ_X_PLAIN) {
@@ -679,6 +697,9 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     if constexpr (Q4K) {
                         q4k_chunk_rows<MMAX, R>(rowp + j * B::kBytes, 8 * B::kRow, c, xp + uj * B::kXsb, xs,
                                                 sums + uj * 8, nsub, acc2, 68);
+                    } else if constexpr (K == kKQ6) {
+                        q6k_chunk_rows<MMAX, R>(rowp, B::skew(uj), 8 * B::kRow, c, xp + uj * B::kXsb + 68 * c, xs,
+                                                sums + uj * 16 + 8 * (c >> 1) + 4 * (c & 1), nsub, acc);
                     } else if constexpr (K == kKQ40) {
                         q40_chunk_rows<MMAX, R>(rowp + j * B::kBytes + 36 * c, 8 * B::kRow, xp + uj * B::kXsb + 72 * c,
                                                 xs, sums + uj * 8 + 2 * c, nsub, acc);
@@ -786,18 +807,23 @@ int warps_of(int mmax) {
     return mmax == 4 ? 12 : 16;
 }
 
-int kind_of(int type) { return type == GGQ_Q4_K ? kKQ4K : type == GGQ_Q4_0 ? kKQ40 : kKQ8; }
+int kind_of(int type) {
+    return type == GGQ_Q4_K ? kKQ4K : type == GGQ_Q4_0 ? kKQ40 : type == GGQ_Q6_K ? kKQ6 : kKQ8;
+}
 
 constexpr int kMaxRing = 8;
 
 size_t tile_bytes(int kind) {
-    return kind == kKQ8 ? (size_t)Blk<kKQ8>::kTile : kind == kKQ4K ? (size_t)Blk<kKQ4K>::kTile : (size_t)Blk<kKQ40>::kTile;
+    return kind == kKQ8 ? (size_t)Blk<kKQ8>::kTile : kind == kKQ4K ? (size_t)Blk<kKQ4K>::kTile
+         : kind == kKQ6 ? (size_t)Blk<kKQ6>::kTile : (size_t)Blk<kKQ40>::kTile;
 }
 int row_box(int kind) {   // 8-byte elements per row of a copy box
-    return kind == kKQ8 ? Blk<kKQ8>::kRow / 8 : kind == kKQ4K ? Blk<kKQ4K>::kRow / 8 : Blk<kKQ40>::kRow / 8;
+    return kind == kKQ8 ? Blk<kKQ8>::kRow / 8 : kind == kKQ4K ? Blk<kKQ4K>::kRow / 8
+         : kind == kKQ6 ? Blk<kKQ6>::kRow / 8 : Blk<kKQ40>::kRow / 8;
 }
 int xsb_of(int kind) { return kind == kKQ40 ? Blk<kKQ40>::kXsb : kind == kKQ4K ? Blk<kKQ4K>::kXsb : Blk<kKQ8>::kXsb; }
-int64_t sb_bytes(int kind) { return kind == kKQ8 ? 272 : 144; }
+int64_t sb_bytes(int kind) { return kind == kKQ8 ? 272 : kind == kKQ6 ? 210 : 144; }
+int sums_per_sb(int kind) { return kind == kKQ6 ? 16 : 8; }
 
 size_t rows_smem(int kind, int mmax, int ring, int64_t cols_max) {
     const int W = warps_of(mmax);
@@ -805,7 +831,7 @@ size_t rows_smem(int kind, int mmax, int ring, int64_t cols_max) {
     const size_t cut = (size_t)2 * W * kGroupRows * mmax * 4 + (size_t)2 * W * 4;
     return (size_t)W * ring * tile_bytes(kind) + kInfoSlots * sizeof(StageInfo) + kPartMax * sizeof(int2) +
            (size_t)mmax * U * xsb_of(kind) * 4 +
-           (size_t)mmax * U * 8 * 4 + cut +
+           (size_t)mmax * U * sums_per_sb(kind) * 4 + cut +
            (size_t)W * ring * 8;
 }
 
@@ -916,7 +942,7 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
     p.ring = rows_ring(kind, mmax, cols_max);
     if (p.ring == 0) return fail(GGQ_EINVAL, "shape needs too much shared memory");
     p.xs = (int)(cols_max / 256 * xsb_of(kind));
-    p.nsub = (int)(cols_max / 32);
+    p.nsub = (int)(cols_max / 256 * sums_per_sb(kind));
     p.counter = counter;
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
@@ -930,6 +956,11 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
         }
         if (mmax == 2) return launch_t<kKQ4K, 2, 16>(inl, p, stream, smem, coop);
         return launch_t<kKQ4K, 4, 12>(inl, p, stream, smem, coop);
+    }
+    if (kind == kKQ6) {
+        if (mmax == 1) return launch_t<kKQ6, 1, 16>(inl, p, stream, smem, coop);
+        if (mmax == 2) return launch_t<kKQ6, 2, 16>(inl, p, stream, smem, coop);
+        return launch_t<kKQ6, 4, 12>(inl, p, stream, smem, coop);
     }
     if (kind == kKQ40) {   // the warp-count override is not instantiated for Q4_0
         if (mmax == 1) return launch_t<kKQ40, 1, 16>(inl, p, stream, smem, coop);
@@ -949,9 +980,11 @@ int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, i
 
 bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_t* rows) {
     if (M > kMaxM || nseg < 1 || nseg > kMaxSeg || cols % 256 || cols > (1 << 20)) return false;
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0) return false;
+    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0 && type != GGQ_Q6_K) return false;
     // a Q4_K / Q4_0 copy box (2 SBs + pad) must not be wider than a row
     if (type != GGQ_Q8_0 && cols < 768) return false;
+    // Q6_K rows (210 bytes per SB) are a multiple of 16 bytes only when cols % 2048 == 0
+    if (type == GGQ_Q6_K && cols % 2048) return false;
     int64_t r = 0;
     for (int s = 0; s < nseg; ++s) r += rows[s];
     if (r * (cols / 256) >= (1ll << 31)) return false;   // SB indices are 32-bit
@@ -991,7 +1024,7 @@ extern "C" int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chai
     clear_error();
     if (!out) return fail(GGQ_EINVAL, "ggq_chain_create: out is NULL");
     *out = nullptr;
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0)
+    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0 && type != GGQ_Q6_K)
         return fail(GGQ_ETYPE, "ggq_chain_create: type %d not supported", type);
     if (M < 1 || M > kMaxM) return fail(GGQ_EINVAL, "ggq_chain_create: M %d outside 1..%d", M, kMaxM);
     if (nstages < 1 || nstages > 65536 || !stages) return fail(GGQ_EINVAL, "ggq_chain_create: bad stage list");

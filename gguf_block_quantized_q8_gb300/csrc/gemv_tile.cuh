@@ -349,6 +349,108 @@ __device__ __forceinline__ void q40_chunk_rows(const uint8_t* rp, int rstride, c
     }
 }
 
+// Chunk c = (half h, quarter pair gp) of a Q6_K super-block for R rows per lane.
+// rp: the lane's first row of the copy in shared memory, whose super-block bytes
+// start at rp + r0 (r0 even: the copy starts at the 16-byte boundary below the
+// super-block); `rstride` bytes to the next of its rows.  The chunk holds the
+// weights 128h + 32g + l for g = gp, gp + 2 and l = 0..31: ql bytes 64h + 32gp
+// + l (low nibble g = gp, high g = gp + 2) and qh bytes 32h + l (2 bits per g).
+// Words are read aligned and realigned with a funnel shift by 8 * (r0 & 3).
+// Each byte of a code word holds one 6-bit code u, masked in place like a
+// Q8_0 byte (x' scaled by its byte position); the pair (g = gp, g = gp + 2) at
+// one (w, b) is one packed FMA.  x' of chunk c: [b][w][pair] at xu + 16b + 2w,
+// activation row m at xu + m*xs.  32 * sum(x) of the four 16-column groups of
+// the chunk ((g, l < 16) for g = gp, gp + 2, then l >= 16) at su + m*ss.
+// acc[r][m] += the chunk's 64 products.
+template <int MMAX, int R>
+__device__ __forceinline__ void q6k_chunk_rows(const uint8_t* rp, int r0, int rstride, int c, const float* xu, int xs,
+                                               const float* su, int ss, float (&acc)[R][MMAX]) {
+    const int h = c >> 1, gp = c & 1;
+    const uint32_t sh = 8u * (uint32_t)(r0 & 3);
+    const int base = r0 & ~3;
+    float ds[R][4];   // d * sc of the four groups
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint8_t* sb = rp + r * rstride + r0;
+        const float d = half_bits_to_float((uint32_t)sb[208] | ((uint32_t)sb[209] << 8));
+        const signed char* sc = reinterpret_cast<const signed char*>(sb + 192 + 8 * h + 2 * gp);
+        ds[r][0] = d * (float)sc[0];   // (gp, l < 16)
+        ds[r][1] = d * (float)sc[4];   // (gp + 2, l < 16)
+        ds[r][2] = d * (float)sc[1];   // (gp, l >= 16)
+        ds[r][3] = d * (float)sc[5];   // (gp + 2, l >= 16)
+    }
+    F2 t[R][MMAX][2];   // [half of the chunk: l < 16, l >= 16]
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) t[r][m][0] = t[r][m][1] = f2_zero();
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t lo[R][4], hi[R][4];   // code words of quarters gp, gp + 2 for words 4*half .. +3
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t* wl = reinterpret_cast<const uint32_t*>(rp + r * rstride + base + 64 * h + 32 * gp + 16 * half);
+            const uint32_t* wh = reinterpret_cast<const uint32_t*>(rp + r * rstride + base + 128 + 32 * h + 16 * half);
+            uint32_t a[5], q[5];
+#pragma unroll
+            for (int i = 0; i < 5; ++i) {
+                a[i] = wl[i];
+                q[i] = wh[i];
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t qlw = __funnelshift_r(a[w], a[w + 1], sh);
+                const uint32_t qhw = __funnelshift_r(q[w], q[w + 1], sh);
+                lo[r][w] = (qlw & 0x0F0F0F0Fu) | ((qhw << (4 - 2 * gp)) & 0x30303030u);
+                hi[r][w] = ((qlw >> 4) & 0x0F0F0F0Fu) | ((qhw >> (2 * gp)) & 0x30303030u);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t mk = b == 0 ? 0x3Fu : b == 1 ? 0x3F00u : 0x3F0000u;
+            float4 xv[MMAX][2];   // pairs of words 4*half .. +3 at byte position b
+#pragma unroll
+            for (int m = 0; m < MMAX; ++m)
+#pragma unroll
+                for (int qq = 0; qq < 2; ++qq)
+                    xv[m][qq] = *reinterpret_cast<const float4*>(xu + m * xs + 16 * b + 8 * half + 4 * qq);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t vl = b < 3 ? lo[r][w] : (lo[r][w] >> 8);
+                    const uint32_t vh = b < 3 ? hi[r][w] : (hi[r][w] >> 8);
+                    uint64_t pr;
+                    asm("{\n\t.reg .b32 l, h;\n\tand.b32 l, %1, %3;\n\tand.b32 h, %2, %3;\n\tmov.b64 %0, {l, h};\n\t}"
+                        : "=l"(pr) : "r"(vl), "r"(vh), "r"(mk));
+#pragma unroll
+                    for (int m = 0; m < MMAX; ++m) {
+                        const float4 x4 = xv[m][w >> 1];
+                        if (w & 1) f2_fma64(t[r][m][half], pr, x4.z, x4.w);
+                        else f2_fma64(t[r][m][half], pr, x4.x, x4.y);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MMAX; ++m) {
+        const float4 s4 = *reinterpret_cast<const float4*>(su + m * ss);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float a0, a1, b0, b1;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(t[r][m][0].v));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(b0), "=f"(b1) : "l"(t[r][m][1].v));
+            float v = acc[r][m];
+            v = fmaf(ds[r][0], fmaf(a0, kTwo96, -s4.x), v);
+            v = fmaf(ds[r][1], fmaf(a1, kTwo96, -s4.y), v);
+            v = fmaf(ds[r][2], fmaf(b0, kTwo96, -s4.z), v);
+            v = fmaf(ds[r][3], fmaf(b1, kTwo96, -s4.w), v);
+            acc[r][m] = v;
+        }
+    }
+}
+
 // One quarter of a Q8_0 period: blocks 2c and 2c+1 (rp: their 68 bytes, 4-byte
 // aligned) against x' of those byte positions (xu: 68 floats per activation
 // row, 16-byte aligned, rows `xs` apart) and 128 * sum(x) of the two blocks

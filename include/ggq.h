@@ -221,8 +221,9 @@ typedef struct ggq_chain ggq_chain;
 
 /*
  * ggq_chain_create -- validate `nstages` stages (1..65536) of type GGQ_Q8_0,
- * GGQ_Q4_K or GGQ_Q4_0 for M activation rows (1..4; Q4_K and Q4_0 stages need
- * cols >= 768), encode their copy descriptors and
+ * GGQ_Q4_K, GGQ_Q4_0 or GGQ_Q6_K for M activation rows (1..4; Q4_K and Q4_0
+ * stages need cols >= 768, Q6_K stages cols % 2048 == 0, so that every row of
+ * 210-byte super-blocks starts on 16 bytes), encode their copy descriptors and
  * store them in device memory on the current device.  The pointers are bound
  * at creation: the chain reads and writes the same buffers on every run.  The
  * caller owns the returned chain and frees it with ggq_chain_free.  Errors:
@@ -311,8 +312,10 @@ void ggq_chain_free(ggq_chain* chain);
  * another kernel fail instead of falling back.
  *
  * Arguments and result as for ggq_gemv, within these limits: type GGQ_Q8_0,
- * GGQ_Q4_K or GGQ_Q4_0 (the last two with cols >= 768), cols a multiple of 256, M in 1..4, x' of one activation row in
- * shared memory (cols up to about 40000 at M = 1); other shapes fail with
+ * GGQ_Q4_K or GGQ_Q4_0 (the last two with cols >= 768) with cols a multiple of
+ * 256, or GGQ_Q6_K with cols a multiple of 2048; M in 1..4, x' of one
+ * activation row in shared memory (cols up to about 40000 at M = 1); other
+ * shapes fail with
  * GGQ_EINVAL.  Calls may overlap on the GPU: they share no device memory.
  */
 int ggq_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,

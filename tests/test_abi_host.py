@@ -185,8 +185,14 @@ def test_compute_entry_points_validate_arguments(ggq):
     assert d(ggq.F16, 16, 2, 256, 16, 0) == -2
     assert d(ggq.Q4_0, 16, 2, 40, 16, 0) == -1                       # cols % 32
     assert d(ggq.Q6_K, 16, 2, 100, 16, 0) == -1                      # cols % 256
-    assert ggq.ggq_chain_create(ggq.Q6_K, 1, [([16], [64], 2048, 16, [16])])[0] == -2   # no Q6_K chains
-    assert ggq.ggq_gemv_noalloc(ggq.Q6_K, 16, 4, 1024, 16, 16, 1, 0) == -2
+    # Q6_K rows start on 16 bytes only when cols % 2048 == 0: other widths are refused
+    assert ggq.ggq_chain_create(ggq.Q6_K, 1, [([16], [64], 1024, 16, [16])])[0] == -1
+    assert "stage 0 shape unsupported" in ggq.lib.ggq_last_error().decode()
+    assert ggq.ggq_gemv_noalloc(ggq.Q6_K, 16, 4, 1024, 16, 16, 1, 0) == -1
+    rc, h = ggq.ggq_chain_create(ggq.Q6_K, 1, [([16], [64], 2048, 16, [16])])
+    assert rc not in (-1, -2)                     # past validation (no device here: fails later)
+    if rc == 0:
+        ggq.ggq_chain_free(h)
     assert g(ggq.Q8_0, 16, 4, 64, 16, 16, 17, 0) == -1
     assert "M 17 outside 1..16" in ggq.lib.ggq_last_error().decode()
 

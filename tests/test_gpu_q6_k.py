@@ -1,6 +1,8 @@
-"""GPU parity for Q6_K weights: decode and row gather bit-exact, GEMV (the
-warp-per-row kernel, M 1..16) within the tolerance, one-hot and integer-valued
-cases exact, against the CPU oracle.
+"""GPU parity for Q6_K weights: decode and row gather bit-exact, GEMV within
+the tolerance, one-hot and integer-valued cases exact, against the CPU oracle.
+GEMVs with cols % 2048 == 0 run on the streaming kernel (M 1..4 a launch, M
+5..16 in groups of 4), the others on the warp-per-row kernel; both are covered,
+and so are Q6_K chains of dependent stages.
 
 Bar as for the other types: |y - y_ref| <= 1e-3 * sum_c |w[r,c] x[c]| + 1e-6
 (y_ref in double).
@@ -55,7 +57,10 @@ def test_dequantize_every_code_extreme_scales_and_special_d(env):
     assert np.array_equal(np.isnan(got), np.isnan(ref))
 
 
-SHAPES = [(1, 256), (31, 512), (33, 2304), (100, 4096), (257, 11008), (4099, 1280)]
+# warp-per-row: cols % 2048 != 0; streaming: (33, 2048) a ragged row group,
+# (100, 4096) fewer groups than SMs, (2056, 6144) 24 SBs a row, (4096, 14336)
+SHAPES = [(1, 256), (31, 512), (33, 2304), (257, 11008), (4099, 1280),
+          (33, 2048), (100, 4096), (2056, 6144), (4096, 14336)]
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
@@ -67,7 +72,7 @@ def test_gemv_q6_k(env, rows, cols, M):
     assert_close(gpu_gemv(env, Q6_K, W, rows, cols, x), y_ref, a_ref, f"q6_k {rows}x{cols} M={M}")
 
 
-@pytest.mark.parametrize("cols", [256, 2304])
+@pytest.mark.parametrize("cols", [256, 2304, 2048, 4096])
 def test_gemv_one_hot_extracts_exact_columns(env, cols):
     rows = 37
     W = weights(rows, cols, stream=3)
@@ -93,6 +98,11 @@ def test_gemv_integer_inputs_are_exact(env, M):
     x = rng.integers(-4, 5, size=(M, cols)).astype(np.float32)
     y = gpu_gemv(env, Q6_K, W, rows, cols, x)
     assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ w.T)
+    # the same weights at cols 2304 (warp-per-row kernel): the first 9 SBs of each row
+    W9 = W.reshape(rows, cols // 256, 210)[:, :1].repeat(9, axis=1).reshape(-1).copy()
+    w9 = np.tile(w[:, :256], 9)
+    y9 = gpu_gemv(env, Q6_K, W9, rows, 2304, np.tile(x[:, :256], 9))
+    assert np.array_equal(y9.astype(np.int64), np.tile(x[:, :256], 9).astype(np.int64) @ w9.T)
 
 
 def test_gemv_multi_q6_k(env):
@@ -145,3 +155,31 @@ def test_embed_rows_bit_exact(env, cols):
     assert ggq.device_status() == 0
     ref = oracle.dequantize(Q6_K, W, rows, cols)[ids]
     assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+# ---- Q6_K chains (the streaming kernel's stage boundaries) ---------------------
+
+from tests.test_gpu_chain import Net, _layer, _fused_layers, _check_fused  # noqa: E402
+
+
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_chain_q6_k_two_layers(env, M):
+    """Two layers (hidden 2048, kv 512, ffn 4096): each stage reads the
+    previous stage's y, checked against the oracle fed with what it read."""
+    stages = _layer("a.", 2048, 512, 4096, "x0") + _layer("b.", 2048, 512, 4096, "a.down")
+    net = Net(env, Q6_K, M, stages, seed=5)
+    for run in range(2):
+        x0 = synth.normal_f32(M * 2048, 140 + run).reshape(M, 2048)
+        net.check(x0, net.run(x0))
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_chain_q6_k_fused_layers(env, M):
+    torch, ggq = env
+    chain, h0, plan, _ = _fused_layers(torch, ggq, Q6_K, M, 2048, 512, 4096, 2, seed=40 + M)
+    for run in range(2):
+        h0.copy_(torch.from_numpy((3.0 * synth.normal_f32(M * 2048, 520 + run)).reshape(M, 2048)))
+        chain.run()
+        torch.cuda.synchronize()
+        assert ggq.device_status() == 0
+        _check_fused(Q6_K, plan)

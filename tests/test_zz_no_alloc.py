@@ -27,7 +27,8 @@ def env():
 
 
 @pytest.mark.parametrize("qtype,rows,cols,M", [(12, 4096, 4096, 1), (12, 1000, 11008, 2), (8, 2048, 2048, 1),
-                                               (8, 777, 4096, 3), (2, 3000, 4096, 1), (2, 500, 1024, 4)])
+                                               (8, 777, 4096, 3), (2, 3000, 4096, 1), (2, 500, 1024, 4),
+                                               (14, 3000, 4096, 1), (14, 1000, 14336, 2)])
 def test_noalloc_matches_oracle_and_gemv_twice(env, qtype, rows, cols, M):
     """Two calls in a row: each result within the parity bound of the
     oracle's float64 GEMV, and of ggq_gemv's result; free device memory is

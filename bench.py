@@ -405,9 +405,8 @@ def q4km_file_pass(torch, ggq, synth, stream, steps: int = 20, layers: int = 32)
            "chain_launches": len(fp.chains), "weight_bytes_per_pass": fp.weight_bytes,
            "q6_k_bytes_per_pass": fp.type_bytes.get(14, 0), "file_bytes": file_bytes,
            "generate_s": round(t_gen, 2), "status": rc,
-           "plan": "per layer [q,k,v] [o] [gate,up] [down], split by type; runs of Q4_K stages as one chain "
-                   "launch each, Q6_K stages as their own launches; attn_v and ffn_down Q6_K in odd layers, "
-                   "Q6_K head"}
+           "plan": "per layer [q,k,v] [o] [gate,up] [down], split by type; every stage (Q4_K, Q6_K, "
+                   "the Q6_K head) in one chain launch of mixed types; attn_v and ffn_down Q6_K in odd layers"}
     del g
     fp.close()
     model.close()

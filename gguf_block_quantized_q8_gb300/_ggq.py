@@ -67,6 +67,8 @@ def _bind(lib):
                               ctypes.POINTER(vp)], ctypes.c_int),
         "ggq_chain_create_ops": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ChainStage),
                                   ctypes.POINTER(ChainOps), ctypes.POINTER(vp)], ctypes.c_int),
+        "ggq_chain_create_typed": ([ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ChainStage),
+                                    ctypes.POINTER(ChainOps), ctypes.POINTER(vp)], ctypes.c_int),
         "ggq_chain_run": ([vp, vp], ctypes.c_int),
         "ggq_embed": ([ctypes.c_int, vp, i64, i64, vp, ctypes.c_int, vp, vp], ctypes.c_int),
         "ggq_chain_reset": ([vp], ctypes.c_int),
@@ -126,10 +128,7 @@ def ggq_gemv_multi(qtype: int, Ws, rows, cols: int, x: int, ys, M: int, stream: 
     return lib.ggq_gemv_multi(qtype, n, Wa, ra, cols, x, ya, M, stream)
 
 
-def ggq_chain_create(qtype: int, M: int, stages, ops=None) -> tuple[int, int]:
-    """stages: sequence of (Ws, rows, cols, x, ys) with device pointers; ops: None, or
-    per stage None or a dict with keys x_op, eps, norm_w, up, res (a list of up to 4
-    pointers or None), pointers as ints; returns (rc, handle)."""
+def _chain_arrays(stages, ops):
     arr = (ChainStage * len(stages))()
     for i, (Ws, rows, cols, x, ys) in enumerate(stages):
         st = arr[i]
@@ -140,21 +139,40 @@ def ggq_chain_create(qtype: int, M: int, stages, ops=None) -> tuple[int, int]:
             st.y[j] = ys[j]
         st.cols = cols
         st.x = x
-    h = ctypes.c_void_p()
     if ops is None:
+        return arr, None
+    oa = (ChainOps * len(stages))()
+    for i, o in enumerate(ops):
+        if not o:
+            continue
+        oa[i].x_op = o.get("x_op", X_PLAIN)
+        oa[i].eps = o.get("eps", 0.0)
+        oa[i].norm_w = o.get("norm_w") or None
+        oa[i].up = o.get("up") or None
+        for j, r in enumerate((o.get("res") or [])[:4]):
+            oa[i].res[j] = r or None
+    return arr, oa
+
+
+def ggq_chain_create(qtype: int, M: int, stages, ops=None) -> tuple[int, int]:
+    """stages: sequence of (Ws, rows, cols, x, ys) with device pointers; ops: None, or
+    per stage None or a dict with keys x_op, eps, norm_w, up, res (a list of up to 4
+    pointers or None), pointers as ints; returns (rc, handle)."""
+    arr, oa = _chain_arrays(stages, ops)
+    h = ctypes.c_void_p()
+    if oa is None:
         rc = lib.ggq_chain_create(qtype, M, len(stages), arr, ctypes.byref(h))
     else:
-        oa = (ChainOps * len(stages))()
-        for i, o in enumerate(ops):
-            if not o:
-                continue
-            oa[i].x_op = o.get("x_op", X_PLAIN)
-            oa[i].eps = o.get("eps", 0.0)
-            oa[i].norm_w = o.get("norm_w") or None
-            oa[i].up = o.get("up") or None
-            for j, r in enumerate((o.get("res") or [])[:4]):
-                oa[i].res[j] = r or None
         rc = lib.ggq_chain_create_ops(qtype, M, len(stages), arr, oa, ctypes.byref(h))
+    return rc, (h.value or 0)
+
+
+def ggq_chain_create_typed(M: int, types, stages, ops=None) -> tuple[int, int]:
+    """ggq_chain_create with one weight type per stage (types[s] for stages[s])."""
+    arr, oa = _chain_arrays(stages, ops)
+    ta = (ctypes.c_int * len(stages))(*[int(t) for t in types][:len(stages)])
+    h = ctypes.c_void_p()
+    rc = lib.ggq_chain_create_typed(M, len(stages), ta, arr, oa, ctypes.byref(h))
     return rc, (h.value or 0)
 
 
@@ -319,10 +337,12 @@ def embed(qtype: int, table, rows: int, cols: int, ids, out=None, stream=None):
 class Chain:
     """A sequence of GEMV stages run as one launch (ggq_chain_create / ggq_chain_run).
 
-    stages: sequence of (Ws, rows, cols, x, ys) with CUDA tensors; the chain keeps
-    references to them (their memory is bound at creation).  ops: None, or per
-    stage None or a dict {x_op: X_RMSNORM / X_SILU_MUL, eps, norm_w, up, res: [..]}
-    with CUDA tensors (ggq_chain_create_ops).
+    qtype: the weight type of every stage, or a list with one per stage
+    (ggq_chain_create_typed).  stages: sequence of (Ws, rows, cols, x, ys) with
+    CUDA tensors; the chain keeps references to them (their memory is bound at
+    creation).  ops: None, or per stage None or a dict {x_op: X_RMSNORM /
+    X_SILU_MUL, eps, norm_w, up, res: [..]} with CUDA tensors
+    (ggq_chain_create_ops).
     """
 
     def __init__(self, qtype: int, M: int, stages, ops=None):
@@ -336,7 +356,12 @@ class Chain:
                     {"x_op": o.get("x_op", X_PLAIN), "eps": o.get("eps", 0.0), "norm_w": ptr(o.get("norm_w")),
                      "up": ptr(o.get("up")), "res": [ptr(t) for t in (o.get("res") or [])]}
                     for o in ops]
-        rc, h = ggq_chain_create(qtype, M, raw, rops)
+        if isinstance(qtype, (list, tuple)):
+            if len(qtype) != len(raw):
+                raise ValueError("one weight type per stage")
+            rc, h = ggq_chain_create_typed(M, qtype, raw, rops)
+        else:
+            rc, h = ggq_chain_create(qtype, M, raw, rops)
         check(rc, "ggq_chain_create")
         self._h = h
         self._keep = list(stages) + ([ops] if ops is not None else [])

@@ -6,7 +6,9 @@ Each translation unit is compiled in parallel into ``_build/`` and linked into
 from __future__ import annotations
 
 import concurrent.futures as cf
+import contextlib
 import os
+import resource
 import shutil
 import subprocess
 import sys
@@ -63,13 +65,33 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
+@contextlib.contextmanager
+def _compiler_stack():
+    """Let the compilers started meanwhile grow their stack to 1 GB (or the hard
+    limit): the device compiler recurses deeply over the largest kernels, and
+    with line info their build needed more than the usual 8 MB on aarch64."""
+    soft, hard = resource.getrlimit(resource.RLIMIT_STACK)
+    want = (1 << 30) if hard == resource.RLIM_INFINITY else min(hard, 1 << 30)
+    raised = soft != resource.RLIM_INFINITY and soft < want
+    if raised:
+        try:
+            resource.setrlimit(resource.RLIMIT_STACK, (want, hard))
+        except (ValueError, OSError):
+            raised = False
+    try:
+        yield
+    finally:
+        if raised:
+            resource.setrlimit(resource.RLIMIT_STACK, (soft, hard))
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile (if stale) and return the path of libggq.so."""
     if not force and not is_stale():
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
-    with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
+    with _compiler_stack(), cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
     tmp = LIB + ".tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lrt"]

@@ -80,6 +80,8 @@ struct StageInfo {
     int units;                  // U = cols / 256
     int x_op;                   // GGQ_X_PLAIN / RMSNORM / SILU_MUL
     float eps;                  // RMSNORM
+    int kind;                   // Kind of the stage's weights
+    int pad_[3];
 };
 constexpr int kInfoVec = sizeof(StageInfo) / 16;   // 16-byte pieces
 // While stage s runs, slots hold stages s .. s + kInfoSlots - 2; stage
@@ -124,7 +126,6 @@ struct Blk {
     static constexpr int kNsb = (K == kKQ8 || K == kKQ6) ? 1 : 2;   // SBs per copy
     static constexpr int kPad = K == kKQ8 ? 0 : 2;            // elements of padding per row
     static constexpr int kRow = K == kKQ6 ? 240 : (kElems * kNsb + kPad) * 8;    // smem bytes per row
-    static constexpr int kSums = K == kKQ6 ? 16 : 8;          // x sums per SB (Q6_K: per 16 columns)
     // first 8-byte element of the copy of SB u, and where the SB starts in it
     __host__ __device__ static constexpr int coord(int u) { return K == kKQ6 ? ((210 * u) & ~15) / 8 : u * kElems; }
     __host__ __device__ static constexpr int skew(int u) { return K == kKQ6 ? (210 * u) & 15 : 0; }
@@ -133,6 +134,41 @@ struct Blk {
     // x' floats per SB: Q4_K four chunks of 64 padded to 68; Q8_0 one per byte
     // of the period; Q4_0 two per byte of its four 36-byte chunks
     static constexpr int kXsb = K == kKQ40 ? 288 : 272;
+};
+
+// The weight kinds one kernel instance decodes: a bit mask over Kind.  With one
+// kind every stage is that kind; with several, a stage's kind is read from its
+// fields (StageInfo::kind) and the copy geometry is chosen per stage.  Ring
+// slots are as large as the largest kind's tile.
+template <int KM>
+struct KindSet {
+    static_assert(KM > 0 && KM < 16, "kind mask");
+    static constexpr bool kMixed = (KM & (KM - 1)) != 0;
+    static constexpr int kFirst = (KM & 1) ? 0 : (KM & 2) ? 1 : (KM & 4) ? 2 : 3;
+    static constexpr int cmax(int a, int b) { return a > b ? a : b; }
+    static constexpr int kTile = cmax(cmax((KM & 1) ? Blk<kKQ8>::kTile : 0, (KM & 2) ? Blk<kKQ4K>::kTile : 0),
+                                      cmax((KM & 4) ? Blk<kKQ40>::kTile : 0, (KM & 8) ? Blk<kKQ6>::kTile : 0));
+    static __device__ __forceinline__ bool has(int k) { return (KM >> k) & 1; }
+    // SBs per copy, bytes per copy and the first 8-byte element of SB u's copy
+    static __device__ __forceinline__ int nsb(int k) {
+        if constexpr (!kMixed) return Blk<kFirst>::kNsb;
+        return (k == kKQ4K || k == kKQ40) ? 2 : 1;
+    }
+    static __device__ __forceinline__ int copy(int k) {
+        if constexpr (!kMixed) return Blk<kFirst>::kCopy;
+        return k == kKQ8 ? Blk<kKQ8>::kCopy : k == kKQ4K ? Blk<kKQ4K>::kCopy : k == kKQ40 ? Blk<kKQ40>::kCopy
+                                                                                   : Blk<kKQ6>::kCopy;
+    }
+    static __device__ __forceinline__ int coord(int k, int u) {
+        if constexpr (!kMixed) return Blk<kFirst>::coord(u);
+        return k == kKQ6 ? Blk<kKQ6>::coord(u) : u * (k == kKQ8 ? Blk<kKQ8>::kElems : Blk<kKQ4K>::kElems);
+    }
+};
+static_assert(Blk<kKQ4K>::kElems == Blk<kKQ40>::kElems, "Q4_K and Q4_0 super-blocks are both 144 bytes");
+
+template <int K>
+struct KindTag {
+    static constexpr int value = K;
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -247,10 +283,10 @@ __device__ __forceinline__ void warp_run(const Groups& G, int U, int w, int& t0,
     t1 = (int)(T * (unsigned)(w + 1) / NW);
 }
 
-template <int K, int MMAX, int W>
+template <int KM, int MMAX, int W>
 __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__ StageDesc inl, const ChainParams p) {
-    using B = Blk<K>;
-    constexpr bool Q4K = K == kKQ4K;
+    using KSet = KindSet<KM>;
+    constexpr int kTileK = KSet::kTile;   // ring slot stride
     constexpr int kThreads = 32 * W;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -258,8 +294,8 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     const int D = p.ring;
 
     // shared memory: [warp rings][stage info slots][group ranges][x'][sums][cut-group parts][barriers]
-    uint8_t* ring = smem + (size_t)warp * D * B::kTile;
-    StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)W * D * B::kTile);
+    uint8_t* ring = smem + (size_t)warp * D * kTileK;
+    StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)W * D * kTileK);
     int2* part = reinterpret_cast<int2*>(infos + kInfoSlots);   // [kPartMax]
     float* xp = reinterpret_cast<float*>(part + kPartMax);
     float* sums = xp + (size_t)MMAX * p.xs;
@@ -286,6 +322,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     // group's matrix and first row, advanced without dividing
     int cs = -1, ct = 0, ct1 = 0, cU = 1, cgi = 0, cu = 0, cseg = 0, crow = 0;
     int cnext = 0;                   // first local group of matrix cseg + 1 (groups advance by one)
+    int ckind = KSet::kFirst;        // weight kind of stage cs
     const StageDesc* csd = &inl;
     const StageInfo* cinf = infos;   // the fields of stage cs
     int scur = 0;                    // stage the CTA is in: slots hold scur .. scur + kInfoSlots - 2
@@ -306,6 +343,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             warp_run<W>(cg, cinf->units, warp, ct, ct1);
         }
         cU = cinf->units;
+        if constexpr (KSet::kMixed) ckind = cinf->kind;
         cgi = ct / cU;
         cu = ct - cgi * cU;
         int nrows;
@@ -316,9 +354,9 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     auto refill = [&]() {   // keep up to D copies in flight or resident
         while (inflight < D) {
             if (ct == ct1 && !next_stage()) break;
-            const int nv = min(min(B::kNsb, cU - cu), ct1 - ct);
-            tma_issue_2d(lane == 0, ring + (size_t)islot * B::kTile, &csd->maps[cseg], &full[islot], B::coord(cu),
-                         crow, B::kCopy, wpol);
+            const int nv = min(min(KSet::nsb(ckind), cU - cu), ct1 - ct);
+            tma_issue_2d(lane == 0, ring + (size_t)islot * kTileK, &csd->maps[cseg], &full[islot],
+                         KSet::coord(ckind, cu), crow, KSet::copy(ckind), wpol);
             ct += nv;
             cu += nv;
             if (cu == cU && ct < ct1) {   // next group of this run: same matrix, 16 rows on, or the next matrix
@@ -344,48 +382,20 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         const StageDesc* d0 = p.table ? p.table : &inl;
         const Groups g0 = cta_groups(part[0]);
         const int U0 = infos[0].units;
+        const int k0 = KSet::kMixed ? infos[0].kind : KSet::kFirst;
         int t, tend;
         warp_run<W>(g0, U0, warp, t, tend);
         for (int k = 0; k < D && t < tend; ++k) {
             const int gi = t / U0, u = t - gi * U0;
             int seg, row, nrows;
             group_at(&infos[0], g0, gi, seg, row, nrows);
-            tma_prefetch_2d(&d0->maps[seg], B::coord(u), row);
-            t += min(min(B::kNsb, U0 - u), tend - t);
+            tma_prefetch_2d(&d0->maps[seg], KSet::coord(k0, u), row);
+            t += min(min(KSet::nsb(k0), U0 - u), tend - t);
         }
     }
     pdl_wait();
     refill();
 
-    // x' placement of the lane's 4 consecutive columns 4l .. 4l+3 of a
-    // 128-column half of an SB (the other half adds kXsb / 2 floats).  Q4_K:
-    // chunk l/16 (68 floats each), byte positions b = 0..3 of word l%8, low or
-    // high nibble ((l/8) odd: high) at q4k_xslot, stride 16.  Q8_0: byte
-    // positions of the period, 34 per block of 32 after its 2-byte scale.
-    // Q4_0: block l/8 of the half (chunk l/16, block (l/8)%2 of the chunk),
-    // weights 4(l%8) .. +3 of the block: byte positions 2 + 4(l%4) .. +3 after
-    // the block's start, high nibble when l%8 >= 4, at 2B + hi, stride 2.
-    int xoff;
-    float4 xsc;
-    {
-        const int hi = (lane >> 3) & 1;
-        if (Q4K) {
-            xoff = (lane >> 4) * 68 + 2 * (lane & 7) + hi;
-            const int k = 4 * lane;
-            xsc = make_float4(q4k_xscale(k), q4k_xscale(k + 1), q4k_xscale(k + 2), q4k_xscale(k + 3));
-        } else if (K == kKQ6) {
-            // chunk (h, gp) with gp = (l/8) % 2, pair slot l/16, word l % 8
-            xoff = ((lane >> 3) & 1) * 68 + 2 * (lane & 7) + (lane >> 4);
-            xsc = make_float4(pow2f(53), pow2f(45), pow2f(37), pow2f(37));
-        } else if (K == kKQ40) {
-            const int b4 = lane >> 3;
-            xoff = (b4 >> 1) * 72 + 2 * (18 * (b4 & 1) + 2 + 4 * (lane & 3)) + ((lane >> 2) & 1);
-            xsc = make_float4(q40_xscale(xoff), q40_xscale(xoff + 2), q40_xscale(xoff + 4), q40_xscale(xoff + 6));
-        } else {
-            xoff = 34 * (lane >> 3) + 2 + 4 * (lane & 7);
-            xsc = make_float4(q8_xscale(xoff), q8_xscale(xoff + 1), q8_xscale(xoff + 2), q8_xscale(xoff + 3));
-        }
-    }
     int cslot = 0;          // ring slot of the next copy to consume
     uint32_t cphase = 0;    // its barrier phase
 
@@ -411,353 +421,404 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
         const int cols = sd->cols, U = sd->units;
         const int xs = p.xs, nsub = p.nsub;
 
-        // ---- x' and the 32-column sums of this stage: kXsb floats per SB (Q4_K:
-        // four chunks of 64 in the q4k_xslot order, each padded by 4; Q8_0: one
-        // float per byte position of the period; Q4_0: two per byte position).
-        // x may have been written by other CTAs: read it from L2.
-        {
-            // Lane l of a warp step takes 4 consecutive values (one float4) of x:
-            // 8 lanes cover a 32-column sub-block, whose sum takes 3 shuffles.
-            // A warp step covers 128 columns of one activation row (cols is a
-            // multiple of 256), half of an SB: the lane's place in it and the
-            // scales of its 4 values are the lane constants xoff and xsc.
-            // Every load of a batch is issued before any is used (one L2 round
-            // trip per batch of kBatch float4 per lane).
-            const int c4 = cols / 4;          // float4 per activation row
-            const int n4 = p.M * c4;
-            const float4* x4 = reinterpret_cast<const float4*>(sd->x);
-            // place the float4 v of warp step qb (the lane's 4 columns): x', and
-            // the sub-block sum from 8 lanes
-            auto place = [&](int qb, float4 v) {
-                float sum = (v.x + v.y) + (v.z + v.w);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                const float sum16 = sum;   // Q6_K: 16 columns
-                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                const int m = MMAX == 1 ? 0 : qb / c4;
-                const int h = qb - m * c4;          // first float4 of the step within the row
-                const int u = h >> 6;               // SB
-                float* dst = xp + (size_t)m * xs + u * B::kXsb + ((h & 32) ? B::kXsb / 2 : 0) + xoff;
-                const float4 e = make_float4(v.x * xsc.x, v.y * xsc.y, v.z * xsc.z, v.w * xsc.w);
-                if (Q4K || K == kKQ6) {
-                    dst[0] = e.x;
-                    dst[16] = e.y;
-                    dst[32] = e.z;
-                    dst[48] = e.w;
-                } else if (K == kKQ40) {
-                    dst[0] = e.x;
-                    dst[2] = e.y;
-                    dst[4] = e.z;
-                    dst[6] = e.w;
+        // ---- the stage's work for its weight kind KS: x' and sums, this warp's
+        // tiles, groups cut between warps
+        auto stage_body = [&](auto ktag) {
+            constexpr int KS = decltype(ktag)::value;
+            using BS = Blk<KS>;
+            constexpr bool Q4K = KS == kKQ4K;
+            // x' placement of the lane's 4 consecutive columns 4l .. 4l+3 of a
+            // 128-column half of an SB (the other half adds kXsb / 2 floats).  Q4_K:
+            // chunk l/16 (68 floats each), byte positions b = 0..3 of word l%8, low or
+            // high nibble ((l/8) odd: high) at q4k_xslot, stride 16.  Q8_0: byte
+            // positions of the period, 34 per block of 32 after its 2-byte scale.
+            // Q4_0: block l/8 of the half (chunk l/16, block (l/8)%2 of the chunk),
+            // weights 4(l%8) .. +3 of the block: byte positions 2 + 4(l%4) .. +3 after
+            // the block's start, high nibble when l%8 >= 4, at 2B + hi, stride 2.
+            int xoff;
+            float4 xsc;
+            {
+                const int hi = (lane >> 3) & 1;
+                if (Q4K) {
+                    xoff = (lane >> 4) * 68 + 2 * (lane & 7) + hi;
+                    const int k = 4 * lane;
+                    xsc = make_float4(q4k_xscale(k), q4k_xscale(k + 1), q4k_xscale(k + 2), q4k_xscale(k + 3));
+                } else if (KS == kKQ6) {
+                    // chunk (h, gp) with gp = (l/8) % 2, pair slot l/16, word l % 8
+                    xoff = ((lane >> 3) & 1) * 68 + 2 * (lane & 7) + (lane >> 4);
+                    xsc = make_float4(pow2f(53), pow2f(45), pow2f(37), pow2f(37));
+                } else if (KS == kKQ40) {
+                    const int b4 = lane >> 3;
+                    xoff = (b4 >> 1) * 72 + 2 * (18 * (b4 & 1) + 2 + 4 * (lane & 3)) + ((lane >> 2) & 1);
+                    xsc = make_float4(q40_xscale(xoff), q40_xscale(xoff + 2), q40_xscale(xoff + 4), q40_xscale(xoff + 6));
                 } else {
-                    dst[0] = e.x;
-                    dst[1] = e.y;
-                    dst[2] = e.z;
-                    dst[3] = e.w;
+                    xoff = 34 * (lane >> 3) + 2 + 4 * (lane & 7);
+                    xsc = make_float4(q8_xscale(xoff), q8_xscale(xoff + 1), q8_xscale(xoff + 2), q8_xscale(xoff + 3));
                 }
-                // the code offsets: Q8_0 bytes are stored XOR 0x80 (128), Q4_0 codes are q + 8,
-                // Q6_K codes q + 32 (sums per 16 columns: slot 8 half + 4 gp + 2 (l >= 16) + g / 2)
-                if constexpr (K == kKQ6) {
-                    if ((lane & 3) == 0)
-                        sums[m * nsub + u * 16 + ((h & 32) >> 2) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) +
-                             (lane >> 4)] = 32.0f * sum16;
-                } else if ((lane & 7) == 0) {
-                    sums[m * nsub + u * 8 + ((h & 32) >> 3) + (lane >> 3)] =
-                        Q4K ? sum : (K == kKQ40 ? 8.0f : 128.0f) * sum;
-                }
-            };
-            const int xop = sd->x_op;
-            if (xop == GGQ_X_PLAIN) {
-                constexpr int kBatch = 8;
-                for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
-                    float4 v[kBatch];
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int q = q0 + i * kThreads + lane;
-                        v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+
+            // ---- x' and the 32-column sums of this stage: kXsb floats per SB (Q4_K:
+            // four chunks of 64 in the q4k_xslot order, each padded by 4; Q8_0: one
+            // float per byte position of the period; Q4_0: two per byte position).
+            // x may have been written by other CTAs: read it from L2.
+            {
+                // Lane l of a warp step takes 4 consecutive values (one float4) of x:
+                // 8 lanes cover a 32-column sub-block, whose sum takes 3 shuffles.
+                // A warp step covers 128 columns of one activation row (cols is a
+                // multiple of 256), half of an SB: the lane's place in it and the
+                // scales of its 4 values are the lane constants xoff and xsc.
+                // Every load of a batch is issued before any is used (one L2 round
+                // trip per batch of kBatch float4 per lane).
+                const int c4 = cols / 4;          // float4 per activation row
+                const int n4 = p.M * c4;
+                const float4* x4 = reinterpret_cast<const float4*>(sd->x);
+                // place the float4 v of warp step qb (the lane's 4 columns): x', and
+                // the sub-block sum from 8 lanes
+                auto place = [&](int qb, float4 v) {
+                    float sum = (v.x + v.y) + (v.z + v.w);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                    const float sum16 = sum;   // Q6_K: 16 columns
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                    const int m = MMAX == 1 ? 0 : qb / c4;
+                    const int h = qb - m * c4;          // first float4 of the step within the row
+                    const int u = h >> 6;               // SB
+                    float* dst = xp + (size_t)m * xs + u * BS::kXsb + ((h & 32) ? BS::kXsb / 2 : 0) + xoff;
+                    const float4 e = make_float4(v.x * xsc.x, v.y * xsc.y, v.z * xsc.z, v.w * xsc.w);
+                    if (Q4K || KS == kKQ6) {
+                        dst[0] = e.x;
+                        dst[16] = e.y;
+                        dst[32] = e.z;
+                        dst[48] = e.w;
+                    } else if (KS == kKQ40) {
+                        dst[0] = e.x;
+                        dst[2] = e.y;
+                        dst[4] = e.z;
+                        dst[6] = e.w;
+                    } else {
+                        dst[0] = e.x;
+                        dst[1] = e.y;
+                        dst[2] = e.z;
+                        dst[3] = e.w;
                     }
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int qb = q0 + i * kThreads;   // warp-uniform, a multiple of 32
-                        if (qb >= n4) break;
-                        place(qb, v[i]);
-                    }
-                }
-            } else {
-                // fused step on x ("GGUF Inferencer in R" section 4).  RMSNORM: the
-                // sum of squares of each activation row first (a CTA reduction
-                // through the cut-group scratch, free until the tiles), then
-                // norm_w * x / sqrt(mean + eps).  SILU_MUL: silu(x) * up.
-                const float4* o4 = reinterpret_cast<const float4*>(xop == GGQ_X_RMSNORM ? sd->norm_w : sd->up);
-                constexpr int kBatch = 4;   // two float4 a step: x and norm_w / up
-                float* red = cut_val;       // [W][MMAX]: per-warp sums of squares
-                float rs[MMAX];
-                auto load2 = [&](int q0, float4 (&v)[kBatch], float4 (&o)[kBatch]) {
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int q = q0 + i * kThreads + lane;
-                        const int qb = q0 + i * kThreads;
-                        const int m = MMAX == 1 ? 0 : qb / c4;
-                        v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        o[i] = q < n4 ? __ldcg(o4 + (xop == GGQ_X_RMSNORM ? q - m * c4 : q))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    // the code offsets: Q8_0 bytes are stored XOR 0x80 (128), Q4_0 codes are q + 8,
+                    // Q6_K codes q + 32 (sums per 16 columns: slot 8 half + 4 gp + 2 (l >= 16) + g / 2)
+                    if constexpr (KS == kKQ6) {
+                        if ((lane & 3) == 0)
+                            sums[m * nsub + u * 16 + ((h & 32) >> 2) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) +
+                                 (lane >> 4)] = 32.0f * sum16;
+                    } else if ((lane & 7) == 0) {
+                        sums[m * nsub + u * 8 + ((h & 32) >> 3) + (lane >> 3)] =
+                            Q4K ? sum : (KS == kKQ40 ? 8.0f : 128.0f) * sum;
                     }
                 };
-                // sums of squares per activation row (ss from this thread) -> rs
-                auto reduce_rs = [&](float (&ss)[MMAX]) {
-#pragma unroll
-                    for (int m = 0; m < MMAX; ++m) {
-                        const float t = warp_sum(ss[m]);
-                        if (lane == 0) red[warp * MMAX + m] = t;
-                    }
-                    __syncthreads();
-#pragma unroll
-                    for (int m = 0; m < MMAX; ++m) {
-                        float t = 0.0f;
-                        for (int w2 = 0; w2 < W; ++w2) t += red[w2 * MMAX + m];   // same order in every thread
-                        rs[m] = 1.0f / sqrtf(t / (float)cols + sd->eps);
-                    }
-                };
-                auto transform = [&](int qb, float4 t, float4 o) {
-                    if (xop == GGQ_X_RMSNORM) {
-                        float r = rs[0];
-#pragma unroll
-                        for (int m = 1; m < MMAX; ++m)
-                            if (qb >= m * c4) r = rs[m];
-                        return make_float4(o.x * (t.x * r), o.y * (t.y * r), o.z * (t.z * r), o.w * (t.w * r));
-                    }
-                    return make_float4(t.x / (1.0f + expf(-t.x)) * o.x, t.y / (1.0f + expf(-t.y)) * o.y,
-                                       t.z / (1.0f + expf(-t.z)) * o.z, t.w / (1.0f + expf(-t.w)) * o.w);
-                };
-                if (MMAX <= 2 && xop == GGQ_X_RMSNORM && n4 <= kThreads * kBatch) {
-                    // one batch a thread: the squares come from the registers the
-                    // values are placed from (one L2 round trip; up to 2 activation
-                    // rows, where the registers allow it)
-                    float4 v[kBatch], o[kBatch];
-                    const int q0 = warp * 32;
-                    load2(q0, v, o);
-                    float ss[MMAX];
-#pragma unroll
-                    for (int m = 0; m < MMAX; ++m) ss[m] = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int qb = q0 + i * kThreads;
-                        const float e = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, v[i].w * v[i].w)));
-#pragma unroll
-                        for (int m = 0; m < MMAX; ++m)
-                            if (qb >= m * c4 && qb < (m + 1) * c4) ss[m] += e;   // zero beyond n4
-                    }
-                    reduce_rs(ss);
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int qb = q0 + i * kThreads;
-                        if (qb >= n4) break;
-                        place(qb, transform(qb, v[i], o[i]));
+                const int xop = sd->x_op;
+                if (xop == GGQ_X_PLAIN) {
+                    constexpr int kBatch = 8;
+                    for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                        float4 v[kBatch];
+    #pragma unroll
+                        for (int i = 0; i < kBatch; ++i) {
+                            const int q = q0 + i * kThreads + lane;
+                            v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+    #pragma unroll
+                        for (int i = 0; i < kBatch; ++i) {
+                            const int qb = q0 + i * kThreads;   // warp-uniform, a multiple of 32
+                            if (qb >= n4) break;
+                            place(qb, v[i]);
+                        }
                     }
                 } else {
-                    if (xop == GGQ_X_RMSNORM) {
-                        // x too long for one batch: a first pass for the squares
-                        float ss[MMAX];
-#pragma unroll
+                    // fused step on x ("GGUF Inferencer in R" section 4).  RMSNORM: the
+                    // sum of squares of each activation row first (a CTA reduction
+                    // through the cut-group scratch, free until the tiles), then
+                    // norm_w * x / sqrt(mean + eps).  SILU_MUL: silu(x) * up.
+                    const float4* o4 = reinterpret_cast<const float4*>(xop == GGQ_X_RMSNORM ? sd->norm_w : sd->up);
+                    constexpr int kBatch = 4;   // two float4 a step: x and norm_w / up
+                    float* red = cut_val;       // [W][MMAX]: per-warp sums of squares
+                    float rs[MMAX];
+                    auto load2 = [&](int q0, float4 (&v)[kBatch], float4 (&o)[kBatch]) {
+    #pragma unroll
+                        for (int i = 0; i < kBatch; ++i) {
+                            const int q = q0 + i * kThreads + lane;
+                            const int qb = q0 + i * kThreads;
+                            const int m = MMAX == 1 ? 0 : qb / c4;
+                            v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            o[i] = q < n4 ? __ldcg(o4 + (xop == GGQ_X_RMSNORM ? q - m * c4 : q))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    };
+                    // sums of squares per activation row (ss from this thread) -> rs
+                    auto reduce_rs = [&](float (&ss)[MMAX]) {
+    #pragma unroll
                         for (int m = 0; m < MMAX; ++m) {
-                            ss[m] = 0.0f;
-                            if (m < p.M) {
-#pragma unroll 4
-                                for (int q = tid; q < c4; q += kThreads) {
-                                    const float4 v = __ldcg(x4 + (size_t)m * c4 + q);
-                                    ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
-                                }
-                            }
+                            const float t = warp_sum(ss[m]);
+                            if (lane == 0) red[warp * MMAX + m] = t;
+                        }
+                        __syncthreads();
+    #pragma unroll
+                        for (int m = 0; m < MMAX; ++m) {
+                            float t = 0.0f;
+                            for (int w2 = 0; w2 < W; ++w2) t += red[w2 * MMAX + m];   // same order in every thread
+                            rs[m] = 1.0f / sqrtf(t / (float)cols + sd->eps);
+                        }
+                    };
+                    auto transform = [&](int qb, float4 t, float4 o) {
+                        if (xop == GGQ_X_RMSNORM) {
+                            float r = rs[0];
+    #pragma unroll
+                            for (int m = 1; m < MMAX; ++m)
+                                if (qb >= m * c4) r = rs[m];
+                            return make_float4(o.x * (t.x * r), o.y * (t.y * r), o.z * (t.z * r), o.w * (t.w * r));
+                        }
+                        return make_float4(t.x / (1.0f + expf(-t.x)) * o.x, t.y / (1.0f + expf(-t.y)) * o.y,
+                                           t.z / (1.0f + expf(-t.z)) * o.z, t.w / (1.0f + expf(-t.w)) * o.w);
+                    };
+                    if (MMAX <= 2 && xop == GGQ_X_RMSNORM && n4 <= kThreads * kBatch) {
+                        // one batch a thread: the squares come from the registers the
+                        // values are placed from (one L2 round trip; up to 2 activation
+                        // rows, where the registers allow it)
+                        float4 v[kBatch], o[kBatch];
+                        const int q0 = warp * 32;
+                        load2(q0, v, o);
+                        float ss[MMAX];
+    #pragma unroll
+                        for (int m = 0; m < MMAX; ++m) ss[m] = 0.0f;
+    #pragma unroll
+                        for (int i = 0; i < kBatch; ++i) {
+                            const int qb = q0 + i * kThreads;
+                            const float e = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, v[i].w * v[i].w)));
+    #pragma unroll
+                            for (int m = 0; m < MMAX; ++m)
+                                if (qb >= m * c4 && qb < (m + 1) * c4) ss[m] += e;   // zero beyond n4
                         }
                         reduce_rs(ss);
-                    }
-                    for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
-                        float4 v[kBatch], o[kBatch];
-                        load2(q0, v, o);
-#pragma unroll
+    #pragma unroll
                         for (int i = 0; i < kBatch; ++i) {
                             const int qb = q0 + i * kThreads;
                             if (qb >= n4) break;
                             place(qb, transform(qb, v[i], o[i]));
                         }
+                    } else {
+                        if (xop == GGQ_X_RMSNORM) {
+                            // x too long for one batch: a first pass for the squares
+                            float ss[MMAX];
+    #pragma unroll
+                            for (int m = 0; m < MMAX; ++m) {
+                                ss[m] = 0.0f;
+                                if (m < p.M) {
+    #pragma unroll 4
+                                    for (int q = tid; q < c4; q += kThreads) {
+                                        const float4 v = __ldcg(x4 + (size_t)m * c4 + q);
+                                        ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
+                                    }
+                                }
+                            }
+                            reduce_rs(ss);
+                        }
+                        for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                            float4 v[kBatch], o[kBatch];
+                            load2(q0, v, o);
+    #pragma unroll
+                            for (int i = 0; i < kBatch; ++i) {
+                                const int qb = q0 + i * kThreads;
+                                if (qb >= n4) break;
+                                place(qb, transform(qb, v[i], o[i]));
+                            }
+                        }
                     }
                 }
             }
-        }
-        if (tid < 2 * W) cut_grp[tid] = -1;
-        __syncthreads();
+            if (tid < 2 * W) cut_grp[tid] = -1;
+            __syncthreads();
 
-        // ---- this warp's tiles
-        constexpr int R = kRowsPerLane;
-        float acc[R][MMAX];     // rows r + 8i of the group
-        float2 acc2[R][MMAX];   // Q4_K: (low-nibble part, high-nibble part)
-#pragma unroll
-        for (int i = 0; i < R; ++i)
-#pragma unroll
-            for (int m = 0; m < MMAX; ++m) {
-                acc[i][m] = 0.0f;
-                acc2[i][m] = make_float2(0.0f, 0.0f);
-            }
-        int cur = -1;   // group being accumulated
-        // the residual of the group's rows (lanes c == 0), read when the warp
-        // starts a group whose first tile is in its run: that warp's part of
-        // the group is the one that carries it (deterministic sum order)
-        float resv[R][MMAX];
-#pragma unroll
-        for (int i = 0; i < R; ++i)
-#pragma unroll
-            for (int m = 0; m < MMAX; ++m) resv[i][m] = 0.0f;
-        auto load_res = [&](int gi) {
-            if (c != 0 || gi * U < t0) return;
-            int seg, row, nrows;
-            group_at(sd, G, gi, seg, row, nrows);
-            const float* rp = sd->res[seg];
-            if (!rp) return;
-            const int rows = sd->rows[seg];
-#pragma unroll
+            // ---- this warp's tiles
+            constexpr int R = kRowsPerLane;
+            float acc[R][MMAX];     // rows r + 8i of the group
+            float2 acc2[R][MMAX];   // Q4_K: (low-nibble part, high-nibble part)
+    #pragma unroll
             for (int i = 0; i < R; ++i)
-#pragma unroll
-                for (int m = 0; m < MMAX; ++m)
-                    resv[i][m] = (r + 8 * i < nrows && m < p.M) ? __ldcg(rp + (int64_t)m * rows + row + r + 8 * i) : 0.0f;
-        };
-
-        // finish group gi: add each row's four chunks, then store the group's
-        // rows if this warp saw all of its SBs, else keep this warp's part
-        auto flush = [&](int gi) {
-#pragma unroll
-            for (int i = 0; i < R; ++i)
-#pragma unroll
+    #pragma unroll
                 for (int m = 0; m < MMAX; ++m) {
-                    if constexpr (Q4K) {
-                        acc[i][m] = acc2[i][m].x + acc2[i][m].y;
-                        acc2[i][m] = make_float2(0.0f, 0.0f);
-                    }
-                    acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], 1);
-                    acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], 2);
+                    acc[i][m] = 0.0f;
+                    acc2[i][m] = make_float2(0.0f, 0.0f);
                 }
-            const bool started = gi * U >= t0;
-            const bool whole = started && (gi + 1) * U <= t1;
-            if (started && c == 0) {
-#pragma unroll
-                for (int i = 0; i < R; ++i)
-#pragma unroll
-                    for (int m = 0; m < MMAX; ++m) {
-                        acc[i][m] += resv[i][m];
-                        resv[i][m] = 0.0f;
-                    }
-            }
-            if (whole) {
+            int cur = -1;   // group being accumulated
+            // the residual of the group's rows (lanes c == 0), read when the warp
+            // starts a group whose first tile is in its run: that warp's part of
+            // the group is the one that carries it (deterministic sum order)
+            float resv[R][MMAX];
+    #pragma unroll
+            for (int i = 0; i < R; ++i)
+    #pragma unroll
+                for (int m = 0; m < MMAX; ++m) resv[i][m] = 0.0f;
+            auto load_res = [&](int gi) {
+                if (c != 0 || gi * U < t0) return;
                 int seg, row, nrows;
                 group_at(sd, G, gi, seg, row, nrows);
-                if (c == 0) {
-                    const int rows = sd->rows[seg];
-#pragma unroll
+                const float* rp = sd->res[seg];
+                if (!rp) return;
+                const int rows = sd->rows[seg];
+    #pragma unroll
+                for (int i = 0; i < R; ++i)
+    #pragma unroll
+                    for (int m = 0; m < MMAX; ++m)
+                        resv[i][m] = (r + 8 * i < nrows && m < p.M) ? __ldcg(rp + (int64_t)m * rows + row + r + 8 * i) : 0.0f;
+            };
+
+            // finish group gi: add each row's four chunks, then store the group's
+            // rows if this warp saw all of its SBs, else keep this warp's part
+            auto flush = [&](int gi) {
+    #pragma unroll
+                for (int i = 0; i < R; ++i)
+    #pragma unroll
+                    for (int m = 0; m < MMAX; ++m) {
+                        if constexpr (Q4K) {
+                            acc[i][m] = acc2[i][m].x + acc2[i][m].y;
+                            acc2[i][m] = make_float2(0.0f, 0.0f);
+                        }
+                        acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], 1);
+                        acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], 2);
+                    }
+                const bool started = gi * U >= t0;
+                const bool whole = started && (gi + 1) * U <= t1;
+                if (started && c == 0) {
+    #pragma unroll
                     for (int i = 0; i < R; ++i)
-                        if (r + 8 * i < nrows) {
-                            float* ys = sd->y[seg] + row + r + 8 * i;
-#pragma unroll
-                            for (int m = 0; m < MMAX; ++m)
-                                if (m < p.M) ys[(int64_t)m * rows] = acc[i][m];
+    #pragma unroll
+                        for (int m = 0; m < MMAX; ++m) {
+                            acc[i][m] += resv[i][m];
+                            resv[i][m] = 0.0f;
                         }
                 }
-            } else {
-                // part of a group that started before this run (slot 0) or that
-                // goes on past it (slot 1)
-                const int k = started ? 1 : 0;
-                if (c == 0) {
-#pragma unroll
-                    for (int i = 0; i < R; ++i)
-#pragma unroll
-                        for (int m = 0; m < MMAX; ++m)
-                            cut_val[((k * W + warp) * kGroupRows + r + 8 * i) * MMAX + m] = acc[i][m];
-                }
-                if (lane == 0) cut_grp[k * W + warp] = gi;
-            }
-#pragma unroll
-            for (int i = 0; i < R; ++i)
-#pragma unroll
-                for (int m = 0; m < MMAX; ++m) acc[i][m] = 0.0f;
-        };
-
-        int gi = t0 / U, u = t0 - (t0 / U) * U;   // (group, SB) of tile t, advanced without dividing
-        for (int t = t0; t < t1;) {
-            const int nv = min(min(B::kNsb, U - u), t1 - t);
-            if (gi != cur) {
-                if (cur >= 0) flush(cur);
-                load_res(gi);
-                cur = gi;
-            }
-            wait_full(&full[cslot], cphase, p.status);
-            const int slot = cslot;
-            const uint8_t* rowp = ring + (size_t)slot * B::kTile + r * B::kRow;
-#pragma unroll
-            for (int j = 0; j < B::kNsb; ++j) {
-                if (j < nv) {
-                    const int uj = u + j;
-                    if constexpr (Q4K) {
-                        q4k_chunk_rows<MMAX, R>(rowp + j * B::kBytes, 8 * B::kRow, c, xp + uj * B::kXsb, xs,
-                                                sums + uj * 8, nsub, acc2, 68);
-                    } else if constexpr (K == kKQ6) {
-                        q6k_chunk_rows<MMAX, R>(rowp, B::skew(uj), 8 * B::kRow, c, xp + uj * B::kXsb + 68 * c, xs,
-                                                sums + uj * 16 + 8 * (c >> 1) + 4 * (c & 1), nsub, acc);
-                    } else if constexpr (K == kKQ40) {
-                        q40_chunk_rows<MMAX, R>(rowp + j * B::kBytes + 36 * c, 8 * B::kRow, xp + uj * B::kXsb + 72 * c,
-                                                xs, sums + uj * 8 + 2 * c, nsub, acc);
-                    } else {
-#pragma unroll
+                if (whole) {
+                    int seg, row, nrows;
+                    group_at(sd, G, gi, seg, row, nrows);
+                    if (c == 0) {
+                        const int rows = sd->rows[seg];
+    #pragma unroll
                         for (int i = 0; i < R; ++i)
-                            q8_chunk<MMAX>(rowp + 8 * i * B::kRow + j * B::kBytes + 68 * c, xp + uj * B::kXsb + 68 * c,
-                                           xs, sums + uj * 8 + 2 * c, nsub, acc[i]);
+                            if (r + 8 * i < nrows) {
+                                float* ys = sd->y[seg] + row + r + 8 * i;
+    #pragma unroll
+                                for (int m = 0; m < MMAX; ++m)
+                                    if (m < p.M) ys[(int64_t)m * rows] = acc[i][m];
+                            }
+                    }
+                } else {
+                    // part of a group that started before this run (slot 0) or that
+                    // goes on past it (slot 1)
+                    const int k = started ? 1 : 0;
+                    if (c == 0) {
+    #pragma unroll
+                        for (int i = 0; i < R; ++i)
+    #pragma unroll
+                            for (int m = 0; m < MMAX; ++m)
+                                cut_val[((k * W + warp) * kGroupRows + r + 8 * i) * MMAX + m] = acc[i][m];
+                    }
+                    if (lane == 0) cut_grp[k * W + warp] = gi;
+                }
+    #pragma unroll
+                for (int i = 0; i < R; ++i)
+    #pragma unroll
+                    for (int m = 0; m < MMAX; ++m) acc[i][m] = 0.0f;
+            };
+
+            int gi = t0 / U, u = t0 - (t0 / U) * U;   // (group, SB) of tile t, advanced without dividing
+            for (int t = t0; t < t1;) {
+                const int nv = min(min(BS::kNsb, U - u), t1 - t);
+                if (gi != cur) {
+                    if (cur >= 0) flush(cur);
+                    load_res(gi);
+                    cur = gi;
+                }
+                wait_full(&full[cslot], cphase, p.status);
+                const int slot = cslot;
+                const uint8_t* rowp = ring + (size_t)slot * kTileK + r * BS::kRow;
+    #pragma unroll
+                for (int j = 0; j < BS::kNsb; ++j) {
+                    if (j < nv) {
+                        const int uj = u + j;
+                        if constexpr (Q4K) {
+                            q4k_chunk_rows<MMAX, R>(rowp + j * BS::kBytes, 8 * BS::kRow, c, xp + uj * BS::kXsb, xs,
+                                                    sums + uj * 8, nsub, acc2, 68);
+                        } else if constexpr (KS == kKQ6) {
+                            q6k_chunk_rows<MMAX, R>(rowp, BS::skew(uj), 8 * BS::kRow, c, xp + uj * BS::kXsb + 68 * c, xs,
+                                                    sums + uj * 16 + 8 * (c >> 1) + 4 * (c & 1), nsub, acc);
+                        } else if constexpr (KS == kKQ40) {
+                            q40_chunk_rows<MMAX, R>(rowp + j * BS::kBytes + 36 * c, 8 * BS::kRow, xp + uj * BS::kXsb + 72 * c,
+                                                    xs, sums + uj * 8 + 2 * c, nsub, acc);
+                        } else {
+    #pragma unroll
+                            for (int i = 0; i < R; ++i)
+                                q8_chunk<MMAX>(rowp + 8 * i * BS::kRow + j * BS::kBytes + 68 * c, xp + uj * BS::kXsb + 68 * c,
+                                               xs, sums + uj * 8 + 2 * c, nsub, acc[i]);
+                        }
                     }
                 }
-            }
-            __syncwarp();   // every lane is done with the buffer
-            if (++cslot == D) {
-                cslot = 0;
-                cphase ^= 1u;
-            }
-            --inflight;
-            refill();
-            t += nv;
-            u += nv;
-            if (u == U) {
-                u = 0;
-                ++gi;
-            }
-        }
-        if (cur >= 0) flush(cur);
-        __syncthreads();
-
-        // ---- groups cut between warps: the warp where the group starts adds the
-        // later warps' parts in order and stores it (lane r: row r)
-        if (cut_grp[W + warp] >= 0 && lane < kGroupRows) {
-            const int gi = cut_grp[W + warp];
-            float tsum[MMAX];
-#pragma unroll
-            for (int m = 0; m < MMAX; ++m) tsum[m] = cut_val[((W + warp) * kGroupRows + lane) * MMAX + m];
-            // the other parts: the later warps whose (non-empty) run starts
-            // inside this group, told from the run bounds alone so that every
-            // load is independent; added in warp order
-            const int g0 = gi * U, g1 = g0 + U;
-#pragma unroll
-            for (int w2 = 1; w2 < W; ++w2) {
-                int a2, b2;
-                warp_run<W>(G, U, w2, a2, b2);
-                const bool part = w2 > warp && a2 < b2 && a2 > g0 && a2 < g1;
-#pragma unroll
-                for (int m = 0; m < MMAX; ++m) {
-                    const float v = cut_val[(w2 * kGroupRows + lane) * MMAX + m];
-                    if (part) tsum[m] += v;
+                __syncwarp();   // every lane is done with the buffer
+                if (++cslot == D) {
+                    cslot = 0;
+                    cphase ^= 1u;
+                }
+                --inflight;
+                refill();
+                t += nv;
+                u += nv;
+                if (u == U) {
+                    u = 0;
+                    ++gi;
                 }
             }
-            int seg, row, nrows;
-            group_at(sd, G, gi, seg, row, nrows);
-            if (lane < nrows) {
-                const int rows = sd->rows[seg];
-                float* ys = sd->y[seg] + row + lane;
-#pragma unroll
-                for (int m = 0; m < MMAX; ++m)
-                    if (m < p.M) ys[(int64_t)m * rows] = tsum[m];
+            if (cur >= 0) flush(cur);
+            __syncthreads();
+
+            // ---- groups cut between warps: the warp where the group starts adds the
+            // later warps' parts in order and stores it (lane r: row r)
+            if (cut_grp[W + warp] >= 0 && lane < kGroupRows) {
+                const int gi = cut_grp[W + warp];
+                float tsum[MMAX];
+    #pragma unroll
+                for (int m = 0; m < MMAX; ++m) tsum[m] = cut_val[((W + warp) * kGroupRows + lane) * MMAX + m];
+                // the other parts: the later warps whose (non-empty) run starts
+                // inside this group, told from the run bounds alone so that every
+                // load is independent; added in warp order
+                const int g0 = gi * U, g1 = g0 + U;
+    #pragma unroll
+                for (int w2 = 1; w2 < W; ++w2) {
+                    int a2, b2;
+                    warp_run<W>(G, U, w2, a2, b2);
+                    const bool part = w2 > warp && a2 < b2 && a2 > g0 && a2 < g1;
+    #pragma unroll
+                    for (int m = 0; m < MMAX; ++m) {
+                        const float v = cut_val[(w2 * kGroupRows + lane) * MMAX + m];
+                        if (part) tsum[m] += v;
+                    }
+                }
+                int seg, row, nrows;
+                group_at(sd, G, gi, seg, row, nrows);
+                if (lane < nrows) {
+                    const int rows = sd->rows[seg];
+                    float* ys = sd->y[seg] + row + lane;
+    #pragma unroll
+                    for (int m = 0; m < MMAX; ++m)
+                        if (m < p.M) ys[(int64_t)m * rows] = tsum[m];
+                }
+            }
+        };
+        if constexpr (!KSet::kMixed) {
+            stage_body(KindTag<KSet::kFirst>{});
+        } else {
+            const int kd = sd->kind;
+            if (kd == kKQ4K) {
+                if constexpr ((KM >> kKQ4K) & 1) stage_body(KindTag<kKQ4K>{});
+            } else if (kd == kKQ6) {
+                if constexpr ((KM >> kKQ6) & 1) stage_body(KindTag<kKQ6>{});
+            } else if (kd == kKQ40) {
+                if constexpr ((KM >> kKQ40) & 1) stage_body(KindTag<kKQ40>{});
+            } else {
+                if constexpr ((KM >> kKQ8) & 1) stage_body(KindTag<kKQ8>{});
             }
         }
 
@@ -795,17 +856,8 @@ int num_sms() {
 
 int mmax_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : 4; }
 
-// Warps per CTA.  GGQ_STREAM_WARPS=8|12|16 overrides the default for M = 1 (a
-// tuning aid; read once, so a chain keeps the layout it was created with).
-int warps_of(int mmax) {
-    static const int env = [] {
-        const char* v = getenv("GGQ_STREAM_WARPS");
-        const int w = v ? atoi(v) : 0;
-        return (w == 8 || w == 12 || w == 16) ? w : 0;
-    }();
-    if (env && mmax == 1) return env;
-    return mmax == 4 ? 12 : 16;
-}
+// Warps per CTA: 16, or 12 where four activation rows need the registers
+int warps_of(int mmax) { return mmax == 4 ? 12 : 16; }
 
 int kind_of(int type) {
     return type == GGQ_Q4_K ? kKQ4K : type == GGQ_Q4_0 ? kKQ40 : type == GGQ_Q6_K ? kKQ6 : kKQ8;
@@ -825,20 +877,43 @@ int xsb_of(int kind) { return kind == kKQ40 ? Blk<kKQ40>::kXsb : kind == kKQ4K ?
 int64_t sb_bytes(int kind) { return kind == kKQ8 ? 272 : kind == kKQ6 ? 210 : 144; }
 int sums_per_sb(int kind) { return kind == kKQ6 ? 16 : 8; }
 
-size_t rows_smem(int kind, int mmax, int ring, int64_t cols_max) {
+// The kernel instance that runs the kinds of a chain: one kind, or Q6_K with
+// Q4_K (Q4_K_M / Q4_K_S files) or with Q4_0 (a Q6_K output head); 0: no
+// instance.  (An instance decoding all four kinds is one kernel function large
+// enough that building it with line info overflowed the compiler's stack.)
+constexpr int kMixQ4K = (1 << kKQ4K) | (1 << kKQ6);
+constexpr int kMixQ40 = (1 << kKQ40) | (1 << kKQ6);
+int mask_of(int kinds) {
+    if (kinds > 0 && (kinds & (kinds - 1)) == 0) return kinds;
+    if ((kinds & ~kMixQ4K) == 0) return kMixQ4K;
+    if ((kinds & ~kMixQ40) == 0) return kMixQ40;
+    return 0;
+}
+
+// the largest per-kind size over the kinds of a mask
+template <typename F>
+int64_t max_over(int kmask, F f) {
+    int64_t v = 0;
+    for (int k = 0; k < 4; ++k)
+        if ((kmask >> k) & 1) v = std::max<int64_t>(v, (int64_t)f(k));
+    return v;
+}
+
+// Shared memory of a launch over stages of the kinds in `kinds`: ring slots
+// of the instance's size, x' and sums for the kinds present
+size_t rows_smem(int kinds, int mmax, int ring, int64_t cols_max) {
     const int W = warps_of(mmax);
     const int64_t U = cols_max / 256;
     const size_t cut = (size_t)2 * W * kGroupRows * mmax * 4 + (size_t)2 * W * 4;
-    return (size_t)W * ring * tile_bytes(kind) + kInfoSlots * sizeof(StageInfo) + kPartMax * sizeof(int2) +
-           (size_t)mmax * U * xsb_of(kind) * 4 +
-           (size_t)mmax * U * sums_per_sb(kind) * 4 + cut +
-           (size_t)W * ring * 8;
+    return (size_t)W * ring * max_over(mask_of(kinds), tile_bytes) + kInfoSlots * sizeof(StageInfo) +
+           kPartMax * sizeof(int2) + (size_t)mmax * U * max_over(kinds, xsb_of) * 4 +
+           (size_t)mmax * U * max_over(kinds, sums_per_sb) * 4 + cut + (size_t)W * ring * 8;
 }
 
-int rows_ring(int kind, int mmax, int64_t cols_max) {
+int rows_ring(int kinds, int mmax, int64_t cols_max) {
     int ring = kMaxRing;
-    while (ring > 1 && rows_smem(kind, mmax, ring, cols_max) > kSmemLimit) --ring;
-    return rows_smem(kind, mmax, ring, cols_max) <= kSmemLimit ? ring : 0;
+    while (ring > 1 && rows_smem(kinds, mmax, ring, cols_max) > kSmemLimit) --ring;
+    return rows_smem(kinds, mmax, ring, cols_max) <= kSmemLimit ? ring : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -890,12 +965,13 @@ int make_stage(int type, int n, const void* const* W, const int64_t* rows, int64
     sd->info.x = x;
     sd->info.cols = (int)cols;
     sd->info.units = (int)(cols / 256);
+    sd->info.kind = kind;
     return GGQ_OK;
 }
 
-template <int K, int MMAX, int W>
+template <int KM, int MMAX, int W>
 int launch_t(const StageDesc& inl, const ChainParams& p, cudaStream_t stream, size_t smem, bool cooperative) {
-    auto kernel = rows_kernel<K, MMAX, W>;
+    auto kernel = rows_kernel<KM, MMAX, W>;
     // largest dynamic smem set so far, per device; host threads may launch
     // concurrently, so the check is atomic and the update serialised
     static std::atomic<int> configured[64] = {};
@@ -929,51 +1005,38 @@ int launch_t(const StageDesc& inl, const ChainParams& p, cudaStream_t stream, si
 }
 
 // Launch the kernel: `table` (device) holds nstages stages, or is null and
-// `inl` is the only stage.
-int launch_rows(int type, int M, const StageDesc& inl, const StageDesc* table, int nstages, int64_t cols_max,
+// `inl` is the only stage; `kinds` is the mask of their weight kinds.
+int launch_rows(int kinds, int M, const StageDesc& inl, const StageDesc* table, int nstages, int64_t cols_max,
                 int* counter, cudaStream_t stream) {
-    const int kind = kind_of(type);
+    const int km = mask_of(kinds);
     const int mmax = mmax_of(M);
-    const int W = warps_of(mmax);
     ChainParams p = {};
     p.table = table;
     p.nstages = nstages;
     p.M = M;
-    p.ring = rows_ring(kind, mmax, cols_max);
+    p.ring = rows_ring(kinds, mmax, cols_max);
     if (p.ring == 0) return fail(GGQ_EINVAL, "shape needs too much shared memory");
-    p.xs = (int)(cols_max / 256 * xsb_of(kind));
-    p.nsub = (int)(cols_max / 256 * sums_per_sb(kind));
+    p.xs = (int)(cols_max / 256 * max_over(kinds, xsb_of));
+    p.nsub = (int)(cols_max / 256 * max_over(kinds, sums_per_sb));
     p.counter = counter;
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
-    const size_t smem = rows_smem(kind, mmax, p.ring, cols_max);
+    const size_t smem = rows_smem(kinds, mmax, p.ring, cols_max);
     const bool coop = nstages > 1;
-    if (kind == kKQ4K) {
-        if (mmax == 1) {
-            if (W == 8) return launch_t<kKQ4K, 1, 8>(inl, p, stream, smem, coop);
-            if (W == 12) return launch_t<kKQ4K, 1, 12>(inl, p, stream, smem, coop);
-            return launch_t<kKQ4K, 1, 16>(inl, p, stream, smem, coop);
-        }
-        if (mmax == 2) return launch_t<kKQ4K, 2, 16>(inl, p, stream, smem, coop);
-        return launch_t<kKQ4K, 4, 12>(inl, p, stream, smem, coop);
+    switch (km * 8 + mmax) {
+#define GGQ_ROWS_CASE(KM)                                                                         \
+    case (KM) * 8 + 1: return launch_t<(KM), 1, 16>(inl, p, stream, smem, coop);                \
+    case (KM) * 8 + 2: return launch_t<(KM), 2, 16>(inl, p, stream, smem, coop);                \
+    case (KM) * 8 + 4: return launch_t<(KM), 4, 12>(inl, p, stream, smem, coop);
+        GGQ_ROWS_CASE(1 << kKQ8)
+        GGQ_ROWS_CASE(1 << kKQ4K)
+        GGQ_ROWS_CASE(1 << kKQ40)
+        GGQ_ROWS_CASE(1 << kKQ6)
+        GGQ_ROWS_CASE(kMixQ4K)
+        GGQ_ROWS_CASE(kMixQ40)
+#undef GGQ_ROWS_CASE
+        default: return fail(GGQ_EINVAL, "no kernel instance for kinds %d, M %d", kinds, M);
     }
-    if (kind == kKQ6) {
-        if (mmax == 1) return launch_t<kKQ6, 1, 16>(inl, p, stream, smem, coop);
-        if (mmax == 2) return launch_t<kKQ6, 2, 16>(inl, p, stream, smem, coop);
-        return launch_t<kKQ6, 4, 12>(inl, p, stream, smem, coop);
-    }
-    if (kind == kKQ40) {   // the warp-count override is not instantiated for Q4_0
-        if (mmax == 1) return launch_t<kKQ40, 1, 16>(inl, p, stream, smem, coop);
-        if (mmax == 2) return launch_t<kKQ40, 2, 16>(inl, p, stream, smem, coop);
-        return launch_t<kKQ40, 4, 12>(inl, p, stream, smem, coop);
-    }
-    if (mmax == 1) {
-        if (W == 8) return launch_t<kKQ8, 1, 8>(inl, p, stream, smem, coop);
-        if (W == 12) return launch_t<kKQ8, 1, 12>(inl, p, stream, smem, coop);
-        return launch_t<kKQ8, 1, 16>(inl, p, stream, smem, coop);
-    }
-    if (mmax == 2) return launch_t<kKQ8, 2, 16>(inl, p, stream, smem, coop);
-    return launch_t<kKQ8, 4, 12>(inl, p, stream, smem, coop);
 }
 
 }  // namespace
@@ -988,7 +1051,7 @@ bool stream_gemv_supported(int type, int64_t cols, int M, int nseg, const int64_
     int64_t r = 0;
     for (int s = 0; s < nseg; ++s) r += rows[s];
     if (r * (cols / 256) >= (1ll << 31)) return false;   // SB indices are 32-bit
-    return rows_ring(kind_of(type), mmax_of(M), cols) > 0;
+    return rows_ring(1 << kind_of(type), mmax_of(M), cols) > 0;
 }
 
 int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
@@ -996,7 +1059,7 @@ int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* 
     StageDesc sd;
     int rc = make_stage(type, nseg, W, rows, cols, x, y, &sd);
     if (rc) return rc;
-    return launch_rows(type, M, sd, nullptr, 1, cols, nullptr, stream);
+    return launch_rows(1 << kind_of(type), M, sd, nullptr, 1, cols, nullptr, stream);
 }
 
 }  // namespace ggq
@@ -1006,7 +1069,7 @@ int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* 
 using namespace ggq;
 
 struct ggq_chain {
-    int type = 0;
+    int kinds = 0;   // mask of the stages' weight kinds
     int M = 0;
     int nstages = 0;
     int64_t cols_max = 0;
@@ -1024,13 +1087,30 @@ extern "C" int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chai
     clear_error();
     if (!out) return fail(GGQ_EINVAL, "ggq_chain_create: out is NULL");
     *out = nullptr;
-    if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0 && type != GGQ_Q6_K)
-        return fail(GGQ_ETYPE, "ggq_chain_create: type %d not supported", type);
-    if (M < 1 || M > kMaxM) return fail(GGQ_EINVAL, "ggq_chain_create: M %d outside 1..%d", M, kMaxM);
     if (nstages < 1 || nstages > 65536 || !stages) return fail(GGQ_EINVAL, "ggq_chain_create: bad stage list");
+    std::vector<int> types((size_t)nstages, type);
+    return ggq_chain_create_typed(M, nstages, types.data(), stages, ops, out);
+}
+
+extern "C" int ggq_chain_create_typed(int M, int nstages, const int* types, const ggq_chain_stage* stages,
+                                      const ggq_chain_ops* ops, ggq_chain** out) {
+    clear_error();
+    if (!out) return fail(GGQ_EINVAL, "ggq_chain_create: out is NULL");
+    *out = nullptr;
+    if (M < 1 || M > kMaxM) return fail(GGQ_EINVAL, "ggq_chain_create: M %d outside 1..%d", M, kMaxM);
+    if (nstages < 1 || nstages > 65536 || !stages || !types)
+        return fail(GGQ_EINVAL, "ggq_chain_create: bad stage list");
     std::vector<StageDesc> host((size_t)nstages);
     int64_t cols_max = 0;
+    int kinds = 0;
     for (int s = 0; s < nstages; ++s) {
+        const int type = types[s];
+        if (type != GGQ_Q8_0 && type != GGQ_Q4_K && type != GGQ_Q4_0 && type != GGQ_Q6_K)
+            return fail(GGQ_ETYPE, "ggq_chain_create: stage %d type %d not supported", s, type);
+        kinds |= 1 << kind_of(type);
+        if (mask_of(kinds) == 0)
+            return fail(GGQ_ETYPE, "ggq_chain_create: stage %d type %d: a chain mixes Q6_K with one other type at most",
+                        s, type);
         const ggq_chain_stage& st = stages[s];
         if (st.n < 1 || st.n > kMaxSeg || !st.x) return fail(GGQ_EINVAL, "ggq_chain_create: stage %d malformed", s);
         if ((reinterpret_cast<uintptr_t>(st.x) & 15) != 0)
@@ -1062,11 +1142,11 @@ extern "C" int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chai
         }
         cols_max = std::max<int64_t>(cols_max, st.cols);
     }
-    if (rows_ring(kind_of(type), mmax_of(M), cols_max) == 0)
+    if (rows_ring(kinds, mmax_of(M), cols_max) == 0)
         return fail(GGQ_EINVAL, "ggq_chain_create: widest stage needs too much shared memory");
     for (int s = 0; s < nstages; ++s) {   // all stages valid: encode them
         const ggq_chain_stage& st = stages[s];
-        int rc = make_stage(type, st.n, st.W, st.rows, st.cols, st.x, st.y, &host[(size_t)s]);
+        int rc = make_stage(types[s], st.n, st.W, st.rows, st.cols, st.x, st.y, &host[(size_t)s]);
         if (rc) return rc;
         if (ops) {
             StageInfo& si = host[(size_t)s].info;
@@ -1091,7 +1171,7 @@ extern "C" int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chai
         delete c;
         return cuda_fail(e, "ggq_chain_create: device state");
     }
-    c->type = type;
+    c->kinds = kinds;
     c->M = M;
     c->nstages = nstages;
     c->cols_max = cols_max;
@@ -1104,7 +1184,7 @@ extern "C" int ggq_chain_run(const ggq_chain* c, void* stream) {
     if (!c) return fail(GGQ_EINVAL, "ggq_chain_run: NULL chain");
     StageDesc none;
     memset(&none, 0, sizeof(none));
-    return launch_rows(c->type, c->M, none, c->table, c->nstages, c->cols_max, c->counter,
+    return launch_rows(c->kinds, c->M, none, c->table, c->nstages, c->cols_max, c->counter,
                        static_cast<cudaStream_t>(stream));
 }
 

@@ -9,10 +9,12 @@ pass is, per layer, the stages [attn_q, attn_k, attn_v], [attn_output],
 quantization names like Q4_K_M": Q4_K_M keeps part of attn_v and ffn_down in
 Q6_K), so a stage whose matrices differ in type is split by type, in order.
 
-Launches: each run of consecutive stages of one type the chain kernel streams
-(Q4_0, Q8_0, Q4_K) is one ``ggq_chain_run``; every other stage (Q6_K, F32) is
-one ``ggq_gemv`` / ``ggq_gemv_multi``.  Everything here is host-side planning:
-the arithmetic runs in the library's kernels.
+Launches: each run of consecutive stages the chain kernel streams (Q8_0;
+Q4_K and Q4_0 with cols >= 768; Q6_K with cols % 2048 == 0), of one type or of
+Q6_K and one other type, is one ``ggq_chain_run``; every other stage (F32, or
+a shape outside those limits) is one ``ggq_gemv`` / ``ggq_gemv_multi``.  A
+Q4_K_M file's whole pass, head included, is then one launch.  Everything here is host-side
+planning: the arithmetic runs in the library's kernels.
 """
 from __future__ import annotations
 
@@ -21,7 +23,17 @@ from . import _ggq
 # the GEMV stages of a layer in dependency order, by GGUF tensor name
 LAYER_STAGES = (("attn_q", "attn_k", "attn_v"), ("attn_output",), ("ffn_gate", "ffn_up"), ("ffn_down",))
 # the types the chain kernel streams
-CHAIN_TYPES = (_ggq.Q4_0, _ggq.Q8_0, _ggq.Q4_K)
+CHAIN_TYPES = (_ggq.Q4_0, _ggq.Q8_0, _ggq.Q4_K, _ggq.Q6_K)
+
+
+def chainable(qtype: int, cols: int) -> bool:
+    """Whether a stage of this type and width can be a chain stage (the limits
+    ggq_chain_create documents; the library checks them again)."""
+    if qtype not in CHAIN_TYPES or cols % 256 or cols > (1 << 20):
+        return False
+    if qtype in (_ggq.Q4_K, _ggq.Q4_0) and cols < 768:
+        return False
+    return not (qtype == _ggq.Q6_K and cols % 2048)
 
 
 def block_count(model) -> int:
@@ -58,15 +70,24 @@ def plan_from_table(model, layers: int | None = None, head: str = "output.weight
     return stages
 
 
-def segments(types):
-    """Launches for stages of the given types, in order: each run of
-    consecutive stages of one chain-kernel type is one chain launch, every
-    other stage a launch of its own.  Returns ``[(start, end, is_chain)]``."""
+def mixable(types) -> bool:
+    """Whether one chain may hold stages of these types: one type, or Q6_K and
+    one other (the mixes ggq_chain_create_typed runs)."""
+    return len(set(types) - {_ggq.Q6_K}) <= 1 and (len(set(types)) == 1 or _ggq.Q8_0 not in types)
+
+
+def segments(types, cols):
+    """Launches for stages of the given types and widths, in order: each run of
+    consecutive chainable stages whose types may share a chain is one chain
+    launch, every other stage a launch of its own.  Returns
+    ``[(start, end, is_chain)]``."""
+    if len(types) != len(cols):
+        raise ValueError("one width per stage")
     out, i = [], 0
     while i < len(types):
-        if types[i] in CHAIN_TYPES:
+        if chainable(types[i], cols[i]):
             j = i
-            while j < len(types) and types[j] == types[i]:
+            while j < len(types) and chainable(types[j], cols[j]) and mixable(types[i:j + 1]):
                 j += 1
             out.append((i, j, True))
             i = j
@@ -103,11 +124,11 @@ class DecodePass:
         self.weight_bytes = sum(s["nbytes"] for s in self.stages)
         self.calls, self.chains = [], []
         try:
-            for i, j, is_chain in segments([s["qtype"] for s in self.stages]):
+            for i, j, is_chain in segments([s["qtype"] for s in self.stages], [s["cols"] for s in self.stages]):
                 if is_chain:
                     raw = [(s["W"], s["rows"], s["cols"], s["x"].data_ptr(), [y.data_ptr() for y in s["ys"]])
                            for s in self.stages[i:j]]
-                    rc, h = _ggq.ggq_chain_create(self.stages[i]["qtype"], M, raw)
+                    rc, h = _ggq.ggq_chain_create_typed(M, [s["qtype"] for s in self.stages[i:j]], raw)
                     _ggq.check(rc, "ggq_chain_create")
                     self.chains.append(h)
                     self.calls.append(("chain", h))

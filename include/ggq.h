@@ -277,6 +277,24 @@ int ggq_chain_create_ops(int type, int M, int nstages, const ggq_chain_stage* st
                          ggq_chain** out);
 
 /*
+ * ggq_chain_create_typed -- ggq_chain_create_ops with a weight type per stage:
+ * types[s] (GGQ_Q8_0, GGQ_Q4_K, GGQ_Q4_0 or GGQ_Q6_K, each with the shape
+ * limits above) for stage s.  Files mix types from layer to layer and within a
+ * layer ("GGUF: The File Format Powering Local LLM Inference", "Understanding
+ * quantization names like Q4_K_M": Q4_K_M keeps part of attn_v and ffn_down in
+ * Q6_K), and this lets the whole decode pass of such a file run as one chain.
+ * A chain whose stages are all of one type runs the same kernel as
+ * ggq_chain_create_ops.  A chain may also mix GGQ_Q6_K with one other type,
+ * GGQ_Q4_K or GGQ_Q4_0 (Q4_K_M and Q4_K_S files; Q4_0 files with a Q6_K output
+ * head): it runs a kernel that decodes each stage by its type (copy ring slots
+ * sized for the larger).  ops may be NULL.  Errors as for ggq_chain_create_ops;
+ * GGQ_ETYPE (naming the stage) for a type outside the four or a mix outside
+ * those two.  Synchronous.
+ */
+int ggq_chain_create_typed(int M, int nstages, const int* types, const ggq_chain_stage* stages,
+                           const ggq_chain_ops* ops, ggq_chain** out);
+
+/*
  * ggq_chain_run -- run every stage of the chain, in order, as one cooperative
  * launch (every CTA resident at once, one per SM) on `stream` (cudaStream_t)
  * on the device the chain was created on.  The chain's stage counter lives in

@@ -217,6 +217,34 @@ def test_chain_create_validates_stages(ggq):
     ggq.ggq_chain_free(0)
 
 
+def test_chain_create_typed_validates_each_stage(ggq):
+    """ggq_chain_create_typed: one type per stage, each checked with its own
+    shape limits; the error names the stage."""
+    ok = ([16], [64], 2048, 16, [16])
+    t = ggq.ggq_chain_create_typed
+    assert t(1, [ggq.Q4_K, ggq.F32], [ok, ok])[0] == -2
+    assert "stage 1 type 0" in ggq.lib.ggq_last_error().decode()
+    assert t(1, [ggq.Q4_K, ggq.F16], [ok, ok])[0] == -2
+    assert t(5, [ggq.Q4_K, ggq.Q6_K], [ok, ok])[0] == -1                               # M = 5
+    assert t(1, [], [])[0] == -1                                                       # no stages
+    q6_narrow = ([16], [64], 1024, 16, [16])                                           # Q6_K needs cols % 2048
+    assert t(1, [ggq.Q4_K, ggq.Q6_K], [q6_narrow, q6_narrow])[0] == -1
+    assert "stage 1 shape unsupported" in ggq.lib.ggq_last_error().decode()
+    q40_narrow = ([16], [64], 512, 16, [16])                                           # Q4_0 needs cols >= 768
+    assert t(1, [ggq.Q6_K, ggq.Q4_0], [ok, q40_narrow])[0] == -1
+    assert "stage 1" in ggq.lib.ggq_last_error().decode()
+    assert t(1, [ggq.Q4_K, ggq.Q6_K, ggq.Q4_0], [ok] * 3)[0] == -2                  # two types besides Q6_K
+    assert "stage 2 type 2" in ggq.lib.ggq_last_error().decode()
+    assert t(1, [ggq.Q8_0, ggq.Q6_K], [ok] * 2)[0] == -2                             # Q8_0 is not mixed
+    for types in ([ggq.Q4_K, ggq.Q6_K, ggq.Q4_K], [ggq.Q6_K, ggq.Q4_0], [ggq.Q8_0, ggq.Q8_0]):
+        rc, h = t(1, types, [ok] * len(types))
+        assert rc not in (-1, -2), types          # past validation (no device here: fails later)
+        if rc == 0:
+            ggq.ggq_chain_free(h)
+    with pytest.raises(ValueError):
+        ggq.Chain([ggq.Q4_K], 1, [])              # one type per stage
+
+
 def test_chain_create_ops_validates_fused_steps(ggq):
     """ggq_chain_create_ops rejects malformed fused steps before touching the device."""
     ok = ([16], [64], 2048, 16, [16])

@@ -42,11 +42,40 @@ def test_plan_splits_stages_by_type_in_order():
 
 
 def test_segments():
+    """Runs of chainable stages of any types are one chain; a stage outside
+    the chain kernel's limits (F32, Q6_K at cols % 2048, Q4_K/Q4_0 below 768
+    columns, cols % 256 for Q8_0) is a launch of its own."""
     b = _bench()
-    assert b.segments([12, 12, 12, 12, 12, 14, 12, 12, 14, 14]) == [
-        (0, 5, True), (5, 6, False), (6, 8, True), (8, 9, False), (9, 10, False)]
-    assert b.segments([]) == []
-    assert b.segments([8, 12, 12, 2, 0]) == [(0, 1, True), (1, 3, True), (3, 4, True), (4, 5, False)]
+    q4km = [12, 12, 12, 12, 12, 14, 12, 12, 14, 14]
+    assert b.segments(q4km, [4096] * 10) == [(0, 10, True)]
+    assert b.segments(q4km, [4096] * 5 + [11008] + [4096] * 4) == [(0, 5, True), (5, 6, False), (6, 10, True)]
+    assert b.segments([], []) == []
+    # a chain holds one type, or Q6_K with Q4_K or with Q4_0
+    assert b.segments([8, 12, 12, 2, 0], [4096] * 5) == [(0, 1, True), (1, 3, True), (3, 4, True), (4, 5, False)]
+    assert b.segments([2, 14, 2, 14, 12, 14], [4096] * 6) == [(0, 4, True), (4, 6, True)]
+    assert b.segments([8, 14], [4096] * 2) == [(0, 1, True), (1, 2, True)]
+    assert b.segments([14, 8, 8], [4096] * 3) == [(0, 1, True), (1, 3, True)]
+    assert b.segments([8, 12, 8, 2, 8], [4096, 512, 4096, 512, 4000]) == [
+        (0, 1, True), (1, 2, False), (2, 3, True), (3, 4, False), (4, 5, False)]
+    assert b.segments([14, 14], [2048, 6144]) == [(0, 2, True)]
+    with pytest.raises(ValueError):
+        b.segments([12], [])
+
+
+def test_mixable():
+    b = _bench()
+    assert b.mixable([12, 14, 12]) and b.mixable([2, 14]) and b.mixable([14]) and b.mixable([8, 8])
+    assert not b.mixable([12, 2]) and not b.mixable([8, 14]) and not b.mixable([12, 14, 2])
+
+
+def test_chainable_limits():
+    b = _bench()
+    assert b.chainable(8, 256) and not b.chainable(8, 288)
+    assert b.chainable(12, 768) and not b.chainable(12, 512)
+    assert b.chainable(2, 1024) and not b.chainable(2, 512)
+    assert b.chainable(14, 2048) and not b.chainable(14, 1024) and not b.chainable(14, 2304)
+    assert not b.chainable(0, 4096) and not b.chainable(1, 4096)
+    assert not b.chainable(8, (1 << 20) + 256)
 
 
 def test_q4km_file_size_matches_the_pages():

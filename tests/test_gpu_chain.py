@@ -32,11 +32,15 @@ def _dev(torch, a):
 
 class Net:
     """Stages given as lists of (name, rows, cols, source); source is 'x0' or
-    the name of an earlier output whose rows equal this stage's cols."""
+    the name of an earlier output whose rows equal this stage's cols.  qtype:
+    one weight type for every stage, or a list with one per stage (a chain of
+    mixed types)."""
 
     def __init__(self, env, qtype, M, stages, seed=0):
         torch, ggq = env
-        self.torch, self.ggq, self.qtype, self.M = torch, ggq, qtype, M
+        self.torch, self.ggq, self.M = torch, ggq, M
+        self.types = list(qtype) if isinstance(qtype, (list, tuple)) else [qtype] * len(stages)
+        self.qtype = {}
         self.W, self.Wd, self.y, self.shape = {}, {}, {}, {}
         cols0 = stages[0][0][2]
         self.x0 = torch.empty((M, cols0), dtype=torch.float32, device="cuda")
@@ -46,7 +50,8 @@ class Net:
             cols = stage[0][2]
             assert all(s[2] == cols and s[3] == src for s in stage)
             for (name, rows, _, _) in stage:
-                self.W[name] = synth.weight_rows(qtype, 100 + 17 * seed + len(self.W), rows, cols)
+                self.qtype[name] = self.types[si]
+                self.W[name] = synth.weight_rows(self.types[si], 100 + 17 * seed + len(self.W), rows, cols)
                 self.Wd[name] = _dev(torch, self.W[name])
                 self.y[name] = torch.full((M, rows), float("nan"), dtype=torch.float32, device="cuda")
                 self.shape[name] = (rows, cols)
@@ -55,7 +60,7 @@ class Net:
                               [self.y[n] for (n, _, _, _) in stage]))
         self.names = [[n for (n, _, _, _) in stage] for stage in stages]
         self.srcs = [stage[0][3] for stage in stages]
-        self.chain = ggq.Chain(qtype, M, self.plan)
+        self.chain = ggq.Chain(qtype if isinstance(qtype, int) else self.types, M, self.plan)
 
     def run(self, x0):
         self.x0.copy_(self.torch.from_numpy(x0))
@@ -73,7 +78,7 @@ class Net:
             assert np.isfinite(x).all()
             for n in names:
                 rows, cols = self.shape[n]
-                y_ref, a_ref = oracle.gemv(self.qtype, self.W[n], rows, cols, x)
+                y_ref, a_ref = oracle.gemv(self.qtype[n], self.W[n], rows, cols, x)
                 ok, w = oracle.tolerance_ok(out[n], y_ref, a_ref, REL, ABS)
                 assert ok, f"{n}: worst error / bound = {w:.3g}"
                 worst = max(worst, w)
@@ -162,6 +167,70 @@ def test_chain_llama8b_layers(env):
     net.check(x0, net.run(x0))
 
 
+# ---- chains of mixed weight types (Q4_K_M-style files) ------------------------
+
+Q8_0, Q4_K, Q4_0, Q6_K = 8, 12, 2, 14
+
+
+def _mixed_stages(other=Q4_K):
+    """Two layers (hidden 2048, kv 512, ffn 4096) as in a Q4_K_M file: q/k,
+    o and gate/up in `other` (Q4_K, or Q4_0), v and down in Q6_K in the first
+    layer, only down in the second."""
+    stages = [
+        [("a.q", 2048, 2048, "x0"), ("a.k", 512, 2048, "x0")],
+        [("a.v", 512, 2048, "x0")],
+        [("a.o", 2048, 2048, "a.q")],
+        [("a.gate", 4096, 2048, "a.o"), ("a.up", 4096, 2048, "a.o")],
+        [("a.down", 2048, 4096, "a.gate")],
+        [("b.q", 2048, 2048, "a.down"), ("b.k", 512, 2048, "a.down"), ("b.v", 512, 2048, "a.down")],
+        [("b.o", 2048, 2048, "b.q")],
+        [("b.gate", 4096, 2048, "b.o"), ("b.up", 4096, 2048, "b.o")],
+        [("b.down", 2048, 4096, "b.gate")],
+    ]
+    types = [other, Q6_K, other, other, Q6_K, other, other, other, Q6_K]
+    return stages, types
+
+
+@pytest.mark.parametrize("other,M", [(Q4_K, 1), (Q4_K, 2), (Q4_K, 3), (Q4_0, 1), (Q4_0, 4)])
+def test_chain_mixed_types(env, other, M):
+    """One launch over stages of two weight types, each stage decoded by its
+    own type; every stage against the oracle fed with what it read."""
+    stages, types = _mixed_stages(other)
+    net = Net(env, types, M, stages, seed=7)
+    for run in range(2):
+        x0 = synth.normal_f32(M * 2048, 150 + run).reshape(M, 2048)
+        net.check(x0, net.run(x0))
+
+
+def test_chain_mixed_stage_equals_uniform_chain(env):
+    """A stage of a mixed chain is computed exactly as in a chain of its own
+    type (same tiles, same order of sums): its outputs are bit-identical."""
+    torch, ggq = env
+    stages, types = _mixed_stages()
+    net = Net(env, types, 1, stages, seed=8)
+    x0 = synth.normal_f32(2048, 160).reshape(1, 2048)
+    out = net.run(x0)
+    for names, qt in ((["a.q", "a.k"], Q4_K), (["a.v"], Q6_K)):
+        ys = [torch.full((1, net.shape[n][0]), float("nan"), dtype=torch.float32, device="cuda") for n in names]
+        ch = ggq.Chain(qt, 1, [([net.Wd[n] for n in names], [net.shape[n][0] for n in names], 2048, net.x0, ys)])
+        ch.run()
+        torch.cuda.synchronize()
+        for n, y in zip(names, ys):
+            assert np.array_equal(y.cpu().numpy().view(np.uint32), out[n].view(np.uint32)), n
+
+
+def test_chain_typed_with_one_type_is_the_uniform_chain(env):
+    """ggq_chain_create_typed with every stage of one type runs the same kernel
+    as ggq_chain_create: bit-identical outputs."""
+    stages = _layer("a.", 2048, 512, 4096, "x0")
+    a = Net(env, Q4_K, 1, stages, seed=9)
+    b = Net(env, [Q4_K] * len(stages), 1, stages, seed=9)
+    x0 = synth.normal_f32(2048, 170).reshape(1, 2048)
+    ya, yb = a.run(x0), b.run(x0)
+    for n in ya:
+        assert np.array_equal(ya[n].view(np.uint32), yb[n].view(np.uint32)), n
+
+
 def test_chain_in_cuda_graph(env):
     torch, ggq = env
     stages = _layer("a.", 1280, 256, 2816, "x0")
@@ -194,39 +263,46 @@ def test_chain_in_cuda_graph(env):
 from oracle import layer_ops  # noqa: E402
 
 
-def _fused_layers(torch, ggq, qtype, M, H, KV, F, layers, seed):
+def _fused_layers(torch, ggq, qtype, M, H, KV, F, layers, seed, types=None):
     """A residual stream through `layers` Llama-style layers as one fused chain:
     [q,k,v](rmsnorm(h)), [o](q) + h, [gate,up](rmsnorm(h2)), [down](silu(gate)*up) + h2.
-    Returns the chain, the buffers and, per stage, what the oracle needs."""
+    types: None (every matrix qtype) or {(layer, name): type} for the matrices
+    that differ; a stage whose matrices differ in type is split by type (same
+    x and fused step).  Returns the chain, the buffers and, per stage, what the
+    oracle needs."""
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()   # noqa: E731
     h0 = torch.empty((M, H), dtype=torch.float32, device="cuda")
-    stages, ops, plan = [], [], []
+    stages, ops, plan, stypes = [], [], [], []
     h = h0
     for l in range(layers):
-        W = {}
+        W, T = {}, {}
         for j, (name, r, c) in enumerate([("q", H, H), ("k", KV, H), ("v", KV, H), ("o", H, H),
                                           ("gate", F, H), ("up", F, H), ("down", H, F)]):
-            W[name] = (synth.weight_rows(qtype, 300 + 31 * seed + 10 * l + j, r, c), r, c)
-        Wd = {n: dev(w) for n, (w, _, _) in W.items()}
-        y = {n: torch.full((M, r), float("nan"), dtype=torch.float32, device="cuda") for n, (_, r, _) in W.items()}
+            T[name] = (types or {}).get((l, name), qtype)
+            W[name] = (synth.weight_rows(T[name], 300 + 31 * seed + 10 * l + j, r, c), r, c, T[name])
+        Wd = {n: dev(w[0]) for n, w in W.items()}
+        y = {n: torch.full((M, w[1]), float("nan"), dtype=torch.float32, device="cuda") for n, w in W.items()}
         g_attn = (1.0 + 0.1 * synth.normal_f32(H, 400 + 7 * seed + 2 * l)).astype(np.float32)
         g_ffn = (1.0 + 0.1 * synth.normal_f32(H, 401 + 7 * seed + 2 * l)).astype(np.float32)
         ga, gf = dev(g_attn), dev(g_ffn)
         eps = 1e-6
-        stages += [([Wd["q"], Wd["k"], Wd["v"]], [H, KV, KV], H, h, [y["q"], y["k"], y["v"]]),
-                   ([Wd["o"]], [H], H, y["q"], [y["o"]]),
-                   ([Wd["gate"], Wd["up"]], [F, F], H, y["o"], [y["gate"], y["up"]]),
-                   ([Wd["down"]], [H], F, y["gate"], [y["down"]])]
-        ops += [{"x_op": ggq.X_RMSNORM, "eps": eps, "norm_w": ga},
-                {"res": [h]},
-                {"x_op": ggq.X_RMSNORM, "eps": eps, "norm_w": gf},
-                {"x_op": ggq.X_SILU_MUL, "up": y["up"], "res": [y["o"]]}]
-        plan += [(["q", "k", "v"], W, y, ("rms", h, g_attn, eps), None),
-                 (["o"], W, y, ("plain", y["q"]), h),
-                 (["gate", "up"], W, y, ("rms", y["o"], g_ffn, eps), None),
-                 (["down"], W, y, ("silu", y["gate"], y["up"]), y["o"])]
+        layer = [(["q", "k", "v"], H, h, {"x_op": ggq.X_RMSNORM, "eps": eps, "norm_w": ga}, ("rms", h, g_attn, eps), None),
+                 (["o"], H, y["q"], {"res": [h]}, ("plain", y["q"]), h),
+                 (["gate", "up"], H, y["o"], {"x_op": ggq.X_RMSNORM, "eps": eps, "norm_w": gf},
+                  ("rms", y["o"], g_ffn, eps), None),
+                 (["down"], F, y["gate"], {"x_op": ggq.X_SILU_MUL, "up": y["up"]}, ("silu", y["gate"], y["up"]), y["o"])]
+        for names, cols, x, op, xin, res in layer:
+            for t in dict.fromkeys(T[n] for n in names):     # split by type, in order of first use
+                part = [n for n in names if T[n] == t]
+                stages.append(([Wd[n] for n in part], [W[n][1] for n in part], cols, x, [y[n] for n in part]))
+                o = dict(op)
+                if res is not None:
+                    o["res"] = [res] * len(part)
+                ops.append(o)
+                stypes.append(t)
+                plan.append((part, W, y, xin, res))
         h = y["down"]
-    chain = ggq.Chain(qtype, M, stages, ops)
+    chain = ggq.Chain(qtype if types is None else stypes, M, stages, ops)
     return chain, h0, plan, (stages, ops)
 
 
@@ -242,8 +318,8 @@ def _check_fused(qtype, plan):
             xr = xa
         assert np.isfinite(xr).all()
         for n in names:
-            w, rows, cols = W[n]
-            wd = oracle.dequantize(qtype, w, rows, cols).astype(np.float64)   # exact decoded weights
+            w, rows, cols, wt = W[n]
+            wd = oracle.dequantize(wt, w, rows, cols).astype(np.float64)   # exact decoded weights
             y_ref = xr @ wd.T
             a_ref = np.abs(xr) @ np.abs(wd).T
             if res is not None:
@@ -269,6 +345,21 @@ def test_chain_fused_layers(env, qtype, M):
         torch.cuda.synchronize()
         assert ggq.device_status() == 0
         _check_fused(qtype, plan)
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_chain_fused_layers_mixed_types(env, M):
+    """Fused layers of a Q4_K_M-style file: v (first layer) and down in Q6_K
+    (v's stage split from q/k, with the same fused step), the rest Q4_K."""
+    torch, ggq = env
+    types = {(0, "v"): Q6_K, (0, "down"): Q6_K, (1, "down"): Q6_K}
+    chain, h0, plan, _ = _fused_layers(torch, ggq, Q4_K, M, 2048, 512, 4096, 2, seed=60 + M, types=types)
+    for run in range(2):
+        h0.copy_(torch.from_numpy((3.0 * synth.normal_f32(M * 2048, 530 + run)).reshape(M, 2048)))
+        chain.run()
+        torch.cuda.synchronize()
+        assert ggq.device_status() == 0
+        _check_fused(Q4_K, plan)
 
 
 def test_chain_fused_residual_into_own_output(env):

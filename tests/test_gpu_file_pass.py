@@ -1,9 +1,9 @@
 """GPU parity for a mixed-type decode pass planned from a file's tensor table:
 a 2-layer Q4_K_M-style GGUF (Q4_K matrices, Q6_K attn_v / ffn_down in layer 1,
 F32 norms, a Q6_K head of 32000 rows) written, loaded with ggq_load, planned by
-the library's planner (gguf_block_quantized_q8_gb300.plan: Q4_K runs as chain
-launches, Q6_K stages on their own) and run twice; every output row of every
-stage checked against the oracle."""
+the library's planner (gguf_block_quantized_q8_gb300.plan: the whole pass,
+Q4_K and Q6_K stages and the head, as one chain of mixed types) and run twice;
+every output row of every stage checked against the oracle."""
 import numpy as np
 import pytest
 
@@ -38,7 +38,7 @@ def test_q4km_file_pass(env, tmp_path):
             xs.append(torch.from_numpy(synth.normal_f32(tl[0]["ne"][0], 9000 + si)).cuda())
             ys.append([torch.full((t["ne"][1],), float("nan"), device="cuda") for t in tl])
         dp = P.DecodePass(stages, xs, ys)
-        assert len(dp.chains) == 2 and dp.launches == 5   # chain, v, chain, down, head
+        assert len(dp.chains) == 1 and dp.launches == 1   # one chain: Q4_K, Q6_K and the head
         for _ in range(2):                                  # twice: chains reset their counters
             dp.run()
             torch.cuda.synchronize()

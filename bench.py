@@ -48,6 +48,9 @@ def args_parse():
     ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES),
                     help="run one configuration's GEMV a few times and exit (a small command to profile)")
     ap.add_argument("--M", type=int, default=1, help="activation rows for --kernel")
+    ap.add_argument("--file-pass-layers", type=int, default=0,
+                    help="run only the Q4_K_M-style file pass with this many layers and exit "
+                         "(a small command to profile its mixed-type chain)")
     return ap.parse_args()
 
 
@@ -810,6 +813,15 @@ def main():
     a = args_parse()
     if a.kernel:
         return run_kernel(a)
+    if a.file_pass_layers:
+        import torch
+        import gguf_block_quantized_q8_gb300 as ggq
+        import synth
+        torch.cuda.set_device(0)
+        stream = torch.cuda.Stream()
+        out = q4km_file_pass(torch, ggq, synth, stream, steps=5, layers=a.file_pass_layers)
+        print(json.dumps({"file_pass_layers": a.file_pass_layers, **out}))
+        return 0 if out["status"] == 0 else 1
     ws, rank, local = dist_setup()
     if a.impl == "reference":
         return run_reference(a, ws, rank)

@@ -92,6 +92,14 @@ __device__ __forceinline__ uint64_t and_pair(uint32_t w, uint32_t m0, uint32_t m
     return r;
 }
 
+// (w0 & m, w1 & m) as one register pair
+__device__ __forceinline__ uint64_t and_two(uint32_t w0, uint32_t w1, uint32_t m) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 l, h;\n\tand.b32 l, %1, %3;\n\tand.b32 h, %2, %3;\n\tmov.b64 %0, {l, h};\n\t}"
+        : "=l"(r) : "r"(w0), "r"(w1), "r"(m));
+    return r;
+}
+
 // acc(2) += a(2) * b(2) on float2 values
 __device__ __forceinline__ void f2_fma(float2& acc, float2 a, float2 b) { acc = __ffma2_rn(a, b, acc); }
 
@@ -355,29 +363,42 @@ __device__ __forceinline__ void q40_chunk_rows(const uint8_t* rp, int rstride, c
 // super-block); `rstride` bytes to the next of its rows.  The chunk holds the
 // weights 128h + 32g + l for g = gp, gp + 2 and l = 0..31: ql bytes 64h + 32gp
 // + l (low nibble g = gp, high g = gp + 2) and qh bytes 32h + l (2 bits per g).
-// Words are read aligned and realigned with a funnel shift by 8 * (r0 & 3).
+// Words are read aligned; when r0 is 2 mod 4 (every odd super-block) they are
+// realigned with a 16-bit funnel shift (ALIGNED: r0 is 0 mod 4, none needed).
 // Each byte of a code word holds one 6-bit code u, masked in place like a
 // Q8_0 byte (x' scaled by its byte position); the pair (g = gp, g = gp + 2) at
-// one (w, b) is one packed FMA.  x' of chunk c: [b][w][pair] at xu + 16b + 2w,
-// activation row m at xu + m*xs.  32 * sum(x) of the four 16-column groups of
-// the chunk ((g, l < 16) for g = gp, gp + 2, then l >= 16) at su + m*ss.
-// acc[r][m] += the chunk's 64 products.
-template <int MMAX, int R>
-__device__ __forceinline__ void q6k_chunk_rows(const uint8_t* rp, int r0, int rstride, int c, const float* xu, int xs,
-                                               const float* su, int ss, float (&acc)[R][MMAX]) {
+// one (w, b) is one packed FMA.  A code word takes the low 4 bits of each byte
+// from the ql word and bits 4-7 from the shifted qh word in one select; bits 6
+// and 7 then hold other fields' bits, which the per-byte 6-bit mask drops.
+// x' of chunk c: [b][w][pair] at xu + 16b + 2w, activation row m at xu + m*xs.
+// 32 * sum(x) of the four 16-column groups of the chunk ((g, l < 16) for g =
+// gp, gp + 2, then l >= 16) at su + m*ss.  acc[r][m] += the chunk's 64 products.
+template <int MMAX, int R, bool ALIGNED>
+__device__ __forceinline__ void q6k_chunk_rows_t(const uint8_t* rp, int r0, int rstride, int c, const float* xu,
+                                                 int xs, const float* su, int ss, float (&acc)[R][MMAX]) {
     const int h = c >> 1, gp = c & 1;
-    const uint32_t sh = 8u * (uint32_t)(r0 & 3);
     const int base = r0 & ~3;
+    const uint32_t shl = 4u - 2u * (uint32_t)gp, shr = 2u * (uint32_t)gp;
     float ds[R][4];   // d * sc of the four groups
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const uint8_t* sb = rp + r * rstride + r0;
-        const float d = half_bits_to_float((uint32_t)sb[208] | ((uint32_t)sb[209] << 8));
-        const signed char* sc = reinterpret_cast<const signed char*>(sb + 192 + 8 * h + 2 * gp);
-        ds[r][0] = d * (float)sc[0];   // (gp, l < 16)
-        ds[r][1] = d * (float)sc[4];   // (gp + 2, l < 16)
-        ds[r][2] = d * (float)sc[1];   // (gp, l >= 16)
-        ds[r][3] = d * (float)sc[5];   // (gp + 2, l >= 16)
+        const float d = half_bits_to_float(*reinterpret_cast<const unsigned short*>(sb + 208));
+        // scales 8h + 2gp + {0, 1} and + {4, 5} (signed bytes) as bytes 0-3 of one
+        // word, offset by 128; 0x4B0000 | byte is the float 2^23 + byte
+        const unsigned short* sc16 = reinterpret_cast<const unsigned short*>(sb + 192 + 8 * h + 2 * gp);
+        const uint32_t sw = ((uint32_t)sc16[0] | ((uint32_t)sc16[2] << 16)) ^ 0x80808080u;
+        const float2 s01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(sw, 0x4B000000u, 0x7650)),
+                                                  __uint_as_float(__byte_perm(sw, 0x4B000000u, 0x7652))),
+                                      make_float2(-8388736.0f, -8388736.0f));   // (sc0, sc4)
+        const float2 s23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(sw, 0x4B000000u, 0x7651)),
+                                                  __uint_as_float(__byte_perm(sw, 0x4B000000u, 0x7653))),
+                                      make_float2(-8388736.0f, -8388736.0f));   // (sc1, sc5)
+        const float2 d01 = __fmul2_rn(s01, make_float2(d, d)), d23 = __fmul2_rn(s23, make_float2(d, d));
+        ds[r][0] = d01.x;   // (gp, l < 16)
+        ds[r][1] = d01.y;   // (gp + 2, l < 16)
+        ds[r][2] = d23.x;   // (gp, l >= 16)
+        ds[r][3] = d23.y;   // (gp + 2, l >= 16)
     }
     F2 t[R][MMAX][2];   // [half of the chunk: l < 16, l >= 16]
 #pragma unroll
@@ -391,18 +412,19 @@ __device__ __forceinline__ void q6k_chunk_rows(const uint8_t* rp, int r0, int rs
         for (int r = 0; r < R; ++r) {
             const uint32_t* wl = reinterpret_cast<const uint32_t*>(rp + r * rstride + base + 64 * h + 32 * gp + 16 * half);
             const uint32_t* wh = reinterpret_cast<const uint32_t*>(rp + r * rstride + base + 128 + 32 * h + 16 * half);
-            uint32_t a[5], q[5];
+            constexpr int kWords = ALIGNED ? 4 : 5;
+            uint32_t a[kWords], q[kWords];
 #pragma unroll
-            for (int i = 0; i < 5; ++i) {
+            for (int i = 0; i < kWords; ++i) {
                 a[i] = wl[i];
                 q[i] = wh[i];
             }
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const uint32_t qlw = __funnelshift_r(a[w], a[w + 1], sh);
-                const uint32_t qhw = __funnelshift_r(q[w], q[w + 1], sh);
-                lo[r][w] = (qlw & 0x0F0F0F0Fu) | ((qhw << (4 - 2 * gp)) & 0x30303030u);
-                hi[r][w] = ((qlw >> 4) & 0x0F0F0F0Fu) | ((qhw >> (2 * gp)) & 0x30303030u);
+                const uint32_t qlw = ALIGNED ? a[w] : __byte_perm(a[w], a[w + 1], 0x5432);
+                const uint32_t qhw = ALIGNED ? q[w] : __byte_perm(q[w], q[w + 1], 0x5432);
+                lo[r][w] = (qlw & 0x0F0F0F0Fu) | ((qhw << shl) & 0xF0F0F0F0u);
+                hi[r][w] = ((qlw >> 4) & 0x0F0F0F0Fu) | ((qhw >> shr) & 0xF0F0F0F0u);
             }
         }
 #pragma unroll
@@ -420,9 +442,7 @@ __device__ __forceinline__ void q6k_chunk_rows(const uint8_t* rp, int r0, int rs
                 for (int w = 0; w < 4; ++w) {
                     const uint32_t vl = b < 3 ? lo[r][w] : (lo[r][w] >> 8);
                     const uint32_t vh = b < 3 ? hi[r][w] : (hi[r][w] >> 8);
-                    uint64_t pr;
-                    asm("{\n\t.reg .b32 l, h;\n\tand.b32 l, %1, %3;\n\tand.b32 h, %2, %3;\n\tmov.b64 %0, {l, h};\n\t}"
-                        : "=l"(pr) : "r"(vl), "r"(vh), "r"(mk));
+                    const uint64_t pr = and_two(vl, vh, mk);
 #pragma unroll
                     for (int m = 0; m < MMAX; ++m) {
                         const float4 x4 = xv[m][w >> 1];
@@ -449,6 +469,15 @@ __device__ __forceinline__ void q6k_chunk_rows(const uint8_t* rp, int r0, int rs
             acc[r][m] = v;
         }
     }
+}
+
+// The chunk for any r0: the copy of an even super-block starts 0 mod 4 bytes
+// below it, that of an odd one 2 mod 4 (210 = 2 mod 4); warp-uniform.
+template <int MMAX, int R>
+__device__ __forceinline__ void q6k_chunk_rows(const uint8_t* rp, int r0, int rstride, int c, const float* xu, int xs,
+                                               const float* su, int ss, float (&acc)[R][MMAX]) {
+    if ((r0 & 2) == 0) q6k_chunk_rows_t<MMAX, R, true>(rp, r0, rstride, c, xu, xs, su, ss, acc);
+    else q6k_chunk_rows_t<MMAX, R, false>(rp, r0, rstride, c, xu, xs, su, ss, acc);
 }
 
 // One quarter of a Q8_0 period: blocks 2c and 2c+1 (rp: their 68 bytes, 4-byte

@@ -141,17 +141,18 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 }
 
 // 32 TMEM lanes x 16 consecutive 32-bit columns -> 16 registers per thread
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 64 accumulator columns of the warp's 32 TMEM lanes: one load, one wait
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B
@@ -352,26 +353,32 @@ __global__ void __launch_bounds__(Dec<Q4K, TH>::kThreads, 1) prefill_kernel(cons
                 const uint4 q1 = *reinterpret_cast<const uint4*>(rp + 32 + 32 * c);
                 const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                 // chunk j (k = 8j .. 8j+7 of the 64): low nibbles, sub-block 2c;
-                // high nibbles, sub-block 2c+1, are k = 32 + 8j ..
+                // high nibbles, sub-block 2c+1, are k = 32 + 8j ..  Four nibbles
+                // of a word are masked at once; byte b then goes under 0x4B0000
+                // (the float 2^23 + q), and pairs take packed arithmetic:
+                // w = a * q - b, exactly as one fma each.
                 uint32_t lo[4][4], hi[4][4];
+                auto four = [](uint32_t n4, float a, float nb, uint32_t& p01, uint32_t& p23) {
+                    const float2 k = make_float2(-8388608.0f, -8388608.0f);
+                    const float2 a2 = make_float2(a, a), nb2 = make_float2(nb, nb);
+                    const float2 f01 = __ffma2_rn(__fadd2_rn(make_float2(__uint_as_float(__byte_perm(n4, 0x4B000000u, 0x7650)),
+                                                                         __uint_as_float(__byte_perm(n4, 0x4B000000u, 0x7651))), k),
+                                                  a2, nb2);
+                    const float2 f23 = __ffma2_rn(__fadd2_rn(make_float2(__uint_as_float(__byte_perm(n4, 0x4B000000u, 0x7652)),
+                                                                         __uint_as_float(__byte_perm(n4, 0x4B000000u, 0x7653))), k),
+                                                  a2, nb2);
+                    p01 = pack_bf16x2(f01.x, f01.y);
+                    p23 = pack_bf16x2(f23.x, f23.y);
+                };
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const uint32_t w = qw[2 * j + half];
-                        float fl[4], fh[4];
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            const uint32_t byte = (w >> (8 * b)) & 0xFFu;
-                            if (kParts == 1 || part == 0)
-                                fl[b] = fmaf(a_lo, __uint_as_float(0x4B000000u | (byte & 15u)) - 8388608.0f, -b_lo);
-                            if (kParts == 1 || part == 1)
-                                fh[b] = fmaf(a_hi, __uint_as_float(0x4B000000u | (byte >> 4)) - 8388608.0f, -b_hi);
-                        }
-                        lo[j][2 * half] = pack_bf16x2(fl[0], fl[1]);
-                        lo[j][2 * half + 1] = pack_bf16x2(fl[2], fl[3]);
-                        hi[j][2 * half] = pack_bf16x2(fh[0], fh[1]);
-                        hi[j][2 * half + 1] = pack_bf16x2(fh[2], fh[3]);
+                        if (kParts == 1 || part == 0)
+                            four(w & 0x0F0F0F0Fu, a_lo, -b_lo, lo[j][2 * half], lo[j][2 * half + 1]);
+                        if (kParts == 1 || part == 1)
+                            four((w >> 4) & 0x0F0F0F0Fu, a_hi, -b_hi, hi[j][2 * half], hi[j][2 * half + 1]);
                     }
                 }
                 // one 64-k stage: a 128-byte row, chunk position j ^ (row % 8)
@@ -427,11 +434,15 @@ __global__ void __launch_bounds__(Dec<Q4K, TH>::kThreads, 1) prefill_kernel(cons
                     uint32_t o[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const uint32_t w = u[h2][2 * (j & 3) + (e >> 1)];
-                        const int b0 = 2 * (e & 1);
-                        const float f0 = d[h2] * (float)(int8_t)(w >> (8 * b0));
-                        const float f1 = d[h2] * (float)(int8_t)(w >> (8 * (b0 + 1)));
-                        o[e] = pack_bf16x2(f0, f1);
+                        // q + 128 under 0x4B0000 is the float 2^23 + 128 + q: q
+                        // exactly after one subtraction, then w = d * q
+                        const uint32_t w = u[h2][2 * (j & 3) + (e >> 1)] ^ 0x80808080u;
+                        const uint32_t b0 = 2 * (e & 1);
+                        const float2 qf = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u | b0)),
+                                                                 __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7651u | b0))),
+                                                     make_float2(-8388736.0f, -8388736.0f));
+                        const float2 f = __fmul2_rn(qf, make_float2(d[h2], d[h2]));
+                        o[e] = pack_bf16x2(f.x, f.y);
                     }
                     *reinterpret_cast<uint4*>(arow + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
@@ -464,23 +475,24 @@ __global__ void __launch_bounds__(Dec<Q4K, TH>::kThreads, 1) prefill_kernel(cons
                 asm volatile("bar.sync 1, %0;" ::"n"(kDecoders) : "memory");
             }
         }
-        for (int col = col0; col < col0 + kCols; col += 16) {
-            float v[16];
-            tmem_ld16(taddr + (uint32_t)col, v);
+        static_assert(kCols % 64 == 0, "the epilogue reads 64 accumulator columns at a time");
+        for (int col = col0; col < col0 + kCols; col += 64) {
+            float v[64];
+            tmem_ld64(taddr + (uint32_t)col, v);
             if (add) {
-                // every old value of the 16 tokens is read before any is written
+                // every old value of the 64 tokens is read before any is written
                 // (one L2 round trip a step, not one per token)
-                float old[16];
+                float old[64];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 64; ++i) {
                     const int tok = tok0 + col + i;
                     old[i] = tok < p.M ? __ldcg(p.Y + (size_t)tok * p.rows + row) : 0.0f;
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] += old[i];
+                for (int i = 0; i < 64; ++i) v[i] += old[i];
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 64; ++i) {
                 const int tok = tok0 + col + i;
                 if (tok < p.M) p.Y[(size_t)tok * p.rows + row] = v[i];
             }

@@ -427,10 +427,13 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
     p.M = M;
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
+    if (type == GGQ_Q4_0 && M >= kSmallMMin && smallm_supported(type, rows, cols, M))
+        return launch_smallm(type, W, rows, cols, x, y, M, stream);   // one pass over W for all M rows
     if (type == GGQ_F32 || type == GGQ_Q4_0 || type == GGQ_Q6_K) {
         if ((type == GGQ_Q4_0 || type == GGQ_Q6_K) && stream_gemv_supported(type, cols, std::min(M, 4), 1, &rows)) {
-            // the streaming kernel takes up to 4 activation rows; M 5..16 runs it
-            // once per group of up to 4 (x and y rows are contiguous)
+            // the streaming kernel takes up to 4 activation rows; M 5..16 (Q6_K, or
+            // a Q4_0 shape the small-M kernel does not take) runs it once per
+            // group of up to 4 (x and y rows are contiguous)
             for (int m0 = 0; m0 < M; m0 += 4) {
                 const void* Ws[1] = {W};
                 float* ys[1] = {y + (int64_t)m0 * rows};

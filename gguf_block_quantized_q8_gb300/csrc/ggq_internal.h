@@ -56,8 +56,9 @@ int launch_gemv_stream(int type, int nseg, const void* const* W, const int64_t* 
 // (cols % 256 == 0), M up to 16
 int launch_gemv_rows(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
                      cudaStream_t stream);
-// small-batch dequant-GEMM on the tensor cores (M up to 16, cols % 256 == 0);
-// ggq_gemv uses it from kSmallMMin activation rows on
+// small-batch dequant-GEMM on the tensor cores (Q8_0, Q4_K, Q4_0; M up to 16,
+// cols % 256 == 0); ggq_gemv uses it from kSmallMMin activation rows on.  When
+// it splits tiles along K it zeroes y first (a memset on the stream).
 constexpr int kSmallMMin = 5;
 bool smallm_supported(int type, int64_t rows, int64_t cols, int M);
 int launch_smallm(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,

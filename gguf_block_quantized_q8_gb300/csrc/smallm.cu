@@ -1,21 +1,35 @@
 // Small-batch dequant-GEMM on the tcgen05 tensor cores: Y[M, rows] = X[M, cols] W^T
-// for a few activation rows (M <= 16), W in Q8_0 or Q4_K ("GGUF: The File
+// for a few activation rows (M <= 16), W in Q8_0, Q4_K or Q4_0 ("GGUF: The File
 // Format...", "How a Q8_0 block is stored": w = d*q; k-quant paragraph:
-// w = d*sc_j*q - dmin*m_j).  Each decoded block is used for all M rows of X.
+// w = d*sc_j*q - dmin*m_j; Q4_0 the Q8_0 layout with 4-bit codes, w = d*(u - 8)).
+// Each decoded block is used for all M rows of X.
 //
-// One CTA computes a 128-row tile of W against all M activation rows
+// Tiles that would leave SMs idle are split along K (whole 256-column blocks)
+// between two CTAs, as halves or, when the tiles fill more than half of the SMs
+// in one wave, as a big part (one CTA a tile) and a small part (several tiles'
+// small parts a CTA).  The call then zeroes Y first and both parts of a split
+// tile add into it (red.global.add): two terms, the same fp32 sum in either
+// order; nothing is shared between launches.
+//
+// A CTA computes its parts one after another; for each, a 128-row tile of W
+// against all M activation rows
 // (UMMA M = 128 W rows, N = 16 activation rows padded with zeros, K = 16):
 //   warp 0      TMA producer: raw blocks of 128 W rows x 256 columns;
-//   warp 1      allocates 32 TMEM columns; one thread issues the MMAs and
+//   warp 1      allocates 64 TMEM columns; one thread issues the MMAs and
 //               commits each stage back to its "empty" barrier;
 //   warps 2..17 decoders: four threads a W row, 16 columns each per 64-column
 //               stage (packed f32x2 arithmetic).  A weight is decoded exactly in fp32 and split into two
 //               bf16 parts, hi = bf16(w) and lo = bf16(w - hi); X is split the
-//               same way.  Three MMAs per 16 columns (hi*hi + hi*lo + lo*hi)
-//               keep each product to ~2^-16 relative with fp32 accumulation,
-//               and every operand keeps the fp32 exponent range.
-//   epilogue    warps 2..5 read the 128 x 16 accumulator (tcgen05.ld; a warp
-//               reaches only its own quarter of the 128 TMEM lanes) and store Y.
+//               same way.  The three products hi*hi + hi*lo + lo*hi keep each
+//               term to ~2^-16 relative with fp32 accumulation, and every
+//               operand keeps the fp32 exponent range.  They take two MMAs per
+//               16 columns: X_hi and X_lo, adjacent in shared memory, are one
+//               N = 32 operand for W_hi (accumulator columns 0-15 and 16-31),
+//               and W_lo * X_hi (N = 16) goes to columns 32-47.  The issuing
+//               thread's MMA rate sets the pace at these small N.
+//   epilogue    warps 2..5 read the three 128 x 16 accumulators (tcgen05.ld; a
+//               warp reaches only its own quarter of the 128 TMEM lanes), add
+//               them and store Y (or add it, for a split tile).
 // Every wait is bounded (ptx.cuh: mbar_wait); a timeout is recorded in the device
 // status word and the kernel runs to completion without the data.
 #include <atomic>
@@ -24,6 +38,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "ggq_internal.h"
@@ -40,7 +55,7 @@ constexpr int kStages = 4;
 constexpr int kRawStages = 2;
 constexpr int kDecoders = 512;
 constexpr int kThreads = 64 + kDecoders;
-constexpr int kTmemCols = 32;
+constexpr int kTmemCols = 64;   // D[0:32] = A_hi [X_hi; X_lo]^T, D[32:48] = A_lo X_hi^T
 
 constexpr int kAPiece = kTileRows * kKStage * 2;   // 16 KB: one bf16 part of a W tile
 constexpr int kBPiece = kN * kKStage * 2;          // 2 KB: one bf16 part of an X tile
@@ -49,14 +64,53 @@ constexpr int kRawMax = kTileRows * 272;                  // Q8_0: 8 blocks a ro
 
 constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kRawStages * kRawMax + 1024 + 256;
 
+// weight layouts: Q8_0 periods of 8 blocks (272 bytes), Q4_K super-blocks and
+// Q4_0 runs of 8 blocks (144 bytes), each 256 columns of a row
+enum SmKind { kSmQ8 = 0, kSmQ4K = 1, kSmQ40 = 2 };
+constexpr int kMaxPieces = 8;
+
 struct SmallParams {
     const float* x;   // [M, cols]
-    float* y;         // [M, rows]
+    float* y;         // [M, rows]; zeroed by the call when tiles are split
     int rows;
     int cols;
     int M;
+    int full_tiles;   // tiles computed whole (CTAs 0 .. full_tiles-1)
+    int nsplit;       // split tiles after them
+    int sb_big;       // big/small layout: 256-column blocks of the big part (0: halves)
+    int k_small;      // big/small layout: small parts a CTA
     int* status;
 };
+
+// The parts a CTA computes: tile, 256-column blocks [sb0, sb1), split or not
+struct Piece {
+    int tile, sb0, sb1;
+    bool split;
+};
+
+__device__ __forceinline__ int pieces_of(const SmallParams& p, int cta) {
+    if (cta < p.full_tiles || p.sb_big == 0) return 1;
+    const int c = cta - p.full_tiles;
+    if (c < p.nsplit) return 1;
+    return min(p.k_small, p.nsplit - (c - p.nsplit) * p.k_small);
+}
+
+__device__ __forceinline__ Piece piece_of(const SmallParams& p, int cta, int i, int nsb_all) {
+    if (cta < p.full_tiles) return Piece{cta, 0, nsb_all, false};
+    const int c = cta - p.full_tiles;
+    if (p.sb_big == 0) {   // halves: CTAs 2j, 2j + 1 of split tile j
+        const int j = c >> 1, part = c & 1;
+        return Piece{p.full_tiles + j, part ? nsb_all / 2 : 0, part ? nsb_all : nsb_all / 2, true};
+    }
+    if (c < p.nsplit) return Piece{p.full_tiles + c, 0, p.sb_big, true};
+    const int j = (c - p.nsplit) * p.k_small + i;
+    return Piece{p.full_tiles + j, p.sb_big, nsb_all, true};
+}
+
+// *p += v at the memory, no value returned
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
@@ -115,6 +169,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
 // kind::f16: D fp32, A and B bf16, both K-major, N = 16, M = 128.
 constexpr uint32_t kIdesc =
     (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kTileRows >> 4) << 24);
+// the same with N = 32: B is X_hi and X_lo stacked (their 16-row pieces are
+// adjacent, so they form one 32-row K-major operand)
+constexpr uint32_t kIdesc32 =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)((2 * kN) >> 3) << 17) | ((uint32_t)(kTileRows >> 4) << 24);
 
 // w -> bf16 pairs hi = bf16(w), lo = bf16(w - hi) (w - hi is exact in fp32)
 __device__ __forceinline__ void split_bf16x2(float2 w, uint32_t& hi, uint32_t& lo) {
@@ -137,16 +195,17 @@ __device__ __forceinline__ void q4k_sm(uint32_t s0, uint32_t s1, uint32_t s2, in
     }
 }
 
-template <bool Q4K>
+template <int K>
 __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_constant__ CUtensorMap wmap,
                                                              const SmallParams p) {
-    constexpr int kRowBytes = Q4K ? 144 : 272;   // raw bytes of one W row per 256 columns
+    constexpr bool Q4K = K == kSmQ4K;
+    constexpr int kRowBytes = K == kSmQ8 ? 272 : 144;   // raw bytes of one W row per 256 columns
     constexpr int kRawBytes = kTileRows * kRowBytes;
+    constexpr int kBoxX = K == kSmQ8 ? 136 : 144;        // TMA x coordinate step (2- or 1-byte elements)
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = blockIdx.x * kTileRows;
-    const int nsb = p.cols / 256;
-    const int nks = nsb * 4;
+    const int nsb_all = p.cols / 256;
+    const int npc = pieces_of(p, blockIdx.x);
 
     const uint32_t base_u32 = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
@@ -157,8 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
     uint64_t* empty = bars + kStages;               // [kStages]  MMA -> decoders
     uint64_t* full_raw = bars + 2 * kStages;        // [kRawStages]  TMA -> decoders
     uint64_t* empty_raw = full_raw + kRawStages;    // [kRawStages]  decoders -> TMA
-    uint64_t* acc_full = empty_raw + kRawStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* acc_full = empty_raw + kRawStages;    // MMA -> epilogue, once a part
+    uint64_t* acc_empty = acc_full + 1;             // epilogue -> MMA: the accumulator has been read
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&wmap);
@@ -171,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             mbar_init(&empty_raw[r], kDecoders);
         }
         mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 128);   // the four epilogue warps
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -185,14 +246,21 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             // the previous kernel in the stream may still be writing W (a caller
             // that rewrites weights in place): warm L2 with the first raw stages,
             // then wait before any copy
-            for (int sb = 0; sb < nsb && sb < kRawStages; ++sb)
-                tma_prefetch_2d(&wmap, sb * (Q4K ? 144 : 136), row0);
+            {
+                const Piece p0 = piece_of(p, blockIdx.x, 0, nsb_all);
+                for (int sb = p0.sb0; sb < p0.sb1 && sb < p0.sb0 + kRawStages; ++sb)
+                    tma_prefetch_2d(&wmap, sb * kBoxX, p0.tile * kTileRows);
+            }
             pdl_wait();
-            for (int sb = 0; sb < nsb; ++sb) {
-                const int r = sb % kRawStages;
-                mbar_wait(&empty_raw[r], ((sb / kRawStages) & 1) ^ 1, p.status);
-                mbar_arrive_expect_tx(&full_raw[r], kRawBytes);
-                tma_load_2d(sRaw + (size_t)r * kRawMax, &wmap, &full_raw[r], sb * (Q4K ? 144 : 136), row0);
+            int gsb = 0;   // raw stages issued (all parts)
+            for (int pc = 0; pc < npc; ++pc) {
+                const Piece pi = piece_of(p, blockIdx.x, pc, nsb_all);
+                for (int sb = pi.sb0; sb < pi.sb1; ++sb, ++gsb) {
+                    const int r = gsb % kRawStages;
+                    mbar_wait(&empty_raw[r], ((gsb / kRawStages) & 1) ^ 1, p.status);
+                    mbar_arrive_expect_tx(&full_raw[r], kRawBytes);
+                    tma_load_2d(sRaw + (size_t)r * kRawMax, &wmap, &full_raw[r], sb * kBoxX, pi.tile * kTileRows);
+                }
             }
         }
         __syncwarp();
@@ -202,17 +270,38 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             // other parts and offsets are the stage-0 one plus (offset >> 4)
             const uint64_t d0 = sw128_desc(smem_u32(sStage));
             constexpr uint32_t kLo = kAPiece >> 4, kBhi = (2 * kAPiece) >> 4, kBlo = (2 * kAPiece + kBPiece) >> 4;
+            // one loop over the stages of all parts (this thread's issue rate
+            // sets the pace, so the loop is kept as plain as for one part);
+            // at a part's end: its accumulator to the epilogue, and the next
+            // part starts once the epilogue has read it
+            int nks = 0;   // stages of all parts
+            for (int pc = 0; pc < npc; ++pc) {
+                const Piece pi = piece_of(p, blockIdx.x, pc, nsb_all);
+                nks += 4 * (pi.sb1 - pi.sb0);
+            }
+            const Piece p0 = piece_of(p, blockIdx.x, 0, nsb_all);
+            int pc = 0, pstart = 0, pend = 4 * (p0.sb1 - p0.sb0);
             for (int ks = 0; ks < nks; ++ks) {
+                if (ks == pend) {
+                    umma_commit(acc_full);
+                    mbar_wait(acc_empty, pc & 1, p.status);
+                    tc_fence_after();
+                    ++pc;
+                    const Piece pi = piece_of(p, blockIdx.x, pc, nsb_all);
+                    pstart = ks;
+                    pend = ks + 4 * (pi.sb1 - pi.sb0);
+                }
                 const int s = ks % kStages;
                 mbar_wait(&full[s], (ks / kStages) & 1, p.status);
                 tc_fence_after();
                 const uint64_t ds = d0 + (uint64_t)((s * kStageBytes) >> 4);
+                const int first = ks == pstart;
 #pragma unroll
                 for (int kk = 0; kk < kKStage / 16; ++kk) {
                     const uint64_t a = ds + 2 * kk;   // 16 bf16 = 32 bytes further along the swizzled rows
-                    umma_bf16(tmem, a, a + kBhi, kIdesc, (ks | kk) != 0);
-                    umma_bf16(tmem, a, a + kBlo, kIdesc, 1);
-                    umma_bf16(tmem, a + kLo, a + kBhi, kIdesc, 1);
+                    const uint32_t acc = !(first && kk == 0);
+                    umma_bf16(tmem, a, a + kBhi, kIdesc32, acc);              // hi*hi, hi*lo
+                    umma_bf16(tmem + 2 * kN, a + kLo, a + kBhi, kIdesc, acc);  // lo*hi
                 }
                 umma_commit(&empty[s]);
             }
@@ -220,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------- decoders (warps 2..9)
+        // ---------------------------------------------------- decoders (warps 2..17)
         const int t = threadIdx.x - 64;
         const int row = t & (kTileRows - 1);   // W row within the tile
         const int qt = t >> 7;                 // which 16 columns of a 64-column stage
@@ -229,112 +318,139 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
         const bool xv = xt < p.M;
         const float* xrow = p.x + (size_t)(xv ? xt : 0) * p.cols + xk;
         pdl_wait();   // X may come from the previous kernel in the stream
-        // X of the next 4 stages in registers, so its loads are in flight early
-        float2 xb[4];
+        int gsb = 0;   // raw stages consumed (all parts): the rings' position
+        for (int pc = 0; pc < npc; ++pc) {
+            const Piece pi = piece_of(p, blockIdx.x, pc, nsb_all);
+            const int nks = 4 * (pi.sb1 - pi.sb0);
+            const float* xp = xrow + (size_t)pi.sb0 * 256;
+            // X of the next 4 stages in registers, so its loads are in flight early
+            float2 xb[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            xb[c] = (xv && c < nks) ? __ldg(reinterpret_cast<const float2*>(xrow + kKStage * c))
-                                    : make_float2(0.f, 0.f);
-        for (int sb = 0; sb < nsb; ++sb) {
-            const int r = sb % kRawStages;
-            mbar_wait(&full_raw[r], (sb / kRawStages) & 1, p.status);
-            const uint8_t* rp = sRaw + (size_t)r * kRawMax + (size_t)row * kRowBytes;
-            uint4 hdr = make_uint4(0, 0, 0, 0);
-            if constexpr (Q4K) hdr = *reinterpret_cast<const uint4*>(rp);
+            for (int c = 0; c < 4; ++c)
+                xb[c] = (xv && c < nks) ? __ldg(reinterpret_cast<const float2*>(xp + kKStage * c))
+                                        : make_float2(0.f, 0.f);
+            for (int lsb = 0; lsb < pi.sb1 - pi.sb0; ++lsb, ++gsb) {
+                const int r = gsb % kRawStages;
+                mbar_wait(&full_raw[r], (gsb / kRawStages) & 1, p.status);
+                const uint8_t* rp = sRaw + (size_t)r * kRawMax + (size_t)row * kRowBytes;
+                uint4 hdr = make_uint4(0, 0, 0, 0);
+                if constexpr (Q4K) hdr = *reinterpret_cast<const uint4*>(rp);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int ks = sb * 4 + c;
-                const int s = ks % kStages;
-                // 16 weights of this thread, exact in fp32, as 8 pairs
-                float2 w[8];
-                if constexpr (Q4K) {
-                    // columns 64c + 16qt .. +15: sub-block 2c + qt/2, qs bytes 32c + 16(qt&1) ..
-                    int sc, m;
-                    q4k_sm(hdr.y, hdr.z, hdr.w, 2 * c + (qt >> 1), sc, m);
-                    const float a = half_bits_to_float(hdr.x) * (float)sc;
-                    const float bm = half_bits_to_float(hdr.x >> 16) * (float)m;
-                    const uint4 q = *reinterpret_cast<const uint4*>(rp + 16 + 32 * c + 16 * (qt & 1));
-                    const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-                    const int ns = 4 * (qt >> 1);   // low or high nibbles
+                for (int c = 0; c < 4; ++c) {
+                    const int lks = lsb * 4 + c;   // stage within the part
+                    const int ks = gsb * 4 + c;    // ring position
+                    const int s = ks % kStages;
+                    // 16 weights of this thread, exact in fp32, as 8 pairs
+                    float2 w[8];
+                    if constexpr (K == kSmQ4K) {
+                        // columns 64c + 16qt .. +15: sub-block 2c + qt/2, qs bytes 32c + 16(qt&1) ..
+                        int sc, m;
+                        q4k_sm(hdr.y, hdr.z, hdr.w, 2 * c + (qt >> 1), sc, m);
+                        const float a = half_bits_to_float(hdr.x) * (float)sc;
+                        const float bm = half_bits_to_float(hdr.x >> 16) * (float)m;
+                        const uint4 q = *reinterpret_cast<const uint4*>(rp + 16 + 32 * c + 16 * (qt & 1));
+                        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+                        const int ns = 4 * (qt >> 1);   // low or high nibbles
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        // 0x4B000000 | q is the float 2^23 + q
-                        const uint32_t n0 = (qw[i >> 1] >> (16 * (i & 1) + ns)) & 15u;
-                        const uint32_t n1 = (qw[i >> 1] >> (16 * (i & 1) + 8 + ns)) & 15u;
-                        const float2 f = make_float2(__uint_as_float(0x4B000000u | n0), __uint_as_float(0x4B000000u | n1));
-                        const float2 qf = __fadd2_rn(f, make_float2(-8388608.0f, -8388608.0f));
-                        w[i] = __ffma2_rn(qf, make_float2(a, a), make_float2(-bm, -bm));
+                        for (int i = 0; i < 8; ++i) {
+                            // 0x4B000000 | q is the float 2^23 + q
+                            const uint32_t n0 = (qw[i >> 1] >> (16 * (i & 1) + ns)) & 15u;
+                            const uint32_t n1 = (qw[i >> 1] >> (16 * (i & 1) + 8 + ns)) & 15u;
+                            const float2 f = make_float2(__uint_as_float(0x4B000000u | n0), __uint_as_float(0x4B000000u | n1));
+                            const float2 qf = __fadd2_rn(f, make_float2(-8388608.0f, -8388608.0f));
+                            w[i] = __ffma2_rn(qf, make_float2(a, a), make_float2(-bm, -bm));
+                        }
+                    } else {
+                        // block 2c + qt/2 of the row's 256 columns: fp16 d at its start,
+                        // then its codes; Q8_0: q bytes 16(qt&1) .. +15 of its 32 (34-byte
+                        // blocks); Q4_0: the low (qt even) or high nibbles of its 16 code
+                        // bytes (18-byte blocks: weight l low nibble, weight 16 + l high)
+                        constexpr int kBlk = K == kSmQ8 ? 34 : 18;
+                        const int off = kBlk * (2 * c + (qt >> 1));
+                        const uint16_t dh = *reinterpret_cast<const uint16_t*>(rp + off);
+                        const int qo = off + 2 + (K == kSmQ8 ? 16 * (qt & 1) : 0);   // 2-byte aligned
+                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(rp + (qo & ~3));
+                        const int sh = 8 * (qo & 3);   // 0 or 16
+                        uint32_t v[5];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) v[i] = wp[i];
+                        v[4] = sh ? wp[4] : 0u;   // only a misaligned start reaches a fifth word
+                        uint32_t u[4];   // the 16 codes, four a word, as unsigned bytes
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t wv = __funnelshift_r(v[i], v[i + 1], sh);
+                            if constexpr (K == kSmQ8) u[i] = wv ^ 0x80808080u;   // q + 128
+                            else u[i] = (qt & 1) ? ((wv >> 4) & 0x0F0F0F0Fu) : (wv & 0x0F0F0F0Fu);   // u = q + 8
+                        }
+                        const float d = half_bits_to_float(dh);
+                        // 0x4B0000 | byte is the float 2^23 + byte; minus 2^23 + the offset: q
+                        constexpr float kOff = K == kSmQ8 ? -8388736.0f : -8388616.0f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t f0 = __byte_perm(u[i >> 1], 0x4B000000u, 0x7650u | (uint32_t)(2 * (i & 1)));
+                            const uint32_t f1 = __byte_perm(u[i >> 1], 0x4B000000u, 0x7650u | (uint32_t)(2 * (i & 1) + 1));
+                            const float2 qf = __fadd2_rn(make_float2(__uint_as_float(f0), __uint_as_float(f1)),
+                                                         make_float2(kOff, kOff));
+                            w[i] = __fmul2_rn(qf, make_float2(d, d));
+                        }
                     }
-                } else {
-                    // block 2c + qt/2 of the row's period: fp16 d at its start, then
-                    // q bytes 16(qt&1) .. +15 of its 32
-                    const int off = 34 * (2 * c + (qt >> 1));
-                    const uint16_t dh = *reinterpret_cast<const uint16_t*>(rp + off);
-                    const int qo = off + 2 + 16 * (qt & 1);   // 2-byte aligned
-                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rp + (qo & ~3));
-                    const int sh = 8 * (qo & 3);   // 0 or 16
-                    uint32_t v[5];
+                    mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
+                    uint8_t* sA = sStage + (size_t)s * kStageBytes;
+                    uint8_t* ahi = sA + (size_t)row * 128;
+                    uint8_t* alo = ahi + kAPiece;
+                    const int sw = row & 7;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) v[i] = wp[i];
-                    v[4] = sh ? wp[4] : 0u;   // only a misaligned start reaches a fifth word
-                    uint32_t u[4];   // the 16 q bytes, four a word, made unsigned (q + 128)
+                    for (int j = 0; j < 2; ++j) {   // 16-byte chunk 2qt + j of the row: columns 16qt + 8j .. +7
+                        uint32_t hi[4], lo[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) u[i] = __funnelshift_r(v[i], v[i + 1], sh) ^ 0x80808080u;
-                    const float d = half_bits_to_float(dh);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        // 0x4B0000 | (q + 128) is the float 2^23 + 128 + q
-                        const uint32_t f0 = __byte_perm(u[i >> 1], 0x4B000000u, 0x7650u | (uint32_t)(2 * (i & 1)));
-                        const uint32_t f1 = __byte_perm(u[i >> 1], 0x4B000000u, 0x7650u | (uint32_t)(2 * (i & 1) + 1));
-                        const float2 qf = __fadd2_rn(make_float2(__uint_as_float(f0), __uint_as_float(f1)),
-                                                     make_float2(-8388736.0f, -8388736.0f));
-                        w[i] = __fmul2_rn(qf, make_float2(d, d));
+                        for (int e = 0; e < 4; ++e) split_bf16x2(w[4 * j + e], hi[e], lo[e]);
+                        const int ch = ((2 * qt + j) ^ sw) << 4;
+                        *reinterpret_cast<uint4*>(ahi + ch) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4*>(alo + ch) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
+                    {
+                        // X: activation row xt, columns xk, xk+1 of this stage
+                        uint32_t hi, lo;
+                        split_bf16x2(xb[c], hi, lo);
+                        uint8_t* bhi = sA + 2 * kAPiece + (size_t)xt * 128;
+                        const int ch = (((xk >> 3) ^ (xt & 7)) << 4) + 4 * ((xk >> 1) & 3);
+                        *reinterpret_cast<uint32_t*>(bhi + ch) = hi;
+                        *reinterpret_cast<uint32_t*>(bhi + kBPiece + ch) = lo;
+                        // next use of this register: stage lks + 4 of the part
+                        xb[c] = (xv && lks + 4 < nks) ? __ldg(reinterpret_cast<const float2*>(xp + kKStage * (lks + 4)))
+                                                      : make_float2(0.f, 0.f);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&full[s]);
                 }
-                mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
-                uint8_t* sA = sStage + (size_t)s * kStageBytes;
-                uint8_t* ahi = sA + (size_t)row * 128;
-                uint8_t* alo = ahi + kAPiece;
-                const int sw = row & 7;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {   // 16-byte chunk 2qt + j of the row: columns 16qt + 8j .. +7
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) split_bf16x2(w[4 * j + e], hi[e], lo[e]);
-                    const int ch = ((2 * qt + j) ^ sw) << 4;
-                    *reinterpret_cast<uint4*>(ahi + ch) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(alo + ch) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
-                {
-                    // X: activation row xt, columns xk, xk+1 of this stage
-                    uint32_t hi, lo;
-                    split_bf16x2(xb[c], hi, lo);
-                    uint8_t* bhi = sA + 2 * kAPiece + (size_t)xt * 128;
-                    const int ch = (((xk >> 3) ^ (xt & 7)) << 4) + 4 * ((xk >> 1) & 3);
-                    *reinterpret_cast<uint32_t*>(bhi + ch) = hi;
-                    *reinterpret_cast<uint32_t*>(bhi + kBPiece + ch) = lo;
-                    // next use of this register: stage ks + 4
-                    xb[c] = (xv && ks + 4 < nks) ? __ldg(reinterpret_cast<const float2*>(xrow + kKStage * (ks + 4)))
-                                                 : make_float2(0.f, 0.f);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&full[s]);
+                mbar_arrive(&empty_raw[r]);
             }
-            mbar_arrive(&empty_raw[r]);
-        }
 
-        // ------------------------------------------------------------ epilogue
-        if (warp < 6) {   // warps 2..5 cover the four TMEM lane quarters
-            mbar_wait(acc_full, 0, p.status);
-            tc_fence_after();
-            const int q = warp & 3;   // TMEM lane quarter of this warp
-            const int yrow = row0 + 32 * q + lane;
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16), v);
-            if (yrow < p.rows) {
+            // -------------------------------------------------------- epilogue
+            if (warp < 6) {   // warps 2..5 cover the four TMEM lane quarters
+                mbar_wait(acc_full, pc & 1, p.status);
+                tc_fence_after();
+                const int q = warp & 3;   // TMEM lane quarter of this warp
+                const int yrow = pi.tile * kTileRows + 32 * q + lane;
+                float v[16], vl[16], vh[16];
+                const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+                tmem_ld16(tq, v);               // hi * hi
+                tmem_ld16(tq + kN, vl);         // hi * lo
+                tmem_ld16(tq + 2 * kN, vh);     // lo * hi
 #pragma unroll
-                for (int i = 0; i < kN; ++i)
-                    if (i < p.M) p.y[(size_t)i * p.rows + yrow] = v[i];
+                for (int i = 0; i < kN; ++i) v[i] += vl[i] + vh[i];
+                tc_fence_before();
+                mbar_arrive(acc_empty);   // the accumulator may take the next part's products
+                if (yrow < p.rows) {
+#pragma unroll
+                    for (int i = 0; i < kN; ++i) {
+                        if (i < p.M) {
+                            float* yp = p.y + (size_t)i * p.rows + yrow;
+                            if (pi.split) red_add_f32(yp, v[i]);
+                            else *yp = v[i];
+                        }
+                    }
+                }
             }
         }
     }
@@ -360,19 +476,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-template <bool Q4K>
-int launch_t(const CUtensorMap& wmap, const SmallParams& p, cudaStream_t stream) {
+template <int K>
+int launch_t(const CUtensorMap& wmap, const SmallParams& p, int grid, cudaStream_t stream) {
     static std::atomic<int> configured[64] = {};   // set once per device; the value set never changes
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(smallm_kernel<Q4K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(smallm_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.rows + kTileRows - 1) / kTileRows));
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
@@ -381,7 +497,7 @@ int launch_t(const CUtensorMap& wmap, const SmallParams& p, cudaStream_t stream)
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, smallm_kernel<Q4K>, wmap, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, smallm_kernel<K>, wmap, p);
     if (e != cudaSuccess) return cuda_fail(e, "small-M launch");
     return GGQ_OK;
 }
@@ -389,22 +505,23 @@ int launch_t(const CUtensorMap& wmap, const SmallParams& p, cudaStream_t stream)
 }  // namespace
 
 bool smallm_supported(int type, int64_t rows, int64_t cols, int M) {
-    return (type == GGQ_Q8_0 || type == GGQ_Q4_K) && M >= 1 && M <= kN && cols >= 256 && cols % 256 == 0 &&
-           cols <= (1 << 24) && rows >= 1 && rows <= 0x7fffffff;
+    return (type == GGQ_Q8_0 || type == GGQ_Q4_K || type == GGQ_Q4_0) && M >= 1 && M <= kN && cols >= 256 &&
+           cols % 256 == 0 && cols <= (1 << 24) && rows >= 1 && rows <= 0x7fffffff;
 }
 
 int launch_smallm(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
                   cudaStream_t stream) {
     auto enc = encoder();
     if (!enc) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled unavailable");
-    const bool q4k = type == GGQ_Q4_K;
-    const int64_t row_bytes = cols / 256 * (q4k ? 144 : 272);
+    const int kind = type == GGQ_Q4_K ? kSmQ4K : type == GGQ_Q4_0 ? kSmQ40 : kSmQ8;
+    const bool bytes = kind != kSmQ8;   // 144-byte runs as bytes; Q8_0 periods as 2-byte elements
+    const int64_t row_bytes = cols / 256 * (bytes ? 144 : 272);
     CUtensorMap wmap;
-    cuuint64_t dims[2] = {(cuuint64_t)(q4k ? row_bytes : row_bytes / 2), (cuuint64_t)rows};
+    cuuint64_t dims[2] = {(cuuint64_t)(bytes ? row_bytes : row_bytes / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)(q4k ? 144 : 136), (cuuint32_t)kTileRows};
+    cuuint32_t box[2] = {(cuuint32_t)(bytes ? 144 : 136), (cuuint32_t)kTileRows};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(&wmap, q4k ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+    CUresult r = enc(&wmap, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
                      const_cast<void*>(W), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(GGQ_ECUDA, "tensor map (W) failed (%d)", (int)r);
@@ -416,7 +533,42 @@ int launch_smallm(int type, const void* W, int64_t rows, int64_t cols, const flo
     p.M = M;
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
-    return q4k ? launch_t<true>(wmap, p, stream) : launch_t<false>(wmap, p, stream);
+    // Split tiles of a partly filled wave along K: halves when they fit the SMs
+    // twice over, else (one wave of more than half the SMs) a big part of sb_big
+    // 256-column blocks a tile and small parts, k_small a CTA, with sb_big the
+    // least for which R + ceil(R / k_small) CTAs fit the SMs.
+    int dev = 0, nsm = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int T = (int)((rows + kTileRows - 1) / kTileRows);
+    const int S = (int)(cols / 256);
+    const int R = T > nsm ? T % nsm : T;
+    int grid = T;
+    if (R > 0 && S >= 2) {
+        if (2 * R <= nsm) {
+            p.nsplit = R;
+            grid = T + R;
+        } else if (R == T) {
+            for (int B = (S * R + nsm - 1) / nsm; B <= S - 1; ++B) {
+                const int k = std::min(B / (S - B), kMaxPieces);
+                if (k >= 1 && R + (R + k - 1) / k <= nsm) {
+                    p.nsplit = R;
+                    p.sb_big = B;
+                    p.k_small = k;
+                    grid = R + (R + k - 1) / k;
+                    break;
+                }
+            }
+        }
+    }
+    p.full_tiles = T - p.nsplit;
+    if (p.nsplit > 0) {   // split tiles add both parts into a zeroed y
+        cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * (size_t)M * (size_t)rows, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "small-M: zero y");
+    }
+    if (kind == kSmQ4K) return launch_t<kSmQ4K>(wmap, p, grid, stream);
+    if (kind == kSmQ40) return launch_t<kSmQ40>(wmap, p, grid, stream);
+    return launch_t<kSmQ8>(wmap, p, grid, stream);
 }
 
 }  // namespace ggq

@@ -156,9 +156,11 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  *          (cols % 256 == 0), GGQ_F32 (any cols >= 1)
  *   W      device, rows x row-bytes, row-major, 16-byte aligned
  *   x      device, fp32 [M, cols] row-major, 16-byte aligned
- *   y      device, fp32 [M, rows] row-major, 4-byte aligned; fully overwritten
+ *   y      device, fp32 [M, rows] row-major, 4-byte aligned; fully overwritten;
+ *          must not overlap W or x (with 5..16 rows it may be zeroed first)
  *   M      1..16 (M > 1 is the small-batch variant: each decoded block is used
- *          for all M rows of x)
+ *          for all M rows of x; from 5 rows on, Q8_0, Q4_K and Q4_0 run on the
+ *          tensor cores in one pass over W)
  *   stream cudaStream_t
  *
  * Finite inputs with |x| < 2^70 are supported.  Errors: GGQ_EINVAL (NULL

@@ -143,6 +143,51 @@ def test_gemv_tensor_core_small_batch(env, qtype, rows, cols, M):
     assert_close(y, y_ref, a_ref, f"type {qtype} {rows}x{cols} M={M}")
 
 
+# Tiles split along K (the y zeroed, both parts added): big/small parts when
+# the 128-row tiles fill more than half of the 152 SMs in one wave (14336 rows:
+# 112 tiles), halves of the last wave's tiles otherwise (20480 rows: 160
+# tiles, 8 of them split; 12800 x 2048: 100 tiles, 8 blocks a row).
+@pytest.mark.parametrize("qtype,rows,cols,M", [(2, 14336, 4096, 16), (12, 14336, 4096, 8), (8, 20480, 1024, 16),
+                                             (2, 12800, 2048, 5), (12, 300, 4096, 9)])
+def test_gemv_tensor_core_split_layouts(env, qtype, rows, cols, M):
+    W = weights(qtype, rows, cols, stream=21)
+    x = xs(M, cols, stream=22)
+    y = gpu_gemv(env, qtype, W, rows, cols, x)
+    y_ref, a_ref = oracle.gemv_dense(qtype, W, rows, cols, x)
+    assert_close(y, y_ref, a_ref, f"type {qtype} {rows}x{cols} M={M}")
+
+
+def test_gemv_tensor_core_split_repeat_and_graph(env):
+    """The two parts of a split tile add in whichever order they finish: the
+    same fp32 sum, so repeated calls agree bit for bit; captured in a CUDA
+    graph (the zeroing of y and the kernel), replays with new x are right."""
+    torch, ggq = env
+    rows, cols, M = 14336, 4096, 16
+    W = weights(8, rows, cols, stream=23)
+    x = xs(M, cols, stream=24)
+    Wd, xd = _dev(torch, W), _dev(torch, x)
+    outs = [ggq.gemv(8, Wd, rows, cols, xd).cpu().numpy() for _ in range(3)]
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+    s = torch.cuda.Stream()
+    y = torch.full((M, rows), float("nan"), dtype=torch.float32, device="cuda")
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            ggq.check(ggq.ggq_gemv(8, Wd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr(), M, s.cuda_stream),
+                      "ggq_gemv")
+    x2 = xs(M, cols, stream=25)
+    xd.copy_(torch.from_numpy(x2))
+    y.fill_(float("nan"))
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ggq.device_status() == 0
+    y_ref, a_ref = oracle.gemv_dense(8, W, rows, cols, x2)
+    assert_close(y.cpu().numpy(), y_ref, a_ref, "graph replay")
+
+
 def test_gemv_tensor_core_integer_inputs_are_exact(env):
     """Q8_0 with d = 1 and small integer x at M = 8: every product and sum is an
     exact integer in fp32, so the bf16 hi/lo parts and the tensor-core sums give

@@ -288,23 +288,33 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     using KSet = KindSet<KM>;
     constexpr int kTileK = KSet::kTile;   // ring slot stride
     constexpr int kThreads = 32 * W;
+    // warps 0 .. WC-1 decode (consumers); warp WC issues every weight copy of
+    // the CTA, lane w for consumer warp w (its copy cursor, its ring)
+    constexpr int WC = W - 1;
+    constexpr int kCThreads = 32 * WC;
+    static_assert(WC >= 1 && WC <= 31, "one producer lane per consumer warp");
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = lane >> 2, c = lane & 3;   // row of the group, chunk of the SB
     const int D = p.ring;
 
-    // shared memory: [warp rings][stage info slots][group ranges][x'][sums][cut-group parts][barriers]
-    uint8_t* ring = smem + (size_t)warp * D * kTileK;
-    StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)W * D * kTileK);
+    // shared memory: [consumer rings][stage info slots][group ranges][x'][sums][cut-group parts][barriers]
+    StageInfo* infos = reinterpret_cast<StageInfo*>(smem + (size_t)WC * D * kTileK);
     int2* part = reinterpret_cast<int2*>(infos + kInfoSlots);   // [kPartMax]
     float* xp = reinterpret_cast<float*>(part + kPartMax);
     float* sums = xp + (size_t)MMAX * p.xs;
-    float* cut_val = sums + (size_t)MMAX * p.nsub;                                // [2][W][8][MMAX]
-    int* cut_grp = reinterpret_cast<int*>(cut_val + 2 * W * kGroupRows * MMAX);   // [2][W]
-    uint64_t* full = reinterpret_cast<uint64_t*>(cut_grp + 2 * W) + warp * D;     // 8-byte aligned: all sizes even
+    float* cut_val = sums + (size_t)MMAX * p.nsub;                                 // [2][WC][16][MMAX]
+    int* cut_grp = reinterpret_cast<int*>(cut_val + 2 * WC * kGroupRows * MMAX);   // [2][WC]
+    uint64_t* full_all = reinterpret_cast<uint64_t*>(cut_grp + 2 * WC);            // [WC][D]; 8-byte aligned: all sizes even
+    uint64_t* empty_all = full_all + WC * D;                                       // [WC][D]
+    // consumer-only CTA barrier (the producer warp runs on its own)
+    auto csync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory"); };
 
-    if (lane == 0) {
-        for (int i = 0; i < D; ++i) mbar_init(&full[i], 1);
+    if (warp < WC && lane == 0) {
+        for (int i = 0; i < D; ++i) {
+            mbar_init(&full_all[warp * D + i], 1);    // the producer's expect_tx; the copy's bytes
+            mbar_init(&empty_all[warp * D + i], 1);   // the consumer warp, done with the slot
+        }
         fence_mbar_init();
     }
     // stages 0 .. kInfoSlots - 2, and the row ranges
@@ -316,107 +326,147 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
     __syncthreads();
     pdl_launch_dependents();
 
-    // ---- copy cursor of this warp: its tiles of every stage, in order, one
-    // copy per (group, up to NSB consecutive SBs)
-    // stage, next tile, end of the run; (group, SB) of the next tile and the
-    // group's matrix and first row, advanced without dividing
-    int cs = -1, ct = 0, ct1 = 0, cU = 1, cgi = 0, cu = 0, cseg = 0, crow = 0;
-    int cnext = 0;                   // first local group of matrix cseg + 1 (groups advance by one)
-    int ckind = KSet::kFirst;        // weight kind of stage cs
-    const StageDesc* csd = &inl;
-    const StageInfo* cinf = infos;   // the fields of stage cs
-    int scur = 0;                    // stage the CTA is in: slots hold scur .. scur + kInfoSlots - 2
-    Groups cg{};
-    int inflight = 0;   // copies issued and not yet consumed
-    int islot = 0;      // ring slot of the next copy
-    const uint64_t wpol = l2_evict_first_policy();   // weights are read once per pass
-    auto next_seg_start = [&]() {
-        return cseg + 1 < cinf->nseg ? cinf->gstart[cseg + 1] - cg.g0 : 0x7fffffff;
-    };
-    // the next stage in which this warp has tiles; false past the last
-    auto next_stage = [&]() {
-        while (ct == ct1) {
-            if (++cs >= p.nstages) return false;
-            csd = p.table ? p.table + cs : &inl;
-            cinf = cs <= scur + kInfoSlots - 2 ? infos + cs % kInfoSlots : &csd->info;
-            cg = cta_groups(cs < kPartMax ? part[cs] : cta_span(cinf, blockIdx.x, gridDim.x));
-            warp_run<W>(cg, cinf->units, warp, ct, ct1);
-        }
-        cU = cinf->units;
-        if constexpr (KSet::kMixed) ckind = cinf->kind;
-        cgi = ct / cU;
-        cu = ct - cgi * cU;
-        int nrows;
-        group_at(cinf, cg, cgi, cseg, crow, nrows);
-        cnext = next_seg_start();
-        return true;
-    };
-    auto refill = [&]() {   // keep up to D copies in flight or resident
-        while (inflight < D) {
-            if (ct == ct1 && !next_stage()) break;
-            const int nv = min(min(KSet::nsb(ckind), cU - cu), ct1 - ct);
-            tma_issue_2d(lane == 0, ring + (size_t)islot * kTileK, &csd->maps[cseg], &full[islot],
-                         KSet::coord(ckind, cu), crow, KSet::copy(ckind), wpol);
-            ct += nv;
-            cu += nv;
-            if (cu == cU && ct < ct1) {   // next group of this run: same matrix, 16 rows on, or the next matrix
-                cu = 0;
-                ++cgi;
-                if (cgi == cnext) {
-                    ++cseg;
-                    crow = 0;
-                    cnext = next_seg_start();
-                } else {
-                    crow += kGroupRows;
+    if (warp == WC) {
+        // ---- producer: lane w walks consumer warp w's tiles of every stage, in
+        // order, one copy per (group, up to NSB consecutive SBs), into ring
+        // slots as the consumer frees them.  Stage fields are read from the
+        // stage table (global memory, L2): the consumers' window moves with
+        // their stage, not with this cursor, which runs ahead.
+        const int w = lane;
+        if (w < WC) {
+            uint8_t* ring = smem + (size_t)w * D * kTileK;
+            uint64_t* full = full_all + w * D;
+            uint64_t* empty = empty_all + w * D;
+            // stage, next tile, end of the run; (group, SB) of the next tile and
+            // the group's matrix and first row, advanced without dividing
+            int cs = -1, ct = 0, ct1 = 0, cU = 1, cgi = 0, cu = 0, cseg = 0, crow = 0;
+            int cnext = 0;                   // first local group of matrix cseg + 1
+            int ckind = KSet::kFirst;        // weight kind of stage cs
+            const StageDesc* csd = &inl;
+            const StageInfo* cinf = &inl.info;
+            Groups cg{};
+            auto next_seg_start = [&]() {
+                return cseg + 1 < cinf->nseg ? cinf->gstart[cseg + 1] - cg.g0 : 0x7fffffff;
+            };
+            // the next stage in which warp w has tiles; false past the last
+            auto next_stage = [&]() {
+                while (ct == ct1) {
+                    if (++cs >= p.nstages) return false;
+                    csd = p.table ? p.table + cs : &inl;
+                    cinf = &csd->info;
+                    cg = cta_groups(cs < kPartMax ? part[cs] : cta_span(cinf, blockIdx.x, gridDim.x));
+                    warp_run<WC>(cg, cinf->units, w, ct, ct1);
+                }
+                cU = cinf->units;
+                if constexpr (KSet::kMixed) ckind = cinf->kind;
+                cgi = ct / cU;
+                cu = ct - cgi * cU;
+                int nrows;
+                group_at(cinf, cg, cgi, cseg, crow, nrows);
+                cnext = next_seg_start();
+                return true;
+            };
+            const uint64_t wpol = l2_evict_first_policy();   // weights are read once per pass
+            // The previous kernel in the stream may still be writing what this
+            // one reads (x, and W too if a caller rewrites weights in place), so
+            // every copy is issued after the wait.  Before it, only L2 is warmed
+            // with warp w's first tiles of stage 0 (a prefetch never decides what
+            // a copy reads).
+            {
+                const StageDesc* d0 = p.table ? p.table : &inl;
+                const Groups g0 = cta_groups(part[0]);
+                const int U0 = infos[0].units;
+                const int k0 = KSet::kMixed ? infos[0].kind : KSet::kFirst;
+                int t, tend;
+                warp_run<WC>(g0, U0, w, t, tend);
+                for (int k = 0; k < D && t < tend; ++k) {
+                    const int gi = t / U0, u = t - gi * U0;
+                    int seg, row, nrows;
+                    group_at(&infos[0], g0, gi, seg, row, nrows);
+                    tma_prefetch_2d(&d0->maps[seg], KSet::coord(k0, u), row);
+                    t += min(min(KSet::nsb(k0), U0 - u), tend - t);
                 }
             }
-            ++inflight;
-            if (++islot == D) islot = 0;
+            pdl_wait();
+            int eslot = 0;
+            uint32_t ephase = 0;
+            // The lanes step together: each round, every lane whose consumer has
+            // freed its next slot issues that copy, under predication, so one
+            // pass through this code serves up to WC copies.  A lane ends after
+            // its last copy; a slot that stays busy beyond the wait limit ends
+            // its lane with the timeout bit set.
+            bool live = ct < ct1 || next_stage();
+            unsigned long long t_wait = 0;   // when this lane began to wait, 0: not waiting
+            for (uint32_t it = 0;; ++it) {
+                const bool ready = live && mbar_try_wait(&empty[eslot], ephase ^ 1u);
+                if (ready) {
+                    t_wait = 0;
+                    const int nv = min(min(KSet::nsb(ckind), cU - cu), ct1 - ct);
+                    tma_issue_2d(true, ring + (size_t)eslot * kTileK, &csd->maps[cseg], &full[eslot],
+                                 KSet::coord(ckind, cu), crow, KSet::copy(ckind), wpol);
+                    ct += nv;
+                    cu += nv;
+                    if (cu == cU && ct < ct1) {   // next group of this run: same matrix, 16 rows on, or the next matrix
+                        cu = 0;
+                        ++cgi;
+                        if (cgi == cnext) {
+                            ++cseg;
+                            crow = 0;
+                            cnext = next_seg_start();
+                        } else {
+                            crow += kGroupRows;
+                        }
+                    }
+                    if (++eslot == D) {
+                        eslot = 0;
+                        ephase ^= 1u;
+                    }
+                    live = ct < ct1 || next_stage();
+                } else if (live && (it & 63u) == 0) {
+                    const unsigned long long now = globaltimer_ns();
+                    if (t_wait == 0) {
+                        t_wait = now;
+                    } else {
+                        const unsigned long long limit = ld_relaxed(p.status) != 0 ? kDrainNs : kWaitLimitNs;
+                        if (now - t_wait > limit) {
+                            atomicOr(p.status, kStatusTimeout);
+                            live = false;
+                        }
+                    }
+                }
+                const unsigned busy = __ballot_sync((1u << WC) - 1u, live);   // the WC producer lanes
+                if (busy == 0) break;
+            }
         }
-    };
-    // The previous kernel in the stream may still be writing what this one
-    // reads (x, and W too if a caller rewrites weights in place), so every copy
-    // is issued after the wait.  Before it, only L2 is warmed with this warp's
-    // first tiles of stage 0 (a prefetch never decides what a copy reads).
-    if (lane == 0) {
-        const StageDesc* d0 = p.table ? p.table : &inl;
-        const Groups g0 = cta_groups(part[0]);
-        const int U0 = infos[0].units;
-        const int k0 = KSet::kMixed ? infos[0].kind : KSet::kFirst;
-        int t, tend;
-        warp_run<W>(g0, U0, warp, t, tend);
-        for (int k = 0; k < D && t < tend; ++k) {
-            const int gi = t / U0, u = t - gi * U0;
-            int seg, row, nrows;
-            group_at(&infos[0], g0, gi, seg, row, nrows);
-            tma_prefetch_2d(&d0->maps[seg], KSet::coord(k0, u), row);
-            t += min(min(KSet::nsb(k0), U0 - u), tend - t);
-        }
+        return;
     }
+
+    // ---- consumers
+    uint8_t* ring = smem + (size_t)warp * D * kTileK;
+    uint64_t* full = full_all + warp * D;
+    uint64_t* empty = empty_all + warp * D;
     pdl_wait();
-    refill();
 
     int cslot = 0;          // ring slot of the next copy to consume
     uint32_t cphase = 0;    // its barrier phase
 
     for (int s = 0; s < p.nstages; ++s) {
         const StageInfo* sd = infos + s % kInfoSlots;
-        scur = s;
         // this CTA's row groups and this warp's tile run: independent of x, so
         // worked out before the stage barrier
         const Groups G = cta_groups(s < kPartMax ? part[s] : cta_span(sd, blockIdx.x, gridDim.x));
         int t0, t1;
-        warp_run<W>(G, sd->units, warp, t0, t1);
+        warp_run<WC>(G, sd->units, warp, t0, t1);
         // the fields of stage s + kInfoSlots - 1, to the slot of stage s - 1
-        // (free: every warp has passed the end of stage s - 1, and copy
-        // cursors never go back); waited for before the end of stage s
-        if (s + kInfoSlots - 1 < p.nstages && warp == W - 1 && lane < kInfoVec)
+        // (free: every consumer warp has passed the end of stage s - 1);
+        // waited for before the end of stage s
+        if (s + kInfoSlots - 1 < p.nstages && warp == WC - 1 && lane < kInfoVec)
             cp_async_16(reinterpret_cast<int4*>(infos + (s + kInfoSlots - 1) % kInfoSlots) + lane,
                         reinterpret_cast<const int4*>(&p.table[s + kInfoSlots - 1].info) + lane);
         if (s > 0) {
             // every CTA has finished stage s-1 (its outputs are visible)
             if (tid == 0) wait_count(p.counter, s * (int)gridDim.x, p.status);
-            __syncthreads();
+            csync();
         }
         const int cols = sd->cols, U = sd->units;
         const int xs = p.xs, nsub = p.nsub;
@@ -515,16 +565,16 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 const int xop = sd->x_op;
                 if (xop == GGQ_X_PLAIN) {
                     constexpr int kBatch = 8;
-                    for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                    for (int q0 = warp * 32; q0 < n4; q0 += kCThreads * kBatch) {
                         float4 v[kBatch];
     #pragma unroll
                         for (int i = 0; i < kBatch; ++i) {
-                            const int q = q0 + i * kThreads + lane;
+                            const int q = q0 + i * kCThreads + lane;
                             v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
     #pragma unroll
                         for (int i = 0; i < kBatch; ++i) {
-                            const int qb = q0 + i * kThreads;   // warp-uniform, a multiple of 32
+                            const int qb = q0 + i * kCThreads;   // warp-uniform, a multiple of 32
                             if (qb >= n4) break;
                             place(qb, v[i]);
                         }
@@ -536,13 +586,13 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     // norm_w * x / sqrt(mean + eps).  SILU_MUL: silu(x) * up.
                     const float4* o4 = reinterpret_cast<const float4*>(xop == GGQ_X_RMSNORM ? sd->norm_w : sd->up);
                     constexpr int kBatch = 4;   // two float4 a step: x and norm_w / up
-                    float* red = cut_val;       // [W][MMAX]: per-warp sums of squares
+                    float* red = cut_val;       // [WC][MMAX]: per-warp sums of squares
                     float rs[MMAX];
                     auto load2 = [&](int q0, float4 (&v)[kBatch], float4 (&o)[kBatch]) {
     #pragma unroll
                         for (int i = 0; i < kBatch; ++i) {
-                            const int q = q0 + i * kThreads + lane;
-                            const int qb = q0 + i * kThreads;
+                            const int q = q0 + i * kCThreads + lane;
+                            const int qb = q0 + i * kCThreads;
                             const int m = MMAX == 1 ? 0 : qb / c4;
                             v[i] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
                             o[i] = q < n4 ? __ldcg(o4 + (xop == GGQ_X_RMSNORM ? q - m * c4 : q))
@@ -556,11 +606,11 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                             const float t = warp_sum(ss[m]);
                             if (lane == 0) red[warp * MMAX + m] = t;
                         }
-                        __syncthreads();
+                        csync();
     #pragma unroll
                         for (int m = 0; m < MMAX; ++m) {
                             float t = 0.0f;
-                            for (int w2 = 0; w2 < W; ++w2) t += red[w2 * MMAX + m];   // same order in every thread
+                            for (int w2 = 0; w2 < WC; ++w2) t += red[w2 * MMAX + m];   // same order in every thread
                             rs[m] = 1.0f / sqrtf(t / (float)cols + sd->eps);
                         }
                     };
@@ -575,7 +625,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                         return make_float4(t.x / (1.0f + expf(-t.x)) * o.x, t.y / (1.0f + expf(-t.y)) * o.y,
                                            t.z / (1.0f + expf(-t.z)) * o.z, t.w / (1.0f + expf(-t.w)) * o.w);
                     };
-                    if (MMAX <= 2 && xop == GGQ_X_RMSNORM && n4 <= kThreads * kBatch) {
+                    if (MMAX <= 2 && xop == GGQ_X_RMSNORM && n4 <= kCThreads * kBatch) {
                         // one batch a thread: the squares come from the registers the
                         // values are placed from (one L2 round trip; up to 2 activation
                         // rows, where the registers allow it)
@@ -587,7 +637,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                         for (int m = 0; m < MMAX; ++m) ss[m] = 0.0f;
     #pragma unroll
                         for (int i = 0; i < kBatch; ++i) {
-                            const int qb = q0 + i * kThreads;
+                            const int qb = q0 + i * kCThreads;
                             const float e = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, v[i].w * v[i].w)));
     #pragma unroll
                             for (int m = 0; m < MMAX; ++m)
@@ -596,7 +646,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                         reduce_rs(ss);
     #pragma unroll
                         for (int i = 0; i < kBatch; ++i) {
-                            const int qb = q0 + i * kThreads;
+                            const int qb = q0 + i * kCThreads;
                             if (qb >= n4) break;
                             place(qb, transform(qb, v[i], o[i]));
                         }
@@ -609,7 +659,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                                 ss[m] = 0.0f;
                                 if (m < p.M) {
     #pragma unroll 4
-                                    for (int q = tid; q < c4; q += kThreads) {
+                                    for (int q = tid; q < c4; q += kCThreads) {
                                         const float4 v = __ldcg(x4 + (size_t)m * c4 + q);
                                         ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
                                     }
@@ -617,12 +667,12 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                             }
                             reduce_rs(ss);
                         }
-                        for (int q0 = warp * 32; q0 < n4; q0 += kThreads * kBatch) {
+                        for (int q0 = warp * 32; q0 < n4; q0 += kCThreads * kBatch) {
                             float4 v[kBatch], o[kBatch];
                             load2(q0, v, o);
     #pragma unroll
                             for (int i = 0; i < kBatch; ++i) {
-                                const int qb = q0 + i * kThreads;
+                                const int qb = q0 + i * kCThreads;
                                 if (qb >= n4) break;
                                 place(qb, transform(qb, v[i], o[i]));
                             }
@@ -630,8 +680,8 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                     }
                 }
             }
-            if (tid < 2 * W) cut_grp[tid] = -1;
-            __syncthreads();
+            if (tid < 2 * WC) cut_grp[tid] = -1;
+            csync();
 
             // ---- this warp's tiles
             constexpr int R = kRowsPerLane;
@@ -715,9 +765,9 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                         for (int i = 0; i < R; ++i)
     #pragma unroll
                             for (int m = 0; m < MMAX; ++m)
-                                cut_val[((k * W + warp) * kGroupRows + r + 8 * i) * MMAX + m] = acc[i][m];
+                                cut_val[((k * WC + warp) * kGroupRows + r + 8 * i) * MMAX + m] = acc[i][m];
                     }
-                    if (lane == 0) cut_grp[k * W + warp] = gi;
+                    if (lane == 0) cut_grp[k * WC + warp] = gi;
                 }
     #pragma unroll
                 for (int i = 0; i < R; ++i)
@@ -757,13 +807,12 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                         }
                     }
                 }
-                __syncwarp();   // every lane is done with the buffer
+                __syncwarp();   // every lane is done with the buffer: the producer may refill it
+                if (lane == 0) mbar_arrive(&empty[cslot]);
                 if (++cslot == D) {
                     cslot = 0;
                     cphase ^= 1u;
                 }
-                --inflight;
-                refill();
                 t += nv;
                 u += nv;
                 if (u == U) {
@@ -772,23 +821,23 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 }
             }
             if (cur >= 0) flush(cur);
-            __syncthreads();
+            csync();
 
             // ---- groups cut between warps: the warp where the group starts adds the
             // later warps' parts in order and stores it (lane r: row r)
-            if (cut_grp[W + warp] >= 0 && lane < kGroupRows) {
-                const int gi = cut_grp[W + warp];
+            if (cut_grp[WC + warp] >= 0 && lane < kGroupRows) {
+                const int gi = cut_grp[WC + warp];
                 float tsum[MMAX];
     #pragma unroll
-                for (int m = 0; m < MMAX; ++m) tsum[m] = cut_val[((W + warp) * kGroupRows + lane) * MMAX + m];
+                for (int m = 0; m < MMAX; ++m) tsum[m] = cut_val[((WC + warp) * kGroupRows + lane) * MMAX + m];
                 // the other parts: the later warps whose (non-empty) run starts
                 // inside this group, told from the run bounds alone so that every
                 // load is independent; added in warp order
                 const int g0 = gi * U, g1 = g0 + U;
     #pragma unroll
-                for (int w2 = 1; w2 < W; ++w2) {
+                for (int w2 = 1; w2 < WC; ++w2) {
                     int a2, b2;
-                    warp_run<W>(G, U, w2, a2, b2);
+                    warp_run<WC>(G, U, w2, a2, b2);
                     const bool part = w2 > warp && a2 < b2 && a2 > g0 && a2 < g1;
     #pragma unroll
                     for (int m = 0; m < MMAX; ++m) {
@@ -822,12 +871,12 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
             }
         }
 
-        // ---- stage s done in this CTA: publish it (the CTA barrier orders every
-        // warp's stores before thread 0's release); the last CTA of the chain
+        // ---- stage s done in this CTA: publish it (the consumer barrier orders
+        // every consumer warp's stores before thread 0's release); the last CTA of the chain
         // resets the counter for the next launch
         if (p.nstages > 1) {
-            if (warp == W - 1) cp_async_wait_all();
-            __syncthreads();
+            if (warp == WC - 1) cp_async_wait_all();
+            csync();
             if (tid == 0) {
                 if (s + 1 < p.nstages) {
                     red_release_add(p.counter, 1);
@@ -856,7 +905,8 @@ int num_sms() {
 
 int mmax_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : 4; }
 
-// Warps per CTA: 16, or 12 where four activation rows need the registers
+// Warps per CTA (one of them issues the copies): 16, or 12 where four
+// activation rows need the registers
 int warps_of(int mmax) { return mmax == 4 ? 12 : 16; }
 
 int kind_of(int type) {
@@ -902,12 +952,12 @@ int64_t max_over(int kmask, F f) {
 // Shared memory of a launch over stages of the kinds in `kinds`: ring slots
 // of the instance's size, x' and sums for the kinds present
 size_t rows_smem(int kinds, int mmax, int ring, int64_t cols_max) {
-    const int W = warps_of(mmax);
+    const int WC = warps_of(mmax) - 1;   // consumer warps (one more warp issues the copies)
     const int64_t U = cols_max / 256;
-    const size_t cut = (size_t)2 * W * kGroupRows * mmax * 4 + (size_t)2 * W * 4;
-    return (size_t)W * ring * max_over(mask_of(kinds), tile_bytes) + kInfoSlots * sizeof(StageInfo) +
+    const size_t cut = (size_t)2 * WC * kGroupRows * mmax * 4 + (size_t)2 * WC * 4;
+    return (size_t)WC * ring * max_over(mask_of(kinds), tile_bytes) + kInfoSlots * sizeof(StageInfo) +
            kPartMax * sizeof(int2) + (size_t)mmax * U * max_over(kinds, xsb_of) * 4 +
-           (size_t)mmax * U * max_over(kinds, sums_per_sb) * 4 + cut + (size_t)W * ring * 8;
+           (size_t)mmax * U * max_over(kinds, sums_per_sb) * 4 + cut + (size_t)2 * WC * ring * 8;
 }
 
 int rows_ring(int kinds, int mmax, int64_t cols_max) {

@@ -7,18 +7,21 @@
 // one.  A single GEMV is a chain of one stage.
 //
 // Work unit: one 256-column block of one row (SB) -- a Q4_K super-block
-// (144 B), a Q8_0 period of 8 blocks (272 B) or a Q4_0 period of 8 blocks
-// (144 B) -- split into four 64-column chunks.  Each matrix's rows form groups of 16 (the last may be shorter),
+// (144 B), a Q8_0 period of 8 blocks (272 B), a Q4_0 period of 8 blocks
+// (144 B) or a Q6_K super-block (210 B) -- split into four 64-column chunks.
+// A launch decodes one weight kind, or Q6_K and one other kind stage by stage.  Each matrix's rows form groups of 16 (the last may be shorter),
 // numbered across the stage's matrices.
 //
 //   * CTA b (one per SM) owns groups [GT*b/G, GT*(b+1)/G) of the stage's GT:
 //     whole rows, so no output is ever split between CTAs and no cross-CTA
 //     reduction exists.
-//   * Its (group, SB) tiles are cut into W equal contiguous runs, one per
-//     warp.  A warp streams its run through its own ring of 2-D bulk tensor
-//     copies (16 rows x up to NSB SBs);
-//     weights do not depend on earlier stages, so the ring runs ahead into the
-//     next stages while the chain waits at a stage boundary.
+//   * Its (group, SB) tiles are cut into W - 1 equal contiguous runs, one per
+//     consumer warp.  Each consumer has a ring of 2-D bulk tensor copies (16
+//     rows x up to NSB SBs); the CTA's last warp issues them all, lane w for
+//     consumer w (its copy cursor), the lanes stepping together and each
+//     refilling its consumer's slots as they are freed.  Weights do not depend
+//     on earlier stages, so the rings run ahead into the next stages while the
+//     chain waits at a stage boundary.
 //   * Lane (r, c) = (lane / 4, lane % 4) decodes chunk c of rows r and r + 8 of
 //     each SB in registers against x', the pre-scaled activations (each x' value
 //     loaded once for both rows).  The 8 lanes of one

@@ -427,7 +427,7 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
     p.M = M;
     p.status = device_status_word();
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
-    if (type == GGQ_Q4_0 && M >= kSmallMMin && smallm_supported(type, rows, cols, M))
+    if ((type == GGQ_Q4_0 || type == GGQ_Q6_K) && M >= kSmallMMin && smallm_supported(type, rows, cols, M))
         return launch_smallm(type, W, rows, cols, x, y, M, stream);   // one pass over W for all M rows
     if (type == GGQ_F32 || type == GGQ_Q4_0 || type == GGQ_Q6_K) {
         if ((type == GGQ_Q4_0 || type == GGQ_Q6_K) && stream_gemv_supported(type, cols, std::min(M, 4), 1, &rows)) {

@@ -65,8 +65,16 @@ constexpr int kRawMax = kTileRows * 272;                  // Q8_0: 8 blocks a ro
 constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kRawStages * kRawMax + 1024 + 256;
 
 // weight layouts: Q8_0 periods of 8 blocks (272 bytes), Q4_K super-blocks and
-// Q4_0 runs of 8 blocks (144 bytes), each 256 columns of a row
-enum SmKind { kSmQ8 = 0, kSmQ4K = 1, kSmQ40 = 2 };
+// Q4_0 runs of 8 blocks (144 bytes), Q6_K super-blocks (210 bytes: copied from
+// the 16-byte boundary below them, 240 bytes a row), each 256 columns of a row
+enum SmKind { kSmQ8 = 0, kSmQ4K = 1, kSmQ40 = 2, kSmQ6 = 3 };
+// TMA x coordinate (elements of the tensor map) of 256-column block sb
+template <int K>
+__device__ __forceinline__ int raw_x(int sb) {
+    if constexpr (K == kSmQ8) return sb * 136;            // 2-byte elements
+    if constexpr (K == kSmQ6) return (210 * sb) & ~15;    // bytes, 16-byte aligned
+    return sb * 144;                                      // bytes
+}
 constexpr int kMaxPieces = 8;
 
 struct SmallParams {
@@ -199,9 +207,8 @@ template <int K>
 __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_constant__ CUtensorMap wmap,
                                                              const SmallParams p) {
     constexpr bool Q4K = K == kSmQ4K;
-    constexpr int kRowBytes = K == kSmQ8 ? 272 : 144;   // raw bytes of one W row per 256 columns
+    constexpr int kRowBytes = K == kSmQ8 ? 272 : K == kSmQ6 ? 240 : 144;   // raw bytes of one W row per 256 columns
     constexpr int kRawBytes = kTileRows * kRowBytes;
-    constexpr int kBoxX = K == kSmQ8 ? 136 : 144;        // TMA x coordinate step (2- or 1-byte elements)
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsb_all = p.cols / 256;
@@ -249,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             {
                 const Piece p0 = piece_of(p, blockIdx.x, 0, nsb_all);
                 for (int sb = p0.sb0; sb < p0.sb1 && sb < p0.sb0 + kRawStages; ++sb)
-                    tma_prefetch_2d(&wmap, sb * kBoxX, p0.tile * kTileRows);
+                    tma_prefetch_2d(&wmap, raw_x<K>(sb), p0.tile * kTileRows);
             }
             pdl_wait();
             int gsb = 0;   // raw stages issued (all parts)
@@ -259,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
                     const int r = gsb % kRawStages;
                     mbar_wait(&empty_raw[r], ((gsb / kRawStages) & 1) ^ 1, p.status);
                     mbar_arrive_expect_tx(&full_raw[r], kRawBytes);
-                    tma_load_2d(sRaw + (size_t)r * kRawMax, &wmap, &full_raw[r], sb * kBoxX, pi.tile * kTileRows);
+                    tma_load_2d(sRaw + (size_t)r * kRawMax, &wmap, &full_raw[r], raw_x<K>(sb), pi.tile * kTileRows);
                 }
             }
         }
@@ -332,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             for (int lsb = 0; lsb < pi.sb1 - pi.sb0; ++lsb, ++gsb) {
                 const int r = gsb % kRawStages;
                 mbar_wait(&full_raw[r], (gsb / kRawStages) & 1, p.status);
-                const uint8_t* rp = sRaw + (size_t)r * kRawMax + (size_t)row * kRowBytes;
+                const uint8_t* rp = sRaw + (size_t)r * kRawMax + (size_t)row * kRowBytes +
+                                    (K == kSmQ6 ? ((210 * (pi.sb0 + lsb)) & 15) : 0);   // the super-block's start
                 uint4 hdr = make_uint4(0, 0, 0, 0);
                 if constexpr (Q4K) hdr = *reinterpret_cast<const uint4*>(rp);
 #pragma unroll
@@ -359,6 +367,45 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
                             const float2 f = make_float2(__uint_as_float(0x4B000000u | n0), __uint_as_float(0x4B000000u | n1));
                             const float2 qf = __fadd2_rn(f, make_float2(-8388608.0f, -8388608.0f));
                             w[i] = __ffma2_rn(qf, make_float2(a, a), make_float2(-bm, -bm));
+                        }
+                    } else if constexpr (K == kSmQ6) {
+                        // weights k = 64c + 16qt + i (i < 16): half h = c/2, quarter
+                        // g = 2(c%2) + qt/2, l = 16(qt%2) + i; low bits in ql[64h +
+                        // 32(g%2) + l] at bit 4(g/2), high bits in qh[32h + l] at bit
+                        // 2g; one scale, sc[4c + qt].  The super-block starts on 2 bytes
+                        // (rp even): words are read aligned and realigned.
+                        const int h = c >> 1, g = 2 * (c & 1) + (qt >> 1), l0 = 16 * (qt & 1);
+                        const int lo_off = 64 * h + 32 * (g & 1) + l0, hi_off = 128 + 32 * h + l0;
+                        const int sh = 8 * ((int)(reinterpret_cast<uintptr_t>(rp)) & 3);   // 0 or 16
+                        const uint32_t* wl = reinterpret_cast<const uint32_t*>(
+                            reinterpret_cast<uintptr_t>(rp + lo_off) & ~(uintptr_t)3);
+                        const uint32_t* wh = reinterpret_cast<const uint32_t*>(
+                            reinterpret_cast<uintptr_t>(rp + hi_off) & ~(uintptr_t)3);
+                        uint32_t a[5], b[5];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            a[i] = wl[i];
+                            b[i] = wh[i];
+                        }
+                        a[4] = sh ? wl[4] : 0u;
+                        b[4] = sh ? wh[4] : 0u;
+                        uint32_t u[4];   // the 16 six-bit codes q + 32, four a word
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t qlw = __funnelshift_r(a[i], a[i + 1], sh);
+                            const uint32_t qhw = __funnelshift_r(b[i], b[i + 1], sh);
+                            u[i] = ((qlw >> (4 * (g >> 1))) & 0x0F0F0F0Fu) | (((qhw >> (2 * g)) & 0x03030303u) << 4);
+                        }
+                        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rp + 208));
+                        const float dsc = d * (float)(int)reinterpret_cast<const int8_t*>(rp + 192)[4 * c + qt];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            // 0x4B0000 | u is the float 2^23 + u; minus 2^23 + 32: q exactly
+                            const uint32_t f0 = __byte_perm(u[i >> 1], 0x4B000000u, 0x7650u | (uint32_t)(2 * (i & 1)));
+                            const uint32_t f1 = __byte_perm(u[i >> 1], 0x4B000000u, 0x7650u | (uint32_t)(2 * (i & 1) + 1));
+                            const float2 qf = __fadd2_rn(make_float2(__uint_as_float(f0), __uint_as_float(f1)),
+                                                         make_float2(-8388640.0f, -8388640.0f));
+                            w[i] = __fmul2_rn(qf, make_float2(dsc, dsc));
                         }
                     } else {
                         // block 2c + qt/2 of the row's 256 columns: fp16 d at its start,
@@ -505,21 +552,25 @@ int launch_t(const CUtensorMap& wmap, const SmallParams& p, int grid, cudaStream
 }  // namespace
 
 bool smallm_supported(int type, int64_t rows, int64_t cols, int M) {
-    return (type == GGQ_Q8_0 || type == GGQ_Q4_K || type == GGQ_Q4_0) && M >= 1 && M <= kN && cols >= 256 &&
-           cols % 256 == 0 && cols <= (1 << 24) && rows >= 1 && rows <= 0x7fffffff;
+    // Q6_K rows (210 bytes per 256 columns) start on 16 bytes only when cols % 2048 == 0
+    if (type == GGQ_Q6_K && cols % 2048) return false;
+    return (type == GGQ_Q8_0 || type == GGQ_Q4_K || type == GGQ_Q4_0 || type == GGQ_Q6_K) && M >= 1 && M <= kN &&
+           cols >= 256 && cols % 256 == 0 && cols <= (1 << 24) && rows >= 1 && rows <= 0x7fffffff;
 }
 
 int launch_smallm(int type, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int M,
                   cudaStream_t stream) {
     auto enc = encoder();
     if (!enc) return fail(GGQ_ECUDA, "cuTensorMapEncodeTiled unavailable");
-    const int kind = type == GGQ_Q4_K ? kSmQ4K : type == GGQ_Q4_0 ? kSmQ40 : kSmQ8;
-    const bool bytes = kind != kSmQ8;   // 144-byte runs as bytes; Q8_0 periods as 2-byte elements
-    const int64_t row_bytes = cols / 256 * (bytes ? 144 : 272);
+    const int kind = type == GGQ_Q4_K ? kSmQ4K : type == GGQ_Q4_0 ? kSmQ40 : type == GGQ_Q6_K ? kSmQ6 : kSmQ8;
+    const bool bytes = kind != kSmQ8;   // 144- and 210-byte units as bytes; Q8_0 periods as 2-byte elements
+    const int64_t row_bytes = cols / 256 * (kind == kSmQ8 ? 272 : kind == kSmQ6 ? 210 : 144);
     CUtensorMap wmap;
     cuuint64_t dims[2] = {(cuuint64_t)(bytes ? row_bytes : row_bytes / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)(bytes ? 144 : 136), (cuuint32_t)kTileRows};
+    // Q6_K: 240 bytes from the 16-byte boundary below each super-block cover its
+    // 210 (a box past the row's end reads zeros)
+    cuuint32_t box[2] = {(cuuint32_t)(kind == kSmQ8 ? 136 : kind == kSmQ6 ? 240 : 144), (cuuint32_t)kTileRows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = enc(&wmap, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
                      const_cast<void*>(W), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -568,6 +619,7 @@ int launch_smallm(int type, const void* W, int64_t rows, int64_t cols, const flo
     }
     if (kind == kSmQ4K) return launch_t<kSmQ4K>(wmap, p, grid, stream);
     if (kind == kSmQ40) return launch_t<kSmQ40>(wmap, p, grid, stream);
+    if (kind == kSmQ6) return launch_t<kSmQ6>(wmap, p, grid, stream);
     return launch_t<kSmQ8>(wmap, p, grid, stream);
 }
 

@@ -1,8 +1,8 @@
 """GPU parity for Q6_K weights: decode and row gather bit-exact, GEMV within
 the tolerance, one-hot and integer-valued cases exact, against the CPU oracle.
-GEMVs with cols % 2048 == 0 run on the streaming kernel (M 1..4 a launch, M
-5..16 in groups of 4), the others on the warp-per-row kernel; both are covered,
-and so are Q6_K chains of dependent stages.
+GEMVs with cols % 2048 == 0 run on the streaming kernel at M 1..4 and on the
+tensor-core small-M kernel at M 5..16, the others on the warp-per-row kernel;
+all are covered, and so are Q6_K chains of dependent stages.
 
 Bar as for the other types: |y - y_ref| <= 1e-3 * sum_c |w[r,c] x[c]| + 1e-6
 (y_ref in double).

@@ -255,10 +255,15 @@ __global__ void __launch_bounds__(Dec<Q4K, TH>::kThreads, 1) prefill_kernel(cons
     uint8_t* sA = sB + (size_t)kStages * kBBytes;            // kStages x (8 or 16 KB)
     uint8_t* sRaw = sA + (size_t)kStages * kABytes;          // kRawStages x 18 KB
     uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + (size_t)kRawStages * kRawSlot);
-    uint64_t* full_b = bars;                     // [kStages]
-    uint64_t* full_a = bars + kStages;           // [kStages]
-    uint64_t* empty = bars + 2 * kStages;        // [kStages]
-    uint64_t* full_raw = bars + 3 * kStages;     // [kRawStages]
+    // B (X) stages are filled and freed per token half: the MMAs of half 0 of a
+    // stage are issued and committed before those of half 1, so its half-0
+    // buffer is refilled half a stage earlier (the next X load has that much
+    // more time to arrive)
+    uint64_t* full_b = bars;                     // [kStages][TH]
+    uint64_t* empty_b = bars + kStages * TH;     // [kStages][TH]
+    uint64_t* full_a = bars + 2 * kStages * TH;  // [kStages]
+    uint64_t* empty = full_a + kStages;          // [kStages]: the A (decoded W) slot
+    uint64_t* full_raw = empty + kStages;        // [kRawStages]
     uint64_t* empty_raw = full_raw + kRawStages; // [kRawStages]
     uint64_t* acc_full = empty_raw + kRawStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -267,7 +272,10 @@ __global__ void __launch_bounds__(Dec<Q4K, TH>::kThreads, 1) prefill_kernel(cons
         prefetch_tensormap(&wmap);
         prefetch_tensormap(&xmap);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full_b[s], 1);
+            for (int h = 0; h < TH; ++h) {
+                mbar_init(&full_b[s * TH + h], 1);
+                mbar_init(&empty_b[s * TH + h], 1);
+            }
             mbar_init(&full_a[s], kDecoders);
             mbar_init(&empty[s], 1);
         }
@@ -298,12 +306,13 @@ __global__ void __launch_bounds__(Dec<Q4K, TH>::kThreads, 1) prefill_kernel(cons
                                 row0);
                 }
                 const int s = ks % kStages;
-                mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, p.status);
-                mbar_arrive_expect_tx(&full_b[s], kBBytes);
 #pragma unroll
-                for (int h = 0; h < TH; ++h)   // tokens beyond M read as zeros
-                    tma_load_2d(sB + (size_t)s * kBBytes + (size_t)h * kHalfBBytes, &xmap, &full_b[s],
+                for (int h = 0; h < TH; ++h) {   // tokens beyond M read as zeros
+                    mbar_wait(&empty_b[s * TH + h], ((ks / kStages) & 1) ^ 1, p.status);
+                    mbar_arrive_expect_tx(&full_b[s * TH + h], kHalfBBytes);
+                    tma_load_2d(sB + (size_t)s * kBBytes + (size_t)h * kHalfBBytes, &xmap, &full_b[s * TH + h],
                                 (ks0 + ks) * kKS, tok0 + h * kTileTok);
+                }
             }
         }
         __syncwarp();
@@ -312,19 +321,18 @@ __global__ void __launch_bounds__(Dec<Q4K, TH>::kThreads, 1) prefill_kernel(cons
             for (int ks = 0; ks < nks; ++ks) {
                 const int s = ks % kStages;
                 const uint32_t ph = (ks / kStages) & 1;
-                mbar_wait(&full_b[s], ph, p.status);
                 mbar_wait(&full_a[s], ph, p.status);
-                tc_fence_after();
                 const uint32_t a_addr = smem_u32(sA + (size_t)s * kABytes);
                 const uint32_t b_addr = smem_u32(sB + (size_t)s * kBBytes);
 #pragma unroll
-                for (int kk = 0; kk < kKS / 16; ++kk) {
-                    // 16 bf16 = 32 bytes further along the swizzled rows; one MMA
-                    // per token half, accumulator columns 256 h ..
+                for (int h = 0; h < TH; ++h) {   // token half h: accumulator columns 256 h ..
+                    mbar_wait(&full_b[s * TH + h], ph, p.status);
+                    tc_fence_after();
 #pragma unroll
-                    for (int h = 0; h < TH; ++h)
+                    for (int kk = 0; kk < kKS / 16; ++kk)   // 16 bf16 = 32 bytes further along the swizzled rows
                         umma_bf16(tmem + (uint32_t)(h * kTileTok), desc(a_addr + 32 * kk),
                                   desc(b_addr + (uint32_t)(h * kHalfBBytes) + 32 * kk), kIdesc, (ks | kk) != 0);
+                    umma_commit(&empty_b[s * TH + h]);
                 }
                 umma_commit(&empty[s]);
             }

@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             // a descriptor's address field is (address >> 4): descriptors of the
             // other parts and offsets are the stage-0 one plus (offset >> 4)
             const uint64_t d0 = sw128_desc(smem_u32(sStage));
-            constexpr uint32_t kLo = kAPiece >> 4, kBhi = (2 * kAPiece) >> 4, kBlo = (2 * kAPiece + kBPiece) >> 4;
+            constexpr uint32_t kLo = kAPiece >> 4, kBhi = (2 * kAPiece) >> 4;   // X_lo follows X_hi: one N = 32 operand
             // one loop over the stages of all parts (this thread's issue rate
             // sets the pace, so the loop is kept as plain as for one part);
             // at a part's end: its accumulator to the epilogue, and the next

@@ -115,22 +115,23 @@ def test_chain_repeat_is_bit_identical(env):
     net.check(x0, a)
 
 
+@pytest.mark.parametrize("qtype", [12, 8, 2, 14])
 @pytest.mark.parametrize("rows", [3000, 151 * 16, 152 * 16, 152 * 16 + 5, 40000])
-def test_chain_single_stage_matches_oracle_and_gemv(env, rows):
-    """A one-stage chain against the oracle and against ggq_gemv.  Row counts
-    below, at and above one 16-row group per SM: chains split a stage of at
-    least that many groups into equal tile ranges, cutting groups between
-    neighbouring CTAs (whose parts are then added), ggq_gemv keeps whole
-    groups; both within the bound, and repeated chain runs bit-identical."""
+def test_chain_single_stage_matches_oracle_and_gemv(env, qtype, rows):
+    """A one-stage chain against the oracle and against ggq_gemv, for each
+    streamed weight type.  Row counts below, at and above one 16-row group per
+    SM, and ragged: each CTA takes whole 16-row groups, whose tiles its
+    consumer warps share in equal runs (a group cut between warps is added in
+    warp order); both within the bound, and repeated chain runs bit-identical."""
     torch, ggq = env
     cols = 4096
-    W = synth.weight_rows(12, 60, rows, cols)
+    W = synth.weight_rows(qtype, 60, rows, cols)
     x = synth.normal_f32(cols, 61).reshape(1, cols)
-    y_ref, a_ref = oracle.gemv(12, W, rows, cols, x)
+    y_ref, a_ref = oracle.gemv(qtype, W, rows, cols, x)
     Wd, xd = _dev(torch, W), _dev(torch, x)
-    y1 = ggq.gemv(12, Wd, rows, cols, xd)
+    y1 = ggq.gemv(qtype, Wd, rows, cols, xd)
     y2 = torch.full_like(y1, float("nan"))
-    ch = ggq.Chain(12, 1, [([Wd], [rows], cols, xd, [y2])])
+    ch = ggq.Chain(qtype, 1, [([Wd], [rows], cols, xd, [y2])])
     outs = []
     for _ in range(3):
         y2.fill_(float("nan"))

@@ -53,3 +53,45 @@ def test_q4km_file_pass(env, tmp_path):
                 ok, worst = oracle.tolerance_ok(y.cpu().numpy().reshape(1, -1), y_ref, a_ref)
                 assert ok, f"{t['name']}: worst error / bound {worst:.3g}"
         dp.close()
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_decode_pass_splits_at_stages_the_chain_kernel_does_not_take(env, M):
+    """A plan whose stages alternate between what the chain kernel streams and
+    what it does not (Q6_K at 2304 columns, F32): chains for the runs, one
+    ggq_gemv / ggq_gemv_multi launch for each other stage, every output
+    against the oracle."""
+    torch, ggq = env
+    from gguf_block_quantized_q8_gb300 import plan as P
+    spec = [(ggq.Q4_K, [(512, 2048)]), (ggq.Q6_K, [(384, 2304)]), (ggq.Q4_K, [(256, 1024), (128, 1024)]),
+            (ggq.F32, [(100, 515)]), (ggq.Q6_K, [(64, 2048)]), (ggq.Q4_K, [(96, 2048)])]
+    keep, stages, xs, ys, host = [], [], [], [], []
+    for si, (qtype, mats) in enumerate(spec):
+        infos, ylist, hw = [], [], []
+        for mi, (rows, cols) in enumerate(mats):
+            W = synth.weight_rows(qtype, 700 + 10 * si + mi, rows, cols)
+            Wd = torch.from_numpy(W).cuda()
+            keep.append(Wd)
+            infos.append({"name": f"s{si}.{mi}", "type": qtype, "ne": [cols, rows], "nbytes": W.nbytes,
+                          "data": Wd.data_ptr()})
+            ylist.append(torch.full((M, rows), float("nan"), device="cuda"))
+            hw.append(W)
+        cols = mats[0][1]
+        x = synth.normal_f32(M * cols, 800 + si).reshape(M, cols)
+        xs.append(torch.from_numpy(x).cuda())
+        ys.append(ylist)
+        stages.append((qtype, infos))
+        host.append((qtype, mats, hw, x))
+    dp = P.DecodePass(stages, xs, ys, M=M)
+    assert P.segments([q for q, _ in stages], [t[0]["ne"][0] for _, t in stages]) == [
+        (0, 1, True), (1, 2, False), (2, 3, True), (3, 4, False), (4, 6, True)]
+    assert len(dp.chains) == 3 and dp.launches == 5
+    dp.run()
+    torch.cuda.synchronize()
+    assert ggq.device_status() == 0
+    for (qtype, mats, hw, x), ylist in zip(host, ys):
+        for (rows, cols), W, y in zip(mats, hw, ylist):
+            y_ref, a_ref = oracle.gemv(qtype, W, rows, cols, x)
+            ok, worst = oracle.tolerance_ok(y.cpu().numpy(), y_ref, a_ref)
+            assert ok, f"type {qtype} {rows}x{cols}: worst error / bound {worst:.3g}"
+    dp.close()

@@ -429,22 +429,26 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
     if (!p.status) return fail(GGQ_ECUDA, "device status word unavailable");
     if ((type == GGQ_Q4_0 || type == GGQ_Q6_K) && M >= kSmallMMin && smallm_supported(type, rows, cols, M))
         return launch_smallm(type, W, rows, cols, x, y, M, stream);   // one pass over W for all M rows
-    if (type == GGQ_F32 || type == GGQ_Q4_0 || type == GGQ_Q6_K) {
-        if ((type == GGQ_Q4_0 || type == GGQ_Q6_K) && stream_gemv_supported(type, cols, std::min(M, 4), 1, &rows)) {
-            // the streaming kernel takes up to 4 activation rows; M 5..16 (Q6_K, or
-            // a Q4_0 shape the small-M kernel does not take) runs it once per
-            // group of up to 4 (x and y rows are contiguous)
-            for (int m0 = 0; m0 < M; m0 += 4) {
+    if (M <= 4 || type == GGQ_Q4_0 || type == GGQ_Q6_K) {
+        // the streaming kernel holds x' for up to 4 activation rows in shared
+        // memory; where all M rows do not fit (4 rows of 14336 columns) or M > 4
+        // (Q6_K, or a Q4_0 shape the small-M kernel does not take), it runs once
+        // per group of g rows, the most that fit (x and y rows are contiguous)
+        int g = std::min(M, 4);
+        while (g > 0 && !stream_gemv_supported(type, cols, g, 1, &rows)) --g;
+        if (g > 0) {
+            for (int m0 = 0; m0 < M; m0 += g) {
                 const void* Ws[1] = {W};
                 float* ys[1] = {y + (int64_t)m0 * rows};
                 const int rc = launch_gemv_stream(type, 1, Ws, &rows, cols, x + (int64_t)m0 * cols, ys,
-                                                  std::min(4, M - m0), stream);
+                                                  std::min(g, M - m0), stream);
                 if (rc) return rc;
             }
             return GGQ_OK;
         }
-        return launch_gemv_rows(type, W, rows, cols, x, y, M, stream);
     }
+    if (type == GGQ_F32 || type == GGQ_Q4_0 || type == GGQ_Q6_K)
+        return launch_gemv_rows(type, W, rows, cols, x, y, M, stream);
     if (type == GGQ_Q8_0 && cols % 256 != 0) {
         const int64_t grid = (rows + kWarps - 1) / kWarps;
         cudaLaunchConfig_t cfg = {};
@@ -461,11 +465,6 @@ int launch_gemv(int type, const void* W, int64_t rows, int64_t cols, const float
     }
     if (M >= kSmallMMin && smallm_supported(type, rows, cols, M))
         return launch_smallm(type, W, rows, cols, x, y, M, stream);
-    if (stream_gemv_supported(type, cols, M, 1, &rows)) {
-        const void* Ws[1] = {W};
-        float* ys[1] = {y};
-        return launch_gemv_stream(type, 1, Ws, &rows, cols, x, ys, M, stream);
-    }
     if (M <= 1) return launch_tma_gemv<1>(type, W, rows, cols, p, stream);
     if (M <= 2) return launch_tma_gemv<2>(type, W, rows, cols, p, stream);
     if (M <= 4) return launch_tma_gemv<4>(type, W, rows, cols, p, stream);

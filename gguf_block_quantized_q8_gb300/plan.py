@@ -104,7 +104,9 @@ class DecodePass:
     by stage i; ys[i]: one CUDA fp32 tensor [M, rows] per matrix of stage i.
     Stage s+1 reads its x only after every output of stage s is written (the
     chain's stage boundaries, or stream order between launches), so an x may be
-    an earlier stage's y.  M is 1..4 (the chain kernel's range).
+    an earlier stage's y.  M is 1..4 (the chain kernel's range); at M > 2 the
+    widest stages of a large model (the 14336-column down projection) leave the
+    chain and run as ggq_gemv calls of their own.
     """
 
     def __init__(self, stages, xs, ys, M: int = 1):
@@ -126,17 +128,53 @@ class DecodePass:
         try:
             for i, j, is_chain in segments([s["qtype"] for s in self.stages], [s["cols"] for s in self.stages]):
                 if is_chain:
-                    raw = [(s["W"], s["rows"], s["cols"], s["x"].data_ptr(), [y.data_ptr() for y in s["ys"]])
-                           for s in self.stages[i:j]]
-                    rc, h = _ggq.ggq_chain_create_typed(M, [s["qtype"] for s in self.stages[i:j]], raw)
-                    _ggq.check(rc, "ggq_chain_create")
-                    self.chains.append(h)
-                    self.calls.append(("chain", h))
+                    self._chain_run(self.stages[i:j])
                 else:
                     self.calls.append(("stage", self.stages[i]))
         except Exception:
             self.close()
             raise
+
+    def _create(self, run):
+        raw = [(s["W"], s["rows"], s["cols"], s["x"].data_ptr(), [y.data_ptr() for y in s["ys"]]) for s in run]
+        return _ggq.ggq_chain_create_typed(self.M, [s["qtype"] for s in run], raw)
+
+    def _chain_run(self, run):
+        """Calls for a run of chainable stages: one chain, unless a stage is too
+        wide for the chain kernel at M rows (the pre-scaled x of all M rows must
+        fit in shared memory: 4 rows of 14336 columns do not).  Such a stage is
+        a ggq_gemv of its own, which runs the rows in groups that fit; the
+        stages between them form chains."""
+        rc, h = self._create(run)
+        if rc == 0:
+            self.chains.append(h)
+            self.calls.append(("chain", h))
+            return
+        if len(run) == 1:
+            if rc != _ggq.EINVAL:
+                _ggq.check(rc, "ggq_chain_create")
+            self.calls.append(("stage", run[0]))
+            return
+        fits = []
+        for s in run:
+            rc1, h1 = self._create([s])
+            if rc1 == 0:
+                _ggq.ggq_chain_free(h1)
+            elif rc1 != _ggq.EINVAL:
+                _ggq.check(rc1, "ggq_chain_create")
+            fits.append(rc1 == 0)
+        if all(fits):   # every stage fits alone, the run does not: not a width limit
+            _ggq.check(rc, "ggq_chain_create")
+        i = 0
+        while i < len(run):
+            j = i + 1
+            while j < len(run) and fits[j] == fits[i]:
+                j += 1
+            if fits[i]:
+                self._chain_run(run[i:j])
+            else:
+                self.calls += [("stage", s) for s in run[i:j]]
+            i = j
 
     @property
     def launches(self) -> int:

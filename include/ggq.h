@@ -160,7 +160,9 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  *          must not overlap W or x (with 5..16 rows it may be zeroed first)
  *   M      1..16 (M > 1 is the small-batch variant: each decoded block is used
  *          for all M rows of x; from 5 rows on, Q8_0, Q4_K and Q4_0 run on the
- *          tensor cores in one pass over W)
+ *          tensor cores in one pass over W; up to 4 rows, where the pre-scaled
+ *          x of all M rows does not fit in shared memory, e.g. 4 rows of 14336
+ *          columns, the rows run in groups, one pass over W per group)
  *   stream cudaStream_t
  *
  * Finite inputs with |x| < 2^70 are supported.  Errors: GGQ_EINVAL (NULL
@@ -225,7 +227,9 @@ typedef struct ggq_chain ggq_chain;
  * ggq_chain_create -- validate `nstages` stages (1..65536) of type GGQ_Q8_0,
  * GGQ_Q4_K, GGQ_Q4_0 or GGQ_Q6_K for M activation rows (1..4; Q4_K and Q4_0
  * stages need cols >= 768, Q6_K stages cols % 2048 == 0, so that every row of
- * 210-byte super-blocks starts on 16 bytes), encode their copy descriptors and
+ * 210-byte super-blocks starts on 16 bytes; the pre-scaled x of all M rows of
+ * the widest stage must fit in shared memory: 2 rows of 14336 columns do, 4 do
+ * not), encode their copy descriptors and
  * store them in device memory on the current device.  The pointers are bound
  * at creation: the chain reads and writes the same buffers on every run.  The
  * caller owns the returned chain and frees it with ggq_chain_free.  Errors:

@@ -95,3 +95,42 @@ def test_decode_pass_splits_at_stages_the_chain_kernel_does_not_take(env, M):
             ok, worst = oracle.tolerance_ok(y.cpu().numpy(), y_ref, a_ref)
             assert ok, f"type {qtype} {rows}x{cols}: worst error / bound {worst:.3g}"
     dp.close()
+
+
+def test_decode_pass_takes_stages_too_wide_for_the_chain_out_of_it(env):
+    """At M = 4 the pre-scaled x of a 14336-column stage does not fit in shared
+    memory: that stage (and a Q6_K one of the same width) runs as ggq_gemv
+    between two chains; at M = 2 the same plan is one chain."""
+    torch, ggq = env
+    from gguf_block_quantized_q8_gb300 import plan as P
+    spec = [(ggq.Q4_K, [(128, 4096), (64, 4096)]), (ggq.Q4_K, [(72, 14336)]), (ggq.Q6_K, [(40, 14336)]),
+            (ggq.Q4_K, [(96, 4096)]), (ggq.Q6_K, [(48, 4096)])]
+    for M, n_chains, n_launches in ((4, 2, 4), (2, 1, 1)):
+        keep, stages, xs, ys, host = [], [], [], [], []
+        for si, (qtype, mats) in enumerate(spec):
+            infos, ylist, hw = [], [], []
+            for mi, (rows, cols) in enumerate(mats):
+                W = synth.weight_rows(qtype, 900 + 10 * si + mi, rows, cols)
+                Wd = torch.from_numpy(W).cuda()
+                keep.append(Wd)
+                infos.append({"name": f"s{si}.{mi}", "type": qtype, "ne": [cols, rows], "nbytes": W.nbytes,
+                              "data": Wd.data_ptr()})
+                ylist.append(torch.full((M, rows), float("nan"), device="cuda"))
+                hw.append(W)
+            cols = mats[0][1]
+            x = synth.normal_f32(M * cols, 950 + si).reshape(M, cols)
+            xs.append(torch.from_numpy(x).cuda())
+            ys.append(ylist)
+            stages.append((qtype, infos))
+            host.append((qtype, mats, hw, x))
+        dp = P.DecodePass(stages, xs, ys, M=M)
+        assert (len(dp.chains), dp.launches) == (n_chains, n_launches), M
+        dp.run()
+        torch.cuda.synchronize()
+        assert ggq.device_status() == 0
+        for (qtype, mats, hw, x), ylist in zip(host, ys):
+            for (rows, cols), W, y in zip(mats, hw, ylist):
+                y_ref, a_ref = oracle.gemv(qtype, W, rows, cols, x)
+                ok, worst = oracle.tolerance_ok(y.cpu().numpy(), y_ref, a_ref)
+                assert ok, f"M={M} type {qtype} {rows}x{cols}: worst error / bound {worst:.3g}"
+        dp.close()

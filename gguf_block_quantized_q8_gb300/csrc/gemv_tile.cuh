@@ -19,10 +19,11 @@ namespace ggq {
 constexpr float kTwo96 = pow2f(96);
 
 // Pre-scale factor of the weight at position k of a Q4_K super-block (natural
-// order): low nibbles sit at bits 0/8/16 (byte 3 shifted down to 16), high
-// nibbles 4 higher.
+// order): low nibbles sit at bits 0/8/16 for bytes 0-2; byte 3 of an even word
+// w = (k/4) % 8 is moved to bits 0-7 and that of the odd word w + 1 to bits
+// 16-23 (one byte_perm for the pair); high nibbles 4 bits higher.
 __device__ __forceinline__ float q4k_xscale(int k) {
-    const int hi = (k >> 5) & 1, b = k & 3;
+    const int hi = (k >> 5) & 1, b = (k & 3) == 3 ? (((k >> 2) & 1) ? 2 : 0) : (k & 3);
     return hi ? (b == 0 ? pow2f(49) : b == 1 ? pow2f(41) : pow2f(33))
               : (b == 0 ? pow2f(53) : b == 1 ? pow2f(45) : pow2f(37));
 }
@@ -160,7 +161,7 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
         for (int m = 0; m < MMAX; ++m) t[r][m][0] = t[r][m][1] = f2_zero();
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-        // nibble masks at byte position b (byte 3 is shifted down to byte 2)
+        // nibble masks at byte position b < 3 (byte 3: see below)
         const uint32_t ml = b == 0 ? 0x0000000Fu : b == 1 ? 0x00000F00u : 0x000F0000u;
         const uint32_t mh = ml << 4;
         // x' of byte position b: (w lo, w hi, w+1 lo, w+1 hi) for w = 0, 2, 4, 6
@@ -174,8 +175,10 @@ __device__ __forceinline__ void q4k_chunk_rows(const uint8_t* rp, int rstride, i
         for (int r = 0; r < R; ++r) {
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
-                const uint32_t v = b < 3 ? wd[r][w] : (wd[r][w] >> 8);
-                const uint64_t pr = and_pair(v, ml, mh);
+                // byte 3 of words w, w + 1 (w even) in one register: bits 0-7, 16-23
+                const uint32_t v = b < 3 ? wd[r][w] : __byte_perm(wd[r][w & ~1], wd[r][w | 1], 0x7733u);
+                const uint64_t pr = b < 3 ? and_pair(v, ml, mh)
+                                          : ((w & 1) ? and_pair(v, 0x000F0000u, 0x00F00000u) : and_pair(v, 0x0Fu, 0xF0u));
 #pragma unroll
                 for (int m = 0; m < MMAX; ++m) {
                     const float4 x4 = xv[m][w >> 1];

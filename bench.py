@@ -669,6 +669,27 @@ def extras(torch, ggq, synth, stream):
                                          [ys[i].data_ptr() for i in grp], 1, sp), "gemv")
     t, n = kernel_time(torch, f2, stream, len(Ws), min_launches=MIN_LAUNCHES // 4)
     out["cfg2_smollm3_layer_q4_k"] = timing(t, 4 * n, len(Ws), nb, launches_per_layer=4)
+    # the same 4 stages as one chain launch (one chain per weight copy: a chain
+    # binds its pointers at creation)
+    chains = []
+    try:
+        for Wc in Ws:
+            rc, h = ggq.ggq_chain_create(12, 1, [([Wc[i].data_ptr() for i in grp], [gs[i].rows for i in grp],
+                                                  gs[grp[0]].cols, xs[gs[grp[0]].cols].data_ptr(),
+                                                  [ys[i].data_ptr() for i in grp]) for grp in groups])
+            ggq.check(rc, "ggq_chain_create")
+            chains.append(h)
+        k = [0]
+
+        def f2c():
+            h = chains[k[0] % len(chains)]
+            k[0] += 1
+            ggq.check(ggq.ggq_chain_run(h, sp), "ggq_chain_run")
+        t, n = kernel_time(torch, f2c, stream, len(chains))
+        out["cfg2_smollm3_layer_q4_k_one_chain"] = timing(t, n, len(Ws), nb, launches_per_layer=1)
+    finally:
+        for h in chains:
+            ggq.ggq_chain_free(h)
     del Ws
 
     # cfg4: Q8_0 14336x4096, M in 1..16

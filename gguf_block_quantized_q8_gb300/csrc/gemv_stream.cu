@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(32 * W, 1) rows_kernel(const __grid_constant__
                 } else if (KS == kKQ6) {
                     // chunk (h, gp) with gp = (l/8) % 2, pair slot l/16, word l % 8
                     xoff = ((lane >> 3) & 1) * 68 + 2 * (lane & 7) + (lane >> 4);
-                    xsc = make_float4(pow2f(53), pow2f(45), pow2f(37), pow2f(37));
+                    xsc = make_float4(pow2f(53), pow2f(45), pow2f(37), (lane >> 4) ? pow2f(37) : pow2f(53));
                 } else if (KS == kKQ40) {
                     const int b4 = lane >> 3;
                     xoff = (b4 >> 1) * 72 + 2 * (18 * (b4 & 1) + 2 + 4 * (lane & 3)) + ((lane >> 2) & 1);

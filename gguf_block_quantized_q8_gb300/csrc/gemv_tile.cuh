@@ -275,12 +275,14 @@ __device__ __forceinline__ void q8_tile_row(const uint8_t* rp, const float* xu, 
 }
 
 // Pre-scale factor of the x' value at slot e = 2B + hi of a Q4_0 chunk (B: the
-// byte position in the chunk, hi: 1 for the high nibble).  Chunks start on
-// 4-byte boundaries, so B mod 4 is the byte's position in its word; byte 3 is
-// shifted down to 2 before masking.
+// byte position in the chunk, mod 36; hi: 1 for the high nibble).  Chunks start
+// on 4-byte boundaries, so B mod 4 is the byte's position in its word.  Byte 3
+// of the code words is gathered pairwise, words (0, 1), (2, 3), (5, 6), (7, 8),
+// by one byte_perm: the first word's at bits 0-7, the second's at 16-23.
 __device__ __forceinline__ float q40_xscale(int e) {
-    const int pos = (e >> 1) & 3, hi = e & 1;
-    const int p = 8 * (pos < 2 ? pos : 2) + 4 * hi;   // bit position of the nibble
+    const int B = (e >> 1) % 36, pos = B & 3, hi = e & 1, wi = B >> 2;
+    const bool first = wi == 0 || wi == 2 || wi == 5 || wi == 7;
+    const int p = (pos < 3 ? 8 * pos : first ? 0 : 16) + 4 * hi;   // bit position of the nibble
     return p == 0 ? pow2f(53) : p == 4 ? pow2f(49) : p == 8 ? pow2f(45) : p == 12 ? pow2f(41)
                               : p == 16 ? pow2f(37) : pow2f(33);
 }
@@ -330,10 +332,15 @@ __device__ __forceinline__ void q40_chunk_rows(const uint8_t* rp, int rstride, c
             for (int k = 0; k < 2; ++k) {
                 const int pos = 2 * q + k;
                 if (pos < p0 || pos >= p1) continue;
-                const uint32_t ml = pos == 0 ? 0x0000000Fu : pos == 1 ? 0x00000F00u : 0x000F0000u;
+                // byte 3: words (0, 1), (2, 3), (5, 6), (7, 8) in one register each
+                const bool first = wi == 0 || wi == 2 || wi == 5 || wi == 7;
+                const uint32_t ml = pos == 0 ? 0x0000000Fu : pos == 1 ? 0x00000F00u
+                                  : (pos == 2 || !first) ? 0x000F0000u : 0x0000000Fu;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const uint32_t v = pos < 3 ? wd[r][wi] : (wd[r][wi] >> 8);
+                    const uint32_t v = pos < 3 ? wd[r][wi]
+                                     : first ? __byte_perm(wd[r][wi], wd[r][wi < 8 ? wi + 1 : wi], 0x7733u)
+                                             : __byte_perm(wd[r][wi > 0 ? wi - 1 : wi], wd[r][wi], 0x7733u);
                     const uint64_t pr = and_pair(v, ml, ml << 4);
 #pragma unroll
                     for (int m = 0; m < MMAX; ++m) {
@@ -373,7 +380,8 @@ __device__ __forceinline__ void q40_chunk_rows(const uint8_t* rp, int rstride, c
 // one (w, b) is one packed FMA.  A code word takes the low 4 bits of each byte
 // from the ql word and bits 4-7 from the shifted qh word in one select; bits 6
 // and 7 then hold other fields' bits, which the per-byte 6-bit mask drops.
-// x' of chunk c: [b][w][pair] at xu + 16b + 2w, activation row m at xu + m*xs.
+// x' of chunk c: [b][w][pair] at xu + 16b + 2w, activation row m at xu + m*xs;
+// byte 3's pair is masked at bits 0-7 (low word) and 16-23 (high word).
 // 32 * sum(x) of the four 16-column groups of the chunk ((g, l < 16) for g =
 // gp, gp + 2, then l >= 16) at su + m*ss.  acc[r][m] += the chunk's 64 products.
 template <int MMAX, int R, bool ALIGNED>
@@ -443,9 +451,9 @@ __device__ __forceinline__ void q6k_chunk_rows_t(const uint8_t* rp, int r0, int 
             for (int r = 0; r < R; ++r) {
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    const uint32_t vl = b < 3 ? lo[r][w] : (lo[r][w] >> 8);
-                    const uint32_t vh = b < 3 ? hi[r][w] : (hi[r][w] >> 8);
-                    const uint64_t pr = and_two(vl, vh, mk);
+                    // byte 3: the low word's at bits 0-7, the high word's at 16-23 (one byte_perm)
+                    const uint64_t pr = b < 3 ? and_two(lo[r][w], hi[r][w], mk)
+                                              : and_pair(__byte_perm(lo[r][w], hi[r][w], 0x7733u), 0x3Fu, 0x3F0000u);
 #pragma unroll
                     for (int m = 0; m < MMAX; ++m) {
                         const float4 x4 = xv[m][w >> 1];

@@ -143,11 +143,13 @@ def test_gemv_tensor_core_small_batch(env, qtype, rows, cols, M):
     assert_close(y, y_ref, a_ref, f"type {qtype} {rows}x{cols} M={M}")
 
 
-# 3 or 4 activation rows whose pre-scaled x does not fit in shared memory at
+# 2-4 activation rows whose pre-scaled x does not fit in shared memory at
 # once (4 x 14336 fp32 = 229 KB): the streaming kernel runs on groups of rows
-# (2 + 1, 2 + 2), y rows of each group at their own offset.
+# (2 + 1, 2 + 2; one row at a time at 32768 columns), y rows of each group at
+# their own offset.
 @pytest.mark.parametrize("qtype,rows,cols,M", [(12, 97, 14336, 3), (12, 70, 14336, 4), (8, 33, 14336, 4),
-                                             (8, 40, 16384, 3), (14, 65, 14336, 4), (2, 50, 14336, 3)])
+                                             (8, 40, 16384, 3), (14, 65, 14336, 4), (2, 50, 14336, 3),
+                                             (12, 40, 32768, 3), (8, 24, 32768, 2)])
 def test_gemv_wide_rows_in_groups(env, qtype, rows, cols, M):
     W = weights(qtype, rows, cols, stream=31)
     x = xs(M, cols, stream=32)

@@ -173,7 +173,7 @@ class ClockSampler:
             self.proc.kill()
         if self.t:
             self.t.join(timeout=2)
-        sm, mx, reasons = [], None, set()
+        sm, mx, pw, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -184,10 +184,15 @@ class ClockSampler:
                 mx = float(f[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3].split()[0]))
+            except (ValueError, IndexError):
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "power_w": statistics.median(pw) if pw else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -281,6 +286,12 @@ class DecodePass:
     def run_launches(self, stream_ptr):
         for st in self.stages:
             self.launch_stage(st, stream_ptr)
+
+    def run_per_tensor(self, stream_ptr):
+        """Every weight matrix as its own ggq_gemv (225 launches for 32 layers)."""
+        for st in self.stages:
+            for W, rows, y in zip(st["W"], st["rows"], st["y"]):
+                self.ggq.check(self.ggq.ggq_gemv(st["qtype"], W, rows, st["cols"], st["x"], y, 1, stream_ptr), "gemv")
 
     @property
     def launches(self):
@@ -958,6 +969,10 @@ def main():
     g_l = capture(torch, lambda: dp.run_launches(sp), stream)
     ms_launches = time_graph(torch, g_l, stream, r_steps)
     del g_l
+    # and as one launch per weight matrix (225 launches)
+    g_t = capture(torch, lambda: dp.run_per_tensor(sp), stream)
+    ms_tensors = time_graph(torch, g_t, stream, r_steps)
+    del g_t
     clk = clocks.stop()
     rc = ggq.device_status()
     if rc:
@@ -1022,6 +1037,9 @@ def main():
                      "timing": "one chain launch per CUDA-graph replay, events on its stream"},
         "per_stage_launches": {"ms_per_step": round(ms_launches, 4), "launches_per_pass": len(dp.stages),
                                "value": round(step_bytes * ws / (ms_launches * 1e-3) / 1e9, 1), "unit": "GB/s"},
+        "per_tensor_launches": {"ms_per_step": round(ms_tensors, 4),
+                                "launches_per_pass": sum(len(st["W"]) for st in dp.stages),
+                                "value": round(step_bytes * ws / (ms_tensors * 1e-3) / 1e9, 1), "unit": "GB/s"},
         "clocks": clk,
         "load": {"generate_s": round(t_gen, 2), "ggq_load_s": round(t_load, 3), "file_bytes": file_bytes},
         "configs": extra,

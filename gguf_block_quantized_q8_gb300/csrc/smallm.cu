@@ -15,8 +15,10 @@
 // against all M activation rows
 // (UMMA M = 128 W rows, N = 16 activation rows padded with zeros, K = 16):
 //   warp 0      TMA producer: raw blocks of 128 W rows x 256 columns;
-//   warp 1      allocates 64 TMEM columns; one thread issues the MMAs and
-//               commits each stage back to its "empty" barrier;
+//   warps 1, 18 one thread each issues MMAs (warp 1 also allocates 64 TMEM
+//               columns): warp 1 those into accumulator columns 0-31, warp 18
+//               those into 32-47; each commits its MMAs of a stage back to the
+//               stage's "empty" barrier, which counts both;
 //   warps 2..17 decoders: four threads a W row, 16 columns each per 64-column
 //               stage (packed f32x2 arithmetic).  A weight is decoded exactly in fp32 and split into two
 //               bf16 parts, hi = bf16(w) and lo = bf16(w - hi); X is split the
@@ -25,8 +27,10 @@
 //               operand keeps the fp32 exponent range.  They take two MMAs per
 //               16 columns: X_hi and X_lo, adjacent in shared memory, are one
 //               N = 32 operand for W_hi (accumulator columns 0-15 and 16-31),
-//               and W_lo * X_hi (N = 16) goes to columns 32-47.  The issuing
-//               thread's MMA rate sets the pace at these small N.
+//               and W_lo * X_hi (N = 16) goes to columns 32-47.  At these
+//               small N an issuing thread's MMA rate sets the pace, so the two
+//               products have a thread each (one thread for both: 37.5 us on
+//               Q8_0 14336 x 4096 at M = 8; two: 34.1).
 //   epilogue    warps 2..5 read the three 128 x 16 accumulators (tcgen05.ld; a
 //               warp reaches only its own quarter of the 128 TMEM lanes), add
 //               them and store Y (or add it, for a split tile).
@@ -54,7 +58,8 @@ constexpr int kKStage = 64;      // columns per stage: one 128-byte swizzle row 
 constexpr int kStages = 4;
 constexpr int kRawStages = 2;
 constexpr int kDecoders = 512;
-constexpr int kThreads = 64 + kDecoders;
+constexpr int kLoWarp = 2 + kDecoders / 32;   // the second MMA-issuing warp, after the decoders
+constexpr int kThreads = 64 + kDecoders + 32;
 constexpr int kTmemCols = 64;   // D[0:32] = A_hi [X_hi; X_lo]^T, D[32:48] = A_lo X_hi^T
 
 constexpr int kAPiece = kTileRows * kKStage * 2;   // 16 KB: one bf16 part of a W tile
@@ -231,13 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
         prefetch_tensormap(&wmap);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], kDecoders);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);   // a commit from each MMA-issuing thread
         }
         for (int r = 0; r < kRawStages; ++r) {
             mbar_init(&full_raw[r], 1);
             mbar_init(&empty_raw[r], kDecoders);
         }
-        mbar_init(acc_full, 1);
+        mbar_init(acc_full, 2);
         mbar_init(acc_empty, 128);   // the four epilogue warps
         fence_mbar_init();
     }
@@ -271,12 +276,19 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kLoWarp) {
         if (lane == 0) {
+            // two issuing threads, one per accumulator: warp 1 issues W_hi x
+            // [X_hi; X_lo] (columns 0-31), warp kLoWarp W_lo x X_hi (columns
+            // 32-47); each commits its own MMAs (the barriers count both)
+            const bool lo = warp == kLoWarp;
             // a descriptor's address field is (address >> 4): descriptors of the
             // other parts and offsets are the stage-0 one plus (offset >> 4)
             const uint64_t d0 = sw128_desc(smem_u32(sStage));
             constexpr uint32_t kLo = kAPiece >> 4, kBhi = (2 * kAPiece) >> 4;   // X_lo follows X_hi: one N = 32 operand
+            const uint64_t a_off = lo ? kLo : 0;
+            const uint32_t d_col = lo ? 2 * kN : 0;
+            const uint32_t idesc = lo ? kIdesc : kIdesc32;
             // one loop over the stages of all parts (this thread's issue rate
             // sets the pace, so the loop is kept as plain as for one part);
             // at a part's end: its accumulator to the epilogue, and the next
@@ -306,9 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
 #pragma unroll
                 for (int kk = 0; kk < kKStage / 16; ++kk) {
                     const uint64_t a = ds + 2 * kk;   // 16 bf16 = 32 bytes further along the swizzled rows
-                    const uint32_t acc = !(first && kk == 0);
-                    umma_bf16(tmem, a, a + kBhi, kIdesc32, acc);              // hi*hi, hi*lo
-                    umma_bf16(tmem + 2 * kN, a + kLo, a + kBhi, kIdesc, acc);  // lo*hi
+                    umma_bf16(tmem + d_col, a + a_off, a + kBhi, idesc, !(first && kk == 0));
                 }
                 umma_commit(&empty[s]);
             }

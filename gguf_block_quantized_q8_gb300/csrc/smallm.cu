@@ -15,10 +15,12 @@
 // against all M activation rows
 // (UMMA M = 128 W rows, N = 16 activation rows padded with zeros, K = 16):
 //   warp 0      TMA producer: raw blocks of 128 W rows x 256 columns;
-//   warps 1, 18 one thread each issues MMAs (warp 1 also allocates 64 TMEM
-//               columns): warp 1 those into accumulator columns 0-31, warp 18
-//               those into 32-47; each commits its MMAs of a stage back to the
-//               stage's "empty" barrier, which counts both;
+//   warps 1, 18 (19, 20) one thread each issues MMAs (warp 1 also allocates
+//               the TMEM columns): warp 1 those into accumulator columns 0-31,
+//               warp 18 those into 32-47, and with four issuers warps 1 and 18
+//               take the even stages and 19, 20 the odd ones (columns 64-111);
+//               each commits its MMAs of a stage back to the stage's "empty"
+//               barrier, which counts the two that use the stage;
 //   warps 2..17 decoders: four threads a W row, 16 columns each per 64-column
 //               stage (packed f32x2 arithmetic).  A weight is decoded exactly in fp32 and split into two
 //               bf16 parts, hi = bf16(w) and lo = bf16(w - hi); X is split the
@@ -28,9 +30,9 @@
 //               16 columns: X_hi and X_lo, adjacent in shared memory, are one
 //               N = 32 operand for W_hi (accumulator columns 0-15 and 16-31),
 //               and W_lo * X_hi (N = 16) goes to columns 32-47.  At these
-//               small N an issuing thread's MMA rate sets the pace, so the two
-//               products have a thread each (one thread for both: 37.5 us on
-//               Q8_0 14336 x 4096 at M = 8; two: 34.1).
+//               small N an issuing thread's MMA rate sets the pace, so the
+//               products have threads of their own (one thread for both: 37.5
+//               us on Q8_0 14336 x 4096 at M = 8; two: 34.1; four: 32.1).
 //   epilogue    warps 2..5 read the three 128 x 16 accumulators (tcgen05.ld; a
 //               warp reaches only its own quarter of the 128 TMEM lanes), add
 //               them and store Y (or add it, for a split tile).
@@ -58,9 +60,7 @@ constexpr int kKStage = 64;      // columns per stage: one 128-byte swizzle row 
 constexpr int kStages = 4;
 constexpr int kRawStages = 2;
 constexpr int kDecoders = 512;
-constexpr int kLoWarp = 2 + kDecoders / 32;   // the second MMA-issuing warp, after the decoders
-constexpr int kThreads = 64 + kDecoders + 32;
-constexpr int kTmemCols = 64;   // D[0:32] = A_hi [X_hi; X_lo]^T, D[32:48] = A_lo X_hi^T
+constexpr int kLoWarp = 2 + kDecoders / 32;   // the further MMA-issuing warps, after the decoders
 
 constexpr int kAPiece = kTileRows * kKStage * 2;   // 16 KB: one bf16 part of a W tile
 constexpr int kBPiece = kN * kKStage * 2;          // 2 KB: one bf16 part of an X tile
@@ -73,6 +73,20 @@ constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kRawStages
 // Q4_0 runs of 8 blocks (144 bytes), Q6_K super-blocks (210 bytes: copied from
 // the 16-byte boundary below them, 240 bytes a row), each 256 columns of a row
 enum SmKind { kSmQ8 = 0, kSmQ4K = 1, kSmQ40 = 2, kSmQ6 = 3 };
+
+// MMA-issuing threads: two (the W_hi and the W_lo product) or four (each of
+// those for the even and for the odd stages, into their own accumulators).
+// Four for Q8_0, Q4_K and Q4_0; Q6_K, whose decoders set the pace, keeps two
+// (the extra warps cost its decoders more than they gain).
+template <int K>
+struct Iss {
+    static constexpr int kN = K == kSmQ6 ? 2 : 4;
+    static constexpr int kThreads = 64 + kDecoders + 32 * (kN - 1);
+    // D[0:32] = A_hi [X_hi; X_lo]^T, D[32:48] = A_lo X_hi^T; with four issuers
+    // the odd stages' products at D[64:112]
+    static constexpr int kTmemCols = kN == 4 ? 128 : 64;
+};
+
 // TMA x coordinate (elements of the tensor map) of 256-column block sb
 template <int K>
 __device__ __forceinline__ int raw_x(int sb) {
@@ -209,9 +223,10 @@ __device__ __forceinline__ void q4k_sm(uint32_t s0, uint32_t s1, uint32_t s2, in
 }
 
 template <int K>
-__global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_constant__ CUtensorMap wmap,
+__global__ void __launch_bounds__(Iss<K>::kThreads, 1) smallm_kernel(const __grid_constant__ CUtensorMap wmap,
                                                              const SmallParams p) {
     constexpr bool Q4K = K == kSmQ4K;
+    constexpr int NI = Iss<K>::kN;   // MMA-issuing threads
     constexpr int kRowBytes = K == kSmQ8 ? 272 : K == kSmQ6 ? 240 : 144;   // raw bytes of one W row per 256 columns
     constexpr int kRawBytes = kTileRows * kRowBytes;
     extern __shared__ uint8_t smem_raw[];
@@ -242,11 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             mbar_init(&full_raw[r], 1);
             mbar_init(&empty_raw[r], kDecoders);
         }
-        mbar_init(acc_full, 2);
+        mbar_init(acc_full, NI);   // a commit from each issuing thread
         mbar_init(acc_empty, 128);   // the four epilogue warps
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == 1) tmem_alloc(tmem_slot, Iss<K>::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -276,18 +291,22 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
             }
         }
         __syncwarp();
-    } else if (warp == 1 || warp == kLoWarp) {
+    } else if (warp == 1 || warp >= kLoWarp) {
         if (lane == 0) {
-            // two issuing threads, one per accumulator: warp 1 issues W_hi x
-            // [X_hi; X_lo] (columns 0-31), warp kLoWarp W_lo x X_hi (columns
-            // 32-47); each commits its own MMAs (the barriers count both)
-            const bool lo = warp == kLoWarp;
+            // NI issuing threads, each into accumulator columns of its own: warp
+            // 1 issues W_hi x [X_hi; X_lo] (columns 0-31), warp kLoWarp W_lo x
+            // X_hi (columns 32-47); with four, these for the even stages and
+            // warps kLoWarp + 1, + 2 the same for the odd ones (columns 64 on).
+            // Each commits its own MMAs; the barriers count the commits.
+            const int iss = warp == 1 ? 0 : warp - kLoWarp + 1;
+            const bool lo = iss & 1;
+            const int par = NI == 4 ? iss >> 1 : 0;
             // a descriptor's address field is (address >> 4): descriptors of the
             // other parts and offsets are the stage-0 one plus (offset >> 4)
             const uint64_t d0 = sw128_desc(smem_u32(sStage));
             constexpr uint32_t kLo = kAPiece >> 4, kBhi = (2 * kAPiece) >> 4;   // X_lo follows X_hi: one N = 32 operand
             const uint64_t a_off = lo ? kLo : 0;
-            const uint32_t d_col = lo ? 2 * kN : 0;
+            const uint32_t d_col = (lo ? 2 * kN : 0) + 64 * par;
             const uint32_t idesc = lo ? kIdesc : kIdesc32;
             // one loop over the stages of all parts (this thread's issue rate
             // sets the pace, so the loop is kept as plain as for one part);
@@ -310,11 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
                     pstart = ks;
                     pend = ks + 4 * (pi.sb1 - pi.sb0);
                 }
+                if (NI == 4 && (ks & 1) != par) continue;   // the other parity's stage
                 const int s = ks % kStages;
                 mbar_wait(&full[s], (ks / kStages) & 1, p.status);
                 tc_fence_after();
                 const uint64_t ds = d0 + (uint64_t)((s * kStageBytes) >> 4);
-                const int first = ks == pstart;
+                // this thread's first stage of the part (a part has at least 4)
+                const int first = ks == pstart + (NI == 4 ? ((par ^ pstart) & 1) : 0);
 #pragma unroll
                 for (int kk = 0; kk < kKStage / 16; ++kk) {
                     const uint64_t a = ds + 2 * kk;   // 16 bf16 = 32 bytes further along the swizzled rows
@@ -494,8 +515,17 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
                 tmem_ld16(tq, v);               // hi * hi
                 tmem_ld16(tq + kN, vl);         // hi * lo
                 tmem_ld16(tq + 2 * kN, vh);     // lo * hi
+                if constexpr (NI == 4) {        // the same for the odd stages
+                    float v2[16], vl2[16], vh2[16];
+                    tmem_ld16(tq + 64, v2);
+                    tmem_ld16(tq + 64 + kN, vl2);
+                    tmem_ld16(tq + 64 + 2 * kN, vh2);
 #pragma unroll
-                for (int i = 0; i < kN; ++i) v[i] += vl[i] + vh[i];
+                    for (int i = 0; i < kN; ++i) v[i] = (v[i] + vl[i] + vh[i]) + (v2[i] + vl2[i] + vh2[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kN; ++i) v[i] += vl[i] + vh[i];
+                }
                 tc_fence_before();
                 mbar_arrive(acc_empty);   // the accumulator may take the next part's products
                 if (yrow < p.rows) {
@@ -515,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallm_kernel(const __grid_consta
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, Iss<K>::kTmemCols);
     }
 }
 
@@ -546,7 +576,7 @@ int launch_t(const CUtensorMap& wmap, const SmallParams& p, int grid, cudaStream
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Iss<K>::kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr;

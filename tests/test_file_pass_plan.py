@@ -110,3 +110,88 @@ def test_decode_pass_checks_its_arguments():
         plan.DecodePass([], [], [], M=5)
     with pytest.raises(ValueError):
         plan.DecodePass([(12, [dict(ne=[256, 2], data=0, nbytes=0)])], [], [])
+
+
+class _Buf:
+    """Stands in for a device tensor: only its address is used."""
+
+    def __init__(self, addr):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
+def _fake_chains(monkeypatch, plan, max_cols):
+    """ggq_chain_create_typed that refuses (EINVAL) a run holding a stage wider
+    than max_cols, as the library does for a stage whose pre-scaled x for M rows
+    would not fit in shared memory; records every run it was asked for."""
+    asked, live = [], set()
+
+    def create(M, types, raw):
+        asked.append([r[2] for r in raw])
+        if any(r[2] > max_cols for r in raw):
+            return plan._ggq.EINVAL, 0
+        h = 1000 + len(asked)
+        live.add(h)
+        return 0, h
+
+    monkeypatch.setattr(plan._ggq, "ggq_chain_create_typed", create)
+    monkeypatch.setattr(plan._ggq, "ggq_chain_free", lambda h: live.discard(h))
+    return asked, live
+
+
+def _stages(cols_list, qtype=12):
+    stages, xs, ys = [], [], []
+    for i, cols in enumerate(cols_list):
+        stages.append((qtype, [dict(ne=[cols, 64], data=16 * (i + 1), nbytes=0)]))
+        xs.append(_Buf(4096 * (i + 1)))
+        ys.append([_Buf(8192 * (i + 1))])
+    return stages, xs, ys
+
+
+def test_decode_pass_takes_too_wide_stages_out_of_the_chain(monkeypatch):
+    """Runs of chainable stages become chains; a stage the chain kernel refuses
+    at this M (too wide) becomes a launch of its own between them, and stages
+    that fit keep sharing one chain on each side of it."""
+    from gguf_block_quantized_q8_gb300 import plan
+    asked, live = _fake_chains(monkeypatch, plan, max_cols=8192)
+    cols = [4096, 4096, 14336, 4096, 4096, 4096, 14336, 14336, 4096]
+    stages, xs, ys = _stages(cols)
+    dp = plan.DecodePass(stages, xs, ys, M=4)
+    kinds = [(k, c["cols"] if k == "stage" else c) for k, c in dp.calls]
+    assert [k for k, _ in kinds] == ["chain", "stage", "chain", "stage", "stage", "chain"]
+    assert [c for k, c in kinds if k == "stage"] == [14336, 14336, 14336]
+    # the whole run first, each stage alone once the run was refused, then the
+    # runs between the too-wide stages
+    assert asked[0] == cols
+    assert asked[1:1 + len(cols)] == [[c] for c in cols]
+    assert asked[1 + len(cols):] == [[4096, 4096], [4096, 4096, 4096], [4096]]
+    assert len(dp.chains) == 3 and live == set(dp.chains)
+    dp.close()
+    assert not live
+
+
+def test_decode_pass_one_chain_when_every_stage_fits(monkeypatch):
+    from gguf_block_quantized_q8_gb300 import plan
+    asked, live = _fake_chains(monkeypatch, plan, max_cols=1 << 20)
+    stages, xs, ys = _stages([4096, 14336, 4096])
+    dp = plan.DecodePass(stages, xs, ys, M=2)
+    assert dp.launches == 1 and asked == [[4096, 14336, 4096]]
+    dp.close()
+    assert not live
+
+
+def test_decode_pass_other_errors_propagate(monkeypatch):
+    """A refusal for another reason than EINVAL is an error, not a split."""
+    from gguf_block_quantized_q8_gb300 import plan
+    live = set()
+
+    def create(M, types, raw):
+        return plan._ggq.ECUDA, 0
+
+    monkeypatch.setattr(plan._ggq, "ggq_chain_create_typed", create)
+    monkeypatch.setattr(plan._ggq, "ggq_chain_free", lambda h: live.discard(h))
+    stages, xs, ys = _stages([4096, 4096])
+    with pytest.raises(Exception):
+        plan.DecodePass(stages, xs, ys, M=1)

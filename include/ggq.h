@@ -159,8 +159,9 @@ int ggq_kv_find(const ggq_model* model, const char* key, int64_t* i); /* GGQ_ENO
  *   y      device, fp32 [M, rows] row-major, 4-byte aligned; fully overwritten;
  *          must not overlap W or x (with 5..16 rows it may be zeroed first)
  *   M      1..16 (M > 1 is the small-batch variant: each decoded block is used
- *          for all M rows of x; from 5 rows on, Q8_0, Q4_K and Q4_0 run on the
- *          tensor cores in one pass over W; up to 4 rows, where the pre-scaled
+ *          for all M rows of x; from 5 rows on, Q8_0, Q4_K, Q4_0 and Q6_K
+ *          (Q6_K with cols % 2048 == 0) run on the tensor cores in one pass
+ *          over W; up to 4 rows, where the pre-scaled
  *          x of all M rows does not fit in shared memory, e.g. 4 rows of 14336
  *          columns, the rows run in groups, one pass over W per group)
  *   stream cudaStream_t
